@@ -1,0 +1,307 @@
+"""Pins of the CPU oracle to things other than itself (no GPU needed).
+
+* the hand-worked example in tests/golden/hand_worked.json (bf16 and FP8);
+* exact rational brute force with a rank-counting top-k on tiny inputs;
+* library special cases: H=1, w=1, q,k >= 0 reduces to a matrix product and a
+  stable sort (numpy), including the tie order;
+* the e4m3 / bf16 decoders against torch's conversions for every code;
+* invariants: causality, -1 padding, the tie rule (also -0.0 == +0.0),
+  key-permutation equivariance, positive homogeneity in w, the FP8 scale
+  shaping against pre-scaled bf16 values, paged == dense;
+* IndexShare source resolution and its rejections.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import brute
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")
+
+
+def _bits(t):
+    if t.dtype == torch.bfloat16:
+        return (t.view(torch.int16).to(torch.int32) & 0xFFFF).tolist()
+    return t.view(torch.uint8).to(torch.int32).tolist()
+
+
+# ---------------------------------------------------------------- decoders
+
+def test_e4m3_decode_all_codes_match_torch():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float32).tolist()
+    for c, r in zip(range(256), ref):
+        v = oracle.decode_e4m3(c)
+        if np.isnan(r):
+            assert np.isnan(v), c
+        else:
+            assert v == r, (c, v, r)
+            assert brute.e4m3_value(c) == r
+    assert oracle.decode_e4m3(0x7E) == 448.0
+
+
+def test_bf16_decode_all_finite_codes_match_torch():
+    codes = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    ref = codes.view(torch.bfloat16).to(torch.float64).numpy()
+    for c in range(0, 65536, 7):
+        r = ref[c]
+        if not np.isfinite(r):
+            continue
+        assert oracle.decode_bf16(c) == r, c
+        assert float(brute.bf16_value(c)) == r
+
+
+# ---------------------------------------------------------------- hand-worked
+
+def _golden_case(kind):
+    g = json.load(open(GOLDEN))
+    q = torch.tensor(g["q"], dtype=torch.float32)
+    k = torch.tensor(g["k"], dtype=torch.float32)
+    w = torch.tensor(g["w"], dtype=torch.float32)
+    qs = ks = None
+    if kind == "bf16":
+        q, k = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    else:
+        q, k = q.to(torch.float8_e4m3fn), k.to(torch.float8_e4m3fn)
+        qs = torch.tensor(g["fp8"]["q_scale"], dtype=torch.float32)
+        ks = torch.tensor(g["fp8"]["k_scale"], dtype=torch.float32)
+    return g, q, k, w, qs, ks
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp8"])
+def test_hand_worked_example(kind):
+    g, q, k, w, qs, ks = _golden_case(kind)
+    topk, scores, _ = oracle.dense(q, k, w, T=g["T"], S=g["S"], H=g["H"], D=g["D"],
+                                   q_pos0=g["q_pos0"], topk_limit=g["topk_limit"],
+                                   k_out=g["k_out"], q_scale=qs, k_scale=ks, want_scores=True)
+    exp = g[kind]
+    assert topk.tolist() == exp["topk"]
+    for t, row in enumerate(exp["scores"]):
+        for s, v in enumerate(row):
+            if v is None:
+                assert scores[t, s] == -np.inf
+            else:
+                assert scores[t, s] == v, (t, s)
+
+
+# ---------------------------------------------------------------- brute force
+
+def _brute_dense(c):
+    return brute.dense(_bits(c.q), _bits(c.k), c.w.tolist(), dtype="bf16" if c.dtype == "bf16" else "fp8",
+                       T=c.T, S=c.S, H=c.H, D=c.D, q_pos0=c.q_pos0, topk_limit=c.topk_limit,
+                       k_out=c.k_out,
+                       q_scale=None if c.q_scale is None else c.q_scale.tolist(),
+                       k_scale=None if c.k_scale is None else c.k_scale.tolist())
+
+
+def _oracle_dense(c, **kw):
+    return oracle.dense(c.q, c.k, c.w, T=c.T, S=c.S, H=c.H, D=c.D, q_pos0=c.q_pos0,
+                        topk_limit=c.topk_limit, k_out=c.k_out, q_scale=c.q_scale,
+                        k_scale=c.k_scale, **kw)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_brute_force_exact_integer_inputs(seed, dtype):
+    # H != D and T != S so a transposed operand or index cannot go unnoticed
+    c = workloads.dense_case(9, 12, 3, 5, 4, q_pos0=2, k_out=6, integer=True, dtype=dtype,
+                             int_range=(-2, 2), seed=seed)
+    bt, bs = _brute_dense(c)
+    topk, scores, _ = _oracle_dense(c, want_scores=True)
+    assert topk.tolist() == bt
+    for t in range(c.T):
+        for s, v in enumerate(bs[t]):
+            assert scores[t, s] == float(v)
+        assert np.all(scores[t, len(bs[t]):] == -np.inf)
+
+
+@pytest.mark.parametrize("seed", [3, 4])
+def test_brute_force_gaussian_inputs(seed):
+    c = workloads.dense_case(6, 10, 4, 8, 3, q_pos0=4, k_out=5, seed=seed)
+    bt, bs = _brute_dense(c)
+    topk, scores, bound = _oracle_dense(c, want_scores=True, want_bound=True)
+    for t in range(c.T):
+        for s, v in enumerate(bs[t]):
+            assert abs(scores[t, s] - float(v)) <= 1e-13 * bound[t, s] + 1e-300
+    # continuous random data: no ties, so the exact ranking is the oracle's
+    assert topk.tolist() == bt
+
+
+def test_brute_force_fp8_gaussian_quantised():
+    c = workloads.dense_case(5, 7, 2, 6, 3, q_pos0=2, dtype="fp8_e4m3", seed=5)
+    bt, bs = _brute_dense(c)
+    topk, scores, bound = _oracle_dense(c, want_scores=True, want_bound=True)
+    for t in range(c.T):
+        for s, v in enumerate(bs[t]):
+            assert abs(scores[t, s] - float(v)) <= 1e-13 * bound[t, s] + 1e-300
+    assert topk.tolist() == bt
+
+
+# ---------------------------------------------------------------- library special case
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_single_head_reduces_to_matmul_and_stable_sort(seed):
+    g = torch.Generator().manual_seed(100 + seed)
+    T, S, D, kk = 20, 40, 16, 9
+    q = torch.randint(0, 4, (T, 1, D), generator=g).to(torch.bfloat16)
+    k = torch.randint(0, 4, (S, D), generator=g).to(torch.bfloat16)
+    w = torch.ones(T, 1)
+    q_pos0 = 10
+    topk, scores, _ = oracle.dense(q, k, w, T=T, S=S, H=1, D=D, q_pos0=q_pos0, topk_limit=kk,
+                                   k_out=kk + 3, want_scores=True)
+    ref = q.to(torch.float64)[:, 0, :].numpy() @ k.to(torch.float64).numpy().T
+    for t in range(T):
+        n = min(q_pos0 + t + 1, S)
+        assert np.array_equal(scores[t, :n], ref[t, :n])
+        # stable argsort of -score == (score desc, index asc); small integers -> many ties
+        order = np.argsort(-ref[t, :n], kind="stable")[:min(kk, n)]
+        exp = list(order) + [-1] * (kk + 3 - len(order))
+        assert topk[t].tolist() == exp
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_causality_future_keys_do_not_matter():
+    c = workloads.dense_case(16, 24, 4, 8, 5, q_pos0=4, integer=True, seed=7)
+    topk, scores, _ = _oracle_dense(c, want_scores=True)
+    k2 = c.k.clone()
+    g = torch.Generator().manual_seed(9)
+    for t in range(c.T):
+        pos = c.q_pos0 + t
+        k2 = c.k.clone()
+        if pos + 1 < c.S:
+            k2[pos + 1:] = torch.randint(-4, 5, (c.S - pos - 1, c.D), generator=g).to(torch.bfloat16)
+        c2 = workloads.DenseCase(**{**c.__dict__, "k": k2})
+        t2, s2, _ = _oracle_dense(c2, rows=[t], want_scores=True)
+        assert t2[0].tolist() == topk[t].tolist()
+        assert np.array_equal(s2[0, :pos + 1], scores[t, :pos + 1])
+        assert topk[t].max() <= pos
+
+
+@pytest.mark.parametrize("limit,k_out", [(5, 5), (5, 8), (40, 40), (1, 3)])
+def test_padding_counts(limit, k_out):
+    c = workloads.dense_case(20, 20, 2, 4, limit, q_pos0=0, k_out=k_out, seed=11)
+    topk, _, _ = _oracle_dense(c)
+    for t in range(c.T):
+        keep = min(limit, t + 1, k_out)
+        row = topk[t].tolist()
+        assert all(v >= 0 for v in row[:keep])
+        assert row[keep:] == [-1] * (k_out - keep)
+        assert len(set(row[:keep])) == keep
+
+
+def test_tie_storm_zero_weights_gives_lowest_indices():
+    c = workloads.dense_case(10, 30, 4, 8, 7, q_pos0=20, seed=12)
+    c.w.zero_()
+    topk, scores, _ = _oracle_dense(c, want_scores=True)
+    for t in range(c.T):
+        keep = min(7, 21 + t)
+        assert topk[t].tolist() == list(range(keep))
+
+
+def test_negative_zero_equals_positive_zero():
+    sc = np.array([[0.0, -0.0, 1.0, -0.0, 0.0, -1.0]])
+    out = oracle.topk_of_scores(sc, [6], 4, 4)
+    assert out[0].tolist() == [2, 0, 1, 3]
+
+
+def test_key_permutation_equivariance():
+    c = workloads.dense_case(8, 32, 4, 8, 6, q_pos0=31, seed=13)   # every query sees every key
+    topk, scores, _ = _oracle_dense(c, want_scores=True)
+    perm = torch.randperm(c.S, generator=torch.Generator().manual_seed(14))
+    c2 = workloads.DenseCase(**{**c.__dict__, "k": c.k[perm].contiguous()})
+    t2, s2, _ = _oracle_dense(c2, want_scores=True)
+    inv = perm.numpy()
+    for t in range(c.T):
+        assert np.array_equal(s2[t], scores[t][inv])
+        assert sorted(inv[t2[t]].tolist()) == sorted(topk[t].tolist())
+
+
+def test_positive_homogeneity_in_w():
+    c = workloads.dense_case(8, 16, 4, 8, 5, q_pos0=8, integer=True, seed=15)
+    topk, scores, _ = _oracle_dense(c, want_scores=True)
+    c2 = workloads.DenseCase(**{**c.__dict__, "w": c.w * 2.0})
+    t2, s2, _ = _oracle_dense(c2, want_scores=True)
+    assert np.array_equal(t2, topk)
+    fin = np.isfinite(scores)
+    assert np.array_equal(s2[fin], 2.0 * scores[fin])
+
+
+def test_fp8_scale_shaping_equals_prescaled_bf16():
+    c = workloads.dense_case(8, 16, 4, 8, 5, q_pos0=8, integer=True, dtype="fp8_e4m3",
+                             int_range=(-3, 3), seed=16)
+    topk, scores, _ = _oracle_dense(c, want_scores=True)
+    qv = c.q.to(torch.float32) * c.q_scale[:, :, None]
+    kv = c.k.to(torch.float32) * c.k_scale[:, None]
+    c2 = workloads.DenseCase(**{**c.__dict__, "q": qv.to(torch.bfloat16), "k": kv.to(torch.bfloat16),
+                                "q_scale": None, "k_scale": None, "dtype": "bf16"})
+    assert torch.equal(c2.q.to(torch.float32), qv) and torch.equal(c2.k.to(torch.float32), kv)
+    t2, s2, _ = _oracle_dense(c2, want_scores=True)
+    assert np.array_equal(t2, topk)
+    assert np.array_equal(s2, scores)
+
+
+def test_paged_equals_dense():
+    pc = workloads.paged_case([37, 5, 64, 130], [3, 5, 1, 7], 4, 8, 6, page_size=16,
+                              integer=True, seed=17)
+    topk, scores, _ = oracle.paged(pc, want_scores=True)
+    pos = oracle.query_positions(pc)
+    cu = pc.cu_q_lens.tolist()
+    for b, L in enumerate(pc.seq_lens.tolist()):
+        npg = (L + 15) // 16
+        pages = pc.block_tables[b, :npg].long()
+        k_dense = pc.k_cache[pages].reshape(-1, pc.D)[:L].contiguous()
+        ql = cu[b + 1] - cu[b]
+        td, sd, _ = oracle.dense(pc.q[cu[b]:cu[b + 1]], k_dense, pc.w[cu[b]:cu[b + 1]], T=ql, S=L,
+                                 H=pc.H, D=pc.D, q_pos0=L - ql, topk_limit=6, k_out=6,
+                                 want_scores=True)
+        assert np.array_equal(td, topk[cu[b]:cu[b + 1]])
+        assert np.array_equal(sd, scores[cu[b]:cu[b + 1], :L])
+        assert pos[cu[b]] == L - ql
+
+
+def test_index_order_is_sorted_score_order_set():
+    c = workloads.dense_case(12, 40, 4, 8, 9, q_pos0=20, integer=True, seed=18)
+    t_score, _, _ = _oracle_dense(c)
+    t_index, _, _ = _oracle_dense(c, order=oracle.ORDER_INDEX)
+    for a, b in zip(t_score, t_index):
+        keep = int((a >= 0).sum())
+        assert sorted(a[:keep].tolist()) == b[:keep].tolist()
+        assert (b[keep:] == -1).all()
+
+
+def test_row_subset_matches_full_run():
+    c = workloads.dense_case(30, 30, 2, 8, 4, q_pos0=0, seed=19)
+    full, sf, _ = _oracle_dense(c, want_scores=True)
+    rows = [0, 7, 29, 13]
+    sub, ss, _ = _oracle_dense(c, rows=rows, want_scores=True)
+    assert np.array_equal(sub, full[rows])
+    assert np.array_equal(ss, sf[rows])
+
+
+# ---------------------------------------------------------------- IndexShare
+
+def test_resolve_sources_chain_and_errors():
+    assert oracle.resolve_indexer_sources(["full", "shared", "shared", "full", "shared"]) == [0, 0, 0, 3, 3]
+    assert oracle.resolve_indexer_sources(workloads.INDEXSHARE_TYPES_12) == [0, 0, 0, 3, 3, 3, 6, 6, 6, 9, 9, 9]
+    with pytest.raises(ValueError):
+        oracle.resolve_indexer_sources(["shared", "full"])
+    with pytest.raises(ValueError):
+        oracle.resolve_indexer_sources(["full", "sharded"])
+    with pytest.raises(ValueError):
+        oracle.resolve_indexer_sources(["full"], num_layers=2)
+
+
+def test_stack_shared_layers_forward_source_unchanged():
+    types = ["full", "shared", "shared", "full", "shared"]
+    layers = [workloads.paged_case([40, 70], [1, 1], 4, 8, 8, page_size=16, seed=20 + i)
+              if t == "full" else None for i, t in enumerate(types)]
+    src, outs = oracle.stack(types, layers)
+    assert src == [0, 0, 0, 3, 3]
+    assert outs[1] is outs[0] and outs[2] is outs[0] and outs[4] is outs[3]
+    assert not np.array_equal(outs[0], outs[3])
