@@ -1,0 +1,197 @@
+/*
+ * dsa_indexer.h -- C ABI of the GB300 (sm_103a) DSA indexer library.
+ *
+ * The DeepSeek-Sparse-Attention indexer that GLM5's glm_moe_dsa layers run
+ * scores every causal query/key pair and keeps each query's best keys
+ * (GLM5 TensorCast adaptation design, section "DSA Indexer 融合语义算子";
+ * cost buckets 6-10 of section "性能模型设计"):
+ *
+ *     x[t,h,s]   = sq[t,h] * sk[s] * sum_d q[t,h,d] * k[s,d]      (sq = sk = 1 for bf16)
+ *     score[t,s] = sum_h w[t,h] * max(x[t,h,s], 0)                 for keys s <= pos(t)
+ *     topk[t,:]  = the min(topk_limit, pos(t)+1) keys of highest score, ties to the
+ *                  lower key index, then -1 up to k_out
+ *
+ * and GLM-5.2 IndexShare (same page, section "GLM-5.2 IndexShare"): a layer
+ * typed "shared" runs no indexer and forwards the top-k of the nearest earlier
+ * "full" layer unchanged.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named q, k, k_cache, w, scales, scores, topk, cu_q_lens,
+ *    seq_lens, block_tables and workspace are DEVICE pointers, owned by the
+ *    caller; the library keeps none of them after returning and allocates no
+ *    device memory.  Pointers named types / src / full_args / topk_out are host.
+ *  - All work is enqueued on `stream` (NULL = legacy default stream) and is
+ *    asynchronous; nothing synchronises except dsa_check_device_status.
+ *  - Host-side validation happens before any launch; a failing call launches
+ *    nothing and returns the status.
+ *  - Device-side checks (a page id outside [0, num_pages), a key position that
+ *    the block table does not cover, a bounded wait that gave up) never trap:
+ *    the kernel records a bit in a library-owned device status word and skips
+ *    the access; dsa_check_device_status reports and clears it.
+ *  - Tensors are dense row-major with the strides implied by their shapes
+ *    (only scores takes an explicit leading dimension).
+ *  - Every device pointer must be 16-byte aligned; row pitches of q/k
+ *    (D * element size) are then multiples of 16 bytes for the supported D.
+ */
+#ifndef DSA_INDEXER_H
+#define DSA_INDEXER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dsa_stream_t; /* the same handle as cudaStream_t */
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, bad indexer_types, ... */
+    DSA_ERR_UNSUPPORTED = 2,      /* valid but not implemented: D, H, dtype mix, k_out */
+    DSA_ERR_CUDA = 3,             /* a CUDA runtime/driver call or launch failed */
+    DSA_ERR_DEVICE_CHECK = 4,     /* a kernel found a bad page id / uncovered key */
+    DSA_ERR_TIMEOUT = 5,          /* a bounded device wait gave up */
+    DSA_ERR_WORKSPACE = 6         /* workspace missing or smaller than required */
+} dsa_status;
+
+typedef enum { DSA_BF16 = 0, DSA_FP8_E4M3 = 1 } dsa_dtype;
+
+typedef enum { DSA_LAYER_FULL = 0, DSA_LAYER_SHARED = 1 } dsa_layer_type;
+
+/* Output order of a top-k row.  Both are unique for a given score row.
+ *  DSA_ORDER_SCORE: by (score desc, key index asc) -- torch.topk's sorted order with
+ *                   deterministic ties (GLM5 LoRA blog, section 1, on tie order).
+ *  DSA_ORDER_INDEX: the same set of keys in ascending key index.             */
+typedef enum { DSA_ORDER_SCORE = 0, DSA_ORDER_INDEX = 1 } dsa_topk_order;
+
+/* Largest k_out / topk_limit the top-k kernels accept. */
+#define DSA_MAX_TOPK 4096
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* dsa_status_string(int status);
+
+/* Library version string (static storage). */
+const char* dsa_version(void);
+
+/* Width of a top-k row: min(topk_limit, active_seq_len), never negative
+ * (GLM5 TensorCast adaptation design, "DSA Indexer 融合语义算子": the op returns
+ * (batch, seq_len, min(topk_limit, active_seq_len))). */
+int dsa_topk_width(int topk_limit, int64_t active_seq_len);
+
+/*
+ * dsa_indexer_scores -- dense scoring of one sequence (cost buckets 6 and 7:
+ * q-k index score MMA; head weight multiply, head reduce, FP8 relu / q-scale /
+ * k-scale shaping).
+ *
+ *   q        [T, H, D]  q_dtype        query rows, query t at position q_pos0 + t
+ *   q_scale  [T, H]     fp32 > 0       FP8 q only (NULL for bf16 q)
+ *   k        [S, D]     k_dtype        keys 0..S-1
+ *   k_scale  [S]        fp32 > 0       FP8 k only (NULL for bf16 k)
+ *   w        [T, H]     fp32           per-head weights (any sign)
+ *   scores   [T, ld_scores] fp32       out: scores[t, s] for s <= min(q_pos0 + t, S - 1);
+ *                                      entries with s > q_pos0 + t are NOT written
+ *
+ * Supported: (q_dtype, k_dtype) in {(BF16, BF16), (FP8, FP8)}; D in {64, 128} for
+ * bf16, D = 128 for FP8; H in {4, 8, 16, 32, 64, 128}; ld_scores >= S and a
+ * multiple of 4; q_pos0 >= 0.  T == 0 or S == 0 is a no-op.
+ * Inputs must be finite; scales must be finite and > 0 (the library applies the
+ * q scale to w and the k scale after the head sum, which commutes with ReLU
+ * only for positive scales).
+ */
+dsa_status dsa_indexer_scores(const void* q, int q_dtype, const float* q_scale,
+                              const void* k, int k_dtype, const float* k_scale,
+                              const float* w, int T, int S, int H, int D, int q_pos0,
+                              float* scores, int64_t ld_scores, dsa_stream_t stream);
+
+/*
+ * dsa_indexer_topk -- per-row top-k of dense scores (cost bucket 8, top-k selection).
+ *
+ *   scores [T, ld_scores] fp32   row t has n_t = max(0, min(q_pos0 + t + 1, S)) visible
+ *                                entries scores[t, 0..n_t-1]; nothing else is read
+ *   topk   [T, k_out] int32      out: min(topk_limit, n_t) key indices, then -1
+ *
+ * topk_limit >= 1, 1 <= k_out <= DSA_MAX_TOPK, topk_limit <= DSA_MAX_TOPK unless
+ * no row is longer than DSA_MAX_TOPK; order is a dsa_topk_order.  Ties between equal
+ * scores go to the lower key index; -0.0 and +0.0 are equal.  NaN scores are
+ * outside the contract.  Needs no workspace.
+ */
+dsa_status dsa_indexer_topk(const float* scores, int64_t ld_scores, int T, int S, int q_pos0,
+                            int topk_limit, int k_out, int order, int32_t* topk,
+                            dsa_stream_t stream);
+
+/*
+ * Fused indexer over a paged key cache for a varlen batch: prefill, chunked
+ * prefill and decode (op inputs indexer_cache, block_tables, seq_lens of section
+ * "DSA Indexer 融合语义算子"; key and scale cache read bytes, buckets 9 and 10).
+ *
+ * Sequence b owns query rows cu_q_lens[b] .. cu_q_lens[b+1]-1; its i-th query
+ * sits at position pos = seq_lens[b] - q_len_b + i and sees keys 0..pos.  Key s
+ * of sequence b is k_cache[block_tables[b * max_pages_per_seq + s / page_size]]
+ * [s % page_size].  Returned indices are logical key positions in the sequence.
+ */
+typedef struct {
+    int q_dtype;                 /* dsa_dtype of q                                   */
+    int k_dtype;                 /* dsa_dtype of k_cache                             */
+    int B;                       /* sequences                                        */
+    int total_q;                 /* cu_q_lens[B] (host copy; rows of q, w, topk)     */
+    int H, D;                    /* indexer heads, head dim                          */
+    int page_size;               /* tokens per page; 64 supported                    */
+    int num_pages;               /* pages in k_cache                                 */
+    int max_pages_per_seq;       /* columns of block_tables                          */
+    int max_seq_len;             /* host upper bound of seq_lens[b]                  */
+    const void* q;               /* [total_q, H, D]                                  */
+    const float* q_scale;        /* [total_q, H] fp32 (FP8 q) or NULL                */
+    const float* w;              /* [total_q, H] fp32                                */
+    const int32_t* cu_q_lens;    /* [B + 1], cu_q_lens[0] = 0, non-decreasing        */
+    const int32_t* seq_lens;     /* [B], q_len_b <= seq_lens[b] <= max_seq_len       */
+    const int32_t* block_tables; /* [B, max_pages_per_seq]                           */
+    const void* k_cache;         /* [num_pages, page_size, D]                        */
+    const float* k_scale_cache;  /* [num_pages, page_size] fp32 (FP8 k) or NULL      */
+    int topk_limit;              /* index_topk / topk_limit                          */
+    int k_out;                   /* columns of topk, >= 1                            */
+    int order;                   /* dsa_topk_order                                   */
+    int32_t* topk;               /* out [total_q, k_out]                             */
+    void* workspace;             /* device scratch, >= dsa_indexer_workspace_size    */
+    size_t workspace_bytes;
+} dsa_indexer_args;
+
+/* Bytes of device workspace dsa_indexer needs for these sizes (pointers may be NULL). */
+dsa_status dsa_indexer_workspace_size(const dsa_indexer_args* args, size_t* bytes);
+
+/* Run the fused indexer.  Same dtype / H / D support as dsa_indexer_scores plus the
+ * (BF16 q, FP8 cache) mix is UNSUPPORTED for now.  The workspace must not be used
+ * by another call that overlaps on the GPU. */
+dsa_status dsa_indexer(const dsa_indexer_args* args, dsa_stream_t stream);
+
+/*
+ * IndexShare source resolution (host only, GLM5 TensorCast adaptation design,
+ * "GLM-5.2 IndexShare"): src[l] = l for a full layer, the nearest earlier full
+ * layer for a shared layer.  types[l] is a dsa_layer_type.  An unknown type or a
+ * shared layer with no earlier full layer returns DSA_ERR_INVALID_ARGUMENT and
+ * leaves src unspecified.
+ */
+dsa_status dsa_resolve_indexer_sources(int L, const int32_t* types, int32_t* src);
+
+/*
+ * dsa_indexer_stack -- an IndexShare stack of L layers.
+ *   full_args[l]  host pointer to the args of full layer l (its own cache, q, w and
+ *                 output buffer); NULL for shared layers (they own no cache).
+ *   topk_out[l]   host array of L device pointers, written by the call: a full layer's
+ *                 entry is full_args[l]->topk, a shared layer's entry is its source
+ *                 layer's buffer -- the same memory, forwarded unchanged, no launch.
+ *   src_out       host [L] or NULL: the resolved source layers.
+ * Every argument is validated before the first launch.
+ */
+dsa_status dsa_indexer_stack(int L, const int32_t* types, const dsa_indexer_args* const* full_args,
+                             int32_t** topk_out, int32_t* src_out, dsa_stream_t stream);
+
+/* Synchronise `stream`, then report and clear the device status word of the current
+ * device: DSA_OK, DSA_ERR_DEVICE_CHECK or DSA_ERR_TIMEOUT (or DSA_ERR_CUDA). */
+dsa_status dsa_check_device_status(dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_INDEXER_H */

@@ -1,0 +1,315 @@
+"""Python binding of the GB300 DSA indexer library (libdsa_indexer.so).
+
+Argument marshalling only: every step of the indexer runs in the CUDA kernels
+behind the C ABI of include/dsa_indexer.h.  Tensors must be CUDA tensors; the
+library is loaded with ctypes and there is no fallback -- if the library is
+missing or a call fails, an exception is raised.
+
+Function names mirror the C ABI:
+  dsa_indexer_scores, dsa_indexer_topk, dsa_indexer, dsa_indexer_workspace_size,
+  dsa_resolve_indexer_sources, dsa_indexer_stack, dsa_check_device_status,
+  dsa_topk_width, dsa_status_string, dsa_version.
+Host helpers from the GLM5 TensorCast adaptation design ("Sparse MLA 配置兼容",
+"GLM-5.2 IndexShare"): resolve_topk_limit, extend_indexer_types_for_mtp,
+indexer_types_to_codes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdsa_indexer.so")
+
+DSA_OK = 0
+DSA_ERR_INVALID_ARGUMENT = 1
+DSA_ERR_UNSUPPORTED = 2
+DSA_ERR_CUDA = 3
+DSA_ERR_DEVICE_CHECK = 4
+DSA_ERR_TIMEOUT = 5
+DSA_ERR_WORKSPACE = 6
+
+DSA_BF16 = 0
+DSA_FP8_E4M3 = 1
+DSA_LAYER_FULL = 0
+DSA_LAYER_SHARED = 1
+DSA_ORDER_SCORE = 0
+DSA_ORDER_INDEX = 1
+DSA_MAX_TOPK = 4096
+
+
+class DsaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {dsa_status_string(status)} ({status})")
+
+
+class dsa_indexer_args(ctypes.Structure):
+    _fields_ = [
+        ("q_dtype", ctypes.c_int), ("k_dtype", ctypes.c_int), ("B", ctypes.c_int),
+        ("total_q", ctypes.c_int), ("H", ctypes.c_int), ("D", ctypes.c_int),
+        ("page_size", ctypes.c_int), ("num_pages", ctypes.c_int),
+        ("max_pages_per_seq", ctypes.c_int), ("max_seq_len", ctypes.c_int),
+        ("q", ctypes.c_void_p), ("q_scale", ctypes.c_void_p), ("w", ctypes.c_void_p),
+        ("cu_q_lens", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+        ("block_tables", ctypes.c_void_p), ("k_cache", ctypes.c_void_p),
+        ("k_scale_cache", ctypes.c_void_p), ("topk_limit", ctypes.c_int), ("k_out", ctypes.c_int),
+        ("order", ctypes.c_int), ("topk", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_LIB = None
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, I64, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        L.dsa_status_string.restype = ctypes.c_char_p
+        L.dsa_status_string.argtypes = [I]
+        L.dsa_version.restype = ctypes.c_char_p
+        L.dsa_topk_width.restype = I
+        L.dsa_topk_width.argtypes = [I, I64]
+        L.dsa_indexer_scores.restype = I
+        L.dsa_indexer_scores.argtypes = [P, I, P, P, I, P, P, I, I, I, I, I, P, I64, P]
+        L.dsa_indexer_topk.restype = I
+        L.dsa_indexer_topk.argtypes = [P, I64, I, I, I, I, I, I, P, P]
+        L.dsa_indexer_workspace_size.restype = I
+        L.dsa_indexer_workspace_size.argtypes = [ctypes.POINTER(dsa_indexer_args), ctypes.POINTER(S)]
+        L.dsa_indexer.restype = I
+        L.dsa_indexer.argtypes = [ctypes.POINTER(dsa_indexer_args), P]
+        L.dsa_resolve_indexer_sources.restype = I
+        L.dsa_resolve_indexer_sources.argtypes = [I, P, P]
+        L.dsa_indexer_stack.restype = I
+        L.dsa_indexer_stack.argtypes = [I, P, P, P, P, P]
+        L.dsa_check_device_status.restype = I
+        L.dsa_check_device_status.argtypes = [P]
+        _LIB = L
+    return _LIB
+
+
+def _check(status: int, where: str):
+    if status != DSA_OK:
+        raise DsaError(status, where)
+
+
+def dsa_status_string(status: int) -> str:
+    return lib().dsa_status_string(int(status)).decode()
+
+
+def dsa_version() -> str:
+    return lib().dsa_version().decode()
+
+
+def dsa_topk_width(topk_limit: int, active_seq_len: int) -> int:
+    return int(lib().dsa_topk_width(int(topk_limit), int(active_seq_len)))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DSA_BF16
+    if t.dtype == torch.float8_e4m3fn:
+        return DSA_FP8_E4M3
+    raise TypeError(f"unsupported element type {t.dtype} (bf16 or float8_e4m3fn)")
+
+
+def _dev(t: Optional[torch.Tensor], name: str, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    """Raw cudaStream_t of `stream` (default: torch's current stream; NULL without CUDA)."""
+    if stream is None:
+        if not torch.cuda.is_available():
+            return None
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def dsa_indexer_scores(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, *, q_pos0: Optional[int] = None,
+                       q_scale: Optional[torch.Tensor] = None, k_scale: Optional[torch.Tensor] = None,
+                       scores: Optional[torch.Tensor] = None, ld: Optional[int] = None,
+                       fill=float("-inf"), stream=None) -> torch.Tensor:
+    """Dense scores [T, ld] fp32 of queries q [T, H, D] against keys k [S, D].
+
+    Entries a query cannot see (s > q_pos0 + t) are left as the output buffer held
+    them: a freshly allocated buffer is filled with ``fill`` (by torch) first."""
+    T, H, D = q.shape
+    S = k.shape[0]
+    if q_pos0 is None:
+        q_pos0 = S - T
+    if ld is None:
+        ld = (S + 3) // 4 * 4
+    if scores is None:
+        scores = torch.full((T, ld), fill, dtype=torch.float32, device=q.device)
+    _check(lib().dsa_indexer_scores(
+        _dev(q, "q"), _dtype_code(q), _dev(q_scale, "q_scale", torch.float32),
+        _dev(k, "k"), _dtype_code(k), _dev(k_scale, "k_scale", torch.float32),
+        _dev(w, "w", torch.float32), T, S, H, D, int(q_pos0), _dev(scores, "scores", torch.float32),
+        int(scores.stride(0)), _stream_ptr(stream)), "dsa_indexer_scores")
+    return scores
+
+
+def dsa_indexer_topk(scores: torch.Tensor, *, T: int, S: int, q_pos0: int, topk_limit: int,
+                     k_out: Optional[int] = None, order: int = DSA_ORDER_SCORE,
+                     topk: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Per-row top-k [T, k_out] int32 of dense scores (row t sees min(q_pos0 + t + 1, S) keys)."""
+    if k_out is None:
+        k_out = topk_limit
+    if topk is None:
+        topk = torch.empty((T, k_out), dtype=torch.int32, device=scores.device)
+    _check(lib().dsa_indexer_topk(_dev(scores, "scores", torch.float32), int(scores.stride(0)), T, S,
+                                  int(q_pos0), int(topk_limit), int(k_out), int(order),
+                                  _dev(topk, "topk", torch.int32), _stream_ptr(stream)), "dsa_indexer_topk")
+    return topk
+
+
+def make_indexer_args(q, w, k_cache, cu_q_lens, seq_lens, block_tables, *, max_seq_len: int, topk_limit: int,
+                      k_out: Optional[int] = None, q_scale=None, k_scale_cache=None, topk=None,
+                      workspace=None, order: int = DSA_ORDER_SCORE, total_q: Optional[int] = None):
+    """Fill a dsa_indexer_args from tensors (allocating topk / workspace with torch if absent).
+
+    Returns (args, keepalive) -- keep the second value alive while the call runs."""
+    total_q = q.shape[0] if total_q is None else total_q
+    H, D = q.shape[1], q.shape[2]
+    B = seq_lens.shape[0]
+    num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+    if k_out is None:
+        k_out = topk_limit
+    if topk is None:
+        topk = torch.empty((total_q, k_out), dtype=torch.int32, device=q.device)
+    a = dsa_indexer_args()
+    a.q_dtype, a.k_dtype = _dtype_code(q), _dtype_code(k_cache)
+    a.B, a.total_q, a.H, a.D = B, total_q, H, D
+    a.page_size, a.num_pages = page_size, num_pages
+    a.max_pages_per_seq, a.max_seq_len = block_tables.shape[1], int(max_seq_len)
+    a.q = _dev(q, "q")
+    a.q_scale = _dev(q_scale, "q_scale", torch.float32)
+    a.w = _dev(w, "w", torch.float32)
+    a.cu_q_lens = _dev(cu_q_lens, "cu_q_lens", torch.int32)
+    a.seq_lens = _dev(seq_lens, "seq_lens", torch.int32)
+    a.block_tables = _dev(block_tables, "block_tables", torch.int32)
+    a.k_cache = _dev(k_cache, "k_cache")
+    a.k_scale_cache = _dev(k_scale_cache, "k_scale_cache", torch.float32)
+    a.topk_limit, a.k_out, a.order = int(topk_limit), int(k_out), int(order)
+    a.topk = _dev(topk, "topk", torch.int32)
+    if workspace is None:
+        nbytes = dsa_indexer_workspace_size(a)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    a.workspace = _dev(workspace, "workspace", torch.uint8)
+    a.workspace_bytes = workspace.numel()
+    return a, (q, w, k_cache, cu_q_lens, seq_lens, block_tables, q_scale, k_scale_cache, topk, workspace)
+
+
+def dsa_indexer_workspace_size(args: dsa_indexer_args) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().dsa_indexer_workspace_size(ctypes.byref(args), ctypes.byref(n)), "dsa_indexer_workspace_size")
+    return int(n.value)
+
+
+def dsa_indexer(q, w, k_cache, cu_q_lens, seq_lens, block_tables, *, max_seq_len: int, topk_limit: int,
+                k_out: Optional[int] = None, q_scale=None, k_scale_cache=None, topk=None, workspace=None,
+                order: int = DSA_ORDER_SCORE, stream=None) -> torch.Tensor:
+    """Fused paged indexer for a varlen batch; returns topk [total_q, k_out] int32."""
+    a, keep = make_indexer_args(q, w, k_cache, cu_q_lens, seq_lens, block_tables, max_seq_len=max_seq_len,
+                                topk_limit=topk_limit, k_out=k_out, q_scale=q_scale,
+                                k_scale_cache=k_scale_cache, topk=topk, workspace=workspace, order=order)
+    _check(lib().dsa_indexer(ctypes.byref(a), _stream_ptr(stream)), "dsa_indexer")
+    return keep[8]
+
+
+def indexer_types_to_codes(indexer_types: Sequence) -> list:
+    """'full' / 'shared' (or the integer codes) -> dsa_layer_type codes; others -> -1."""
+    out = []
+    for t in indexer_types:
+        if t in ("full", DSA_LAYER_FULL):
+            out.append(DSA_LAYER_FULL)
+        elif t in ("shared", DSA_LAYER_SHARED):
+            out.append(DSA_LAYER_SHARED)
+        else:
+            out.append(-1)
+    return out
+
+
+def dsa_resolve_indexer_sources(indexer_types: Sequence, num_layers: Optional[int] = None) -> list:
+    """Source layer of every layer through the C ABI; ValueError like the reference flow
+    for a short list, an unknown type or a shared layer with no earlier full layer."""
+    codes = indexer_types_to_codes(indexer_types)
+    if num_layers is not None and len(codes) < num_layers:
+        raise ValueError("indexer_types shorter than the number of layers")
+    L = len(codes)
+    types = (ctypes.c_int32 * max(L, 1))(*codes)
+    src = (ctypes.c_int32 * max(L, 1))()
+    st = lib().dsa_resolve_indexer_sources(L, ctypes.cast(types, ctypes.c_void_p), ctypes.cast(src, ctypes.c_void_p))
+    if st == DSA_ERR_INVALID_ARGUMENT:
+        raise ValueError("invalid indexer_types: unknown type or shared layer without an earlier full layer")
+    _check(st, "dsa_resolve_indexer_sources")
+    return list(src[:L])
+
+
+def dsa_indexer_stack(indexer_types: Sequence, full_layer_args: Sequence, stream=None):
+    """Run an IndexShare stack.  full_layer_args[l] is a dsa_indexer_args (full layers)
+    or None (shared layers).  Returns (topk device pointers per layer, source layers)."""
+    codes = indexer_types_to_codes(indexer_types)
+    L = len(codes)
+    types = (ctypes.c_int32 * max(L, 1))(*codes)
+    arr = (ctypes.POINTER(dsa_indexer_args) * max(L, 1))()
+    for i, a in enumerate(full_layer_args):
+        arr[i] = ctypes.pointer(a) if a is not None else ctypes.POINTER(dsa_indexer_args)()
+    outs = (ctypes.c_void_p * max(L, 1))()
+    src = (ctypes.c_int32 * max(L, 1))()
+    st = lib().dsa_indexer_stack(L, ctypes.cast(types, ctypes.c_void_p), ctypes.cast(arr, ctypes.c_void_p),
+                                 ctypes.cast(outs, ctypes.c_void_p), ctypes.cast(src, ctypes.c_void_p),
+                                 _stream_ptr(stream))
+    _check(st, "dsa_indexer_stack")
+    return [outs[i] for i in range(L)], list(src[:L])
+
+
+def dsa_check_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status (DSA_OK, ...)."""
+    return int(lib().dsa_check_device_status(_stream_ptr(stream)))
+
+
+# ---- host helpers (GLM5 TensorCast adaptation design) -----------------------------
+
+def resolve_topk_limit(explicit=None, indexer=None, config=None, indexer_config=None) -> int:
+    """top-k width in the order of section "Sparse MLA 配置兼容": an explicit value, then
+    the indexer's own topk_limit, then topk_limit on the attention / indexer config, then
+    the GLM5-style index_topk; AttributeError("topk_limit") when none exists."""
+    if explicit is not None:
+        return int(explicit)
+    if indexer is not None and getattr(indexer, "topk_limit", None) is not None:
+        return int(indexer.topk_limit)
+    for cfg in (config, indexer_config):
+        if cfg is not None and getattr(cfg, "topk_limit", None) is not None:
+            return int(cfg.topk_limit)
+    for cfg in (config, indexer_config):
+        if cfg is not None and getattr(cfg, "index_topk", None) is not None:
+            return int(cfg.index_topk)
+    raise AttributeError("topk_limit")
+
+
+def extend_indexer_types_for_mtp(indexer_types: Sequence[str], num_mtp_layers: int) -> list:
+    """Append one 'full' per MTP block (an MTP block cannot consume the main stack's
+    top-k, section "GLM-5.2 IndexShare"); an empty list or zero MTP layers is unchanged."""
+    types = list(indexer_types)
+    if not types or num_mtp_layers <= 0:
+        return types
+    return types + ["full"] * int(num_mtp_layers)

@@ -1,0 +1,468 @@
+// api.cu -- the C ABI of include/dsa_indexer.h: argument validation, tensor-map
+// encoding, work-list construction and kernel launches.
+//
+// IndexShare (GLM5 TensorCast adaptation design, "GLM-5.2 IndexShare"): full layers
+// run the indexer; a shared layer runs nothing and forwards the nearest earlier full
+// layer's top-k buffer; a shared layer without an earlier full layer, or an unknown
+// type, is rejected before anything is launched.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <climits>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "dsa_indexer.h"
+#include "internal.h"
+
+namespace dsa {
+
+__device__ unsigned g_device_status;
+
+unsigned* device_status_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+  return static_cast<unsigned*>(p);
+}
+
+namespace {
+
+constexpr size_t kMaxSmem = 232448;          // opt-in dynamic shared memory per CTA on sm_100-class parts
+constexpr size_t kScoreChunkBudget = 64ull << 20;  // target bytes of fp32 scores kept per chunk (L2 resident)
+
+// ---------------------------------------------------------------- work list (paged path)
+__global__ void prep_items_kernel(const int32_t* cu_q_lens, const int32_t* seq_lens, int NQ, int KC, int R, int cap,
+                                  int n_chunks, int max_seq_len, int max_pages_per_seq, int page_size,
+                                  WorkItem* items, int* counts, unsigned* status) {
+  const int b = blockIdx.x;
+  const int cu0 = cu_q_lens[b], cu1 = cu_q_lens[b + 1];
+  const int q_len = cu1 - cu0;
+  const int L = seq_lens[b];
+  if (q_len <= 0) return;
+  if (L > max_seq_len || q_len > L || cu0 < 0 ||
+      static_cast<long long>(L) > static_cast<long long>(max_pages_per_seq) * page_size) {
+    if (threadIdx.x == 0) atomicOr(status, kStatusUncovered);
+    return;
+  }
+  for (int c = cu0 / R; c <= (cu1 - 1) / R && c < n_chunks; ++c) {
+    const int seg0 = max(cu0, c * R), seg1 = min(cu1, (c + 1) * R);
+    const int nqb = (seg1 - seg0 + NQ - 1) / NQ;
+    for (int j = threadIdx.x; j < nqb; j += blockDim.x) {
+      const int row0 = seg0 + j * NQ;
+      const int nrows = min(NQ, seg1 - row0);
+      const int pos0 = L - q_len + (row0 - cu0);
+      const int n_kt = (pos0 + nrows - 1 + kBlockM) / kBlockM;
+      const int n_it = KC > 0 ? (n_kt + KC - 1) / KC : 1;
+      const int slot = atomicAdd(&counts[c], n_it);
+      if (slot + n_it > cap) {
+        atomicOr(status, kStatusUncovered);
+        continue;
+      }
+      for (int k = 0; k < n_it; ++k) {
+        const int kt0 = KC > 0 ? k * KC : 0;
+        const int kt1 = KC > 0 ? min(n_kt, (k + 1) * KC) : n_kt;
+        WorkItem w;
+        w.row0 = row0;
+        w.pos0 = pos0;
+        w.kt = kt0 | (kt1 << 16);
+        w.bn = b | (nrows << 24);
+        items[static_cast<long long>(c) * cap + slot + k] = w;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- helpers
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_h(int H) { return H == 4 || H == 8 || H == 16 || H == 32 || H == 64 || H == 128; }
+
+dsa_status check_dtypes(int q_dtype, int k_dtype, int D, bool have_qs, bool have_ks) {
+  if ((q_dtype != DSA_BF16 && q_dtype != DSA_FP8_E4M3) || (k_dtype != DSA_BF16 && k_dtype != DSA_FP8_E4M3))
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (q_dtype != k_dtype) return DSA_ERR_UNSUPPORTED;
+  if (q_dtype == DSA_BF16) {
+    if (D != 64 && D != 128) return DSA_ERR_UNSUPPORTED;
+  } else {
+    if (D != 128) return DSA_ERR_UNSUPPORTED;
+    if (!have_qs || !have_ks) return DSA_ERR_INVALID_ARGUMENT;
+  }
+  return DSA_OK;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Row-major [rows, D] operand, 128-byte swizzled boxes of {128 bytes, box_rows}.
+bool make_map_2d(CUtensorMap* m, const void* base, bool fp8, int D, long long rows, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const int esz = fp8 ? 1 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Paged cache [num_pages, page_size, D], boxes of {128 bytes, page_size rows, 1 page}.
+bool make_map_paged(CUtensorMap* m, const void* base, bool fp8, int D, int page_size, int num_pages) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const int esz = fp8 ? 1 : 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(page_size),
+                        static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * esz, static_cast<cuuint64_t>(D) * esz * page_size};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(page_size), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Deepest key-tile ring that fits in shared memory (>= 2), or 0.
+int pick_stages(const ScoreArgs& a) {
+  for (int s = kMaxKStages; s >= 2; --s)
+    if (score_smem_bytes(a, s) <= kMaxSmem) return s;
+  return 0;
+}
+
+// Shared memory requested per CTA: at least half an SM's worth, so that no two score
+// CTAs (each holding all 512 TMEM columns) ever share an SM.
+size_t score_launch_smem(const ScoreArgs& a) {
+  return std::max<size_t>(score_smem_bytes(a, a.num_k_stages), 120 * 1024);
+}
+
+dsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+struct PagedPlan {
+  bool decode;
+  int NQ, N, KC, R, n_chunks, cap;
+  long long ld;
+  size_t off_counts, off_items, off_scores, total;
+};
+
+dsa_status plan_paged(const dsa_indexer_args* a, PagedPlan* p) {
+  if (!a) return DSA_ERR_INVALID_ARGUMENT;
+  if (a->B < 0 || a->total_q < 0 || a->H <= 0 || a->D <= 0 || a->page_size <= 0 || a->num_pages < 0 ||
+      a->max_pages_per_seq < 0 || a->max_seq_len < 0 || a->topk_limit < 1 || a->k_out < 1)
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (a->k_out > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (a->order != DSA_ORDER_SCORE && a->order != DSA_ORDER_INDEX) return DSA_ERR_INVALID_ARGUMENT;
+  if (!supported_h(a->H)) return DSA_ERR_UNSUPPORTED;
+  if (a->page_size != 16 && a->page_size != 32 && a->page_size != 64 && a->page_size != 128)
+    return DSA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(a->max_seq_len) > static_cast<long long>(a->max_pages_per_seq) * a->page_size)
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (a->max_seq_len >= (1 << 16) * kBlockM) return DSA_ERR_UNSUPPORTED;  // key-tile ids are 16-bit
+  dsa_status st = check_dtypes(a->q_dtype, a->k_dtype, a->D, a->q_scale != nullptr, a->k_scale_cache != nullptr);
+  if (st != DSA_OK) return st;
+  const int ns = std::max(num_sms(), 1);
+  p->decode = a->total_q <= a->B;
+  p->N = p->decode ? std::max(64, a->H) : 256;
+  p->NQ = p->N / a->H;
+  p->ld = (std::max(a->max_seq_len, 1) + 3) & ~3LL;
+  long long R = static_cast<long long>(kScoreChunkBudget / (static_cast<size_t>(p->ld) * 4));
+  R = std::max<long long>(R - R % p->NQ, p->NQ);
+  if (R >= a->total_q) R = std::max(a->total_q, 1);
+  p->R = static_cast<int>(R);
+  p->n_chunks = std::max(1, (a->total_q + p->R - 1) / p->R);
+  const long long qb_per_chunk = (p->R + p->NQ - 1) / p->NQ + std::min<long long>(a->B, p->R) + 1;
+  p->KC = qb_per_chunk < 2LL * ns ? 16 : 0;
+  const long long kt_max = (a->max_seq_len + kBlockM - 1) / kBlockM;
+  const long long per_qb = p->KC > 0 ? (kt_max + p->KC - 1) / p->KC : 1;
+  const long long cap = qb_per_chunk * std::max<long long>(per_qb, 1);
+  if (cap > INT_MAX / 2) return DSA_ERR_UNSUPPORTED;
+  p->cap = static_cast<int>(cap);
+  size_t off = 0;
+  p->off_counts = off;
+  off += ((static_cast<size_t>(p->n_chunks) * 4 + 255) / 256) * 256;
+  p->off_items = off;
+  off += ((static_cast<size_t>(p->n_chunks) * p->cap * sizeof(WorkItem) + 255) / 256) * 256;
+  p->off_scores = off;
+  off += static_cast<size_t>(p->R) * static_cast<size_t>(p->ld) * 4;
+  p->total = off;
+  return DSA_OK;
+}
+
+dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t st) {
+  if (a->total_q == 0 || a->B == 0) return DSA_OK;
+  unsigned* status = device_status_ptr();
+  if (!status) return DSA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+  int* counts = reinterpret_cast<int*>(ws + p.off_counts);
+  WorkItem* items = reinterpret_cast<WorkItem*>(ws + p.off_items);
+  float* scores = reinterpret_cast<float*>(ws + p.off_scores);
+  const bool fp8 = a->q_dtype == DSA_FP8_E4M3;
+
+  ScoreArgs s{};
+  s.paged = 1;
+  s.q_fp8 = fp8;
+  s.k_fp8 = a->k_dtype == DSA_FP8_E4M3;
+  s.H = a->H;
+  s.D = a->D;
+  s.NQ = p.NQ;
+  s.N = p.N;
+  s.page_size = a->page_size;
+  s.num_pages = a->num_pages;
+  s.max_pages_per_seq = a->max_pages_per_seq;
+  s.block_tables = a->block_tables;
+  s.total_rows = a->total_q;
+  s.w = a->w;
+  s.q_scale = a->q_scale;
+  s.k_scale = a->k_scale_cache;
+  s.scores = scores;
+  s.ld = p.ld;
+  s.status = status;
+  s.num_k_stages = pick_stages(s);
+  if (s.num_k_stages < 2) return DSA_ERR_UNSUPPORTED;
+
+  CUtensorMap tq, tk;
+  if (!make_map_2d(&tq, a->q, fp8, a->D, static_cast<long long>(a->total_q) * a->H, p.N)) return DSA_ERR_CUDA;
+  if (!make_map_paged(&tk, a->k_cache, s.k_fp8, a->D, a->page_size, std::max(a->num_pages, 1)))
+    return DSA_ERR_CUDA;
+
+  cudaError_t e = cudaMemsetAsync(counts, 0, static_cast<size_t>(p.n_chunks) * 4, st);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  prep_items_kernel<<<a->B, 128, 0, st>>>(a->cu_q_lens, a->seq_lens, p.NQ, p.KC, p.R, p.cap, p.n_chunks,
+                                          a->max_seq_len, a->max_pages_per_seq, a->page_size, items, counts,
+                                          status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return DSA_ERR_CUDA;
+  const int ns = std::max(num_sms(), 1);
+  const size_t smem = score_launch_smem(s);
+  for (int c = 0; c < p.n_chunks; ++c) {
+    s.items = items + static_cast<long long>(c) * p.cap;
+    s.n_items = counts + c;
+    s.items_cap = p.cap;
+    s.row_base = c * p.R;
+    if ((e = launch_score(s, &tq, &tk, ns, smem, st)) != cudaSuccess) return DSA_ERR_CUDA;
+    TopkArgs t{};
+    t.scores = scores;
+    t.ld = p.ld;
+    t.n_rows = std::min(p.R, a->total_q - c * p.R);
+    t.paged = 1;
+    t.row_base = c * p.R;
+    t.B = a->B;
+    t.cu_q_lens = a->cu_q_lens;
+    t.seq_lens = a->seq_lens;
+    t.max_n = p.ld;
+    t.topk_limit = a->topk_limit;
+    t.k_out = a->k_out;
+    t.order = a->order;
+    t.topk = a->topk;
+    if ((e = launch_topk(t, a->max_seq_len, st)) != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  return DSA_OK;
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+const char* dsa_status_string(int s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARGUMENT: return "DSA_ERR_INVALID_ARGUMENT";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_DEVICE_CHECK: return "DSA_ERR_DEVICE_CHECK";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+    default: return "DSA_ERR_UNKNOWN";
+  }
+}
+
+const char* dsa_version(void) { return "dsa_indexer sm_103a 0.1"; }
+
+int dsa_topk_width(int topk_limit, int64_t active_seq_len) {
+  long long w = std::min<long long>(topk_limit, active_seq_len);
+  return w > 0 ? static_cast<int>(w) : 0;
+}
+
+dsa_status dsa_indexer_scores(const void* q, int q_dtype, const float* q_scale, const void* k, int k_dtype,
+                              const float* k_scale, const float* w, int T, int S, int H, int D, int q_pos0,
+                              float* scores, int64_t ld_scores, dsa_stream_t stream) {
+  if (T < 0 || S < 0 || q_pos0 < 0 || H <= 0 || D <= 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (T == 0 || S == 0) return DSA_OK;
+  if (!q || !k || !w || !scores) return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(w) || !aligned16(scores) || (q_scale && !aligned16(q_scale)) ||
+      (k_scale && !aligned16(k_scale)))
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (ld_scores < S || (ld_scores & 3) != 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (!supported_h(H)) return DSA_ERR_UNSUPPORTED;
+  dsa_status st = check_dtypes(q_dtype, k_dtype, D, q_scale != nullptr, k_scale != nullptr);
+  if (st != DSA_OK) return st;
+  if (static_cast<long long>(T) * H > INT_MAX || static_cast<long long>(q_pos0) + T > INT_MAX)
+    return DSA_ERR_UNSUPPORTED;
+  if (S >= (1 << 16) * kBlockM) return DSA_ERR_UNSUPPORTED;
+  unsigned* status = device_status_ptr();
+  if (!status) return DSA_ERR_CUDA;
+  const bool fp8 = q_dtype == DSA_FP8_E4M3;
+
+  ScoreArgs a{};
+  a.paged = 0;
+  a.q_fp8 = fp8;
+  a.k_fp8 = fp8;
+  a.H = H;
+  a.D = D;
+  a.N = 256;
+  a.NQ = 256 / H;
+  a.T = T;
+  a.S = S;
+  a.q_pos0 = q_pos0;
+  a.n_dense_items = (T + a.NQ - 1) / a.NQ;
+  a.total_rows = T;
+  a.w = w;
+  a.q_scale = fp8 ? q_scale : nullptr;
+  a.k_scale = fp8 ? k_scale : nullptr;
+  a.scores = scores;
+  a.ld = ld_scores;
+  a.status = status;
+  a.num_k_stages = pick_stages(a);
+  if (a.num_k_stages < 2) return DSA_ERR_UNSUPPORTED;
+
+  CUtensorMap tq, tk;
+  if (!make_map_2d(&tq, q, fp8, D, static_cast<long long>(T) * H, a.N)) return DSA_ERR_CUDA;
+  if (!make_map_2d(&tk, k, fp8, D, S, kBlockM)) return DSA_ERR_CUDA;
+  const int grid = std::min(std::max(num_sms(), 1), a.n_dense_items);
+  return from_cuda(launch_score(a, &tq, &tk, grid, score_launch_smem(a), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_indexer_topk(const float* scores, int64_t ld_scores, int T, int S, int q_pos0, int topk_limit,
+                            int k_out, int order, int32_t* topk, dsa_stream_t stream) {
+  if (T < 0 || S < 0 || q_pos0 < 0 || topk_limit < 1 || k_out < 1) return DSA_ERR_INVALID_ARGUMENT;
+  if (order != DSA_ORDER_SCORE && order != DSA_ORDER_INDEX) return DSA_ERR_INVALID_ARGUMENT;
+  if (k_out > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!topk || (S > 0 && !scores)) return DSA_ERR_INVALID_ARGUMENT;
+  if (S > 0 && (!aligned16(scores) || ld_scores < S || (ld_scores & 3) != 0)) return DSA_ERR_INVALID_ARGUMENT;
+  TopkArgs t{};
+  t.scores = scores;
+  t.ld = ld_scores;
+  t.n_rows = T;
+  t.paged = 0;
+  t.S = S;
+  t.q_pos0 = q_pos0;
+  t.max_n = S;
+  t.topk_limit = topk_limit;
+  t.k_out = k_out;
+  t.order = order;
+  t.topk = topk;
+  const long long longest = std::min<long long>(S, static_cast<long long>(q_pos0) + T);
+  return from_cuda(launch_topk(t, static_cast<int>(std::max<long long>(longest, 1)),
+                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_indexer_workspace_size(const dsa_indexer_args* args, size_t* bytes) {
+  if (!bytes) return DSA_ERR_INVALID_ARGUMENT;
+  PagedPlan p;
+  dsa_status st = plan_paged(args, &p);
+  if (st != DSA_OK) return st;
+  *bytes = p.total;
+  return DSA_OK;
+}
+
+static dsa_status validate_paged_pointers(const dsa_indexer_args* a, const PagedPlan& p) {
+  if (a->total_q == 0 || a->B == 0) return DSA_OK;
+  if (!a->q || !a->w || !a->cu_q_lens || !a->seq_lens || !a->block_tables || !a->k_cache || !a->topk)
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(a->q) || !aligned16(a->w) || !aligned16(a->k_cache) || (a->q_scale && !aligned16(a->q_scale)) ||
+      (a->k_scale_cache && !aligned16(a->k_scale_cache)))
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (a->num_pages < 1 || a->max_pages_per_seq < 1) return DSA_ERR_INVALID_ARGUMENT;
+  if (!a->workspace || a->workspace_bytes < p.total || !aligned16(a->workspace)) return DSA_ERR_WORKSPACE;
+  return DSA_OK;
+}
+
+dsa_status dsa_indexer(const dsa_indexer_args* args, dsa_stream_t stream) {
+  PagedPlan p;
+  dsa_status st = plan_paged(args, &p);
+  if (st != DSA_OK) return st;
+  if ((st = validate_paged_pointers(args, p)) != DSA_OK) return st;
+  return run_paged(args, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dsa_status dsa_resolve_indexer_sources(int L, const int32_t* types, int32_t* src) {
+  if (L < 0 || (L > 0 && (!types || !src))) return DSA_ERR_INVALID_ARGUMENT;
+  int last_full = -1;
+  for (int l = 0; l < L; ++l) {
+    if (types[l] == DSA_LAYER_FULL) {
+      last_full = l;
+      src[l] = l;
+    } else if (types[l] == DSA_LAYER_SHARED) {
+      if (last_full < 0) return DSA_ERR_INVALID_ARGUMENT;
+      src[l] = last_full;
+    } else {
+      return DSA_ERR_INVALID_ARGUMENT;
+    }
+  }
+  return DSA_OK;
+}
+
+dsa_status dsa_indexer_stack(int L, const int32_t* types, const dsa_indexer_args* const* full_args,
+                             int32_t** topk_out, int32_t* src_out, dsa_stream_t stream) {
+  if (L < 0 || (L > 0 && (!types || !full_args || !topk_out))) return DSA_ERR_INVALID_ARGUMENT;
+  int32_t* src = static_cast<int32_t*>(std::malloc(sizeof(int32_t) * static_cast<size_t>(std::max(L, 1))));
+  if (!src) return DSA_ERR_INVALID_ARGUMENT;
+  dsa_status st = dsa_resolve_indexer_sources(L, types, src);
+  // validate every full layer before the first launch
+  for (int l = 0; st == DSA_OK && l < L; ++l) {
+    if (src[l] == l) {
+      if (!full_args[l]) { st = DSA_ERR_INVALID_ARGUMENT; break; }
+      PagedPlan p;
+      st = plan_paged(full_args[l], &p);
+      if (st == DSA_OK) st = validate_paged_pointers(full_args[l], p);
+    } else if (full_args[l] != nullptr) {
+      st = DSA_ERR_INVALID_ARGUMENT;  // a shared layer owns no indexer inputs or cache
+    }
+  }
+  for (int l = 0; st == DSA_OK && l < L; ++l) {
+    if (src[l] == l) {
+      st = dsa_indexer(full_args[l], stream);
+      topk_out[l] = full_args[l]->topk;
+    } else {
+      topk_out[l] = topk_out[src[l]];
+    }
+  }
+  if (st == DSA_OK && src_out)
+    for (int l = 0; l < L; ++l) src_out[l] = src[l];
+  std::free(src);
+  return st;
+}
+
+dsa_status dsa_check_device_status(dsa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof v) != cudaSuccess) return DSA_ERR_CUDA;
+  if (v == 0) return DSA_OK;
+  if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess) return DSA_ERR_CUDA;
+  if (v & (kStatusSmemAlign | kStatusTmemAlloc)) return DSA_ERR_CUDA;
+  if (v & kStatusTimeout) return DSA_ERR_TIMEOUT;
+  return DSA_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"

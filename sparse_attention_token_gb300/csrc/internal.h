@@ -1,0 +1,83 @@
+// internal.h -- declarations shared by the translation units of the library.
+// Nothing here is part of the public C ABI (include/dsa_indexer.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dsa {
+
+// Bits of the device status word (library-owned __device__ variable).
+enum : unsigned {
+  kStatusBadPage = 1u,       // a block-table entry outside [0, num_pages)
+  kStatusUncovered = 2u,     // a key position the block table does not cover / bad lengths
+  kStatusTimeout = 4u,       // a bounded mbarrier wait gave up
+  kStatusSmemAlign = 8u,     // dynamic shared memory not 1024-byte aligned
+  kStatusTmemAlloc = 16u,    // TMEM allocation returned an unusable address
+};
+
+constexpr int kBlockM = 128;             // keys per MMA tile (TMEM lanes)
+constexpr int kScoreThreads = 320;       // warp 0 TMA, warp 1 MMA/TMEM, warps 2..9 epilogue
+constexpr int kMaxKStages = 8;
+constexpr int kTmemCols = 512;           // two accumulators at column 0 and 256
+constexpr int kMaxN = 256;               // MMA N (queries x heads per tile)
+
+// One unit of scoring work: NQ (or fewer) consecutive query rows of one
+// sequence against key tiles [kt0, kt1).
+struct WorkItem {
+  int row0;      // first query row (global row of q / w / topk)
+  int pos0;      // position of row0 in its sequence
+  int kt;        // kt0 | kt1 << 16
+  int bn;        // b | nrows << 24
+};
+
+struct ScoreArgs {
+  int paged;          // 0: dense k[S, D]; 1: paged k_cache[num_pages, page_size, D]
+  int q_fp8, k_fp8;   // element type of q / keys (1 = e4m3, 0 = bf16)
+  int H, D, NQ, N;    // N = NQ * H
+  int num_k_stages;
+  // dense single sequence
+  int T, S, q_pos0, n_dense_items;
+  // paged varlen
+  int page_size, num_pages, max_pages_per_seq;
+  const int32_t* block_tables;
+  const WorkItem* items;
+  const int* n_items;
+  int items_cap;      // capacity of the items segment (clamps *n_items)
+  int row_base;       // global query row stored in scores row 0
+  int total_rows;     // rows of q / w (bounds for cp.async of w and q_scale)
+  // common
+  const float* w;
+  const float* q_scale;   // [rows, H] or null
+  const float* k_scale;   // dense [S] / paged [num_pages * page_size] or null
+  float* scores;
+  long long ld;
+  unsigned* status;   // device status word
+};
+
+struct TopkArgs {
+  const float* scores;
+  long long ld;
+  int n_rows;          // rows handled by this launch (one CTA each)
+  // dense: row t -> n = clamp(q_pos0 + t + 1, 0, S); output row t
+  int paged;
+  int S, q_pos0;
+  // paged: CTA i handles global row row_base + i
+  int row_base, B;
+  const int32_t* cu_q_lens;
+  const int32_t* seq_lens;
+  long long max_n;     // no row reads more than this many entries
+  int topk_limit, k_out, order;
+  int32_t* topk;
+};
+
+// Host launchers (return a cudaError_t).
+cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
+                         int grid, size_t smem_bytes, cudaStream_t st);
+size_t score_smem_bytes(const ScoreArgs& a, int num_k_stages);
+cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st);
+unsigned* device_status_ptr();   // address of the status word on the current device
+
+}  // namespace dsa

@@ -1,0 +1,518 @@
+// score_tc.cu -- DSA indexer scoring on the sm_103a tensor cores.
+//
+// Computes, for a block of query rows and a range of 128-key tiles,
+//     score[t, s] = ks[s] * sum_h w'[t, h] * max(sum_d q[t, h, d] * k[s, d], 0),   w' = w * q_scale
+// (GLM5 TensorCast adaptation design, "性能模型设计" buckets 6 and 7: the q-k index
+// score MMA, then head weight multiply, head reduce and the FP8 relu / q-scale /
+// k-scale shaping).  The [T, H, S] intermediate never leaves the SM: it lives in
+// TMEM and is reduced over heads by the epilogue warps.
+//
+// Tile orientation: MMA M = 128 keys (one TMEM lane per key), N = queries x heads
+// (each query's H heads are H consecutive TMEM columns), K = D.  A TMEM lane then
+// holds every head of one (key, query) pair, so the head reduction is in-thread.
+//
+// Warp roles (320 threads, one CTA per SM, persistent over work items):
+//   warp 0      TMA producer: q tile (N x D) per item into a 2-deep ring, key tiles
+//               (128 x D, dense or gathered page by page through block_tables) into
+//               an nK-deep ring, per-item w / q_scale and per-tile k_scale by cp.async.
+//   warp 1      TMEM allocator; lane 0 issues tcgen05.mma into two 256-column fp32
+//               accumulators (double buffered) and commits to mbarriers.
+//   warps 2..9  epilogue: tcgen05.ld, ReLU, head-weighted sum, k scale, causal mask,
+//               coalesced fp32 stores.  Prefill tiles (N = 256) are split by columns
+//               between two warpgroups; decode tiles (N = max(64, H)) alternate
+//               between the warpgroups tile by tile.
+// Every wait is bounded; on a timeout the kernel records kStatusTimeout, all roles
+// leave their loops, in-flight copies and MMAs are drained (bounded) and TMEM freed.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dsa {
+
+namespace {
+
+struct SmemPlan {
+  uint32_t q[2];
+  uint32_t k[kMaxKStages];
+  uint32_t wbuf, qsbuf, ksbuf, bars, misc, total;
+};
+
+__host__ __device__ inline SmemPlan plan_smem(int N, int D, int q_fp8, int k_fp8, int nK) {
+  SmemPlan p{};
+  uint32_t off = 0;
+  const uint32_t qb = static_cast<uint32_t>(N) * D * (q_fp8 ? 1 : 2);
+  const uint32_t kb = static_cast<uint32_t>(kBlockM) * D * (k_fp8 ? 1 : 2);
+  for (int i = 0; i < 2; ++i) { p.q[i] = off; off += qb; }
+  for (int i = 0; i < kMaxKStages; ++i) { p.k[i] = off; if (i < nK) off += kb; }
+  p.wbuf = off;  off += 2u * N * 4u;
+  p.qsbuf = off; if (q_fp8) off += 2u * N * 4u;
+  p.ksbuf = off; if (k_fp8) off += static_cast<uint32_t>(nK) * kBlockM * 4u;
+  p.bars = off;  off += 32u * 8u;
+  p.misc = off;  off += 16u;
+  p.total = off;
+  return p;
+}
+
+// Barrier slots inside the bars region.
+enum {
+  kBarQFull = 0, kBarQEmpty = 2, kBarTFull = 4, kBarTEmpty = 6, kBarFold = 8,  // fold: 4 slots
+  kBarDone = 12, kBarKFull = 13, kBarKEmpty = 13 + kMaxKStages
+};
+
+struct ItemInfo {
+  int row0, pos0, kt0, kt1, b, nrows;
+};
+
+template <int NQ>
+__device__ __forceinline__ bool fetch_item(const ScoreArgs& a, int n_items, int it, ItemInfo& I) {
+  const long long G = gridDim.x, c = blockIdx.x;
+  const long long idx = static_cast<long long>(it) * G + ((it & 1) ? (G - 1 - c) : c);
+  if (idx >= n_items) return false;
+  if (!a.paged) {
+    // query blocks in decreasing order of causal work
+    const int qb = a.n_dense_items - 1 - static_cast<int>(idx);
+    I.row0 = qb * NQ;
+    I.nrows = min(NQ, a.T - I.row0);
+    I.pos0 = a.q_pos0 + I.row0;
+    I.b = 0;
+    const int last = min(I.pos0 + I.nrows - 1, a.S - 1);
+    I.kt0 = 0;
+    I.kt1 = (last + kBlockM) / kBlockM;
+  } else {
+    const WorkItem w = a.items[idx];
+    I.row0 = w.row0;
+    I.pos0 = w.pos0;
+    I.kt0 = w.kt & 0xFFFF;
+    I.kt1 = (w.kt >> 16) & 0xFFFF;
+    I.b = w.bn & 0xFFFFFF;
+    I.nrows = (w.bn >> 24) & 0xFF;
+  }
+  return true;
+}
+
+template <int H, bool DECODE>
+struct Cfg {
+  static constexpr int N = DECODE ? (H >= 64 ? H : 64) : 256;
+  static constexpr int NQ = N / H;
+  static constexpr int NCOLS = DECODE ? N : N / 2;  // columns one epilogue thread reduces
+  static constexpr int QH = NCOLS / H;               // queries in those columns
+  static constexpr int EPI_T_ARRIVALS = DECODE ? 4 : 8;
+};
+
+// ------------------------------------------------------------------ producer (warp 0)
+template <int H, bool DECODE>
+__device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensorMap* tmap_q,
+                                              const CUtensorMap* tmap_k, uint8_t* smem, const SmemPlan& P,
+                                              uint64_t* bars, volatile int* abort, int n_items) {
+  using C = Cfg<H, DECODE>;
+  constexpr int N = C::N;
+  const int lane = threadIdx.x & 31;
+  const int nK = a.num_k_stages;
+  const int q_esz = a.q_fp8 ? 1 : 2, k_esz = a.k_fp8 ? 1 : 2;
+  const int n_atoms_q = a.D * q_esz / 128, n_atoms_k = a.D * k_esz / 128;
+  const int box_q = 128 / q_esz, box_k = 128 / k_esz;
+  const uint32_t q_bytes = static_cast<uint32_t>(N) * a.D * q_esz;
+  float* wbuf = reinterpret_cast<float*>(smem + P.wbuf);
+  float* qsbuf = reinterpret_cast<float*>(smem + P.qsbuf);
+  float* ksbuf = reinterpret_cast<float*>(smem + P.ksbuf);
+  const int PS = a.page_size;
+  const int ppt = a.paged ? kBlockM / PS : 1;
+  const uint32_t page_bytes = static_cast<uint32_t>(PS) * a.D * k_esz;
+
+  uint32_t nq = 0, nk = 0;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    ItemInfo I;
+    if (!fetch_item<C::NQ>(a, n_items, it, I)) break;
+    // ---- q tile, w and q_scale of this item
+    {
+      const int s = nq & 1;
+      int good = 1;
+      if (lane == 0) good = ptx::mbar_wait(&bars[kBarQEmpty + s], ((nq >> 1) & 1) ^ 1, abort, a.status, kStatusTimeout);
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (!good) { ok = false; break; }
+      const long long base = static_cast<long long>(I.row0) * H;
+      const long long lim = static_cast<long long>(a.total_rows) * H;
+      for (int c = lane; c < N / 4; c += 32) {
+        const long long e = base + 4ll * c;
+        const bool v = e + 4 <= lim;
+        ptx::cp_async_16(wbuf + s * N + 4 * c, v ? static_cast<const void*>(a.w + e) : static_cast<const void*>(a.w),
+                         v ? 16u : 0u);
+        if (a.q_fp8)
+          ptx::cp_async_16(qsbuf + s * N + 4 * c,
+                           v ? static_cast<const void*>(a.q_scale + e) : static_cast<const void*>(a.q_scale),
+                           v ? 16u : 0u);
+      }
+      ptx::cp_async_mbar_arrive_noinc(&bars[kBarQFull + s]);
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(&bars[kBarQFull + s], q_bytes);
+        for (int at = 0; at < n_atoms_q; ++at)
+          ptx::tma_load_2d(smem + P.q[s] + at * N * 128, tmap_q, &bars[kBarQFull + s], at * box_q, I.row0 * H);
+      }
+      ++nq;
+    }
+    // ---- key tiles
+    const int32_t* bt_row = a.paged ? a.block_tables + static_cast<long long>(I.b) * a.max_pages_per_seq : nullptr;
+    int win0 = -(1 << 30);
+    int pg_win = -1;
+    const int pos_last = I.pos0 + I.nrows - 1;
+    for (int kt = I.kt0; kt < I.kt1; ++kt) {
+      const int s = nk % nK;
+      int good = 1;
+      if (lane == 0) good = ptx::mbar_wait(&bars[kBarKEmpty + s], ((nk / nK) & 1) ^ 1, abort, a.status, kStatusTimeout);
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (!good) { ok = false; break; }
+      uint64_t* full = &bars[kBarKFull + s];
+      uint8_t* dst = smem + P.k[s];
+      if (!a.paged) {
+        if (a.k_fp8) {
+          const long long e = static_cast<long long>(kt) * kBlockM + 4 * lane;
+          float* d4 = ksbuf + s * kBlockM + 4 * lane;
+          if (e + 4 <= a.S) {
+            ptx::cp_async_16(d4, a.k_scale + e, 16u);
+          } else {
+            for (int j = 0; j < 4; ++j) {
+              const bool v = e + j < a.S;
+              ptx::cp_async_4(d4 + j, v ? a.k_scale + e + j : a.k_scale, v ? 4u : 0u);
+            }
+          }
+          ptx::cp_async_mbar_arrive_noinc(full);
+        }
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(full, static_cast<uint32_t>(kBlockM) * a.D * k_esz);
+          for (int at = 0; at < n_atoms_k; ++at)
+            ptx::tma_load_2d(dst + at * kBlockM * 128, tmap_k, full, at * box_k, kt * kBlockM);
+        }
+      } else {
+        const int lp0 = kt * ppt;
+        if (lp0 < win0 || lp0 + ppt > win0 + 32) {
+          win0 = lp0;
+          const int lp = win0 + lane;
+          pg_win = lp < a.max_pages_per_seq ? __ldg(bt_row + lp) : -1;
+        }
+        // page j of this tile is handled by lane j
+        int phys = -1;
+        bool valid = false;
+        {
+          const int j = lane;
+          const int src_lane = (lp0 - win0 + (j < ppt ? j : 0)) & 31;
+          const int pg = __shfl_sync(0xffffffffu, pg_win, src_lane);
+          const bool needed = j < ppt && static_cast<long long>(lp0 + j) * PS <= pos_last;
+          valid = needed && pg >= 0 && pg < a.num_pages;
+          if (needed && !valid) atomicOr(a.status, kStatusBadPage);
+          phys = valid ? pg : -1;
+        }
+        const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+        if (a.k_fp8) {
+          // lane l copies scale floats [4l, 4l + 4) of the tile
+          const int j = (4 * lane) / PS;
+          const int pj = __shfl_sync(0xffffffffu, phys, j);
+          const bool v = (vmask >> j) & 1u;
+          const float* src = v ? a.k_scale + static_cast<long long>(pj) * PS + (4 * lane) % PS : a.k_scale;
+          ptx::cp_async_16(ksbuf + s * kBlockM + 4 * lane, src, v ? 16u : 0u);
+          ptx::cp_async_mbar_arrive_noinc(full);
+        }
+        int pj_all[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pj_all[j] = __shfl_sync(0xffffffffu, phys, j);
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(vmask)) * page_bytes);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (j < ppt && ((vmask >> j) & 1u)) {
+              for (int at = 0; at < n_atoms_k; ++at)
+                ptx::tma_load_3d(dst + at * kBlockM * 128 + j * PS * 128, tmap_k, full, at * box_k, 0, pj_all[j]);
+            }
+          }
+        }
+      }
+      ++nk;
+    }
+  }
+  // Drain: wait (bounded) until the copies this warp issued into the rings have
+  // landed, so none can write shared memory after the CTA exits.
+  if (lane == 0) {
+    const int kq = nq < 2 ? static_cast<int>(nq) : 2;
+    for (int i = 1; i <= kq; ++i) {
+      const uint32_t u = nq - i;
+      ptx::mbar_wait_drain(&bars[kBarQFull + (u & 1)], (u >> 1) & 1, a.status, kStatusTimeout, 200000000ull);
+    }
+    const int kk = nk < static_cast<uint32_t>(nK) ? static_cast<int>(nk) : nK;
+    for (int i = 1; i <= kk; ++i) {
+      const uint32_t u = nk - i;
+      ptx::mbar_wait_drain(&bars[kBarKFull + (u % nK)], (u / nK) & 1, a.status, kStatusTimeout, 200000000ull);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer (warp 1, lane 0)
+template <int H, bool DECODE>
+__device__ __forceinline__ void mma_role(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P, uint64_t* bars,
+                                         volatile int* abort, int n_items, uint32_t tmem_base) {
+  using C = Cfg<H, DECODE>;
+  constexpr int N = C::N;
+  const int nK = a.num_k_stages;
+  const bool f8 = a.k_fp8 != 0;
+  const uint32_t idesc = ptx::idesc_f32acc(kBlockM, N, !f8);
+  const int esz = f8 ? 1 : 2;
+  const int nsteps = a.D * esz / 32;  // 32 bytes of K per MMA (16 bf16 or 32 e4m3)
+  const uint32_t sbase = ptx::smem_u32(smem);
+  uint32_t nq = 0, nk = 0, nt = 0;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    ItemInfo I;
+    if (!fetch_item<C::NQ>(a, n_items, it, I)) break;
+    const int sq = nq & 1;
+    if (!ptx::mbar_wait(&bars[kBarQFull + sq], (nq >> 1) & 1, abort, a.status, kStatusTimeout)) break;
+    const uint32_t q_addr = sbase + P.q[sq];
+    for (int kt = I.kt0; kt < I.kt1; ++kt) {
+      const int sk = nk % nK;
+      const int acc = nt & 1;
+      if (!ptx::mbar_wait(&bars[kBarKFull + sk], (nk / nK) & 1, abort, a.status, kStatusTimeout) ||
+          !ptx::mbar_wait(&bars[kBarTEmpty + acc], ((nt >> 1) & 1) ^ 1, abort, a.status, kStatusTimeout)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
+      const uint32_t k_addr = sbase + P.k[sk];
+      for (int j = 0; j < nsteps; ++j) {
+        const uint32_t a_addr = k_addr + (j >> 2) * (kBlockM * 128) + (j & 3) * 32;
+        const uint32_t b_addr = q_addr + (j >> 2) * (N * 128) + (j & 3) * 32;
+        const uint64_t ad = ptx::sw128_kmajor_desc(a_addr);
+        const uint64_t bd = ptx::sw128_kmajor_desc(b_addr);
+        if (f8) ptx::mma_f8(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
+        else ptx::mma_bf16(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit(&bars[kBarKEmpty + sk]);
+      ptx::mma_commit(&bars[kBarTFull + acc]);
+      ++nk;
+      ++nt;
+    }
+    if (!ok) break;
+    ptx::mma_commit(&bars[kBarQEmpty + sq]);
+    ++nq;
+  }
+  // every MMA issued above has finished once this commit arrives
+  ptx::mma_commit(&bars[kBarDone]);
+  ptx::mbar_wait_drain(&bars[kBarDone], 0, a.status, kStatusTimeout, 200000000ull);
+}
+
+// Every lane waits (each observes the barrier itself); the outcome is made uniform
+// across the warp so that .sync.aligned TMEM loads never run on a partial warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* status) {
+  const bool ok = ptx::mbar_wait(bar, parity, abort, status, kStatusTimeout);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// ------------------------------------------------------------------ epilogue (warps 2..9)
+template <int H, bool DECODE>
+__device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P,
+                                              uint64_t* bars, volatile int* abort, int n_items,
+                                              uint32_t tmem_base) {
+  using C = Cfg<H, DECODE>;
+  constexpr int N = C::N;
+  constexpr int NCOLS = C::NCOLS;
+  constexpr int QH = C::QH;
+  constexpr int NCH = NCOLS / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = (warp - 2) >> 2;
+  const int quarter = warp & 3;            // TMEM lane quarter this warp may access
+  const int m = quarter * 32 + lane;       // key row of the tile
+  const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+  const int col0 = DECODE ? 0 : half * NCOLS;
+  const int q0 = col0 / H;
+  const int nK = a.num_k_stages;
+  float* wbuf = reinterpret_cast<float*>(smem + P.wbuf);
+  const float* qsbuf = reinterpret_cast<const float*>(smem + P.qsbuf);
+  const float* ksbuf = reinterpret_cast<const float*>(smem + P.ksbuf);
+  const int fold_t = DECODE ? static_cast<int>(threadIdx.x) - 64 : static_cast<int>(threadIdx.x) - 64 - half * 128;
+
+  uint32_t nq = 0, nk = 0, nt = 0;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    ItemInfo I;
+    if (!fetch_item<C::NQ>(a, n_items, it, I)) break;
+    const int sq = nq & 1;
+    if (!warp_wait(&bars[kBarQFull + sq], (nq >> 1) & 1, abort, a.status)) break;
+    float* wq = wbuf + sq * N;
+    if (a.q_fp8) {
+      // fold the q scale into w once per item (in place, each thread one column)
+      const int c = DECODE ? fold_t : col0 + fold_t;
+      if (!DECODE || fold_t < N) wq[c] *= qsbuf[sq * N + c];
+      uint64_t* fb = &bars[kBarFold + sq * 2 + (DECODE ? 0 : half)];
+      ptx::mbar_arrive(fb);
+      if (!warp_wait(fb, (nq >> 1) & 1, abort, a.status)) break;
+    }
+    for (int kt = I.kt0; kt < I.kt1; ++kt) {
+      const int sk = nk % nK;
+      const int acc = nt & 1;
+      const bool mine = DECODE ? (acc == half) : true;
+      if (mine) {
+        if (a.k_fp8 && !warp_wait(&bars[kBarKFull + sk], (nk / nK) & 1, abort, a.status)) {
+          ok = false;
+          break;
+        }
+        if (!warp_wait(&bars[kBarTFull + acc], (nt >> 1) & 1, abort, a.status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        float accq[QH];
+#pragma unroll
+        for (int j = 0; j < QH; ++j) accq[j] = 0.f;
+        const uint32_t tcol = tmem_base + lane_addr + static_cast<uint32_t>(acc * 256 + col0);
+        uint32_t xa[32], xb[32];
+        ptx::tmem_ld_32x32b_x32(tcol, xa);
+        ptx::tmem_ld_wait_regs(xa);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          if (c + 1 < NCH) ptx::tmem_ld_32x32b_x32(tcol + 32 * (c + 1), xb);
+          const float4* w4 = reinterpret_cast<const float4*>(wq + col0 + 32 * c);
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 wv = w4[i4];
+            const int cc = 32 * c + 4 * i4;
+            accq[(cc + 0) / H] = fmaf(wv.x, fmaxf(__uint_as_float(xa[4 * i4 + 0]), 0.f), accq[(cc + 0) / H]);
+            accq[(cc + 1) / H] = fmaf(wv.y, fmaxf(__uint_as_float(xa[4 * i4 + 1]), 0.f), accq[(cc + 1) / H]);
+            accq[(cc + 2) / H] = fmaf(wv.z, fmaxf(__uint_as_float(xa[4 * i4 + 2]), 0.f), accq[(cc + 2) / H]);
+            accq[(cc + 3) / H] = fmaf(wv.w, fmaxf(__uint_as_float(xa[4 * i4 + 3]), 0.f), accq[(cc + 3) / H]);
+          }
+          if (c + 1 < NCH) {
+            ptx::tmem_ld_wait_regs(xb);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) xa[i] = xb[i];
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars[kBarTEmpty + acc]);
+        float ks = 1.f;
+        if (a.k_fp8) {
+          ks = ksbuf[sk * kBlockM + m];
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&bars[kBarKEmpty + sk]);
+        }
+        const int s = kt * kBlockM + m;
+        const bool key_ok = a.paged || s < a.S;
+#pragma unroll
+        for (int j = 0; j < QH; ++j) {
+          const int qi = q0 + j;
+          if (qi < I.nrows && key_ok && s <= I.pos0 + qi) {
+            float* dst = a.scores + static_cast<long long>(I.row0 + qi - a.row_base) * a.ld + s;
+            *dst = accq[j] * ks;
+          }
+        }
+      }
+      ++nk;
+      ++nt;
+    }
+    if (!ok) break;
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&bars[kBarQEmpty + sq]);
+    ++nq;
+  }
+}
+
+template <int H, bool DECODE>
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                 const ScoreArgs a) {
+  using C = Cfg<H, DECODE>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((ptx::smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusSmemAlign);
+    return;
+  }
+  const SmemPlan P = plan_smem(C::N, a.D, a.q_fp8, a.k_fp8, a.num_k_stages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + P.misc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + P.misc + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&bars[kBarQFull + s], 1 + 32);
+      ptx::mbar_init(&bars[kBarQEmpty + s], 1 + 8);
+      ptx::mbar_init(&bars[kBarTFull + s], 1);
+      ptx::mbar_init(&bars[kBarTEmpty + s], C::EPI_T_ARRIVALS);
+      ptx::mbar_init(&bars[kBarFold + 2 * s + 0], DECODE ? 256 : 128);
+      ptx::mbar_init(&bars[kBarFold + 2 * s + 1], 128);
+    }
+    ptx::mbar_init(&bars[kBarDone], 1);
+    for (int s = 0; s < a.num_k_stages; ++s) {
+      ptx::mbar_init(&bars[kBarKFull + s], 1 + (a.k_fp8 ? 32 : 0));
+      ptx::mbar_init(&bars[kBarKEmpty + s], 1 + (a.k_fp8 ? C::EPI_T_ARRIVALS : 0));
+    }
+    *abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_holder, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmap_q);
+    ptx::prefetch_tmap(&tmap_k);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int n_items = a.paged ? min(*a.n_items, a.items_cap) : a.n_dense_items;
+
+  if ((tmem_base & 0xFFFFu) != 0) {
+    // the two accumulators assume the allocation starts at column 0
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusTmemAlloc);
+  } else if (warp == 0) {
+    producer_role<H, DECODE>(a, &tmap_q, &tmap_k, smem, P, bars, abort, n_items);
+  } else if (warp == 1) {
+    if (lane == 0) mma_role<H, DECODE>(a, smem, P, bars, abort, n_items, tmem_base);
+    __syncwarp();
+  } else {
+    epilogue_role<H, DECODE>(a, smem, P, bars, abort, n_items, tmem_base);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int H, bool DECODE>
+cudaError_t launch_t(const ScoreArgs& a, const CUtensorMap* tq, const CUtensorMap* tk, int grid, size_t smem,
+                     cudaStream_t st) {
+  auto kern = score_kernel<H, DECODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kScoreThreads, smem, st>>>(*tq, *tk, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t score_smem_bytes(const ScoreArgs& a, int num_k_stages) {
+  return plan_smem(a.N, a.D, a.q_fp8, a.k_fp8, num_k_stages).total;
+}
+
+cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k, int grid,
+                         size_t smem_bytes, cudaStream_t st) {
+  const bool dec = a.N != 256;
+#define DSA_CASE(HH)                                                                        \
+  case HH:                                                                                  \
+    return dec ? launch_t<HH, true>(a, tmap_q, tmap_k, grid, smem_bytes, st)               \
+               : launch_t<HH, false>(a, tmap_q, tmap_k, grid, smem_bytes, st);
+  switch (a.H) {
+    DSA_CASE(4)
+    DSA_CASE(8)
+    DSA_CASE(16)
+    DSA_CASE(32)
+    DSA_CASE(64)
+    DSA_CASE(128)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef DSA_CASE
+}
+
+}  // namespace dsa

@@ -1,0 +1,185 @@
+"""The C ABI boundary without a GPU: the library loads, exports every function
+include/dsa_indexer.h declares, validates arguments before any launch, and the
+host-only IndexShare logic and helpers follow the GLM5 TensorCast adaptation
+design ("Sparse MLA 配置兼容", "GLM-5.2 IndexShare")."""
+import ctypes
+import os
+import re
+import types as _types
+
+import pytest
+
+import oracle
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa_indexer.h")
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    import __graft_entry__ as g
+    g.build()
+    import sparse_attention_token_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\**\s+\**(dsa_[a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["dsa_indexer_scores", "dsa_indexer_topk", "dsa_indexer", "dsa_indexer_workspace_size",
+              "dsa_indexer_stack", "dsa_resolve_indexer_sources", "dsa_check_device_status",
+              "dsa_status_string", "dsa_topk_width", "dsa_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(dsa):
+    L = ctypes.CDLL(dsa.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(dsa):
+    assert dsa.dsa_status_string(0) == "DSA_OK"
+    assert dsa.dsa_status_string(6) == "DSA_ERR_WORKSPACE"
+    assert dsa.dsa_status_string(99) == "DSA_ERR_UNKNOWN"
+    assert "sm_103a" in dsa.dsa_version()
+
+
+@pytest.mark.parametrize("limit,n,exp", [(2048, 100, 100), (2048, 5000, 2048), (64, 0, 0), (64, -3, 0)])
+def test_topk_width(dsa, limit, n, exp):
+    assert dsa.dsa_topk_width(limit, n) == exp
+
+
+def test_scores_validation_happens_before_any_launch(dsa):
+    L = dsa.lib()
+    fake = 1 << 20  # never dereferenced: every call below fails validation first
+    ok = lambda *a: L.dsa_indexer_scores(*a)
+    base = dict(q=fake, qd=0, qs=None, k=fake, kd=0, ks=None, w=fake, T=4, S=8, H=64, D=128, p0=4,
+                sc=fake, ld=8, st=None)
+
+    def call(**kw):
+        a = {**base, **kw}
+        return ok(a["q"], a["qd"], a["qs"], a["k"], a["kd"], a["ks"], a["w"], a["T"], a["S"], a["H"], a["D"],
+                  a["p0"], a["sc"], a["ld"], a["st"])
+
+    assert call(q=None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert call(q=fake + 4) == dsa.DSA_ERR_INVALID_ARGUMENT           # misaligned
+    assert call(ld=6) == dsa.DSA_ERR_INVALID_ARGUMENT                 # ld < S
+    assert call(ld=10) == dsa.DSA_ERR_INVALID_ARGUMENT                # ld not a multiple of 4
+    assert call(H=48) == dsa.DSA_ERR_UNSUPPORTED
+    assert call(D=96) == dsa.DSA_ERR_UNSUPPORTED
+    assert call(qd=1, kd=0) == dsa.DSA_ERR_UNSUPPORTED                # dtype mix
+    assert call(qd=1, kd=1) == dsa.DSA_ERR_INVALID_ARGUMENT           # FP8 without scales
+    assert call(qd=1, kd=1, qs=fake, ks=fake, D=64) == dsa.DSA_ERR_UNSUPPORTED
+    assert call(qd=7) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert call(T=-1) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert call(p0=-1) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert call(T=0) == dsa.DSA_OK                                    # empty: nothing to do
+
+
+def test_topk_validation(dsa):
+    L = dsa.lib()
+    fake = 1 << 20
+    assert L.dsa_indexer_topk(fake, 8, 4, 8, 4, 0, 4, 0, fake, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert L.dsa_indexer_topk(fake, 8, 4, 8, 4, 4, 0, 0, fake, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert L.dsa_indexer_topk(fake, 8, 4, 8, 4, 4, 5000, 0, fake, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_indexer_topk(fake, 8, 4, 8, 4, 4, 4, 2, fake, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert L.dsa_indexer_topk(fake, 8, 4, 8, 4, 4, 4, 0, None, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert L.dsa_indexer_topk(fake, 8, 0, 8, 4, 4, 4, 0, fake, None) == dsa.DSA_OK
+
+
+def _args(dsa, **kw):
+    a = dsa.dsa_indexer_args()
+    a.q_dtype = a.k_dtype = 0
+    a.B, a.total_q, a.H, a.D = 2, 2, 64, 128
+    a.page_size, a.num_pages, a.max_pages_per_seq, a.max_seq_len = 64, 10, 5, 300
+    a.topk_limit, a.k_out, a.order = 64, 64, 0
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_workspace_size_and_paged_validation(dsa):
+    n = dsa.dsa_indexer_workspace_size(_args(dsa))
+    assert n >= 2 * 300 * 4                               # at least the fp32 score rows
+    for bad in [dict(page_size=48), dict(H=3), dict(k_out=5000), dict(max_seq_len=321),
+                dict(q_dtype=1, k_dtype=0), dict(order=3), dict(topk_limit=0)]:
+        with pytest.raises(dsa.DsaError):
+            dsa.dsa_indexer_workspace_size(_args(dsa, **bad))
+    L = dsa.lib()
+    a = _args(dsa)                                        # valid sizes, null pointers
+    assert L.dsa_indexer(ctypes.byref(a), None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    fake = 1 << 20
+    for f in ["q", "w", "cu_q_lens", "seq_lens", "block_tables", "k_cache", "topk"]:
+        setattr(a, f, fake)
+    assert L.dsa_indexer(ctypes.byref(a), None) == dsa.DSA_ERR_WORKSPACE
+    a.workspace, a.workspace_bytes = fake, n - 16
+    assert L.dsa_indexer(ctypes.byref(a), None) == dsa.DSA_ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------- IndexShare host logic
+
+@pytest.mark.parametrize("types", [
+    ["full", "shared", "shared"] * 4,
+    ["full", "full", "shared", "full"],
+    ["full"],
+    [],
+])
+def test_resolve_sources_matches_oracle(dsa, types):
+    assert dsa.dsa_resolve_indexer_sources(types) == oracle.resolve_indexer_sources(types)
+
+
+@pytest.mark.parametrize("types", [["shared"], ["shared", "full"], ["full", "dense"], ["full", None]])
+def test_resolve_sources_rejects(dsa, types):
+    with pytest.raises(ValueError):
+        dsa.dsa_resolve_indexer_sources(types)
+    with pytest.raises(ValueError):
+        oracle.resolve_indexer_sources(types)
+
+
+def test_resolve_sources_length_check(dsa):
+    with pytest.raises(ValueError):
+        dsa.dsa_resolve_indexer_sources(["full", "shared"], num_layers=3)
+
+
+def test_stack_rejects_bad_lists_before_launch(dsa):
+    with pytest.raises(dsa.DsaError):
+        dsa.dsa_indexer_stack(["shared", "full"], [None, None])
+    with pytest.raises(dsa.DsaError):
+        dsa.dsa_indexer_stack(["full", "shared"], [None, None])       # full layer without args
+    with pytest.raises(dsa.DsaError):
+        dsa.dsa_indexer_stack(["full", "oops"], [None, None])
+
+
+def test_mtp_extension(dsa):
+    base = ["full", "shared", "shared"]
+    assert dsa.extend_indexer_types_for_mtp(base, 2) == base + ["full", "full"]
+    assert dsa.extend_indexer_types_for_mtp(base, 0) == base
+    assert dsa.extend_indexer_types_for_mtp([], 3) == []
+
+
+def test_topk_limit_resolution_order(dsa):
+    ns = _types.SimpleNamespace
+    assert dsa.resolve_topk_limit(explicit=7, indexer=ns(topk_limit=8)) == 7
+    assert dsa.resolve_topk_limit(indexer=ns(topk_limit=8), config=ns(topk_limit=9)) == 8
+    assert dsa.resolve_topk_limit(config=ns(topk_limit=9, index_topk=10)) == 9
+    assert dsa.resolve_topk_limit(config=ns(), indexer_config=ns(topk_limit=11)) == 11
+    assert dsa.resolve_topk_limit(config=ns(index_topk=2048)) == 2048          # GLM5 style
+    assert dsa.resolve_topk_limit(indexer=ns(topk_limit=None), config=ns(topk_limit=None, index_topk=5)) == 5
+    with pytest.raises(AttributeError, match="topk_limit"):
+        dsa.resolve_topk_limit(config=ns(), indexer_config=ns())
+
+
+def test_workload_shapes():
+    c = workloads.tiny_exact_prefill()
+    assert (c.T, c.S, c.H, c.D, c.topk_limit) == (512, 512, 4, 64, 64)
+    assert float(c.q.float().abs().max()) <= 4 and float(c.w.abs().max()) <= 2
+    st = workloads.indexshare_stack(B=2, ctx=256)
+    assert st.indexer_types == workloads.INDEXSHARE_TYPES_12
+    assert sum(l is not None for l in st.layers) == 4

@@ -1,0 +1,274 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Integer-valued inputs (fp32 accumulation exact) must match bit for bit, scores and
+indices including their order; Gaussian inputs must meet the tolerances of
+tests/parity.py.  Shapes span several 128-key tiles, ragged tails, every supported
+head count, both top-k orders, dense and paged keys, bf16 and FP8.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.parity import RTOL, assert_scores_close, assert_topk_valid
+
+pytestmark = pytest.mark.gpu
+
+dsa = pytest.importorskip("sparse_attention_token_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+    yield
+    assert dsa.dsa_check_device_status() == dsa.DSA_OK
+
+
+DEV = "cuda"
+
+
+def run_dense(c, order=0, topk_limit=None, k_out=None):
+    topk_limit = c.topk_limit if topk_limit is None else topk_limit
+    k_out = c.k_out if k_out is None else k_out
+    q, k, w = c.q.to(DEV), c.k.to(DEV), c.w.to(DEV)
+    qs = None if c.q_scale is None else c.q_scale.to(DEV)
+    ks = None if c.k_scale is None else c.k_scale.to(DEV)
+    sc = dsa.dsa_indexer_scores(q, k, w, q_pos0=c.q_pos0, q_scale=qs, k_scale=ks)
+    tk = dsa.dsa_indexer_topk(sc, T=c.T, S=c.S, q_pos0=c.q_pos0, topk_limit=topk_limit, k_out=k_out,
+                              order=order)
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_status() == dsa.DSA_OK
+    return sc.cpu().numpy(), tk.cpu().numpy()
+
+
+def oracle_dense(c, order=0, topk_limit=None, k_out=None, rows=None):
+    return oracle.dense(c.q, c.k, c.w, T=c.T, S=c.S, H=c.H, D=c.D, q_pos0=c.q_pos0,
+                        topk_limit=c.topk_limit if topk_limit is None else topk_limit,
+                        k_out=c.k_out if k_out is None else k_out, q_scale=c.q_scale, k_scale=c.k_scale,
+                        order=order, rows=rows, want_scores=True, want_bound=True)
+
+
+def n_vis_dense(c, rows=None):
+    rows = range(c.T) if rows is None else rows
+    return [max(0, min(c.q_pos0 + t + 1, c.S)) for t in rows]
+
+
+# ----------------------------------------------------------------------------- dense
+
+@pytest.mark.parametrize("order", [0, 1])
+def test_tiny_exact_prefill_bit_exact(order):
+    c = workloads.tiny_exact_prefill()
+    sc, tk = run_dense(c, order=order)
+    rt, rs, rb = oracle_dense(c, order=order)
+    assert_scores_close(sc[:, :c.S], rs, rb, 0, exact=True)
+    assert np.array_equal(tk, rt)
+
+
+@pytest.mark.parametrize("H,D", [(4, 64), (8, 128), (16, 64), (32, 128), (64, 128), (128, 128), (64, 64)])
+def test_dense_integer_exact_all_heads(H, D):
+    T, S = 77, 301                 # ragged: 3 key tiles, partial query block
+    c = workloads.dense_case(T, S, H, D, 40, q_pos0=S - T, k_out=45, integer=True, int_range=(-2, 2),
+                             seed=H + D)
+    sc, tk = run_dense(c)
+    rt, rs, rb = oracle_dense(c)
+    assert_scores_close(sc[:, :S], rs, rb, 0, exact=True)
+    assert np.array_equal(tk, rt)
+
+
+@pytest.mark.parametrize("q_pos0,T,S", [(0, 300, 300), (0, 40, 300), (500, 64, 300), (130, 1, 129)])
+def test_dense_positions_and_padding(q_pos0, T, S):
+    c = workloads.dense_case(T, S, 64, 128, 100, q_pos0=q_pos0, k_out=128, integer=True, int_range=(-2, 2),
+                             seed=3)
+    sc, tk = run_dense(c)
+    rt, rs, rb = oracle_dense(c)
+    assert_scores_close(sc[:, :S], rs, rb, 0, exact=True)
+    assert np.array_equal(tk, rt)
+    # entries no query may see are not written (the binding pre-fills -inf)
+    for t in range(T):
+        n = min(q_pos0 + t + 1, S)
+        assert np.all(np.isneginf(sc[t, n:S]))
+
+
+def test_dense_gaussian_bf16_tolerance():
+    c = workloads.dense_case(260, 700, 64, 128, 96, q_pos0=440, seed=5, w_std=1 / 8)
+    sc, tk = run_dense(c)
+    rt, rs, rb = oracle_dense(c)
+    assert_scores_close(sc[:, :c.S], rs, rb, RTOL["bf16"], exact=False)
+    assert_topk_valid(tk, rt, rs, rb, n_vis_dense(c), c.topk_limit, RTOL["bf16"], exact=False)
+
+
+def test_dense_fp8_integer_exact():
+    c = workloads.dense_case(70, 400, 64, 128, 50, q_pos0=330, dtype="fp8_e4m3", integer=True,
+                             int_range=(-3, 3), seed=6)
+    sc, tk = run_dense(c)
+    rt, rs, rb = oracle_dense(c)
+    assert_scores_close(sc[:, :c.S], rs, rb, 0, exact=True)
+    assert np.array_equal(tk, rt)
+
+
+def test_dense_fp8_gaussian_tolerance():
+    c = workloads.dense_case(130, 500, 64, 128, 64, q_pos0=370, dtype="fp8_e4m3", seed=7, w_std=1 / 8)
+    sc, tk = run_dense(c)
+    rt, rs, rb = oracle_dense(c)
+    assert_scores_close(sc[:, :c.S], rs, rb, RTOL["fp8_e4m3"], exact=False)
+    assert_topk_valid(tk, rt, rs, rb, n_vis_dense(c), c.topk_limit, RTOL["fp8_e4m3"], exact=False)
+
+
+def test_dense_deterministic():
+    c = workloads.dense_case(128, 1000, 64, 128, 256, q_pos0=872, seed=8)
+    a = run_dense(c)
+    b = run_dense(c)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ----------------------------------------------------------------------------- top-k alone
+
+def _topk_on(scores32: np.ndarray, q_pos0: int, S: int, limit: int, k_out: int, order: int):
+    T = scores32.shape[0]
+    ld = (S + 3) // 4 * 4
+    buf = torch.full((T, ld), float("nan"), dtype=torch.float32)
+    buf[:, :S] = torch.from_numpy(scores32)
+    tk = dsa.dsa_indexer_topk(buf.to(DEV), T=T, S=S, q_pos0=q_pos0, topk_limit=limit, k_out=k_out, order=order)
+    torch.cuda.synchronize()
+    nv = [max(0, min(q_pos0 + t + 1, S)) for t in range(T)]
+    ref = oracle.topk_of_scores(scores32.astype(np.float64), nv, limit, k_out, order=order)
+    return tk.cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("order", [0, 1])
+@pytest.mark.parametrize("S,limit", [(5000, 2048), (20000, 2048), (70000, 4096), (3000, 3000), (9000, 1)])
+def test_topk_tie_storms_exact(S, limit, order):
+    g = torch.Generator().manual_seed(S + limit)
+    T = 6
+    sc = torch.randint(-3, 4, (T, S), generator=g).to(torch.float32).numpy()
+    sc[1] = 0.0
+    sc[2, ::2] = -0.0                       # -0.0 and +0.0 are equal
+    sc[3] = np.arange(S, dtype=np.float32)  # strictly increasing: the last keys win
+    got, ref = _topk_on(sc, S - T, S, limit, limit + 5, order)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("S", [100, 2049, 8192, 16385, 65536])
+def test_topk_gaussian_exact(S):
+    g = torch.Generator().manual_seed(S)
+    T = 4
+    sc = torch.randn((T, S), generator=g).numpy().astype(np.float32)
+    got, ref = _topk_on(sc, S - T, S, 2048, 2048, 0)
+    assert np.array_equal(got, ref)
+
+
+def test_topk_causal_rows_prefill_shape():
+    g = torch.Generator().manual_seed(1)
+    T = S = 3000
+    sc = torch.randn((T, S), generator=g).numpy().astype(np.float32)
+    got, ref = _topk_on(sc, 0, S, 2048, 2048, 0)
+    assert np.array_equal(got, ref)
+
+
+# ----------------------------------------------------------------------------- paged
+
+def run_paged(pc, order=0, topk_limit=None, k_out=None):
+    to = lambda t: None if t is None else t.to(DEV)
+    tk = dsa.dsa_indexer(to(pc.q), to(pc.w), to(pc.k_cache), to(pc.cu_q_lens), to(pc.seq_lens),
+                         to(pc.block_tables), max_seq_len=pc.max_seq_len,
+                         topk_limit=pc.topk_limit if topk_limit is None else topk_limit,
+                         k_out=pc.k_out if k_out is None else k_out, q_scale=to(pc.q_scale),
+                         k_scale_cache=to(pc.k_scale_cache), order=order)
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_status() == dsa.DSA_OK
+    return tk.cpu().numpy()
+
+
+@pytest.mark.parametrize("page_size", [16, 64, 128])
+def test_paged_decode_integer_exact(page_size):
+    lens = [1, 63, 64, 65, 129, 1000, 2047, 3000]
+    pc = workloads.paged_case(lens, [1] * len(lens), 64, 128, 512, page_size=page_size, integer=True, seed=9)
+    got = run_paged(pc)
+    ref, _, _ = oracle.paged(pc)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("H", [4, 32, 64, 128])
+def test_paged_decode_heads(H):
+    lens = [700, 5, 1300]
+    pc = workloads.paged_case(lens, [1, 1, 1], H, 128, 256, page_size=64, integer=True, seed=10 + H)
+    got = run_paged(pc)
+    ref, _, _ = oracle.paged(pc)
+    assert np.array_equal(got, ref)
+
+
+def test_paged_varlen_prefill_integer_exact():
+    lens, qlens = [900, 40, 1500, 300], [300, 40, 17, 1]
+    pc = workloads.paged_case(lens, qlens, 64, 128, 128, page_size=64, integer=True, seed=11)
+    for order in (0, 1):
+        got = run_paged(pc, order=order)
+        ref, _, _ = oracle.paged(pc, order=order)
+        assert np.array_equal(got, ref)
+
+
+def test_paged_fp8_integer_exact():
+    lens, qlens = [1000, 257, 64], [3, 257, 1]
+    pc = workloads.paged_case(lens, qlens, 64, 128, 200, page_size=64, q_dtype="fp8_e4m3",
+                              k_dtype="fp8_e4m3", integer=True, seed=12)
+    got = run_paged(pc)
+    ref, _, _ = oracle.paged(pc)
+    assert np.array_equal(got, ref)
+
+
+def test_paged_fp8_gaussian_tolerance():
+    lens, qlens = [3000, 1200], [1, 200]
+    pc = workloads.paged_case(lens, qlens, 64, 128, 300, page_size=64, q_dtype="fp8_e4m3",
+                              k_dtype="fp8_e4m3", w_std=1 / 8, seed=13)
+    got = run_paged(pc)
+    ref, rs, rb = oracle.paged(pc, want_scores=True, want_bound=True)
+    pos = oracle.query_positions(pc)
+    assert_topk_valid(got, ref, rs, rb, pos + 1, pc.topk_limit, RTOL["fp8_e4m3"], exact=False)
+
+
+def test_paged_bad_page_is_reported_not_faulted():
+    pc = workloads.paged_case([500, 300], [1, 1], 64, 128, 64, page_size=64, integer=True, seed=14)
+    bt = pc.block_tables.clone()
+    bt[1, 2] = pc.num_pages + 1000          # out of range: must be skipped and reported
+    to = lambda t: t.to(DEV)
+    dsa.dsa_indexer(to(pc.q), to(pc.w), to(pc.k_cache), to(pc.cu_q_lens), to(pc.seq_lens), to(bt),
+                    max_seq_len=pc.max_seq_len, topk_limit=64)
+    assert dsa.dsa_check_device_status() == dsa.DSA_ERR_DEVICE_CHECK
+    assert dsa.dsa_check_device_status() == dsa.DSA_OK   # reading clears it
+
+
+# ----------------------------------------------------------------------------- IndexShare
+
+def test_indexshare_stack_forwards_source_buffers():
+    types = ["full", "shared", "shared", "full", "shared"]
+    cases = [workloads.paged_case([400, 90], [1, 1], 64, 128, 64, page_size=64, integer=True, seed=20 + i)
+             if t == "full" else None for i, t in enumerate(types)]
+    keep, args = [], []
+    for c in cases:
+        if c is None:
+            args.append(None)
+            continue
+        a, kk = dsa.make_indexer_args(c.q.to(DEV), c.w.to(DEV), c.k_cache.to(DEV), c.cu_q_lens.to(DEV),
+                                      c.seq_lens.to(DEV), c.block_tables.to(DEV), max_seq_len=c.max_seq_len,
+                                      topk_limit=64)
+        args.append(a)
+        keep.append(kk)
+    ptrs, src = dsa.dsa_indexer_stack(types, args)
+    torch.cuda.synchronize()
+    assert src == [0, 0, 0, 3, 3]
+    assert ptrs[1] == ptrs[0] and ptrs[2] == ptrs[0] and ptrs[4] == ptrs[3] and ptrs[0] != ptrs[3]
+    ref_src, ref = oracle.stack(types, cases)
+    assert ref_src == src
+    assert np.array_equal(keep[0][8].cpu().numpy(), ref[0])
+    assert np.array_equal(keep[1][8].cpu().numpy(), ref[3])
+
+
+def test_indexshare_rejects_before_launch():
+    c = workloads.paged_case([100], [1], 64, 128, 16, page_size=64, integer=True, seed=30)
+    a, _k = dsa.make_indexer_args(c.q.to(DEV), c.w.to(DEV), c.k_cache.to(DEV), c.cu_q_lens.to(DEV),
+                                  c.seq_lens.to(DEV), c.block_tables.to(DEV), max_seq_len=100, topk_limit=16)
+    with pytest.raises(dsa.DsaError):
+        dsa.dsa_indexer_stack(["shared", "full"], [None, a])
+    with pytest.raises(dsa.DsaError):
+        dsa.dsa_indexer_stack(["full", "full"], [a, None])      # a full layer without its cache
