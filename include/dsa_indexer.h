@@ -165,6 +165,32 @@ dsa_status dsa_indexer_workspace_size(const dsa_indexer_args* args, size_t* byte
 dsa_status dsa_indexer(const dsa_indexer_args* args, dsa_stream_t stream);
 
 /*
+ * dsa_indexer_static -- dsa_indexer for callers that cannot allocate device memory.
+ * The pages have no counterpart of this entry point; it exists for library users.
+ *
+ * Some callers cannot hand the library a workspace: plugin hosts that pass only the
+ * input and output tensors, and serving loops that reserve nearly all device memory
+ * up front and forbid allocation during a step (cudaMalloc / cudaFree may synchronise
+ * the device and stall every stream).  This call runs the same kernels as dsa_indexer
+ * with their scratch (work-list counters, work items, fp32 score rows) in one
+ * library-owned device array of DSA_STATIC_WORKSPACE_BYTES, which every GPU that
+ * loads this code holds until the process exits.  args->workspace and
+ * args->workspace_bytes are ignored; every other field means what it means for
+ * dsa_indexer, and the caller still provides every input and the topk output.
+ *  - A problem whose dsa_indexer_workspace_size exceeds DSA_STATIC_WORKSPACE_BYTES
+ *    returns DSA_ERR_WORKSPACE before anything is launched (use dsa_indexer with a
+ *    caller workspace for it).
+ *  - The first call on a device looks up the array's device address with that device
+ *    current; make that first call before any stream capture.
+ *  - All calls on a device share the array and it keeps the last call's contents; each
+ *    call clears the part that must start at zero (the work-list counters).  Calls that
+ *    overlap on the GPU (other streams, other host threads) race on the array: serialise them.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define DSA_STATIC_WORKSPACE_BYTES ((size_t)24 << 20)
+dsa_status dsa_indexer_static(const dsa_indexer_args* args, dsa_stream_t stream);
+
+/*
  * IndexShare source resolution (host only, GLM5 TensorCast adaptation design,
  * "GLM-5.2 IndexShare"): src[l] = l for a full layer, the nearest earlier full
  * layer for a shared layer.  types[l] is a dsa_layer_type.  An unknown type or a

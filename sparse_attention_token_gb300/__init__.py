@@ -313,3 +313,28 @@ def extend_indexer_types_for_mtp(indexer_types: Sequence[str], num_mtp_layers: i
     if not types or num_mtp_layers <= 0:
         return types
     return types + ["full"] * int(num_mtp_layers)
+
+
+# ---- no-allocation variant ----------------------------------------------------------
+
+DSA_STATIC_WORKSPACE_BYTES = 24 << 20
+
+
+def dsa_indexer_static(q, w, k_cache, cu_q_lens, seq_lens, block_tables, *, max_seq_len: int, topk_limit: int,
+                       k_out: Optional[int] = None, q_scale=None, k_scale_cache=None, topk=None,
+                       order: int = DSA_ORDER_SCORE, stream=None) -> torch.Tensor:
+    """dsa_indexer without a workspace, for callers that cannot allocate device memory
+    (plugin hosts that only pass tensors, serving loops that forbid allocation during a
+    step).  The library keeps the scratch in a fixed device array of
+    DSA_STATIC_WORKSPACE_BYTES; larger problems raise DsaError(DSA_ERR_WORKSPACE).
+    Calls that overlap on the GPU share that array and must be serialised."""
+    a, keep = make_indexer_args(q, w, k_cache, cu_q_lens, seq_lens, block_tables, max_seq_len=max_seq_len,
+                                topk_limit=topk_limit, k_out=k_out, q_scale=q_scale,
+                                k_scale_cache=k_scale_cache, topk=topk,
+                                workspace=torch.empty(0, dtype=torch.uint8, device=q.device), order=order)
+    a.workspace, a.workspace_bytes = None, 0
+    fn = lib().dsa_indexer_static
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.POINTER(dsa_indexer_args), ctypes.c_void_p]
+    _check(fn(ctypes.byref(a), _stream_ptr(stream)), "dsa_indexer_static")
+    return keep[8]
