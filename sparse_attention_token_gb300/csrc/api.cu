@@ -34,7 +34,7 @@ constexpr size_t kScoreChunkBudget = 64ull << 20;  // target bytes of fp32 score
 // ---------------------------------------------------------------- work list (paged path)
 __global__ void prep_items_kernel(const int32_t* cu_q_lens, const int32_t* seq_lens, int NQ, int KC, int R, int cap,
                                   int n_chunks, int max_seq_len, int max_pages_per_seq, int page_size,
-                                  WorkItem* items, int* counts, unsigned* status) {
+                                  int tile_keys, WorkItem* items, int* counts, unsigned* status) {
   const int b = blockIdx.x;
   const int cu0 = cu_q_lens[b], cu1 = cu_q_lens[b + 1];
   const int q_len = cu1 - cu0;
@@ -52,7 +52,7 @@ __global__ void prep_items_kernel(const int32_t* cu_q_lens, const int32_t* seq_l
       const int row0 = seg0 + j * NQ;
       const int nrows = min(NQ, seg1 - row0);
       const int pos0 = L - q_len + (row0 - cu0);
-      const int n_kt = (pos0 + nrows - 1 + kBlockM) / kBlockM;
+      const int n_kt = (pos0 + nrows - 1 + tile_keys) / tile_keys;
       const int n_it = KC > 0 ? (n_kt + KC - 1) / KC : 1;
       const int slot = atomicAdd(&counts[c], n_it);
       if (slot + n_it > cap) {
@@ -148,17 +148,36 @@ int pick_stages(const ScoreArgs& a) {
   return 0;
 }
 
-// Shared memory requested per CTA: at least half an SM's worth, so that no two score
-// CTAs (each holding all 512 TMEM columns) ever share an SM.
+int pick_stages_pair(const ScoreArgs& a) {
+  for (int s = kMaxKStages; s >= 2; --s)
+    if (score_pair_smem_bytes(a, s) <= kMaxSmem) return s;
+  return 0;
+}
+
+// Prefill tiles (N = 256) run on the single-SM kernel; DSA_PAIR_MMA=1 selects the
+// CTA-pair (2-SM MMA) kernel instead, which is correct but measured slower on GB300.
+bool use_pair_mma() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = std::getenv("DSA_PAIR_MMA");
+    v = (e && e[0] == '1') ? 1 : 0;
+  }
+  return v == 1;
+}
+
 size_t score_launch_smem(const ScoreArgs& a) {
   return std::max<size_t>(score_smem_bytes(a, a.num_k_stages), 120 * 1024);
+}
+
+size_t score_pair_launch_smem(const ScoreArgs& a) {
+  return std::max<size_t>(score_pair_smem_bytes(a, a.num_k_stages), 120 * 1024);
 }
 
 dsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
 struct PagedPlan {
-  bool decode;
-  int NQ, N, KC, R, n_chunks, cap;
+  bool decode, pair;
+  int NQ, N, KC, R, n_chunks, cap, tile_keys;
   long long ld;
   size_t off_counts, off_items, off_scores, total;
 };
@@ -176,12 +195,15 @@ dsa_status plan_paged(const dsa_indexer_args* a, PagedPlan* p) {
   if (static_cast<long long>(a->max_seq_len) > static_cast<long long>(a->max_pages_per_seq) * a->page_size)
     return DSA_ERR_INVALID_ARGUMENT;
   if (a->max_seq_len >= (1 << 16) * kBlockM) return DSA_ERR_UNSUPPORTED;  // key-tile ids are 16-bit
+  if (a->max_seq_len > INT_MAX - 2 * kBlockM) return DSA_ERR_UNSUPPORTED;
   dsa_status st = check_dtypes(a->q_dtype, a->k_dtype, a->D, a->q_scale != nullptr, a->k_scale_cache != nullptr);
   if (st != DSA_OK) return st;
   const int ns = std::max(num_sms(), 1);
   p->decode = a->total_q <= a->B;
   p->N = p->decode ? std::max(64, a->H) : 256;
   p->NQ = p->N / a->H;
+  p->pair = !p->decode && use_pair_mma();
+  p->tile_keys = p->pair ? 2 * kBlockM : kBlockM;
   p->ld = (std::max(a->max_seq_len, 1) + 3) & ~3LL;
   long long R = static_cast<long long>(kScoreChunkBudget / (static_cast<size_t>(p->ld) * 4));
   R = std::max<long long>(R - R % p->NQ, p->NQ);
@@ -189,8 +211,8 @@ dsa_status plan_paged(const dsa_indexer_args* a, PagedPlan* p) {
   p->R = static_cast<int>(R);
   p->n_chunks = std::max(1, (a->total_q + p->R - 1) / p->R);
   const long long qb_per_chunk = (p->R + p->NQ - 1) / p->NQ + std::min<long long>(a->B, p->R) + 1;
-  p->KC = qb_per_chunk < 2LL * ns ? 16 : 0;
-  const long long kt_max = (a->max_seq_len + kBlockM - 1) / kBlockM;
+  p->KC = qb_per_chunk < 2LL * ns ? (p->pair ? 8 : 16) : 0;
+  const long long kt_max = (a->max_seq_len + p->tile_keys - 1) / p->tile_keys;
   const long long per_qb = p->KC > 0 ? (kt_max + p->KC - 1) / p->KC : 1;
   const long long cap = qb_per_chunk * std::max<long long>(per_qb, 1);
   if (cap > INT_MAX / 2) return DSA_ERR_UNSUPPORTED;
@@ -235,28 +257,31 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
   s.scores = scores;
   s.ld = p.ld;
   s.status = status;
-  s.num_k_stages = pick_stages(s);
+  s.num_k_stages = p.pair ? pick_stages_pair(s) : pick_stages(s);
   if (s.num_k_stages < 2) return DSA_ERR_UNSUPPORTED;
 
   CUtensorMap tq, tk;
-  if (!make_map_2d(&tq, a->q, fp8, a->D, static_cast<long long>(a->total_q) * a->H, p.N)) return DSA_ERR_CUDA;
+  if (!make_map_2d(&tq, a->q, fp8, a->D, static_cast<long long>(a->total_q) * a->H, p.pair ? p.N / 2 : p.N))
+    return DSA_ERR_CUDA;
   if (!make_map_paged(&tk, a->k_cache, s.k_fp8, a->D, a->page_size, std::max(a->num_pages, 1)))
     return DSA_ERR_CUDA;
 
   cudaError_t e = cudaMemsetAsync(counts, 0, static_cast<size_t>(p.n_chunks) * 4, st);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   prep_items_kernel<<<a->B, 128, 0, st>>>(a->cu_q_lens, a->seq_lens, p.NQ, p.KC, p.R, p.cap, p.n_chunks,
-                                          a->max_seq_len, a->max_pages_per_seq, a->page_size, items, counts,
-                                          status);
+                                          a->max_seq_len, a->max_pages_per_seq, a->page_size, p.tile_keys, items,
+                                          counts, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return DSA_ERR_CUDA;
   const int ns = std::max(num_sms(), 1);
-  const size_t smem = score_launch_smem(s);
+  const size_t smem = p.pair ? score_pair_launch_smem(s) : score_launch_smem(s);
   for (int c = 0; c < p.n_chunks; ++c) {
     s.items = items + static_cast<long long>(c) * p.cap;
     s.n_items = counts + c;
     s.items_cap = p.cap;
     s.row_base = c * p.R;
-    if ((e = launch_score(s, &tq, &tk, ns, smem, st)) != cudaSuccess) return DSA_ERR_CUDA;
+    e = p.pair ? launch_score_pair(s, &tq, &tk, std::max(2, ns & ~1), smem, st)
+               : launch_score(s, &tq, &tk, ns, smem, st);
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
     TopkArgs t{};
     t.scores = scores;
     t.ld = p.ld;
@@ -342,13 +367,20 @@ dsa_status dsa_indexer_scores(const void* q, int q_dtype, const float* q_scale, 
   a.scores = scores;
   a.ld = ld_scores;
   a.status = status;
-  a.num_k_stages = pick_stages(a);
+  const bool pair = use_pair_mma();
+  a.num_k_stages = pair ? pick_stages_pair(a) : pick_stages(a);
   if (a.num_k_stages < 2) return DSA_ERR_UNSUPPORTED;
 
   CUtensorMap tq, tk;
-  if (!make_map_2d(&tq, q, fp8, D, static_cast<long long>(T) * H, a.N)) return DSA_ERR_CUDA;
+  if (!make_map_2d(&tq, q, fp8, D, static_cast<long long>(T) * H, pair ? a.N / 2 : a.N)) return DSA_ERR_CUDA;
   if (!make_map_2d(&tk, k, fp8, D, S, kBlockM)) return DSA_ERR_CUDA;
-  const int grid = std::min(std::max(num_sms(), 1), a.n_dense_items);
+  const int ns = std::max(num_sms(), 1);
+  if (pair) {
+    const int pairs = std::max(1, std::min(ns / 2, a.n_dense_items));
+    return from_cuda(launch_score_pair(a, &tq, &tk, 2 * pairs, score_pair_launch_smem(a),
+                                       reinterpret_cast<cudaStream_t>(stream)));
+  }
+  const int grid = std::min(ns, a.n_dense_items);
   return from_cuda(launch_score(a, &tq, &tk, grid, score_launch_smem(a), reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -245,47 +245,50 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
 }
 
 // ------------------------------------------------------------------ MMA issuer (warp 1, lane 0)
-template <int H, bool DECODE>
-__device__ __forceinline__ void mma_role(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P, uint64_t* bars,
+// The single issuing thread is on the tensor core's critical path, so the loop keeps
+// everything in registers: stage index and phase advance incrementally, stage
+// addresses come from one multiply, and the per-step descriptors are the first
+// step's descriptors plus a compile-time offset in their 16-byte address field.
+template <int H, bool DECODE, bool F8, int NSTEPS>
+__device__ __forceinline__ void mma_loop(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P, uint64_t* bars,
                                          volatile int* abort, int n_items, uint32_t tmem_base) {
   using C = Cfg<H, DECODE>;
   constexpr int N = C::N;
   const int nK = a.num_k_stages;
-  const bool f8 = a.k_fp8 != 0;
-  const uint32_t idesc = ptx::idesc_f32acc(kBlockM, N, !f8);
-  const int esz = f8 ? 1 : 2;
-  const int nsteps = a.D * esz / 32;  // 32 bytes of K per MMA (16 bf16 or 32 e4m3)
+  const uint32_t idesc = ptx::idesc_f32acc(kBlockM, N, !F8);
   const uint32_t sbase = ptx::smem_u32(smem);
-  uint32_t nq = 0, nk = 0, nt = 0;
+  const uint32_t k_stage_bytes = P.k[1] - P.k[0];
+  const uint32_t k_base = sbase + P.k[0];
+  uint32_t nq = 0, nt = 0;
+  uint32_t sk = 0, kphase = 0;  // key ring slot and its phase parity
   bool ok = true;
   for (int it = 0; ok; ++it) {
     ItemInfo I;
     if (!fetch_item<C::NQ>(a, n_items, it, I)) break;
     const int sq = nq & 1;
     if (!ptx::mbar_wait(&bars[kBarQFull + sq], (nq >> 1) & 1, abort, a.status, kStatusTimeout)) break;
-    const uint32_t q_addr = sbase + P.q[sq];
+    const uint64_t bdesc0 = ptx::sw128_kmajor_desc(sbase + P.q[sq]);
     for (int kt = I.kt0; kt < I.kt1; ++kt) {
-      const int sk = nk % nK;
       const int acc = nt & 1;
-      if (!ptx::mbar_wait(&bars[kBarKFull + sk], (nk / nK) & 1, abort, a.status, kStatusTimeout) ||
+      if (!ptx::mbar_wait(&bars[kBarKFull + sk], kphase, abort, a.status, kStatusTimeout) ||
           !ptx::mbar_wait(&bars[kBarTEmpty + acc], ((nt >> 1) & 1) ^ 1, abort, a.status, kStatusTimeout)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
-      const uint32_t k_addr = sbase + P.k[sk];
-      for (int j = 0; j < nsteps; ++j) {
-        const uint32_t a_addr = k_addr + (j >> 2) * (kBlockM * 128) + (j & 3) * 32;
-        const uint32_t b_addr = q_addr + (j >> 2) * (N * 128) + (j & 3) * 32;
-        const uint64_t ad = ptx::sw128_kmajor_desc(a_addr);
-        const uint64_t bd = ptx::sw128_kmajor_desc(b_addr);
-        if (f8) ptx::mma_f8(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
+      const uint64_t adesc0 = ptx::sw128_kmajor_desc(k_base + sk * k_stage_bytes);
+#pragma unroll
+      for (int j = 0; j < NSTEPS; ++j) {
+        // step j reads 32 bytes of K at atom (j / 4), byte (j % 4) * 32 of each row
+        const uint64_t ad = adesc0 + static_cast<uint64_t>(((j >> 2) * (kBlockM * 128) + (j & 3) * 32) >> 4);
+        const uint64_t bd = bdesc0 + static_cast<uint64_t>(((j >> 2) * (N * 128) + (j & 3) * 32) >> 4);
+        if (F8) ptx::mma_f8(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
         else ptx::mma_bf16(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
       }
       ptx::mma_commit(&bars[kBarKEmpty + sk]);
       ptx::mma_commit(&bars[kBarTFull + acc]);
-      ++nk;
+      if (++sk == static_cast<uint32_t>(nK)) { sk = 0; kphase ^= 1u; }
       ++nt;
     }
     if (!ok) break;
@@ -295,6 +298,15 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& a, uint8_t* smem, cons
   // every MMA issued above has finished once this commit arrives
   ptx::mma_commit(&bars[kBarDone]);
   ptx::mbar_wait_drain(&bars[kBarDone], 0, a.status, kStatusTimeout, 200000000ull);
+}
+
+template <int H, bool DECODE>
+__device__ __forceinline__ void mma_role(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P, uint64_t* bars,
+                                         volatile int* abort, int n_items, uint32_t tmem_base) {
+  // 32 bytes of K per MMA: 16 bf16 or 32 e4m3 values
+  if (a.k_fp8) mma_loop<H, DECODE, true, 4>(a, smem, P, bars, abort, n_items, tmem_base);
+  else if (a.D == 128) mma_loop<H, DECODE, false, 8>(a, smem, P, bars, abort, n_items, tmem_base);
+  else mma_loop<H, DECODE, false, 4>(a, smem, P, bars, abort, n_items, tmem_base);
 }
 
 // Every lane waits (each observes the barrier itself); the outcome is made uniform
@@ -357,9 +369,13 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
           break;
         }
         ptx::tc_fence_after();
-        float accq[QH];
+        // NP packed (f32x2) partial sums per query: independent FMA chains
+        constexpr int NP = (32 / (2 * QH)) > 4 ? 4 : ((32 / (2 * QH)) < 1 ? 1 : (32 / (2 * QH)));
+        float2 part[QH][NP];
 #pragma unroll
-        for (int j = 0; j < QH; ++j) accq[j] = 0.f;
+        for (int j = 0; j < QH; ++j)
+#pragma unroll
+          for (int p = 0; p < NP; ++p) part[j][p] = make_float2(0.f, 0.f);
         const uint32_t tcol = tmem_base + lane_addr + static_cast<uint32_t>(acc * 256 + col0);
         uint32_t xa[32], xb[32];
         ptx::tmem_ld_32x32b_x32(tcol, xa);
@@ -371,17 +387,29 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
 #pragma unroll
           for (int i4 = 0; i4 < 8; ++i4) {
             const float4 wv = w4[i4];
-            const int cc = 32 * c + 4 * i4;
-            accq[(cc + 0) / H] = fmaf(wv.x, fmaxf(__uint_as_float(xa[4 * i4 + 0]), 0.f), accq[(cc + 0) / H]);
-            accq[(cc + 1) / H] = fmaf(wv.y, fmaxf(__uint_as_float(xa[4 * i4 + 1]), 0.f), accq[(cc + 1) / H]);
-            accq[(cc + 2) / H] = fmaf(wv.z, fmaxf(__uint_as_float(xa[4 * i4 + 2]), 0.f), accq[(cc + 2) / H]);
-            accq[(cc + 3) / H] = fmaf(wv.w, fmaxf(__uint_as_float(xa[4 * i4 + 3]), 0.f), accq[(cc + 3) / H]);
+            const int cc = 32 * c + 4 * i4;  // column (within this thread's range) of wv.x
+            const int jq = cc / H;          // H >= 4, so the 4 columns share a query
+            const int p0 = ((cc % H) / 2) % NP, p1 = ((cc % H) / 2 + 1) % NP;
+            const float r0 = fmaxf(__uint_as_float(xa[4 * i4 + 0]), 0.f);
+            const float r1 = fmaxf(__uint_as_float(xa[4 * i4 + 1]), 0.f);
+            const float r2 = fmaxf(__uint_as_float(xa[4 * i4 + 2]), 0.f);
+            const float r3 = fmaxf(__uint_as_float(xa[4 * i4 + 3]), 0.f);
+            ptx::ffma2(part[jq][p0], make_float2(wv.x, wv.y), make_float2(r0, r1));
+            ptx::ffma2(part[jq][p1], make_float2(wv.z, wv.w), make_float2(r2, r3));
           }
           if (c + 1 < NCH) {
             ptx::tmem_ld_wait_regs(xb);
 #pragma unroll
             for (int i = 0; i < 32; ++i) xa[i] = xb[i];
           }
+        }
+        float accq[QH];
+#pragma unroll
+        for (int j = 0; j < QH; ++j) {
+          float t = 0.f;
+#pragma unroll
+          for (int p = 0; p < NP; ++p) t += part[j][p].x + part[j][p].y;
+          accq[j] = t;
         }
         ptx::tc_fence_before();
         __syncwarp();

@@ -1,27 +1,43 @@
 // topk.cu -- per-row top-k of indexer scores (GLM5 TensorCast adaptation design,
 // "性能模型设计" bucket 8, top-k selection; output width min(topk_limit, n_visible)).
 //
-// One CTA of 512 threads per row.  Scores become order-preserving unsigned keys
-// (larger score -> larger key; -0.0 folded onto +0.0).  Selecting the best
-// `keep` keys under the rule (score desc, index asc) is done in three steps:
-//   1. radix select of the threshold key T: histograms of the top 11 bits, then
-//      the next 11 and the last 10 bits restricted to the threshold bucket, giving
-//      the count of keys above T and `need` = how many keys equal to T to take;
-//   2. an ordered compaction in key-index order (block-wide prefix sums), which
-//      keeps every key above T and the `need` lowest-index keys equal to T;
-//   3. for DSA_ORDER_SCORE, a stable LSD radix sort (8-bit digits, descending) of
-//      the kept keys, which leaves equal scores in ascending index order.
-// Rows up to cache_cap keys are staged in shared memory once; longer rows are
-// re-read from global memory (L2) by each pass.
+// One CTA of 256 threads per row.  Scores become order-preserving unsigned keys
+// (larger score -> larger key; -0.0 folded onto +0.0).  The best `keep` keys under
+// (score desc, index asc) are found as follows.
+//   1. One pass over the row builds a histogram of the top 12 key bits; a suffix
+//      scan finds the bucket b where the running count reaches `keep`.
+//   2. Fast path (the keys in buckets >= b fit the candidate buffer): an
+//      order-preserving compaction (each warp owns a contiguous segment of the row;
+//      ballots and warp prefix sums, no block-wide scans) copies every key of
+//      bucket >= b with its index, in index order.
+//        score order: a stable LSD radix sort (8-bit digits, descending, digits that
+//        never change skipped) of the candidates; the first `keep` are the answer
+//        (ties keep ascending index because the input was in index order);
+//        index order: the exact threshold inside bucket b is refined on the
+//        candidates alone, then one ordered pass writes the selected indices.
+//   3. Slow path (a huge threshold bucket, e.g. many equal scores): the exact
+//      threshold key T and `need` (how many keys equal to T to keep, lowest index
+//      first) are refined over the whole row with two more histogram passes, then
+//      the ordered compaction keeps exactly `keep` keys, sorted as above.
+#include <type_traits>
+
 #include "internal.h"
 
 namespace dsa {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = kThreads * 4;
+constexpr int kBins = 4096;            // top 12 key bits
+constexpr int kMaxRounds = 16;         // sort: candidates per warp / 32
+constexpr int kHistWords = kBins + kBins / 16;  // histogram with one pad word per 16 bins
+constexpr int kSortBits = 9;           // radix sort digit width
+constexpr int kSortBins = 1 << kSortBits;
+
+// Histogram slot of bin b: one pad word after every 16 bins, so a thread reading 16
+// consecutive bins while its neighbours read the next 16 hits distinct banks.
+__device__ __forceinline__ int hslot(uint32_t b) { return static_cast<int>(b + (b >> 4)); }
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -29,7 +45,7 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive prefix sum over the block (thread order); *total gets the block sum.
+// Exclusive prefix sum over the block in thread order; *total gets the block sum.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
@@ -40,144 +56,315 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, u
   }
   if (lane == 31) red[warp] = x;
   __syncthreads();
-  if (warp == 0) {
-    uint32_t t = lane < kWarps ? red[lane] : 0u;
+  uint32_t before = 0, tot = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
-    }
-    if (lane < kWarps) red[lane] = t;  // inclusive warp totals
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t r = red[w];
+    before += w < warp ? r : 0u;
+    tot += r;
   }
-  __syncthreads();
-  const uint32_t before = warp > 0 ? red[warp - 1] : 0u;
-  *total = red[kWarps - 1];
+  *total = tot;
   __syncthreads();  // red is reused by the next call
   return before + x - v;
 }
 
-// Warp-aggregated shared-memory histogram increment (all 32 lanes must call).
-__device__ __forceinline__ void hist_add(uint32_t* hist, bool active, uint32_t bin) {
-  const uint32_t key = active ? bin : 0xFFFFFFFFu;
-  const uint32_t peers = __match_any_sync(0xffffffffu, key);
+// Warp-inclusive prefix sum.
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x) {
   const int lane = threadIdx.x & 31;
-  if (active && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
 }
 
-// Find the bucket b (scanning from the top) where the running count reaches `want`:
-// out[0] = b, out[1] = keys in buckets above b, out[2] = keys in bucket b.
+// Bucket where the running count from the top reaches `want` (nbins = 16 * kThreads
+// or 256).  out = {bucket, keys above it, keys in it}.  Thread t scans the bins
+// nbins - per*(t+1) .. nbins - per*t - 1, highest first.
 __device__ __forceinline__ void find_bucket(const uint32_t* hist, int nbins, uint32_t want, uint32_t* red,
                                             uint32_t* out) {
-  const int per = nbins / kThreads;  // 4 or 2 bins per thread, highest bins to thread 0
+  const int per = nbins / kThreads;  // 16 or 1
   const int hi = nbins - per * static_cast<int>(threadIdx.x);
+  uint32_t c[16];
   uint32_t s = 0;
-  for (int j = 1; j <= per; ++j) s += hist[hi - j];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    c[j] = j < per ? hist[hslot(static_cast<uint32_t>(hi - 1 - j))] : 0u;
+    s += c[j];
+  }
   uint32_t tot;
   uint32_t run = block_excl_scan(s, red, &tot);
-  for (int j = 1; j <= per; ++j) {
-    const uint32_t c = hist[hi - j];
-    if (run < want && run + c >= want) {
-      out[0] = static_cast<uint32_t>(hi - j);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j < per && run < want && run + c[j] >= want) {
+      out[0] = static_cast<uint32_t>(hi - 1 - j);
       out[1] = run;
-      out[2] = c;
+      out[2] = c[j];
     }
-    run += c;
+    run += c[j];
   }
   __syncthreads();
 }
 
-struct RowSrc {
-  const float* p;
-  const uint32_t* cache;  // null when the row is not staged
-  long long n;
-};
-
-// Keys i..i+3 of the row (cnt valid, the rest unspecified).
-__device__ __forceinline__ int load4(const RowSrc& r, long long i, uint32_t (&u)[4]) {
-  const long long rem = r.n - i;
-  const int cnt = rem >= 4 ? 4 : (rem > 0 ? static_cast<int>(rem) : 0);
-  if (r.cache) {
-    if (cnt == 4) {
-      const uint4 v = *reinterpret_cast<const uint4*>(r.cache + i);
-      u[0] = v.x; u[1] = v.y; u[2] = v.z; u[3] = v.w;
-    } else {
-      for (int j = 0; j < cnt; ++j) u[j] = r.cache[i + j];
-    }
-  } else {
-    if (cnt == 4) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(r.p + i));
-      u[0] = order_key(f.x); u[1] = order_key(f.y); u[2] = order_key(f.z); u[3] = order_key(f.w);
-    } else {
-      for (int j = 0; j < cnt; ++j) u[j] = order_key(__ldg(r.p + i + j));
-    }
+// Four consecutive keys of the row starting at i (cnt of them valid, the rest 0).
+__device__ __forceinline__ int load4(const float* p, long long n, long long i, uint32_t (&u)[4]) {
+  const long long rem = n - i;
+  if (rem >= 4) {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(p + i));
+    u[0] = order_key(f.x); u[1] = order_key(f.y); u[2] = order_key(f.z); u[3] = order_key(f.w);
+    return 4;
   }
-  return cnt;
+  const int c = rem > 0 ? static_cast<int>(rem) : 0;
+  for (int j = 0; j < 4; ++j) u[j] = j < c ? order_key(__ldg(p + i + j)) : 0u;
+  return c;
 }
 
-// Stable LSD radix sort of n <= 4096 (key, value) pairs by key, descending.
-// Returns the buffer pair holding the result (a or b).
-__device__ uint32_t* radix_sort_desc(uint32_t* ka, uint32_t* va, uint32_t* kb, uint32_t* vb, int n, uint32_t* cnt,
-                                     uint32_t* red, uint32_t** vals_out) {
+// A row is split into kWarps contiguous segments, one per warp; a segment is read
+// in blocks of 128 keys (lane l holds keys 4l..4l+3 of the block), so the order
+// (segment, block, lane, element) is the key-index order.
+__device__ __forceinline__ long long seg_len(long long n) { return ((n + kWarps - 1) / kWarps + 127) & ~127LL; }
+
+// Segment read from global memory on every pass (any row length).
+struct GlobalSeg {
+  static constexpr int kMax = 1 << 28;
+  const float* p;
+  long long s0, s1;
+  int nb;
+  __device__ void init(const float* row, long long n) {
+    const long long seg = seg_len(n);
+    p = row;
+    s0 = (threadIdx.x >> 5) * seg;
+    s1 = min(n, s0 + seg);
+    nb = s1 > s0 ? static_cast<int>((s1 - s0 + 127) / 128) : 0;
+  }
+  __device__ __forceinline__ int quad(int j, uint32_t (&u)[4], long long& i) const {
+    i = s0 + 128LL * j + 4 * (threadIdx.x & 31);
+    if (i >= s1) { u[0] = u[1] = u[2] = u[3] = 0u; return 0; }
+    return load4(p, s1, i, u);
+  }
+};
+
+// Segment held in registers, loaded once with every load in flight (rows up to
+// kWarps * NB * 128 keys).  Call quad() only with compile-time j (unrolled loops).
+template <int NB>
+struct RegSeg {
+  static constexpr int kMax = NB;
+  uint32_t v[NB][4];
+  int c[NB];
+  long long s0;
+  int nb;
+  __device__ void init(const float* row, long long n) {
+    const long long seg = seg_len(n);
+    s0 = (threadIdx.x >> 5) * seg;
+    const long long s1 = min(n, s0 + seg);
+    nb = s1 > s0 ? static_cast<int>((s1 - s0 + 127) / 128) : 0;
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const long long i = s0 + 128LL * j + 4 * (threadIdx.x & 31);
+      c[j] = (j < nb && i < s1) ? load4(row, s1, i, v[j]) : 0;
+      if (c[j] == 0) v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0u;
+    }
+  }
+  __device__ __forceinline__ int quad(int j, uint32_t (&u)[4], long long& i) const {
+    i = s0 + 128LL * j + 4 * (threadIdx.x & 31);
+    u[0] = v[j][0]; u[1] = v[j][1]; u[2] = v[j][2]; u[3] = v[j][3];
+    return c[j];
+  }
+};
+
+// hist[(u >> shift) & mask] += 1 for every key of the row with (u >> pshift) == pre
+// (pshift = 32: every key).
+template <class RS>
+__device__ __forceinline__ void seg_hist(const RS& rs, uint32_t* hist, int shift, uint32_t mask, int pshift,
+                                         uint32_t pre) {
+#pragma unroll
+  for (int j = 0; j < RS::kMax; ++j) {
+    if (j >= rs.nb) break;
+    uint32_t u[4];
+    long long i;
+    const int c = rs.quad(j, u, i);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < c && (pshift >= 32 || (u[e] >> pshift) == pre)) atomicAdd(&hist[hslot((u[e] >> shift) & mask)], 1u);
+  }
+}
+
+// Order-preserving compaction: key u (index i) is kept iff
+//   u > T, or u == T and it is among the first `need` keys equal to T (index order),
+// and kept keys are written to (ck, ci) in index order.  Returns the number kept.
+template <class RS>
+__device__ uint32_t seg_compact(const RS& rs, uint32_t T, uint32_t need, uint32_t* ck, uint32_t* ci,
+                                uint32_t* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool ties = need != 0 && need != 0xFFFFFFFFu;
+  // pass 1: keys equal to T per warp (only when ties matter), then kept keys per warp
+  uint32_t eq_before = 0;
+  if (ties) {
+    uint32_t ce = 0;
+#pragma unroll
+    for (int j = 0; j < RS::kMax; ++j) {
+      if (j >= rs.nb) break;
+      uint32_t u[4];
+      long long i;
+      const int c = rs.quad(j, u, i);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ce += (e < c && u[e] == T) ? 1u : 0u;
+    }
+    ce = __reduce_add_sync(0xffffffffu, ce);
+    if (lane == 0) red[warp] = ce;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) eq_before += w < warp ? red[w] : 0u;
+    __syncthreads();
+  }
+  uint32_t kept = 0;
+  {
+    uint32_t run = eq_before;
+#pragma unroll
+    for (int j = 0; j < RS::kMax; ++j) {
+      if (j >= rs.nb) break;
+      uint32_t u[4];
+      long long i;
+      const int c = rs.quad(j, u, i);
+      uint32_t e4 = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) e4 += (e < c && u[e] == T) ? 1u : 0u;
+      const uint32_t ie = ties ? warp_incl_scan(e4) : e4;
+      uint32_t r = run + ie - e4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (e < c) {
+          if (u[e] > T) ++kept;
+          else if (u[e] == T) { kept += r < need ? 1u : 0u; ++r; }
+        }
+      }
+      if (ties) run += __shfl_sync(0xffffffffu, ie, 31);
+    }
+  }
+  kept = __reduce_add_sync(0xffffffffu, kept);
+  if (lane == 0) red[warp] = kept;
+  __syncthreads();
+  uint32_t base = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t r = red[w];
+    base += w < warp ? r : 0u;
+    total += r;
+  }
+  __syncthreads();
+  // pass 2: write
+  {
+    uint32_t run = eq_before;
+#pragma unroll
+    for (int j = 0; j < RS::kMax; ++j) {
+      if (j >= rs.nb) break;
+      uint32_t u[4];
+      long long i;
+      const int c = rs.quad(j, u, i);
+      uint32_t e4 = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) e4 += (e < c && u[e] == T) ? 1u : 0u;
+      const uint32_t ie = ties ? warp_incl_scan(e4) : e4;
+      uint32_t r = run + ie - e4;
+      uint32_t m = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (e < c) {
+          if (u[e] > T) m |= 1u << e;
+          else if (u[e] == T) { if (r < need) m |= 1u << e; ++r; }
+        }
+      }
+      const uint32_t k = __popc(m);
+      const uint32_t incl = warp_incl_scan(k);
+      uint32_t pos = base + incl - k;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if ((m >> e) & 1u) {
+          ck[pos] = u[e];
+          ci[pos] = static_cast<uint32_t>(i + e);
+          ++pos;
+        }
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+      if (ties) run += __shfl_sync(0xffffffffu, ie, 31);
+    }
+  }
+  __syncthreads();
+  return total;
+}
+
+// Stable LSD radix sort of n (key, value) pairs by key, descending.  Only the bits
+// below the highest bit in which the keys differ are sorted, kSortBits per pass (keys
+// of one row's candidates usually differ in their low ~25 bits: 3 passes).
+// n <= kWarps * 32 * kMaxRounds.  The sorted buffers come back in sk_out / sv_out.
+__device__ void radix_sort_desc(uint32_t* ka, uint32_t* va, uint32_t* kb, uint32_t* vb, int n, uint32_t* cnt,
+                                uint32_t* red, uint32_t** sk_out, uint32_t** sv_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // bits that differ between keys: digits that never change are skipped
   uint32_t diff = 0;
   if (n > 0) {
     const uint32_t k0 = ka[0];
     for (int i = tid; i < n; i += kThreads) diff |= ka[i] ^ k0;
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) diff |= __shfl_xor_sync(0xffffffffu, diff, o);
+  diff = __reduce_or_sync(0xffffffffu, diff);
   if (lane == 0) red[warp] = diff;
   __syncthreads();
   diff = 0;
+#pragma unroll
   for (int w = 0; w < kWarps; ++w) diff |= red[w];
   __syncthreads();
+  const int nbits = 32 - __clz(diff);  // 0 when all keys are equal
 
-  const int CH = (((n + kWarps - 1) / kWarps) + 31) & ~31;  // elements per warp, multiple of 32
-  const int rounds = CH / 32;                                // <= 8 for n <= 4096
+  const int CH = (((n + kWarps - 1) / kWarps) + 31) & ~31;  // keys per warp, multiple of 32
+  const int rounds = CH / 32;
   uint32_t *sk = ka, *sv = va, *dk = kb, *dv = vb;
-  for (int sh = 0; sh < 32; sh += 8) {
-    if (((diff >> sh) & 255u) == 0) continue;
-    for (int i = tid; i < kWarps * 256; i += kThreads) cnt[i] = 0;
+  for (int sh = 0; sh < nbits; sh += kSortBits) {
+    for (int i = tid; i < kWarps * kSortBins; i += kThreads) cnt[i] = 0;
     __syncthreads();
-    uint32_t offs[8], digs[8];
+    uint32_t offs[kMaxRounds];
+    uint32_t digs[kMaxRounds];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
+    for (int r = 0; r < kMaxRounds; ++r) {
+      const int e = warp * CH + r * 32 + lane;
+      digs[r] = (r < rounds && e < n) ? (kSortBins - 1) - ((sk[e] >> sh) & (kSortBins - 1)) : kSortBins;
+    }
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
       offs[r] = 0;
-      digs[r] = 256;
       if (r < rounds) {
-        const int e = warp * CH + r * 32 + lane;
-        const bool valid = e < n;
-        const uint32_t d = valid ? 255u - ((sk[e] >> sh) & 255u) : 256u;
+        const uint32_t d = digs[r];
+        const bool valid = d < kSortBins;
         const uint32_t peers = __match_any_sync(0xffffffffu, d);
         const uint32_t rank = __popc(peers & ((1u << lane) - 1u));
-        const uint32_t before = valid ? cnt[warp * 256 + d] : 0u;
+        const uint32_t before = valid ? cnt[warp * kSortBins + d] : 0u;
         __syncwarp();
-        if (valid && rank == 0) cnt[warp * 256 + d] = before + __popc(peers);
+        if (valid && rank == 0) cnt[warp * kSortBins + d] = before + __popc(peers);
         __syncwarp();
         offs[r] = before + rank;
-        digs[r] = d;
       }
     }
     __syncthreads();
     {
-      // exclusive scan in (digit, warp) order: thread t owns digit t/2, warps (t&1)*8 .. +7
-      const int d = tid >> 1, w0 = (tid & 1) * 8;
-      uint32_t v[8], s = 0;
+      // exclusive scan in (digit, warp) order: thread t owns digits 2t and 2t+1 for all warps
+      uint32_t v[2][kWarps], s = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) { v[j] = cnt[(w0 + j) * 256 + d]; s += v[j]; }
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) { v[q][w] = cnt[w * kSortBins + 2 * tid + q]; s += v[q][w]; }
       uint32_t tot;
       uint32_t ex = block_excl_scan(s, red, &tot);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) { cnt[(w0 + j) * 256 + d] = ex; ex += v[j]; }
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) { cnt[w * kSortBins + 2 * tid + q] = ex; ex += v[q][w]; }
     }
     __syncthreads();
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
+    for (int r = 0; r < kMaxRounds; ++r) {
       if (r < rounds) {
         const int e = warp * CH + r * 32 + lane;
         if (e < n) {
-          const uint32_t dest = cnt[warp * 256 + digs[r]] + offs[r];
+          const uint32_t dest = cnt[warp * kSortBins + digs[r]] + offs[r];
           dk[dest] = sk[e];
           dv[dest] = sv[e];
         }
@@ -188,19 +375,132 @@ __device__ uint32_t* radix_sort_desc(uint32_t* ka, uint32_t* va, uint32_t* kb, u
     t = sk; sk = dk; dk = t;
     t = sv; sv = dv; dv = t;
   }
-  *vals_out = sv;
-  return sk;
+  *sk_out = sk;
+  *sv_out = sv;
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int cache_cap, int ksel_cap) {
+// Score order by buckets: the candidates' keys usually span a narrow range, so one
+// counting pass over at most 4096 equal-width buckets between their minimum and
+// maximum leaves a few keys per bucket; each key's final slot is its bucket's start
+// plus the number of bucket-mates that beat it (higher key, or equal key and lower
+// index).  Writes out[slot] = index for slots < keep.  Returns false (writing
+// nothing) when some bucket holds more than kBucketLimit keys -- many equal or
+// clustered scores -- so the caller sorts with the radix sort instead.
+constexpr int kBucketLimit = 64;
+constexpr int kSortBuckets = 4096;
+
+__device__ bool bucket_rank_out(const uint32_t* ck, const uint32_t* ci, int n, int keep, uint32_t* bk,
+                                uint32_t* bi, uint32_t* cur, uint32_t* red, int32_t* out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  for (int i = tid; i < n; i += kThreads) {
+    const uint32_t u = ck[i];
+    lo = min(lo, u);
+    hi = max(hi, u);
+  }
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) {
+    red[warp] = lo;
+    red[kWarps + warp] = hi;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    lo = min(lo, red[w]);
+    hi = max(hi, red[kWarps + w]);
+  }
+  int sh = 0;
+  while (((hi >> sh) - (lo >> sh)) >= static_cast<uint32_t>(kSortBuckets)) ++sh;
+  const uint32_t base = lo >> sh;
+  const int nb = static_cast<int>((hi >> sh) - base) + 1;
+  for (int b = tid; b < nb; b += kThreads) cur[hslot(b)] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += kThreads) atomicAdd(&cur[hslot((ck[i] >> sh) - base)], 1u);
+  __syncthreads();
+  // descending exclusive scan: start[b] = keys in buckets above b; thread t owns 16 bins
+  uint32_t c[16], sum = 0, mx = 0;
+  const int b_hi = nb - 16 * tid;  // bins b_hi-1 .. b_hi-16, highest first
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int b = b_hi - 1 - j;
+    c[j] = b >= 0 ? cur[hslot(b)] : 0u;
+    sum += c[j];
+    mx = max(mx, c[j]);
+  }
+  uint32_t tot;
+  uint32_t run = block_excl_scan(sum, red, &tot);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  mx = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) mx = max(mx, red[w]);
+  __syncthreads();  // red is free again before any caller reuses it
+  if (mx > static_cast<uint32_t>(kBucketLimit)) return false;  // uniform across the block
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int b = b_hi - 1 - j;
+    if (b >= 0) cur[hslot(b)] = run;
+    run += c[j];
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += kThreads) {
+    const uint32_t u = ck[i];
+    const uint32_t pos = atomicAdd(&cur[hslot((u >> sh) - base)], 1u);
+    bk[pos] = u;
+    bi[pos] = ci[i];
+  }
+  __syncthreads();
+  // cur[b] is now the end of bucket b; bucket b starts where bucket b + 1 ends
+  for (int p = tid; p < n; p += kThreads) {
+    const uint32_t u = bk[p], idx = bi[p];
+    const int b = static_cast<int>((u >> sh) - base);
+    const uint32_t q0 = b + 1 < nb ? cur[hslot(b + 1)] : 0u, q1 = cur[hslot(b)];
+    uint32_t rank = q0;
+    for (uint32_t q = q0; q < q1; ++q) {
+      const uint32_t v = bk[q];
+      rank += (v > u || (v == u && bi[q] < idx)) ? 1u : 0u;
+    }
+    if (rank < static_cast<uint32_t>(keep)) out[rank] = static_cast<int32_t>(idx);
+  }
+  return true;
+}
+
+// Exact threshold among the keys of 12-bit bucket d1, of which `want` are still to
+// be taken: two histogram passes (the next 12 bits, then the last 8) over the keys
+// that `feed(hist, shift, mask, pshift, pre)` counts.  T = the threshold key,
+// need = how many keys equal to T to take (lowest index first).
+template <class Feed>
+__device__ void refine_threshold(Feed feed, uint32_t d1, uint32_t want, uint32_t* hist, uint32_t* red,
+                                 uint32_t* info, uint32_t* T_out, uint32_t* need_out) {
+  for (int i = threadIdx.x; i < kHistWords; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  feed(hist, 8, 4095u, 20, d1);
+  __syncthreads();
+  find_bucket(hist, kBins, want, red, info);
+  const uint32_t d2 = info[0];
+  want -= info[1];
+  const uint32_t pre = (d1 << 12) | d2;  // top 24 bits of the threshold
+  for (int i = threadIdx.x; i < kHistWords; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  feed(hist, 0, 255u, 8, pre);
+  __syncthreads();
+  find_bucket(hist, 256, want, red, info);
+  *T_out = (pre << 8) | info[0];
+  *need_out = want - info[1];
+}
+
+template <int NB>  // NB > 0: rows up to kWarps * NB * 128 keys held in registers; 0: any length
+__global__ void __launch_bounds__(kThreads, 3) topk_kernel(const TopkArgs a, int cand_cap) {
   extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ uint32_t red[32];
-  __shared__ uint32_t sel_info[4];
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);  // 16 KB: histogram / sort counters
-  const int regionB = cache_cap > 2 * ksel_cap ? cache_cap : 2 * ksel_cap;
-  uint32_t* cache = hist + kWarps * 256;                 // row cache, later sort scratch
-  uint32_t* selk = cache + regionB;
-  uint32_t* seli = selk + ksel_cap;
+  __shared__ uint32_t red[2 * kWarps];
+  __shared__ uint32_t info[4];
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);  // kHistWords counters, later sort counters
+  uint32_t* ck = hist + kHistWords;                          // candidates: keys, indices, sort scratch
+  uint32_t* ci = ck + cand_cap;
+  uint32_t* tk = ci + cand_cap;
+  uint32_t* ti = tk + cand_cap;
   const int tid = threadIdx.x;
 
   // ---- which row, how many visible keys
@@ -235,120 +535,99 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int ca
   const int keep = static_cast<int>(keep_ll);
   for (int i = keep + tid; i < a.k_out; i += kThreads) out[i] = -1;
   if (keep == 0) return;
-
-  RowSrc rs{src, nullptr, n};
-  uint32_t T = 0;          // threshold key
-  uint32_t need = 0;       // keys equal to T to keep (lowest indices first)
-  if (n <= keep) {
-    need = static_cast<uint32_t>(n);  // every key is kept
-  } else {
-    const bool cached = n <= cache_cap;
-    // ---- pass 1: top 11 bits over the whole row (and stage the row)
-    for (int i = tid; i < 2048; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    for (long long base = 0; base < n; base += kChunk) {
-      const long long i = base + 4 * tid;
-      uint32_t u[4] = {0u, 0u, 0u, 0u};
-      const int c = load4(rs, i, u);
-      if (cached) {
-        if (c == 4) *reinterpret_cast<uint4*>(cache + i) = make_uint4(u[0], u[1], u[2], u[3]);
-        else for (int j = 0; j < c; ++j) cache[i + j] = u[j];
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) hist_add(hist, j < c, u[j] >> 21);
-    }
-    __syncthreads();
-    if (cached) rs.cache = cache;
-    uint32_t want = static_cast<uint32_t>(keep);
-    find_bucket(hist, 2048, want, red, sel_info);
-    const uint32_t d1 = sel_info[0];
-    uint32_t above = sel_info[1];
-    if (sel_info[2] == want - above) {
-      T = (d1 << 21) - 1u;  // the whole bucket is kept: select keys >= d1 << 21
-      need = 0;
-    } else {
-      // ---- pass 2: bits 10..20 inside bucket d1
-      want -= above;
-      uint32_t above_total = above;
-      for (int i = tid; i < 2048; i += kThreads) hist[i] = 0;
-      __syncthreads();
-      for (long long base = 0; base < n; base += kChunk) {
-        uint32_t u[4] = {0u, 0u, 0u, 0u};
-        const int c = load4(rs, base + 4 * tid, u);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) hist_add(hist, j < c && (u[j] >> 21) == d1, (u[j] >> 10) & 2047u);
-      }
-      __syncthreads();
-      find_bucket(hist, 2048, want, red, sel_info);
-      const uint32_t d2 = sel_info[0];
-      above = sel_info[1];
-      const uint32_t pre2 = (d1 << 11) | d2;
-      if (sel_info[2] == want - above) {
-        T = (pre2 << 10) - 1u;
-        need = 0;
-      } else {
-        // ---- pass 3: bits 0..9 inside bucket (d1, d2)
-        want -= above;
-        above_total += above;
-        for (int i = tid; i < 1024; i += kThreads) hist[i] = 0;
-        __syncthreads();
-        for (long long base = 0; base < n; base += kChunk) {
-          uint32_t u[4] = {0u, 0u, 0u, 0u};
-          const int c = load4(rs, base + 4 * tid, u);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) hist_add(hist, j < c && (u[j] >> 10) == pre2, u[j] & 1023u);
-        }
-        __syncthreads();
-        find_bucket(hist, 1024, want, red, sel_info);
-        T = (pre2 << 10) | sel_info[0];
-        need = want - sel_info[1];
-      }
-      (void)above_total;
-    }
-  }
-
-  // ---- ordered compaction: keys > T, then the first `need` keys == T, in index order
   const bool by_score = a.order == 0;
-  uint32_t g_run = 0, e_run = 0;  // keys > T and == T seen in earlier chunks
-  const bool take_all = n <= keep;
-  for (long long base = 0; base < n; base += kChunk) {
-    const long long i = base + 4 * tid;
-    uint32_t u[4] = {0u, 0u, 0u, 0u};
-    const int c = load4(rs, i, u);
-    uint32_t cg = 0, ce = 0;
-    for (int j = 0; j < c; ++j) {
-      if (take_all || u[j] > T) ++cg;
-      else if (u[j] == T) ++ce;
-    }
-    uint32_t tot;
-    const uint32_t pre = block_excl_scan((cg << 16) | ce, red, &tot);
-    uint32_t g = g_run + (pre >> 16), e = e_run + (pre & 0xFFFFu);
-    for (int j = 0; j < c; ++j) {
-      int pos = -1;
-      if (take_all || u[j] > T) {
-        pos = static_cast<int>(g + (e < need ? e : need));
-        ++g;
-      } else if (u[j] == T) {
-        if (e < need) pos = static_cast<int>(g + e);
-        ++e;
+
+  using RS = typename std::conditional<NB == 0, GlobalSeg, RegSeg<(NB > 0 ? NB : 1)>>::type;
+  RS rs;
+  rs.init(src, n);
+  auto feed_row = [&](uint32_t* h, int shift, uint32_t mask, int pshift, uint32_t pre) {
+    seg_hist(rs, h, shift, mask, pshift, pre);
+  };
+
+  uint32_t n_cand;
+  uint32_t T = 0, need = 0xFFFFFFFFu;  // kept: key > T, or == T among the first `need`
+  bool exact = true;                   // the candidates are exactly the kept keys
+  if (n <= keep) {
+    n_cand = seg_compact(rs, 0u, 0xFFFFFFFFu, ck, ci, red);  // every key
+  } else {
+    for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    seg_hist(rs, hist, 20, 4095u, 32, 0u);
+    __syncthreads();
+    find_bucket(hist, kBins, static_cast<uint32_t>(keep), red, info);
+    const uint32_t d1 = info[0], above = info[1], in_b = info[2];
+    const uint32_t want = static_cast<uint32_t>(keep) - above;
+    if (in_b == want) {
+      T = (d1 << 20) - 1u;  // the whole threshold bucket is kept
+      need = 0;
+      n_cand = seg_compact(rs, T, need, ck, ci, red);
+    } else if (above + in_b <= static_cast<uint32_t>(cand_cap)) {
+      // fast path: every key of buckets >= d1, in index order
+      n_cand = seg_compact(rs, (d1 << 20) - 1u, 0u, ck, ci, red);
+      exact = false;
+      if (!by_score) {
+        const uint32_t nc = n_cand;
+        auto feed_cand = [&](uint32_t* h, int shift, uint32_t mask, int pshift, uint32_t pre) {
+          for (uint32_t i = tid; i < nc; i += kThreads) {
+            const uint32_t u = ck[i];
+            if ((u >> pshift) == pre) atomicAdd(&h[hslot((u >> shift) & mask)], 1u);
+          }
+        };
+        refine_threshold(feed_cand, d1, want, hist, red, info, &T, &need);
       }
-      if (pos >= 0) {
-        if (by_score) {
-          selk[pos] = u[j];
-          seli[pos] = static_cast<uint32_t>(i + j);
-        } else {
-          out[pos] = static_cast<int32_t>(i + j);
-        }
-      }
+    } else {
+      // slow path (huge threshold bucket): exact threshold over the row, exactly `keep` keys
+      refine_threshold(feed_row, d1, want, hist, red, info, &T, &need);
+      n_cand = seg_compact(rs, T, need, ck, ci, red);
     }
-    g_run += tot >> 16;
-    e_run += tot & 0xFFFFu;
   }
-  if (!by_score) return;
-  __syncthreads();
-  uint32_t* vals;
-  radix_sort_desc(selk, seli, cache, cache + ksel_cap, keep, hist, red, &vals);
-  for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(vals[i]);
+
+  if (by_score) {
+    if (bucket_rank_out(ck, ci, static_cast<int>(n_cand), keep, tk, ti, hist, red, out)) return;
+    uint32_t *sk, *sv;
+    radix_sort_desc(ck, ci, tk, ti, static_cast<int>(n_cand), hist, red, &sk, &sv);
+    for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(sv[i]);
+    return;
+  }
+  if (exact) {  // candidates are the kept keys, already in index order
+    for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(ci[i]);
+    return;
+  }
+  // index order from the fast-path candidates: keep key > T and the first `need` == T
+  {
+    const int lane = tid & 31, warp = tid >> 5;
+    const uint32_t per = ((n_cand + kWarps - 1) / kWarps + 31) & ~31u;
+    const uint32_t c0 = warp * per, c1 = min(n_cand, c0 + per);
+    uint32_t cgt = 0, ceq = 0;
+    for (uint32_t i = c0 + lane; i < c1; i += 32) {
+      cgt += ck[i] > T ? 1u : 0u;
+      ceq += ck[i] == T ? 1u : 0u;
+    }
+    cgt = __reduce_add_sync(0xffffffffu, cgt);
+    ceq = __reduce_add_sync(0xffffffffu, ceq);
+    if (lane == 0) red[warp] = cgt;
+    __syncthreads();
+    uint32_t gbase = 0;
+    for (int w = 0; w < warp; ++w) gbase += red[w];
+    __syncthreads();
+    if (lane == 0) red[warp] = ceq;
+    __syncthreads();
+    uint32_t ebase = 0;
+    for (int w = 0; w < warp; ++w) ebase += red[w];
+    for (uint32_t i0 = c0; i0 < c1; i0 += 32) {
+      const uint32_t i = i0 + lane;
+      const bool valid = i < c1;
+      const uint32_t u = valid ? ck[i] : 0u;
+      const bool gt = valid && u > T, eq = valid && u == T;
+      const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+      const uint32_t lt = (1u << lane) - 1u;
+      const uint32_t g = gbase + __popc(bg & lt), e = ebase + __popc(be & lt);
+      if (gt) out[g + (e < need ? e : need)] = static_cast<int32_t>(ci[i]);
+      else if (eq && e < need) out[g + e] = static_cast<int32_t>(ci[i]);
+      gbase += __popc(bg);
+      ebase += __popc(be);
+    }
+  }
 }
 
 }  // namespace
@@ -358,15 +637,22 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
   int keep_cap = a.k_out < a.topk_limit ? a.k_out : a.topk_limit;
   if (keep_cap > max_row_len) keep_cap = max_row_len;
   if (keep_cap < 1) keep_cap = 1;
-  const int ksel_cap = (keep_cap + 3) & ~3;
-  const int cache_cap = max_row_len <= 16384 ? ((max_row_len + 3) & ~3) : 0;
-  const int regionB = cache_cap > 2 * ksel_cap ? cache_cap : 2 * ksel_cap;
-  const size_t smem = (static_cast<size_t>(kWarps) * 256 + regionB + 2 * ksel_cap) * 4;
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  topk_kernel<<<a.n_rows, kThreads, smem, st>>>(a, cache_cap, ksel_cap);
-  return cudaGetLastError();
+  // room for the kept keys plus a threshold bucket of up to max(512, keep/4) keys
+  int cap = keep_cap + (keep_cap / 4 > 512 ? keep_cap / 4 : 512);
+  const int max_cap = kWarps * 32 * kMaxRounds;
+  if (cap > max_cap) cap = max_cap;
+  if (cap < keep_cap) return cudaErrorInvalidValue;
+  cap = (cap + 31) & ~31;
+  const size_t smem = (static_cast<size_t>(kHistWords) + 4 * static_cast<size_t>(cap)) * 4;
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<a.n_rows, kThreads, smem, st>>>(a, cap);
+    return cudaGetLastError();
+  };
+  if (max_row_len <= kWarps * 8 * 128) return go(topk_kernel<8>);
+  if (max_row_len <= kWarps * 16 * 128) return go(topk_kernel<16>);
+  return go(topk_kernel<0>);
 }
 
 }  // namespace dsa
