@@ -233,6 +233,117 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 h2d=h2d, d2h=d2h, status=status, case=case, e2e_steps=e2e_steps)
 
 
+
+# ----------------------------------------------------------------------------- other workloads
+# Measured after the headline (same process, same GPU); inputs generated on the device
+# with a seeded generator where they are large.
+
+def _time_events(fn, iters, stream):
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def _paged_on_device(B, lens, q_len, H, D, page, q_fp8, k_fp8, seed, dev):
+    """Seeded device-side paged case: N(0,1) keys (e4m3 with per-token amax/448 scales when
+    k_fp8), q N(0,1) (e4m3 per (t,h) when q_fp8), w N(0,1)/8, pages in a random permutation."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    lens = [int(x) for x in lens]
+    pages = [(L + page - 1) // page for L in lens]
+    num_pages = sum(pages) + 1
+    perm = torch.randperm(num_pages, generator=g, device=dev).to(torch.int32)
+    mp = max(pages)
+    bt = torch.full((B, mp), -1, dtype=torch.int32, device=dev)
+    cur = 0
+    for b, npg in enumerate(pages):
+        bt[b, :npg] = perm[cur:cur + npg]
+        cur += npg
+    total_q = q_len * B
+    kf = torch.randn((num_pages, page, D), generator=g, device=dev, dtype=torch.float32)
+    qf = torch.randn((total_q, H, D), generator=g, device=dev, dtype=torch.float32)
+    w = torch.randn((total_q, H), generator=g, device=dev, dtype=torch.float32) / 8.0
+
+    def quant(x):
+        amax = x.abs().amax(dim=-1, keepdim=True)
+        sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+        return (x / sc).to(torch.float8_e4m3fn), sc.squeeze(-1).contiguous()
+
+    k_cache, k_scale = quant(kf) if k_fp8 else (kf.to(torch.bfloat16), None)
+    q, q_scale = quant(qf) if q_fp8 else (qf.to(torch.bfloat16), None)
+    del kf, qf
+    cu = torch.arange(0, total_q + 1, q_len, dtype=torch.int32, device=dev)
+    seq = torch.tensor(lens, dtype=torch.int32, device=dev)
+    return dict(q=q, q_scale=q_scale, w=w, k_cache=k_cache, k_scale_cache=k_scale, cu_q_lens=cu, seq_lens=seq,
+                block_tables=bt, max_seq_len=max(lens))
+
+
+def run_other_workloads(dev, stream, peaks):
+    import sparse_attention_token_gb300 as dsa
+    out = {}
+    bf16_peak = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
+    # chunked prefill: 8192 queries at 57344..65535 vs 65536 keys, e4m3 q and k
+    c = _paged_on_device(1, [65536], 8192, 64, 128, 64, True, True, 4, dev)
+    args, keep = dsa.make_indexer_args(c["q"], c["w"], c["k_cache"], c["cu_q_lens"], c["seq_lens"],
+                                       c["block_tables"], max_seq_len=c["max_seq_len"], topk_limit=2048,
+                                       q_scale=c["q_scale"], k_scale_cache=c["k_scale_cache"])
+    L = dsa.lib()
+    import ctypes
+    call = lambda: L.dsa_indexer(ctypes.byref(args), stream.cuda_stream)
+    ms = _time_events(call, 3, stream)
+    pairs = sum(57344 + i + 1 for i in range(8192))
+    flops = 2 * 64 * 128 * pairs
+    out["chunked_prefill_fp8"] = {
+        "workload": "8192 queries at 57344..65535 vs a 65536-key paged cache (page 64), e4m3 q/k with fp32 scales, "
+                    "H=64, D=128, index_topk=2048",
+        "ms_per_step": ms, "scores_per_s": pairs / (ms / 1e3), "topk_rows_per_s": 8192 / (ms / 1e3),
+        "tc_frac_step": flops / (ms / 1e3) / 1e12 / (2 * bf16_peak),
+        "peak": f"e4m3 dense = 2 x measured bf16 ({2 * bf16_peak:.0f} TFLOP/s, nominal ratio)"}
+    del c, args, keep
+    torch.cuda.empty_cache()
+    # IndexShare: 12 layers [full, shared, shared] x 4, decode B=32 at 32768 keys, bf16 caches
+    types = ["full", "shared", "shared"] * 4
+    fulls, keeps = [], []
+    for li in range(4):
+        c = _paged_on_device(32, [32768] * 32, 1, 64, 128, 64, False, False, 100 + li, dev)
+        a, k2 = dsa.make_indexer_args(c["q"], c["w"], c["k_cache"], c["cu_q_lens"], c["seq_lens"],
+                                      c["block_tables"], max_seq_len=c["max_seq_len"], topk_limit=2048)
+        fulls.append(a)
+        keeps.append((c, k2))
+    layer_args = []
+    fi = 0
+    for t in types:
+        if t == "full":
+            layer_args.append(fulls[fi])
+            fi += 1
+        else:
+            layer_args.append(None)
+    stack_ms = _time_events(lambda: dsa.dsa_indexer_stack(types, layer_args, stream=stream), 5, stream)
+    allfull_ms = _time_events(lambda: [L.dsa_indexer(ctypes.byref(fulls[i % 4]), stream.cuda_stream)
+                                       for i in range(12)], 5, stream)
+    keys = 32 * 32768
+    bytes_full = keys * 128 * 2 + 32 * 64 * 128 * 2 + 32 * 64 * 4 * 2 + 32 * 2048 * 4
+    out["indexshare_stack"] = {
+        "workload": "12 layers [full, shared, shared] x 4, decode B=32 at 32768 keys, bf16 paged caches "
+                    "(one per full layer), H=64, D=128, index_topk=2048",
+        "ms_stack": stack_ms, "ms_all_full": allfull_ms, "speedup_vs_all_full": allfull_ms / stack_ms,
+        "full_layer_ms": stack_ms / 4,
+        "hbm_gbs_full_layers": 4 * bytes_full / (stack_ms / 1e3) / 1e9,
+        "hbm_frac_full_layers": 4 * bytes_full / (stack_ms / 1e3) / 1e9 / hbm,
+        "bytes_per_full_layer": bytes_full}
+    del keeps, fulls, layer_args
+    torch.cuda.empty_cache()
+    return out
+
+
 def cpu_sample_rows(n_rows: int):
     """Stratified sample of query rows (positions spread over the sequence, first and last included)."""
     if n_rows >= T:
@@ -305,6 +416,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -355,6 +467,9 @@ def main():
             "clocks": r["clocks"],
             "device_status": r["status"],
         }
+        if not args.no_extra:
+            line["workloads"] = run_other_workloads(torch.device("cuda", local_rank),
+                                                    torch.cuda.current_stream(), peaks)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(r["case"])
         print(json.dumps(line), flush=True)
