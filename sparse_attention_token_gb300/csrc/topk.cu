@@ -125,9 +125,11 @@ __device__ __forceinline__ int load4(const float* p, long long n, long long i, u
 // (segment, block, lane, element) is the key-index order.
 __device__ __forceinline__ long long seg_len(long long n) { return ((n + kWarps - 1) / kWarps + 127) & ~127LL; }
 
-// Segment read from global memory on every pass (any row length).
+// Segment read from global memory on every pass (any row length).  visit() walks the
+// segment in batches of kBatch blocks whose loads are all issued before any is used,
+// so a pass over a long row costs a few memory latencies, not one per block.
 struct GlobalSeg {
-  static constexpr int kMax = 1 << 28;
+  static constexpr int kBatch = 16;
   const float* p;
   long long s0, s1;
   int nb;
@@ -138,18 +140,30 @@ struct GlobalSeg {
     s1 = min(n, s0 + seg);
     nb = s1 > s0 ? static_cast<int>((s1 - s0 + 127) / 128) : 0;
   }
-  __device__ __forceinline__ int quad(int j, uint32_t (&u)[4], long long& i) const {
-    i = s0 + 128LL * j + 4 * (threadIdx.x & 31);
-    if (i >= s1) { u[0] = u[1] = u[2] = u[3] = 0u; return 0; }
-    return load4(p, s1, i, u);
+  // f(u[4], first index, valid count) for every block of this lane, in index order.
+  template <class F>
+  __device__ __forceinline__ void visit(F f) const {
+    const int lane = threadIdx.x & 31;
+    for (int j0 = 0; j0 < nb; j0 += kBatch) {
+      uint32_t u[kBatch][4];
+      int c[kBatch];
+#pragma unroll
+      for (int jj = 0; jj < kBatch; ++jj) {
+        const long long i = s0 + 128LL * (j0 + jj) + 4 * lane;
+        c[jj] = (j0 + jj < nb && i < s1) ? load4(p, s1, i, u[jj]) : 0;
+      }
+#pragma unroll
+      for (int jj = 0; jj < kBatch; ++jj) {
+        if (j0 + jj < nb) f(u[jj], s0 + 128LL * (j0 + jj) + 4 * lane, c[jj]);
+      }
+    }
   }
 };
 
 // Segment held in registers, loaded once with every load in flight (rows up to
-// kWarps * NB * 128 keys).  Call quad() only with compile-time j (unrolled loops).
+// kWarps * NB * 128 keys).
 template <int NB>
 struct RegSeg {
-  static constexpr int kMax = NB;
   uint32_t v[NB][4];
   int c[NB];
   long long s0;
@@ -166,10 +180,16 @@ struct RegSeg {
       if (c[j] == 0) v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0u;
     }
   }
-  __device__ __forceinline__ int quad(int j, uint32_t (&u)[4], long long& i) const {
-    i = s0 + 128LL * j + 4 * (threadIdx.x & 31);
-    u[0] = v[j][0]; u[1] = v[j][1]; u[2] = v[j][2]; u[3] = v[j][3];
-    return c[j];
+  template <class F>
+  __device__ __forceinline__ void visit(F f) const {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      if (j < nb) {
+        uint32_t u[4] = {v[j][0], v[j][1], v[j][2], v[j][3]};
+        f(u, s0 + 128LL * j + 4 * lane, c[j]);
+      }
+    }
   }
 };
 
@@ -178,16 +198,11 @@ struct RegSeg {
 template <class RS>
 __device__ __forceinline__ void seg_hist(const RS& rs, uint32_t* hist, int shift, uint32_t mask, int pshift,
                                          uint32_t pre) {
-#pragma unroll
-  for (int j = 0; j < RS::kMax; ++j) {
-    if (j >= rs.nb) break;
-    uint32_t u[4];
-    long long i;
-    const int c = rs.quad(j, u, i);
+  rs.visit([&](const uint32_t (&u)[4], long long, int c) {
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       if (e < c && (pshift >= 32 || (u[e] >> pshift) == pre)) atomicAdd(&hist[hslot((u[e] >> shift) & mask)], 1u);
-  }
+  });
 }
 
 // Order-preserving compaction: key u (index i) is kept iff
@@ -198,19 +213,13 @@ __device__ uint32_t seg_compact(const RS& rs, uint32_t T, uint32_t need, uint32_
                                 uint32_t* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool ties = need != 0 && need != 0xFFFFFFFFu;
-  // pass 1: keys equal to T per warp (only when ties matter), then kept keys per warp
   uint32_t eq_before = 0;
   if (ties) {
     uint32_t ce = 0;
-#pragma unroll
-    for (int j = 0; j < RS::kMax; ++j) {
-      if (j >= rs.nb) break;
-      uint32_t u[4];
-      long long i;
-      const int c = rs.quad(j, u, i);
+    rs.visit([&](const uint32_t (&u)[4], long long, int c) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) ce += (e < c && u[e] == T) ? 1u : 0u;
-    }
+    });
     ce = __reduce_add_sync(0xffffffffu, ce);
     if (lane == 0) red[warp] = ce;
     __syncthreads();
@@ -218,15 +227,11 @@ __device__ uint32_t seg_compact(const RS& rs, uint32_t T, uint32_t need, uint32_
     for (int w = 0; w < kWarps; ++w) eq_before += w < warp ? red[w] : 0u;
     __syncthreads();
   }
+  // pass 1: kept keys per warp
   uint32_t kept = 0;
   {
     uint32_t run = eq_before;
-#pragma unroll
-    for (int j = 0; j < RS::kMax; ++j) {
-      if (j >= rs.nb) break;
-      uint32_t u[4];
-      long long i;
-      const int c = rs.quad(j, u, i);
+    rs.visit([&](const uint32_t (&u)[4], long long, int c) {
       uint32_t e4 = 0;
 #pragma unroll
       for (int e = 0; e < 4; ++e) e4 += (e < c && u[e] == T) ? 1u : 0u;
@@ -240,7 +245,7 @@ __device__ uint32_t seg_compact(const RS& rs, uint32_t T, uint32_t need, uint32_
         }
       }
       if (ties) run += __shfl_sync(0xffffffffu, ie, 31);
-    }
+    });
   }
   kept = __reduce_add_sync(0xffffffffu, kept);
   if (lane == 0) red[warp] = kept;
@@ -256,12 +261,7 @@ __device__ uint32_t seg_compact(const RS& rs, uint32_t T, uint32_t need, uint32_
   // pass 2: write
   {
     uint32_t run = eq_before;
-#pragma unroll
-    for (int j = 0; j < RS::kMax; ++j) {
-      if (j >= rs.nb) break;
-      uint32_t u[4];
-      long long i;
-      const int c = rs.quad(j, u, i);
+    rs.visit([&](const uint32_t (&u)[4], long long i, int c) {
       uint32_t e4 = 0;
 #pragma unroll
       for (int e = 0; e < 4; ++e) e4 += (e < c && u[e] == T) ? 1u : 0u;
@@ -288,7 +288,7 @@ __device__ uint32_t seg_compact(const RS& rs, uint32_t T, uint32_t need, uint32_
       }
       base += __shfl_sync(0xffffffffu, incl, 31);
       if (ties) run += __shfl_sync(0xffffffffu, ie, 31);
-    }
+    });
   }
   __syncthreads();
   return total;
@@ -491,31 +491,45 @@ __device__ void refine_threshold(Feed feed, uint32_t d1, uint32_t want, uint32_t
   *need_out = want - info[1];
 }
 
-template <int NB>  // NB > 0: rows up to kWarps * NB * 128 keys held in registers; 0: any length
-__global__ void __launch_bounds__(kThreads, 3) topk_kernel(const TopkArgs a, int cand_cap) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ uint32_t red[2 * kWarps];
-  __shared__ uint32_t info[4];
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);  // kHistWords counters, later sort counters
-  uint32_t* ck = hist + kHistWords;                          // candidates: keys, indices, sort scratch
-  uint32_t* ci = ck + cand_cap;
-  uint32_t* tk = ci + cand_cap;
-  uint32_t* ti = tk + cand_cap;
-  const int tid = threadIdx.x;
+// Shared-memory layout of every top-k kernel (dynamic part).
+struct TopkSmem {
+  uint32_t* hist;   // kHistWords counters, later sort counters
+  uint32_t* ck;     // candidates: keys
+  uint32_t* ci;     //             indices
+  uint32_t* tk;     // sort scratch
+  uint32_t* ti;
+  uint32_t* merged; // cluster kernel: the row's merged histogram
+};
 
-  // ---- which row, how many visible keys
+__device__ __forceinline__ TopkSmem topk_smem(uint8_t* smem, int cand_cap) {
+  TopkSmem m;
+  m.hist = reinterpret_cast<uint32_t*>(smem);
+  m.ck = m.hist + kHistWords;
+  m.ci = m.ck + cand_cap;
+  m.tk = m.ci + cand_cap;
+  m.ti = m.tk + cand_cap;
+  m.merged = m.ti + cand_cap;
+  return m;
+}
+
+struct RowInfo {
   long long n;
   const float* src;
   int32_t* out;
+  int keep;
+};
+
+__device__ __forceinline__ RowInfo row_info(const TopkArgs& a, int r_local) {
+  RowInfo R;
   if (!a.paged) {
-    const int t = blockIdx.x;
+    const int t = r_local;
     long long v = static_cast<long long>(a.q_pos0) + t + 1;
     if (v > a.S) v = a.S;
-    n = v > 0 ? v : 0;
-    src = a.scores + static_cast<long long>(t) * a.ld;
-    out = a.topk + static_cast<long long>(t) * a.k_out;
+    R.n = v > 0 ? v : 0;
+    R.src = a.scores + static_cast<long long>(t) * a.ld;
+    R.out = a.topk + static_cast<long long>(t) * a.k_out;
   } else {
-    const int r = a.row_base + blockIdx.x;
+    const int r = a.row_base + r_local;
     int lo = 0, hi = a.B;  // last b with cu_q_lens[b] <= r
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -524,110 +538,347 @@ __global__ void __launch_bounds__(kThreads, 3) topk_kernel(const TopkArgs a, int
     const int b = lo;
     const int q_len = a.cu_q_lens[b + 1] - a.cu_q_lens[b];
     const long long pos = static_cast<long long>(a.seq_lens[b]) - q_len + (r - a.cu_q_lens[b]);
-    n = pos + 1 > 0 ? pos + 1 : 0;
-    src = a.scores + static_cast<long long>(blockIdx.x) * a.ld;
-    out = a.topk + static_cast<long long>(r) * a.k_out;
+    R.n = pos + 1 > 0 ? pos + 1 : 0;
+    R.src = a.scores + static_cast<long long>(r_local) * a.ld;
+    R.out = a.topk + static_cast<long long>(r) * a.k_out;
   }
-  if (n > a.max_n) n = a.max_n;
-  long long keep_ll = n;
+  if (R.n > a.max_n) R.n = a.max_n;
+  long long keep_ll = R.n;
   if (keep_ll > a.topk_limit) keep_ll = a.topk_limit;
   if (keep_ll > a.k_out) keep_ll = a.k_out;
-  const int keep = static_cast<int>(keep_ll);
-  for (int i = keep + tid; i < a.k_out; i += kThreads) out[i] = -1;
-  if (keep == 0) return;
-  const bool by_score = a.order == 0;
+  R.keep = static_cast<int>(keep_ll);
+  return R;
+}
 
-  using RS = typename std::conditional<NB == 0, GlobalSeg, RegSeg<(NB > 0 ? NB : 1)>>::type;
-  RS rs;
-  rs.init(src, n);
-  auto feed_row = [&](uint32_t* h, int shift, uint32_t mask, int pshift, uint32_t pre) {
-    seg_hist(rs, h, shift, mask, pshift, pre);
-  };
-
-  uint32_t n_cand;
-  uint32_t T = 0, need = 0xFFFFFFFFu;  // kept: key > T, or == T among the first `need`
-  bool exact = true;                   // the candidates are exactly the kept keys
-  if (n <= keep) {
-    n_cand = seg_compact(rs, 0u, 0xFFFFFFFFu, ck, ci, red);  // every key
-  } else {
-    for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    seg_hist(rs, hist, 20, 4095u, 32, 0u);
-    __syncthreads();
-    find_bucket(hist, kBins, static_cast<uint32_t>(keep), red, info);
-    const uint32_t d1 = info[0], above = info[1], in_b = info[2];
-    const uint32_t want = static_cast<uint32_t>(keep) - above;
-    if (in_b == want) {
-      T = (d1 << 20) - 1u;  // the whole threshold bucket is kept
-      need = 0;
-      n_cand = seg_compact(rs, T, need, ck, ci, red);
-    } else if (above + in_b <= static_cast<uint32_t>(cand_cap)) {
-      // fast path: every key of buckets >= d1, in index order
-      n_cand = seg_compact(rs, (d1 << 20) - 1u, 0u, ck, ci, red);
-      exact = false;
-      if (!by_score) {
-        const uint32_t nc = n_cand;
-        auto feed_cand = [&](uint32_t* h, int shift, uint32_t mask, int pshift, uint32_t pre) {
-          for (uint32_t i = tid; i < nc; i += kThreads) {
-            const uint32_t u = ck[i];
-            if ((u >> pshift) == pre) atomicAdd(&h[hslot((u >> shift) & mask)], 1u);
-          }
-        };
-        refine_threshold(feed_cand, d1, want, hist, red, info, &T, &need);
-      }
-    } else {
-      // slow path (huge threshold bucket): exact threshold over the row, exactly `keep` keys
-      refine_threshold(feed_row, d1, want, hist, red, info, &T, &need);
-      n_cand = seg_compact(rs, T, need, ck, ci, red);
-    }
-  }
-
+// Final output from candidates (ck, ci) in index order:
+//   exact    -- the candidates are exactly the kept keys;
+//   otherwise every key of 12-bit bucket >= d1 (`want` still to take from bucket d1).
+__device__ void finish_row(const TopkSmem& m, uint32_t n_cand, bool exact, uint32_t d1, uint32_t want, int keep,
+                           bool by_score, int32_t* out, uint32_t* red, uint32_t* info) {
+  const int tid = threadIdx.x;
   if (by_score) {
-    if (bucket_rank_out(ck, ci, static_cast<int>(n_cand), keep, tk, ti, hist, red, out)) return;
+    if (bucket_rank_out(m.ck, m.ci, static_cast<int>(n_cand), keep, m.tk, m.ti, m.hist, red, out)) return;
     uint32_t *sk, *sv;
-    radix_sort_desc(ck, ci, tk, ti, static_cast<int>(n_cand), hist, red, &sk, &sv);
+    radix_sort_desc(m.ck, m.ci, m.tk, m.ti, static_cast<int>(n_cand), m.hist, red, &sk, &sv);
     for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(sv[i]);
     return;
   }
-  if (exact) {  // candidates are the kept keys, already in index order
-    for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(ci[i]);
+  if (exact) {
+    for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(m.ci[i]);
     return;
   }
-  // index order from the fast-path candidates: keep key > T and the first `need` == T
-  {
-    const int lane = tid & 31, warp = tid >> 5;
-    const uint32_t per = ((n_cand + kWarps - 1) / kWarps + 31) & ~31u;
-    const uint32_t c0 = warp * per, c1 = min(n_cand, c0 + per);
+  uint32_t T, need;
+  const uint32_t nc = n_cand;
+  const uint32_t* ckp = m.ck;
+  auto feed_cand = [&](uint32_t* h, int shift, uint32_t mask, int pshift, uint32_t pre) {
+    for (uint32_t i = tid; i < nc; i += kThreads) {
+      const uint32_t u = ckp[i];
+      if ((u >> pshift) == pre) atomicAdd(&h[hslot((u >> shift) & mask)], 1u);
+    }
+  };
+  refine_threshold(feed_cand, d1, want, m.hist, red, info, &T, &need);
+  const int lane = tid & 31, warp = tid >> 5;
+  const uint32_t per = ((n_cand + kWarps - 1) / kWarps + 31) & ~31u;
+  const uint32_t c0 = warp * per, c1 = min(n_cand, c0 + per);
+  uint32_t cgt = 0, ceq = 0;
+  for (uint32_t i = c0 + lane; i < c1; i += 32) {
+    cgt += m.ck[i] > T ? 1u : 0u;
+    ceq += m.ck[i] == T ? 1u : 0u;
+  }
+  cgt = __reduce_add_sync(0xffffffffu, cgt);
+  ceq = __reduce_add_sync(0xffffffffu, ceq);
+  if (lane == 0) red[warp] = cgt;
+  __syncthreads();
+  uint32_t gbase = 0;
+  for (int w = 0; w < warp; ++w) gbase += red[w];
+  __syncthreads();
+  if (lane == 0) red[warp] = ceq;
+  __syncthreads();
+  uint32_t ebase = 0;
+  for (int w = 0; w < warp; ++w) ebase += red[w];
+  for (uint32_t i0 = c0; i0 < c1; i0 += 32) {
+    const uint32_t i = i0 + lane;
+    const bool valid = i < c1;
+    const uint32_t u = valid ? m.ck[i] : 0u;
+    const bool gt = valid && u > T, eq = valid && u == T;
+    const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+    const uint32_t lt = (1u << lane) - 1u;
+    const uint32_t g = gbase + __popc(bg & lt), e = ebase + __popc(be & lt);
+    if (gt) out[g + (e < need ? e : need)] = static_cast<int32_t>(m.ci[i]);
+    else if (eq && e < need) out[g + e] = static_cast<int32_t>(m.ci[i]);
+    gbase += __popc(bg);
+    ebase += __popc(be);
+  }
+}
+
+// The whole top-k of one row by one CTA, reading the row through RS.
+template <class RS>
+__device__ void row_topk(const RS& rs, long long n, int keep, bool by_score, int32_t* out, int cand_cap,
+                         const TopkSmem& m, uint32_t* red, uint32_t* info) {
+  const int tid = threadIdx.x;
+  uint32_t n_cand;
+  bool exact = true;
+  uint32_t d1 = 0, want = 0;
+  if (n <= keep) {
+    n_cand = seg_compact(rs, 0u, 0xFFFFFFFFu, m.ck, m.ci, red);  // every key
+  } else {
+    for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = 0;
+    __syncthreads();
+    seg_hist(rs, m.hist, 20, 4095u, 32, 0u);
+    __syncthreads();
+    find_bucket(m.hist, kBins, static_cast<uint32_t>(keep), red, info);
+    d1 = info[0];
+    const uint32_t above = info[1], in_b = info[2];
+    want = static_cast<uint32_t>(keep) - above;
+    if (in_b == want) {
+      n_cand = seg_compact(rs, (d1 << 20) - 1u, 0u, m.ck, m.ci, red);  // the whole bucket is kept
+    } else if (above + in_b <= static_cast<uint32_t>(cand_cap)) {
+      n_cand = seg_compact(rs, (d1 << 20) - 1u, 0u, m.ck, m.ci, red);  // every key of buckets >= d1
+      exact = false;
+    } else {
+      // huge threshold bucket: exact threshold over the row, exactly `keep` keys
+      uint32_t T, need;
+      auto feed_row = [&](uint32_t* h, int shift, uint32_t mask, int pshift, uint32_t pre) {
+        seg_hist(rs, h, shift, mask, pshift, pre);
+      };
+      refine_threshold(feed_row, d1, want, m.hist, red, info, &T, &need);
+      n_cand = seg_compact(rs, T, need, m.ck, m.ci, red);
+    }
+  }
+  finish_row(m, n_cand, exact, d1, want, keep, by_score, out, red, info);
+}
+
+template <int NB>  // NB > 0: rows up to kWarps * NB * 128 keys held in registers; 0: any length
+__global__ void __launch_bounds__(kThreads, NB == 8 ? 3 : 2) topk_kernel(const TopkArgs a, int cand_cap) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ uint32_t red[2 * kWarps];
+  __shared__ uint32_t info[4];
+  const TopkSmem m = topk_smem(smem, cand_cap);
+  const RowInfo R = row_info(a, blockIdx.x);
+  for (int i = R.keep + threadIdx.x; i < a.k_out; i += kThreads) R.out[i] = -1;
+  if (R.keep == 0) return;
+  using RS = typename std::conditional<NB == 0, GlobalSeg, RegSeg<(NB > 0 ? NB : 1)>>::type;
+  RS rs;
+  rs.init(R.src, R.n);
+  row_topk(rs, R.n, R.keep, a.order == 0, R.out, cand_cap, m, red, info);
+}
+
+// ---------------------------------------------------------------- long rows: a cluster of CTAs per row
+constexpr int kClusterCtas = 8;
+
+__device__ __forceinline__ uint32_t dsmem_ld(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t mapa(const void* p, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(d)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Sum the kClusterCtas local histograms (m.hist of every CTA) into m.merged of every CTA:
+// CTA r adds up bins [r, r + 1) * kBins / kClusterCtas, then every CTA gathers the rest.
+__device__ void cluster_merge_hist(const TopkSmem& m, uint32_t rank) {
+  constexpr int kSlice = kBins / kClusterCtas;
+  cluster_barrier();  // every local histogram is complete
+  for (int b = rank * kSlice + threadIdx.x; b < static_cast<int>(rank + 1) * kSlice; b += kThreads) {
+    uint32_t s = 0;
+#pragma unroll
+    for (int j = 0; j < kClusterCtas; ++j) s += dsmem_ld(mapa(&m.hist[hslot(b)], j));
+    m.merged[hslot(b)] = s;
+  }
+  cluster_barrier();  // every slice is merged
+  for (int b = threadIdx.x; b < kBins; b += kThreads) {
+    const uint32_t owner = static_cast<uint32_t>(b / kSlice);
+    if (owner != rank) m.merged[hslot(b)] = dsmem_ld(mapa(&m.merged[hslot(b)], owner));
+  }
+  cluster_barrier();  // no CTA reads another's histograms after this
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkArgs a, int cand_cap) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ uint32_t red[2 * kWarps];
+  __shared__ uint32_t info[4];
+  __shared__ uint32_t counts[kClusterCtas];
+  const TopkSmem m = topk_smem(smem, cand_cap);
+  const uint32_t rank = cluster_rank();
+  const RowInfo R = row_info(a, blockIdx.x / kClusterCtas);
+  const int tid = threadIdx.x;
+  if (rank == 0)
+    for (int i = R.keep + tid; i < a.k_out; i += kThreads) R.out[i] = -1;
+  if (R.keep == 0) return;  // the same decision in every CTA of the cluster
+  const bool by_score = a.order == 0;
+  // this CTA's contiguous part of the row
+  const long long part = ((R.n + kClusterCtas - 1) / kClusterCtas + 1023) & ~1023LL;
+  const long long lo = min(R.n, static_cast<long long>(rank) * part);
+  const long long len = min(R.n - lo, part);
+  RegSeg<NB> rs;
+  rs.init(R.src + lo, len);
+
+  const bool take_all = R.n <= R.keep;
+  uint32_t T = 0;         // candidates: keys > T (every key when take_all)
+  uint32_t d1 = 0, want = 0;
+  bool exact = take_all;
+  bool fallback = false;  // tie-heavy row: the first CTA finishes it alone
+  if (!take_all) {
+    for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = 0;
+    __syncthreads();
+    seg_hist(rs, m.hist, 20, 4095u, 32, 0u);
+    __syncthreads();
+    cluster_merge_hist(m, rank);
+    find_bucket(m.merged, kBins, static_cast<uint32_t>(R.keep), red, info);
+    d1 = info[0];
+    const uint32_t above = info[1], in_b = info[2];
+    want = static_cast<uint32_t>(R.keep) - above;
+    T = (d1 << 20) - 1u;
+    exact = in_b == want;
+    if (!exact && above + in_b > static_cast<uint32_t>(cand_cap)) {
+      // one more level, cluster-wide: bits 8..19 inside bucket d1
+      for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = 0;
+      __syncthreads();
+      seg_hist(rs, m.hist, 8, 4095u, 20, d1);
+      __syncthreads();
+      cluster_merge_hist(m, rank);
+      find_bucket(m.merged, kBins, want, red, info);
+      const uint32_t d2 = info[0], above2 = info[1], in_b2 = info[2];
+      const uint32_t pre = (d1 << 12) | d2;
+      T = (pre << 8) - 1u;  // candidates: top 24 bits >= pre
+      want -= above2;
+      exact = in_b2 == want;
+      if (!exact) {
+        // the threshold sits inside 24-bit bucket pre: keep that level for the refinement
+        if (above + above2 + in_b2 > static_cast<uint32_t>(cand_cap)) fallback = true;
+        d1 = pre;  // finish_row refines inside (top 24 bits == pre) below
+      }
+    }
+  }
+  if (fallback) {
+    cluster_barrier();
+    if (rank != 0) return;
+    GlobalSeg gs;
+    gs.init(R.src, R.n);
+    row_topk(gs, R.n, R.keep, by_score, R.out, cand_cap, m, red, info);
+    return;
+  }
+  // candidates of this CTA, counted, then written in index order into CTA 0's buffers
+  uint32_t cnt = 0;
+  rs.visit([&](const uint32_t (&u)[4], long long, int c) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cnt += (e < c && (take_all || u[e] > T)) ? 1u : 0u;
+  });
+  cnt = __reduce_add_sync(0xffffffffu, cnt);
+  const int lane = tid & 31, warp = tid >> 5;
+  if (lane == 0) red[warp] = cnt;
+  __syncthreads();
+  uint32_t wbase = 0, ctotal = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    wbase += w < warp ? red[w] : 0u;
+    ctotal += red[w];
+  }
+  if (tid == 0) dsmem_st(mapa(&counts[rank], 0), ctotal);
+  cluster_barrier();
+  uint32_t cbase = 0, n_cand = 0;
+  if (tid < kClusterCtas) counts[tid] = rank == 0 ? counts[tid] : dsmem_ld(mapa(&counts[tid], 0));
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kClusterCtas; ++j) {
+    cbase += j < static_cast<int>(rank) ? counts[j] : 0u;
+    n_cand += counts[j];
+  }
+  const bool overflow = n_cand > static_cast<uint32_t>(cand_cap);  // same in every CTA
+  if (!overflow) {
+    const uint32_t ck0 = mapa(m.ck, 0), ci0 = mapa(m.ci, 0);
+    uint32_t base = cbase + wbase;
+    rs.visit([&](const uint32_t (&u)[4], long long i, int c) {
+      uint32_t msk = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) msk |= ((e < c && (take_all || u[e] > T)) ? 1u : 0u) << e;
+      const uint32_t k = __popc(msk);
+      const uint32_t incl = warp_incl_scan(k);
+      uint32_t pos = base + incl - k;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if ((msk >> e) & 1u) {
+          dsmem_st(ck0 + 4u * pos, u[e]);
+          dsmem_st(ci0 + 4u * pos, static_cast<uint32_t>(lo + i + e));
+          ++pos;
+        }
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    });
+  }
+  cluster_barrier();  // CTA 0 holds every candidate; nobody touches its memory after this
+  if (rank != 0) return;
+  if (overflow) {
+    GlobalSeg gs;
+    gs.init(R.src, R.n);
+    row_topk(gs, R.n, R.keep, by_score, R.out, cand_cap, m, red, info);
+    return;
+  }
+  if (!by_score && !exact && (d1 >> 12) != 0) {
+    // index order with a 24-bit threshold prefix: refine the last 8 bits on the candidates
+    uint32_t need;
+    const uint32_t nc = n_cand, pre = d1;
+    const uint32_t* ckp = m.ck;
+    for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = 0;
+    __syncthreads();
+    for (uint32_t i = tid; i < nc; i += kThreads)
+      if ((ckp[i] >> 8) == pre) atomicAdd(&m.hist[hslot(ckp[i] & 255u)], 1u);
+    __syncthreads();
+    find_bucket(m.hist, 256, want, red, info);
+    const uint32_t Tx = (pre << 8) | info[0];
+    need = want - info[1];
+    // keep key > Tx and the first `need` keys == Tx (candidates are in index order)
+    const uint32_t per = ((nc + kWarps - 1) / kWarps + 31) & ~31u;
+    const uint32_t c0 = warp * per, c1 = min(nc, c0 + per);
     uint32_t cgt = 0, ceq = 0;
     for (uint32_t i = c0 + lane; i < c1; i += 32) {
-      cgt += ck[i] > T ? 1u : 0u;
-      ceq += ck[i] == T ? 1u : 0u;
+      cgt += ckp[i] > Tx ? 1u : 0u;
+      ceq += ckp[i] == Tx ? 1u : 0u;
     }
     cgt = __reduce_add_sync(0xffffffffu, cgt);
     ceq = __reduce_add_sync(0xffffffffu, ceq);
     if (lane == 0) red[warp] = cgt;
     __syncthreads();
-    uint32_t gbase = 0;
-    for (int w = 0; w < warp; ++w) gbase += red[w];
+    uint32_t gb = 0;
+    for (int w = 0; w < warp; ++w) gb += red[w];
     __syncthreads();
     if (lane == 0) red[warp] = ceq;
     __syncthreads();
-    uint32_t ebase = 0;
-    for (int w = 0; w < warp; ++w) ebase += red[w];
+    uint32_t eb = 0;
+    for (int w = 0; w < warp; ++w) eb += red[w];
     for (uint32_t i0 = c0; i0 < c1; i0 += 32) {
       const uint32_t i = i0 + lane;
       const bool valid = i < c1;
-      const uint32_t u = valid ? ck[i] : 0u;
-      const bool gt = valid && u > T, eq = valid && u == T;
+      const uint32_t u = valid ? ckp[i] : 0u;
+      const bool gt = valid && u > Tx, eq = valid && u == Tx;
       const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
       const uint32_t lt = (1u << lane) - 1u;
-      const uint32_t g = gbase + __popc(bg & lt), e = ebase + __popc(be & lt);
-      if (gt) out[g + (e < need ? e : need)] = static_cast<int32_t>(ci[i]);
-      else if (eq && e < need) out[g + e] = static_cast<int32_t>(ci[i]);
-      gbase += __popc(bg);
-      ebase += __popc(be);
+      const uint32_t g = gb + __popc(bg & lt), e = eb + __popc(be & lt);
+      if (gt) R.out[g + (e < need ? e : need)] = static_cast<int32_t>(m.ci[i]);
+      else if (eq && e < need) R.out[g + e] = static_cast<int32_t>(m.ci[i]);
+      gb += __popc(bg);
+      eb += __popc(be);
     }
+    return;
   }
+  finish_row(m, n_cand, exact, d1, want, R.keep, by_score, R.out, red, info);
 }
 
 }  // namespace
@@ -650,8 +901,31 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
     kern<<<a.n_rows, kThreads, smem, st>>>(a, cap);
     return cudaGetLastError();
   };
+  // rows longer than one CTA's registers hold, but within a cluster's: one cluster per row
+  auto go_cluster = [&](auto kern) -> cudaError_t {
+    const size_t csmem = smem + static_cast<size_t>(kHistWords) * 4;  // + merged histogram
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(csmem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.n_rows) * kClusterCtas, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = csmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a, cap);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  };
   if (max_row_len <= kWarps * 8 * 128) return go(topk_kernel<8>);
   if (max_row_len <= kWarps * 16 * 128) return go(topk_kernel<16>);
+  if (max_row_len <= kClusterCtas * kWarps * 8 * 128) return go_cluster(topk_cluster_kernel<8>);
+  if (max_row_len <= kClusterCtas * kWarps * 16 * 128) return go_cluster(topk_cluster_kernel<16>);
   return go(topk_kernel<0>);
 }
 
