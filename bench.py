@@ -309,6 +309,31 @@ def run_other_workloads(dev, stream, peaks):
         "peak": f"e4m3 dense = 2 x measured bf16 ({2 * bf16_peak:.0f} TFLOP/s, nominal ratio)"}
     del c, args, keep
     torch.cuda.empty_cache()
+    # decode: B=64 single queries, contexts U[4096, 65536], bf16 q against an e4m3 cache
+    import workloads
+    lens = workloads.decode_lens(64, 4096, 65536, 0)
+    c = _paged_on_device(64, lens, 1, 64, 128, 64, False, True, 5, dev)
+    args, keep = dsa.make_indexer_args(c["q"], c["w"], c["k_cache"], c["cu_q_lens"], c["seq_lens"],
+                                       c["block_tables"], max_seq_len=c["max_seq_len"], topk_limit=2048,
+                                       k_scale_cache=c["k_scale_cache"])
+    rc = L.dsa_indexer(ctypes.byref(args), stream.cuda_stream)
+    if rc != 0:
+        raise RuntimeError(f"dsa_indexer (bf16 q, e4m3 cache): {dsa.dsa_status_string(rc)}")
+    ms = _time_events(lambda: L.dsa_indexer(ctypes.byref(args), stream.cuda_stream), 10, stream)
+    keys = sum(lens)
+    # algorithmic bytes: e4m3 keys + fp32 key scales + page ids + q + w + int32 top-k out
+    dec_bytes = keys * (128 + 4) + sum((x + 63) // 64 for x in lens) * 4 + 64 * 64 * 128 * 2 + 64 * 64 * 4 \
+        + 64 * 2048 * 4
+    out["decode_b64_fp8_cache"] = {
+        "workload": "decode B=64, one query per sequence, contexts U[4096, 65536] (seeded), bf16 q, "
+                    "paged e4m3 cache (page 64) with fp32 per-token scales, H=64, D=128, index_topk=2048",
+        "ms_per_step": ms, "keys_per_s": keys / (ms / 1e3), "keys": keys,
+        "algorithmic_bytes": dec_bytes, "hbm_gbs": dec_bytes / (ms / 1e3) / 1e9,
+        "hbm_frac": dec_bytes / (ms / 1e3) / 1e9 / hbm,
+        "note": "includes the fp32 score round trip (4 B written + 4 B read per key) that is not in the "
+                "algorithmic bytes"}
+    del c, args, keep
+    torch.cuda.empty_cache()
     # IndexShare: 12 layers [full, shared, shared] x 4, decode B=32 at 32768 keys, bf16 caches
     types = ["full", "shared", "shared"] * 4
     fulls, keeps = [], []

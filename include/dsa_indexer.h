@@ -159,8 +159,13 @@ typedef struct {
 /* Bytes of device workspace dsa_indexer needs for these sizes (pointers may be NULL). */
 dsa_status dsa_indexer_workspace_size(const dsa_indexer_args* args, size_t* bytes);
 
-/* Run the fused indexer.  Same dtype / H / D support as dsa_indexer_scores plus the
- * (BF16 q, FP8 cache) mix is UNSUPPORTED for now.  The workspace must not be used
+/* Run the fused indexer.  Same dtype / H / D support as dsa_indexer_scores, plus
+ * BF16 q against an FP8-e4m3 cache (GLM5 TensorCast adaptation design, background
+ * item 5: the indexer cache takes the FP8 dtype when attention is quantised).  That
+ * mix is taken on decode batches (total_q <= B) with D = 128 and k_scale_cache set
+ * (q_scale is ignored): the keys are widened to bf16 on chip, so every product is
+ * exact; the two e4m3 NaN codes are not accepted there (they decode as 480).  On a
+ * prefill batch the mix returns DSA_ERR_UNSUPPORTED.  The workspace must not be used
  * by another call that overlaps on the GPU. */
 dsa_status dsa_indexer(const dsa_indexer_args* args, dsa_stream_t stream);
 

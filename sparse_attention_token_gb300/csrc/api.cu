@@ -176,7 +176,7 @@ size_t score_pair_launch_smem(const ScoreArgs& a) {
 dsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
 struct PagedPlan {
-  bool decode, pair;
+  bool decode, pair, mixed;
   int NQ, N, KC, R, n_chunks, cap, tile_keys;
   long long ld;
   size_t off_counts, off_items, off_scores, total;
@@ -196,10 +196,17 @@ dsa_status plan_paged(const dsa_indexer_args* a, PagedPlan* p) {
     return DSA_ERR_INVALID_ARGUMENT;
   if (a->max_seq_len >= (1 << 16) * kBlockM) return DSA_ERR_UNSUPPORTED;  // key-tile ids are 16-bit
   if (a->max_seq_len > INT_MAX - 2 * kBlockM) return DSA_ERR_UNSUPPORTED;
-  dsa_status st = check_dtypes(a->q_dtype, a->k_dtype, a->D, a->q_scale != nullptr, a->k_scale_cache != nullptr);
-  if (st != DSA_OK) return st;
-  const int ns = std::max(num_sms(), 1);
   p->decode = a->total_q <= a->B;
+  p->mixed = a->q_dtype == DSA_BF16 && a->k_dtype == DSA_FP8_E4M3;
+  if (p->mixed) {
+    // bf16 queries against an e4m3 cache: keys are widened to bf16 on chip (decode shapes)
+    if (!p->decode || a->D != 128) return DSA_ERR_UNSUPPORTED;
+    if (!a->k_scale_cache) return DSA_ERR_INVALID_ARGUMENT;
+  } else {
+    dsa_status st = check_dtypes(a->q_dtype, a->k_dtype, a->D, a->q_scale != nullptr, a->k_scale_cache != nullptr);
+    if (st != DSA_OK) return st;
+  }
+  const int ns = std::max(num_sms(), 1);
   p->N = p->decode ? std::max(64, a->H) : 256;
   p->NQ = p->N / a->H;
   p->pair = !p->decode && use_pair_mma();
@@ -242,6 +249,7 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
   s.paged = 1;
   s.q_fp8 = fp8;
   s.k_fp8 = a->k_dtype == DSA_FP8_E4M3;
+  s.mixed = p.mixed;
   s.H = a->H;
   s.D = a->D;
   s.NQ = p.NQ;
@@ -263,7 +271,7 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
   CUtensorMap tq, tk;
   if (!make_map_2d(&tq, a->q, fp8, a->D, static_cast<long long>(a->total_q) * a->H, p.pair ? p.N / 2 : p.N))
     return DSA_ERR_CUDA;
-  if (!make_map_paged(&tk, a->k_cache, s.k_fp8, a->D, a->page_size, std::max(a->num_pages, 1)))
+  if (!make_map_paged(&tk, a->k_cache, s.k_fp8 != 0, a->D, a->page_size, std::max(a->num_pages, 1)))
     return DSA_ERR_CUDA;
 
   cudaError_t e = cudaMemsetAsync(counts, 0, static_cast<size_t>(p.n_chunks) * 4, st);

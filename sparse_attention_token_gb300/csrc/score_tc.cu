@@ -33,20 +33,22 @@ namespace {
 struct SmemPlan {
   uint32_t q[2];
   uint32_t k[kMaxKStages];
+  uint32_t k8[kMaxKStages];  // e4m3 staging of the keys (mixed mode)
   uint32_t wbuf, qsbuf, ksbuf, bars, misc, total;
 };
 
-__host__ __device__ inline SmemPlan plan_smem(int N, int D, int q_fp8, int k_fp8, int nK) {
+__host__ __device__ inline SmemPlan plan_smem(int N, int D, int q_fp8, int k_fp8, int nK, int mixed = 0) {
   SmemPlan p{};
   uint32_t off = 0;
   const uint32_t qb = static_cast<uint32_t>(N) * D * (q_fp8 ? 1 : 2);
-  const uint32_t kb = static_cast<uint32_t>(kBlockM) * D * (k_fp8 ? 1 : 2);
+  const uint32_t kb = static_cast<uint32_t>(kBlockM) * D * ((k_fp8 && !mixed) ? 1 : 2);
   for (int i = 0; i < 2; ++i) { p.q[i] = off; off += qb; }
   for (int i = 0; i < kMaxKStages; ++i) { p.k[i] = off; if (i < nK) off += kb; }
+  for (int i = 0; i < kMaxKStages; ++i) { p.k8[i] = off; if (mixed && i < nK) off += static_cast<uint32_t>(kBlockM) * D; }
   p.wbuf = off;  off += 2u * N * 4u;
   p.qsbuf = off; if (q_fp8) off += 2u * N * 4u;
   p.ksbuf = off; if (k_fp8) off += static_cast<uint32_t>(nK) * kBlockM * 4u;
-  p.bars = off;  off += 32u * 8u;
+  p.bars = off;  off += 48u * 8u;
   p.misc = off;  off += 16u;
   p.total = off;
   return p;
@@ -55,7 +57,9 @@ __host__ __device__ inline SmemPlan plan_smem(int N, int D, int q_fp8, int k_fp8
 // Barrier slots inside the bars region.
 enum {
   kBarQFull = 0, kBarQEmpty = 2, kBarTFull = 4, kBarTEmpty = 6, kBarFold = 8,  // fold: 4 slots
-  kBarDone = 12, kBarKFull = 13, kBarKEmpty = 13 + kMaxKStages
+  kBarDone = 12, kBarKFull = 13, kBarKEmpty = 13 + kMaxKStages,
+  kBarK8Full = 13 + 2 * kMaxKStages,   // mixed: e4m3 key tile (and its scales) landed
+  kBarK8Empty = 13 + 3 * kMaxKStages   // mixed: e4m3 staging slot converted
 };
 
 struct ItemInfo {
@@ -158,11 +162,16 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
     for (int kt = I.kt0; kt < I.kt1; ++kt) {
       const int s = nk % nK;
       int good = 1;
-      if (lane == 0) good = ptx::mbar_wait(&bars[kBarKEmpty + s], ((nk / nK) & 1) ^ 1, abort, a.status, kStatusTimeout);
+      if (lane == 0) {
+        good = ptx::mbar_wait(&bars[kBarKEmpty + s], ((nk / nK) & 1) ^ 1, abort, a.status, kStatusTimeout);
+        if (good && a.mixed)
+          good = ptx::mbar_wait(&bars[kBarK8Empty + s], ((nk / nK) & 1) ^ 1, abort, a.status, kStatusTimeout);
+      }
       good = __shfl_sync(0xffffffffu, good, 0);
       if (!good) { ok = false; break; }
-      uint64_t* full = &bars[kBarKFull + s];
-      uint8_t* dst = smem + P.k[s];
+      // mixed: the e4m3 tile and its scales land in the staging slot; converters fill P.k
+      uint64_t* full = a.mixed ? &bars[kBarK8Full + s] : &bars[kBarKFull + s];
+      uint8_t* dst = smem + (a.mixed ? P.k8[s] : P.k[s]);
       if (!a.paged) {
         if (a.k_fp8) {
           const long long e = static_cast<long long>(kt) * kBlockM + 4 * lane;
@@ -239,7 +248,8 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
     const int kk = nk < static_cast<uint32_t>(nK) ? static_cast<int>(nk) : nK;
     for (int i = 1; i <= kk; ++i) {
       const uint32_t u = nk - i;
-      ptx::mbar_wait_drain(&bars[kBarKFull + (u % nK)], (u / nK) & 1, a.status, kStatusTimeout, 200000000ull);
+      ptx::mbar_wait_drain(&bars[(a.mixed ? kBarK8Full : kBarKFull) + (u % nK)], (u / nK) & 1, a.status, kStatusTimeout,
+                           200000000ull);
     }
   }
 }
@@ -303,8 +313,8 @@ __device__ __forceinline__ void mma_loop(const ScoreArgs& a, uint8_t* smem, cons
 template <int H, bool DECODE>
 __device__ __forceinline__ void mma_role(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P, uint64_t* bars,
                                          volatile int* abort, int n_items, uint32_t tmem_base) {
-  // 32 bytes of K per MMA: 16 bf16 or 32 e4m3 values
-  if (a.k_fp8) mma_loop<H, DECODE, true, 4>(a, smem, P, bars, abort, n_items, tmem_base);
+  // 32 bytes of K per MMA: 16 bf16 or 32 e4m3 values; mixed mode multiplies bf16 by widened keys
+  if (a.q_fp8) mma_loop<H, DECODE, true, 4>(a, smem, P, bars, abort, n_items, tmem_base);
   else if (a.D == 128) mma_loop<H, DECODE, false, 8>(a, smem, P, bars, abort, n_items, tmem_base);
   else mma_loop<H, DECODE, false, 4>(a, smem, P, bars, abort, n_items, tmem_base);
 }
@@ -314,6 +324,70 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& a, uint8_t* smem, cons
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* status) {
   const bool ok = ptx::mbar_wait(bar, parity, abort, status, kStatusTimeout);
   return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// ------------------------------------------------------------------ key widening (mixed mode, warps 10..13)
+// Two e4m3 codes -> two bf16, exactly (every e4m3 value, subnormals included, is a
+// bf16 value).  `t` holds the codes in bits 15..8 and 31..24.  Moving the code's
+// exponent and mantissa bits under bf16's exponent/mantissa boundary gives a bf16
+// whose exponent is biased by 127 instead of 7 (an e4m3 subnormal lands on a bf16
+// subnormal with the same mantissa); one multiply by 2^120 removes the bias gap.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t t) {
+  const uint32_t v = (t & 0x80008000u) | ((t >> 4) & 0x07F007F0u);
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x7B807B80u));  // 0x7B80 = 2^120
+  return r;
+}
+
+// Widen every staged e4m3 key tile (128 rows x D=128 bytes, 128-byte swizzle) into the
+// bf16 MMA layout (two 128-byte atom columns, same swizzle).  Each warp converts 32
+// rows, 4 rows per step: lane l takes 16-byte chunk l%8 of row l/8.
+template <int H, bool DECODE>
+__device__ __forceinline__ void convert_role(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P, uint64_t* bars,
+                                             volatile int* abort, int n_items) {
+  using C = Cfg<H, DECODE>;
+  const int cw = (static_cast<int>(threadIdx.x) >> 5) - 10;
+  const int lane = threadIdx.x & 31;
+  const int nK = a.num_k_stages;
+  uint32_t sk = 0, kph = 0;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    ItemInfo I;
+    if (!fetch_item<C::NQ>(a, n_items, it, I)) break;
+    for (int kt = I.kt0; kt < I.kt1; ++kt) {
+      if (!warp_wait(&bars[kBarK8Full + sk], kph, abort, a.status)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* src = smem + P.k8[sk];
+      uint8_t* dst = smem + P.k[sk];
+#pragma unroll 2
+      for (int st = 0; st < 8; ++st) {
+        const int r = cw * 32 + st * 4 + (lane >> 3);
+        const int j = lane & 7;
+        const uint4 v = *reinterpret_cast<const uint4*>(src + r * 128 + ((j ^ (r & 7)) << 4));
+        const uint4 o0 = make_uint4(e4m3x2_to_bf16x2(__byte_perm(v.x, 0, 0x1404)),
+                                    e4m3x2_to_bf16x2(__byte_perm(v.x, 0, 0x3424)),
+                                    e4m3x2_to_bf16x2(__byte_perm(v.y, 0, 0x1404)),
+                                    e4m3x2_to_bf16x2(__byte_perm(v.y, 0, 0x3424)));
+        const uint4 o1 = make_uint4(e4m3x2_to_bf16x2(__byte_perm(v.z, 0, 0x1404)),
+                                    e4m3x2_to_bf16x2(__byte_perm(v.z, 0, 0x3424)),
+                                    e4m3x2_to_bf16x2(__byte_perm(v.w, 0, 0x1404)),
+                                    e4m3x2_to_bf16x2(__byte_perm(v.w, 0, 0x3424)));
+        uint8_t* rowp = dst + (j >> 2) * (kBlockM * 128) + r * 128;
+        const int c0 = (2 * j) & 7;
+        *reinterpret_cast<uint4*>(rowp + ((c0 ^ (r & 7)) << 4)) = o0;
+        *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)) = o1;
+      }
+      ptx::fence_proxy_async_smem();  // the tensor core reads these through the async proxy
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(&bars[kBarKFull + sk]);
+        ptx::mbar_arrive(&bars[kBarK8Empty + sk]);
+      }
+      if (++sk == static_cast<uint32_t>(nK)) { sk = 0; kph ^= 1u; }
+    }
+  }
 }
 
 // ------------------------------------------------------------------ epilogue (warps 2..9)
@@ -441,8 +515,8 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
   }
 }
 
-template <int H, bool DECODE>
-__global__ void __launch_bounds__(kScoreThreads, 1)
+template <int H, bool DECODE, bool MIXED>
+__global__ void __launch_bounds__(MIXED ? kMixedThreads : kScoreThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                  const ScoreArgs a) {
   using C = Cfg<H, DECODE>;
@@ -452,7 +526,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     if (threadIdx.x == 0) atomicOr(a.status, kStatusSmemAlign);
     return;
   }
-  const SmemPlan P = plan_smem(C::N, a.D, a.q_fp8, a.k_fp8, a.num_k_stages);
+  const SmemPlan P = plan_smem(C::N, a.D, a.q_fp8, a.k_fp8, a.num_k_stages, MIXED ? 1 : 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + P.misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + P.misc + 4);
@@ -468,8 +542,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
     ptx::mbar_init(&bars[kBarDone], 1);
     for (int s = 0; s < a.num_k_stages; ++s) {
-      ptx::mbar_init(&bars[kBarKFull + s], 1 + (a.k_fp8 ? 32 : 0));
+      ptx::mbar_init(&bars[kBarKFull + s], MIXED ? 4 : 1 + (a.k_fp8 ? 32 : 0));
       ptx::mbar_init(&bars[kBarKEmpty + s], 1 + (a.k_fp8 ? C::EPI_T_ARRIVALS : 0));
+      ptx::mbar_init(&bars[kBarK8Full + s], 1 + 32);
+      ptx::mbar_init(&bars[kBarK8Empty + s], 4);
     }
     *abort = 0;
     ptx::fence_mbar_init();
@@ -496,6 +572,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) mma_role<H, DECODE>(a, smem, P, bars, abort, n_items, tmem_base);
     __syncwarp();
+  } else if (MIXED && warp >= 10) {
+    convert_role<H, DECODE>(a, smem, P, bars, abort, n_items);
   } else {
     epilogue_role<H, DECODE>(a, smem, P, bars, abort, n_items, tmem_base);
   }
@@ -507,20 +585,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   }
 }
 
-template <int H, bool DECODE>
+template <int H, bool DECODE, bool MIXED>
 cudaError_t launch_t(const ScoreArgs& a, const CUtensorMap* tq, const CUtensorMap* tk, int grid, size_t smem,
                      cudaStream_t st) {
-  auto kern = score_kernel<H, DECODE>;
+  auto kern = score_kernel<H, DECODE, MIXED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, kScoreThreads, smem, st>>>(*tq, *tk, a);
+  kern<<<grid, MIXED ? kMixedThreads : kScoreThreads, smem, st>>>(*tq, *tk, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t score_smem_bytes(const ScoreArgs& a, int num_k_stages) {
-  return plan_smem(a.N, a.D, a.q_fp8, a.k_fp8, num_k_stages).total;
+  return plan_smem(a.N, a.D, a.q_fp8, a.k_fp8, num_k_stages, a.mixed).total;
 }
 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k, int grid,
@@ -528,8 +606,9 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap* tmap_q, const CU
   const bool dec = a.N != 256;
 #define DSA_CASE(HH)                                                                        \
   case HH:                                                                                  \
-    return dec ? launch_t<HH, true>(a, tmap_q, tmap_k, grid, smem_bytes, st)               \
-               : launch_t<HH, false>(a, tmap_q, tmap_k, grid, smem_bytes, st);
+    return dec ? (a.mixed ? launch_t<HH, true, true>(a, tmap_q, tmap_k, grid, smem_bytes, st)          \
+                          : launch_t<HH, true, false>(a, tmap_q, tmap_k, grid, smem_bytes, st))        \
+               : launch_t<HH, false, false>(a, tmap_q, tmap_k, grid, smem_bytes, st);
   switch (a.H) {
     DSA_CASE(4)
     DSA_CASE(8)

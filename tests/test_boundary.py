@@ -112,6 +112,12 @@ def test_workspace_size_and_paged_validation(dsa):
                 dict(q_dtype=1, k_dtype=0), dict(order=3), dict(topk_limit=0)]:
         with pytest.raises(dsa.DsaError):
             dsa.dsa_indexer_workspace_size(_args(dsa, **bad))
+    # bf16 queries with an e4m3 cache: decode shapes only, and the key scales are required
+    assert dsa.dsa_indexer_workspace_size(_args(dsa, q_dtype=0, k_dtype=1, k_scale_cache=1 << 20)) >= n
+    with pytest.raises(dsa.DsaError):
+        dsa.dsa_indexer_workspace_size(_args(dsa, q_dtype=0, k_dtype=1))
+    with pytest.raises(dsa.DsaError):
+        dsa.dsa_indexer_workspace_size(_args(dsa, q_dtype=0, k_dtype=1, k_scale_cache=1 << 20, total_q=3))
     L = dsa.lib()
     a = _args(dsa)                                        # valid sizes, null pointers
     assert L.dsa_indexer(ctypes.byref(a), None) == dsa.DSA_ERR_INVALID_ARGUMENT

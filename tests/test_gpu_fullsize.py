@@ -83,3 +83,21 @@ def test_chunked_prefill_fp8_full_size_sampled_rows():
     for i, r in enumerate(rows):
         n = int(pos[r]) + 1
         check_topk_row(tk[r], rt[i], rs[i, :n], RTOL["fp8_e4m3"] * rb[i, :n], n, pc.topk_limit, True)
+
+
+def test_decode_b64_bf16_q_fp8_cache_full_size_sampled_rows():
+    pc = workloads.decode_b64_fp8()
+    to = lambda t: None if t is None else t.cuda()
+    got = dsa.dsa_indexer(to(pc.q), to(pc.w), to(pc.k_cache), to(pc.cu_q_lens), to(pc.seq_lens),
+                          to(pc.block_tables), max_seq_len=pc.max_seq_len, topk_limit=pc.topk_limit,
+                          q_scale=None, k_scale_cache=to(pc.k_scale_cache))
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_status() == dsa.DSA_OK
+    tk = got.cpu().numpy()
+    assert np.all(tk >= 0)  # every context holds >= 4096 keys: no padding
+    rows = sample_rows(pc.B, 4, n=12, seed=2)
+    rt, rs, rb = oracle.paged(pc, rows=rows, want_scores=True, want_bound=True)
+    lens = pc.seq_lens.numpy()
+    for i, r in enumerate(rows):
+        n = int(lens[r])
+        check_topk_row(tk[r], rt[i], rs[i, :n], RTOL["bf16"] * rb[i, :n], n, pc.topk_limit, True)

@@ -226,6 +226,38 @@ def test_paged_fp8_gaussian_tolerance():
     pos = oracle.query_positions(pc)
     assert_topk_valid(got, ref, rs, rb, pos + 1, pc.topk_limit, RTOL["fp8_e4m3"], exact=False)
 
+# --------------------------------------------------- bf16 queries, e4m3 paged cache
+
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_mixed_decode_every_e4m3_code_exact(page_size):
+    pc = workloads.e4m3_code_sweep_decode(seed=40 + page_size, page_size=page_size)
+    for order in (0, 1):
+        got = run_paged(pc, order=order)
+        ref, _, _ = oracle.paged(pc, order=order)
+        assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("H", [4, 16, 64, 128])
+def test_mixed_decode_integer_exact(H):
+    lens = [1, 64, 65, 129, 700, 1000, 2047, 3000]
+    pc = workloads.paged_case(lens, [1] * len(lens), H, 128, 256, page_size=64, q_dtype="bf16",
+                              k_dtype="fp8_e4m3", integer=True, seed=41 + H)
+    got = run_paged(pc)
+    ref, _, _ = oracle.paged(pc)
+    assert np.array_equal(got, ref)
+
+
+def test_mixed_decode_gaussian_tolerance():
+    # bf16 x e4m3 products are exact in fp32: only the accumulation order differs
+    lens = [4096, 5000, 300, 1, 7777]
+    pc = workloads.paged_case(lens, [1] * len(lens), 64, 128, 2048, page_size=64, q_dtype="bf16",
+                              k_dtype="fp8_e4m3", w_std=1 / 8, seed=45)
+    got = run_paged(pc)
+    ref, rs, rb = oracle.paged(pc, want_scores=True, want_bound=True)
+    pos = oracle.query_positions(pc)
+    assert_topk_valid(got, ref, rs, rb, pos + 1, pc.topk_limit, RTOL["bf16"], exact=False)
+
+
 
 def test_paged_bad_page_is_reported_not_faulted():
     pc = workloads.paged_case([500, 300], [1, 1], 64, 128, 64, page_size=64, integer=True, seed=14)

@@ -255,6 +255,37 @@ def chunked_prefill_fp8(seed: int = 0, n_new: int = 8192, ctx: int = 65536) -> P
                       w_std=1.0 / 8.0, seed=seed)
 
 
+def e4m3_code_sweep_decode(seed: int = 0, B: int = 8, H: int = 64, page_size: int = 64) -> PagedCase:
+    """Decode against an e4m3 cache in which every finite e4m3 code (254 of them, both
+    zeros and all subnormals included) appears once per sequence in one column d_b.
+    Query b is +-1 at d_b in head 0 (other heads random integers), w is +-1 on head 0
+    and 0 elsewhere, so each score is one decoded code times its power-of-two key
+    scale: exact in any precision, ties only where the ReLU gives 0.  q is bf16."""
+    g = _gen(seed)
+    codes = torch.tensor([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=torch.uint8)
+    n = codes.numel()
+    pc = paged_case([n] * B, [1] * B, H, 128, n, page_size=page_size, k_out=n + 2,
+                    q_dtype=BF16, k_dtype=FP8, integer=True, seed=seed)
+    raw = torch.randint(0, 254, (pc.k_cache.shape[0], page_size, 128), generator=g).to(torch.uint8)
+    raw = torch.where(raw >= 0x7F, raw + 1, raw)          # skip the NaN code 0x7F (0xFF is out of range)
+    cols = (torch.randperm(128, generator=g)[:B]).tolist()
+    q = randint_values((B, H, 128), -4, 4, g)
+    w = torch.zeros((B, H))
+    for b in range(B):
+        perm = codes[torch.randperm(n, generator=g)]
+        for j in range(n):
+            page = int(pc.block_tables[b, j // page_size])
+            raw[page, j % page_size, cols[b]] = perm[j]
+        sign = 1.0 if (b % 2 == 0) else -1.0
+        q[b, 0, :] = 0
+        q[b, 0, cols[b]] = sign
+        w[b, 0] = 1.0 if torch.randint(0, 2, (1,), generator=g).item() else -1.0
+    pc.k_cache = raw.view(torch.float8_e4m3fn).contiguous()
+    pc.q = q.to(torch.bfloat16).contiguous()
+    pc.w = w.contiguous()
+    return pc
+
+
 INDEXSHARE_TYPES_12 = ["full", "shared", "shared"] * 4
 
 
