@@ -11,16 +11,20 @@
 // (each query's H heads are H consecutive TMEM columns), K = D.  A TMEM lane then
 // holds every head of one (key, query) pair, so the head reduction is in-thread.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over work items):
+// Warp roles (320 threads, 448 with the key converters; one CTA per SM, persistent
+// over work items):
 //   warp 0      TMA producer: q tile (N x D) per item into a 2-deep ring, key tiles
 //               (128 x D, dense or gathered page by page through block_tables) into
-//               an nK-deep ring, per-item w / q_scale and per-tile k_scale by cp.async.
+//               an nK-deep ring, per-item w / q_scale by cp.async, per-tile k_scale by
+//               cp.async (dense keys) or one bulk copy per page (paged keys).
 //   warp 1      TMEM allocator; lane 0 issues tcgen05.mma into two 256-column fp32
 //               accumulators (double buffered) and commits to mbarriers.
 //   warps 2..9  epilogue: tcgen05.ld, ReLU, head-weighted sum, k scale, causal mask,
 //               coalesced fp32 stores.  Prefill tiles (N = 256) are split by columns
 //               between two warpgroups; decode tiles (N = max(64, H)) alternate
 //               between the warpgroups tile by tile.
+//   warps 10-13 only for bf16 queries against e4m3 keys (decode): widen each staged
+//               e4m3 key tile to bf16 in the MMA's shared-memory layout.
 // Every wait is bounded; on a timeout the kernel records kStatusTimeout, all roles
 // leave their loops, in-flight copies and MMAs are drained (bounded) and TMEM freed.
 #include "internal.h"
@@ -147,11 +151,11 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
                            v ? 16u : 0u);
       }
       ptx::cp_async_mbar_arrive_noinc(&bars[kBarQFull + s]);
-      if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(&bars[kBarQFull + s], q_bytes);
-        for (int at = 0; at < n_atoms_q; ++at)
-          ptx::tma_load_2d(smem + P.q[s] + at * N * 128, tmap_q, &bars[kBarQFull + s], at * box_q, I.row0 * H);
-      }
+      if (lane == 0) ptx::mbar_arrive_expect_tx(&bars[kBarQFull + s], q_bytes);
+      __syncwarp();
+      // one TMA instruction: lane `at` copies 128-byte atom column `at`
+      if (lane < n_atoms_q)
+        ptx::tma_load_2d(smem + P.q[s] + lane * N * 128, tmap_q, &bars[kBarQFull + s], lane * box_q, I.row0 * H);
       ++nq;
     }
     // ---- key tiles
@@ -172,6 +176,8 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
       // mixed: the e4m3 tile and its scales land in the staging slot; converters fill P.k
       uint64_t* full = a.mixed ? &bars[kBarK8Full + s] : &bars[kBarKFull + s];
       uint8_t* dst = smem + (a.mixed ? P.k8[s] : P.k[s]);
+      // Each TMA instruction costs the issuing warp a fixed time however many lanes
+      // issue it, so every copy of a tile goes out in one instruction, one lane per copy.
       if (!a.paged) {
         if (a.k_fp8) {
           const long long e = static_cast<long long>(kt) * kBlockM + 4 * lane;
@@ -186,11 +192,9 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
           }
           ptx::cp_async_mbar_arrive_noinc(full);
         }
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(full, static_cast<uint32_t>(kBlockM) * a.D * k_esz);
-          for (int at = 0; at < n_atoms_k; ++at)
-            ptx::tma_load_2d(dst + at * kBlockM * 128, tmap_k, full, at * box_k, kt * kBlockM);
-        }
+        if (lane == 0) ptx::mbar_arrive_expect_tx(full, static_cast<uint32_t>(kBlockM) * a.D * k_esz);
+        __syncwarp();
+        if (lane < n_atoms_k) ptx::tma_load_2d(dst + lane * kBlockM * 128, tmap_k, full, lane * box_k, kt * kBlockM);
       } else {
         const int lp0 = kt * ppt;
         if (lp0 < win0 || lp0 + ppt > win0 + 32) {
@@ -198,40 +202,25 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
           const int lp = win0 + lane;
           pg_win = lp < a.max_pages_per_seq ? __ldg(bt_row + lp) : -1;
         }
-        // page j of this tile is handled by lane j
-        int phys = -1;
-        bool valid = false;
-        {
-          const int j = lane;
-          const int src_lane = (lp0 - win0 + (j < ppt ? j : 0)) & 31;
-          const int pg = __shfl_sync(0xffffffffu, pg_win, src_lane);
-          const bool needed = j < ppt && static_cast<long long>(lp0 + j) * PS <= pos_last;
-          valid = needed && pg >= 0 && pg < a.num_pages;
-          if (needed && !valid) atomicOr(a.status, kStatusBadPage);
-          phys = valid ? pg : -1;
-        }
-        const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-        if (a.k_fp8) {
-          // lane l copies scale floats [4l, 4l + 4) of the tile
-          const int j = (4 * lane) / PS;
-          const int pj = __shfl_sync(0xffffffffu, phys, j);
-          const bool v = (vmask >> j) & 1u;
-          const float* src = v ? a.k_scale + static_cast<long long>(pj) * PS + (4 * lane) % PS : a.k_scale;
-          ptx::cp_async_16(ksbuf + s * kBlockM + 4 * lane, src, v ? 16u : 0u);
-          ptx::cp_async_mbar_arrive_noinc(full);
-        }
-        int pj_all[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) pj_all[j] = __shfl_sync(0xffffffffu, phys, j);
+        // lane l copies atom column (l % n_atoms_k) of page (l / n_atoms_k) of this tile
+        const int j = n_atoms_k == 2 ? (lane >> 1) : lane;
+        const int at = lane - j * n_atoms_k;
+        const int pg = __shfl_sync(0xffffffffu, pg_win, (lp0 - win0 + (j < ppt ? j : 0)) & 31);
+        const bool needed = j < ppt && static_cast<long long>(lp0 + j) * PS <= pos_last;
+        const bool valid = needed && pg >= 0 && pg < a.num_pages;
+        if (needed && !valid && at == 0) atomicOr(a.status, kStatusBadPage);
+        const unsigned vmask = __ballot_sync(0xffffffffu, valid && at == 0);
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(vmask)) * page_bytes);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (j < ppt && ((vmask >> j) & 1u)) {
-              for (int at = 0; at < n_atoms_k; ++at)
-                ptx::tma_load_3d(dst + at * kBlockM * 128 + j * PS * 128, tmap_k, full, at * box_k, 0, pj_all[j]);
-            }
-          }
+          // page rows, plus (e4m3) the page's fp32 key scales
+          const uint32_t per_page = page_bytes + (a.k_fp8 ? static_cast<uint32_t>(PS) * 4u : 0u);
+          ptx::mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(vmask)) * per_page);
+        }
+        __syncwarp();
+        if (valid) {
+          ptx::tma_load_3d(dst + at * kBlockM * 128 + j * PS * 128, tmap_k, full, at * box_k, 0, pg);
+          if (a.k_fp8 && at == 0)
+            ptx::bulk_load(ksbuf + s * kBlockM + j * PS, a.k_scale + static_cast<long long>(pg) * PS,
+                           static_cast<uint32_t>(PS) * 4u, full);
         }
       }
       ++nk;
@@ -376,8 +365,11 @@ __device__ __forceinline__ void convert_role(const ScoreArgs& a, uint8_t* smem, 
                                     e4m3x2_to_bf16x2(__byte_perm(v.w, 0, 0x3424)));
         uint8_t* rowp = dst + (j >> 2) * (kBlockM * 128) + r * 128;
         const int c0 = (2 * j) & 7;
-        *reinterpret_cast<uint4*>(rowp + ((c0 ^ (r & 7)) << 4)) = o0;
-        *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)) = o1;
+        // lanes j < 4 write the even chunk first, lanes j >= 4 the odd one: the eight
+        // lanes of a row then hit eight different bank groups in each store
+        const bool odd_first = j >= 4;
+        *reinterpret_cast<uint4*>(rowp + (((c0 + (odd_first ? 1 : 0)) ^ (r & 7)) << 4)) = odd_first ? o1 : o0;
+        *reinterpret_cast<uint4*>(rowp + (((c0 + (odd_first ? 0 : 1)) ^ (r & 7)) << 4)) = odd_first ? o0 : o1;
       }
       ptx::fence_proxy_async_smem();  // the tensor core reads these through the async proxy
       __syncwarp();
@@ -542,9 +534,10 @@ __global__ void __launch_bounds__(MIXED ? kMixedThreads : kScoreThreads, 1)
     }
     ptx::mbar_init(&bars[kBarDone], 1);
     for (int s = 0; s < a.num_k_stages; ++s) {
-      ptx::mbar_init(&bars[kBarKFull + s], MIXED ? 4 : 1 + (a.k_fp8 ? 32 : 0));
+      // dense e4m3 key scales come by cp.async (32 lane arrivals); paged ones by bulk copy
+      ptx::mbar_init(&bars[kBarKFull + s], MIXED ? 4 : 1 + ((a.k_fp8 && !a.paged) ? 32 : 0));
       ptx::mbar_init(&bars[kBarKEmpty + s], 1 + (a.k_fp8 ? C::EPI_T_ARRIVALS : 0));
-      ptx::mbar_init(&bars[kBarK8Full + s], 1 + 32);
+      ptx::mbar_init(&bars[kBarK8Full + s], 1);
       ptx::mbar_init(&bars[kBarK8Empty + s], 4);
     }
     *abort = 0;
