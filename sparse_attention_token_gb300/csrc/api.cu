@@ -143,7 +143,9 @@ bool make_map_paged(CUtensorMap* m, const void* base, bool fp8, int D, int page_
 
 // Deepest key-tile ring that fits in shared memory (>= 2), or 0.
 int pick_stages(const ScoreArgs& a) {
-  for (int s = kMaxKStages; s >= 2; --s)
+  // mixed mode: each stage also holds 64 TMEM columns next to the two accumulators
+  const int top = a.mixed ? std::min(kMaxKStages, mixed_stage_limit(a.N)) : kMaxKStages;
+  for (int s = top; s >= 2; --s)
     if (score_smem_bytes(a, s) <= kMaxSmem) return s;
   return 0;
 }

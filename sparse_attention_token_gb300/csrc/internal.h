@@ -79,6 +79,9 @@ struct TopkArgs {
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
                          int grid, size_t smem_bytes, cudaStream_t st);
 size_t score_smem_bytes(const ScoreArgs& a, int num_k_stages);
+// Key stages the mixed (bf16 q, e4m3 keys) decode kernel can hold in TMEM beside its two
+// N-column accumulators: 64 columns per stage in the two 256-column halves.
+inline int mixed_stage_limit(int N) { return 2 * ((256 - N) / 64); }
 // Prefill (N = 256) on CTA pairs: grid = 2 x pairs, work items in 256-key tiles.
 cudaError_t launch_score_pair(const ScoreArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k, int grid,
                               size_t smem_bytes, cudaStream_t st);

@@ -24,7 +24,7 @@
 //               between two warpgroups; decode tiles (N = max(64, H)) alternate
 //               between the warpgroups tile by tile.
 //   warps 10-13 only for bf16 queries against e4m3 keys (decode): widen each staged
-//               e4m3 key tile to bf16 in the MMA's shared-memory layout.
+//               e4m3 key tile to bf16 into TMEM, the MMA's A operand there.
 // Every wait is bounded; on a timeout the kernel records kStatusTimeout, all roles
 // leave their loops, in-flight copies and MMAs are drained (bounded) and TMEM freed.
 #include "internal.h"
@@ -45,7 +45,8 @@ __host__ __device__ inline SmemPlan plan_smem(int N, int D, int q_fp8, int k_fp8
   SmemPlan p{};
   uint32_t off = 0;
   const uint32_t qb = static_cast<uint32_t>(N) * D * (q_fp8 ? 1 : 2);
-  const uint32_t kb = static_cast<uint32_t>(kBlockM) * D * ((k_fp8 && !mixed) ? 1 : 2);
+  // mixed: the widened keys live in TMEM, only the e4m3 staging ring is in shared memory
+  const uint32_t kb = mixed ? 0u : static_cast<uint32_t>(kBlockM) * D * (k_fp8 ? 1 : 2);
   for (int i = 0; i < 2; ++i) { p.q[i] = off; off += qb; }
   for (int i = 0; i < kMaxKStages; ++i) { p.k[i] = off; if (i < nK) off += kb; }
   for (int i = 0; i < kMaxKStages; ++i) { p.k8[i] = off; if (mixed && i < nK) off += static_cast<uint32_t>(kBlockM) * D; }
@@ -56,6 +57,13 @@ __host__ __device__ inline SmemPlan plan_smem(int N, int D, int q_fp8, int k_fp8
   p.misc = off;  off += 16u;
   p.total = off;
   return p;
+}
+
+// Mixed mode: TMEM column of key stage s widened to bf16 (128 lanes x 64 columns).  The
+// accumulators take columns [0, N) and [256, 256 + N); the stages fill the rest.
+__device__ __forceinline__ uint32_t mixed_a_col(int s, int N) {
+  const int per = (256 - N) / 64;
+  return static_cast<uint32_t>(s < per ? N + 64 * s : 256 + N + 64 * (s - per));
 }
 
 // Barrier slots inside the bars region.
@@ -248,7 +256,7 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
 // everything in registers: stage index and phase advance incrementally, stage
 // addresses come from one multiply, and the per-step descriptors are the first
 // step's descriptors plus a compile-time offset in their 16-byte address field.
-template <int H, bool DECODE, bool F8, int NSTEPS>
+template <int H, bool DECODE, bool F8, int NSTEPS, bool ATMEM = false>
 __device__ __forceinline__ void mma_loop(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P, uint64_t* bars,
                                          volatile int* abort, int n_items, uint32_t tmem_base) {
   using C = Cfg<H, DECODE>;
@@ -276,14 +284,24 @@ __device__ __forceinline__ void mma_loop(const ScoreArgs& a, uint8_t* smem, cons
       }
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
-      const uint64_t adesc0 = ptx::sw128_kmajor_desc(k_base + sk * k_stage_bytes);
+      if constexpr (ATMEM) {
+        // keys widened into TMEM: step j takes columns [8j, 8j + 8) (16 bf16 of K)
+        const uint32_t a_tmem = tmem_base + mixed_a_col(static_cast<int>(sk), N);
 #pragma unroll
-      for (int j = 0; j < NSTEPS; ++j) {
-        // step j reads 32 bytes of K at atom (j / 4), byte (j % 4) * 32 of each row
-        const uint64_t ad = adesc0 + static_cast<uint64_t>(((j >> 2) * (kBlockM * 128) + (j & 3) * 32) >> 4);
-        const uint64_t bd = bdesc0 + static_cast<uint64_t>(((j >> 2) * (N * 128) + (j & 3) * 32) >> 4);
-        if (F8) ptx::mma_f8(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
-        else ptx::mma_bf16(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
+        for (int j = 0; j < NSTEPS; ++j) {
+          const uint64_t bd = bdesc0 + static_cast<uint64_t>(((j >> 2) * (N * 128) + (j & 3) * 32) >> 4);
+          ptx::mma_bf16_ts(d_tmem, a_tmem + 8 * j, bd, idesc, j > 0 ? 1u : 0u);
+        }
+      } else {
+        const uint64_t adesc0 = ptx::sw128_kmajor_desc(k_base + sk * k_stage_bytes);
+#pragma unroll
+        for (int j = 0; j < NSTEPS; ++j) {
+          // step j reads 32 bytes of K at atom (j / 4), byte (j % 4) * 32 of each row
+          const uint64_t ad = adesc0 + static_cast<uint64_t>(((j >> 2) * (kBlockM * 128) + (j & 3) * 32) >> 4);
+          const uint64_t bd = bdesc0 + static_cast<uint64_t>(((j >> 2) * (N * 128) + (j & 3) * 32) >> 4);
+          if (F8) ptx::mma_f8(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
+          else ptx::mma_bf16(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
+        }
       }
       ptx::mma_commit(&bars[kBarKEmpty + sk]);
       ptx::mma_commit(&bars[kBarTFull + acc]);
@@ -304,6 +322,7 @@ __device__ __forceinline__ void mma_role(const ScoreArgs& a, uint8_t* smem, cons
                                          volatile int* abort, int n_items, uint32_t tmem_base) {
   // 32 bytes of K per MMA: 16 bf16 or 32 e4m3 values; mixed mode multiplies bf16 by widened keys
   if (a.q_fp8) mma_loop<H, DECODE, true, 4>(a, smem, P, bars, abort, n_items, tmem_base);
+  else if (DECODE && a.mixed) mma_loop<H, DECODE, false, 8, DECODE>(a, smem, P, bars, abort, n_items, tmem_base);
   else if (a.D == 128) mma_loop<H, DECODE, false, 8>(a, smem, P, bars, abort, n_items, tmem_base);
   else mma_loop<H, DECODE, false, 4>(a, smem, P, bars, abort, n_items, tmem_base);
 }
@@ -328,15 +347,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t t) {
   return r;
 }
 
-// Widen every staged e4m3 key tile (128 rows x D=128 bytes, 128-byte swizzle) into the
-// bf16 MMA layout (two 128-byte atom columns, same swizzle).  Each warp converts 32
-// rows, 4 rows per step: lane l takes 16-byte chunk l%8 of row l/8.
+// Widen every staged e4m3 key tile (128 rows x D=128 bytes, 128-byte swizzle) to bf16
+// straight into TMEM, where the MMA reads it as its A operand.  Warp w owns TMEM lanes
+// [32 (w % 4), 32 (w % 4) + 32): lane l converts key row 32 (w % 4) + l, 64 columns.
 template <int H, bool DECODE>
 __device__ __forceinline__ void convert_role(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P, uint64_t* bars,
-                                             volatile int* abort, int n_items) {
+                                             volatile int* abort, int n_items, uint32_t tmem_base) {
   using C = Cfg<H, DECODE>;
-  const int cw = (static_cast<int>(threadIdx.x) >> 5) - 10;
+  const int quarter = (threadIdx.x >> 5) & 3;
   const int lane = threadIdx.x & 31;
+  const int r = quarter * 32 + lane;
+  const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
   const int nK = a.num_k_stages;
   uint32_t sk = 0, kph = 0;
   bool ok = true;
@@ -348,30 +369,29 @@ __device__ __forceinline__ void convert_role(const ScoreArgs& a, uint8_t* smem, 
         ok = false;
         break;
       }
-      const uint8_t* src = smem + P.k8[sk];
-      uint8_t* dst = smem + P.k[sk];
-#pragma unroll 2
-      for (int st = 0; st < 8; ++st) {
-        const int r = cw * 32 + st * 4 + (lane >> 3);
-        const int j = lane & 7;
-        const uint4 v = *reinterpret_cast<const uint4*>(src + r * 128 + ((j ^ (r & 7)) << 4));
-        const uint4 o0 = make_uint4(e4m3x2_to_bf16x2(__byte_perm(v.x, 0, 0x1404)),
-                                    e4m3x2_to_bf16x2(__byte_perm(v.x, 0, 0x3424)),
-                                    e4m3x2_to_bf16x2(__byte_perm(v.y, 0, 0x1404)),
-                                    e4m3x2_to_bf16x2(__byte_perm(v.y, 0, 0x3424)));
-        const uint4 o1 = make_uint4(e4m3x2_to_bf16x2(__byte_perm(v.z, 0, 0x1404)),
-                                    e4m3x2_to_bf16x2(__byte_perm(v.z, 0, 0x3424)),
-                                    e4m3x2_to_bf16x2(__byte_perm(v.w, 0, 0x1404)),
-                                    e4m3x2_to_bf16x2(__byte_perm(v.w, 0, 0x3424)));
-        uint8_t* rowp = dst + (j >> 2) * (kBlockM * 128) + r * 128;
-        const int c0 = (2 * j) & 7;
-        // lanes j < 4 write the even chunk first, lanes j >= 4 the odd one: the eight
-        // lanes of a row then hit eight different bank groups in each store
-        const bool odd_first = j >= 4;
-        *reinterpret_cast<uint4*>(rowp + (((c0 + (odd_first ? 1 : 0)) ^ (r & 7)) << 4)) = odd_first ? o1 : o0;
-        *reinterpret_cast<uint4*>(rowp + (((c0 + (odd_first ? 0 : 1)) ^ (r & 7)) << 4)) = odd_first ? o0 : o1;
+      const uint8_t* row = smem + P.k8[sk] + r * 128;
+      const uint32_t acol = tmem_base + lane_addr + mixed_a_col(static_cast<int>(sk), C::N);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t o[32];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          // logical 16-byte chunk c = e4m3 elements [16c, 16c + 16) -> columns [8c, 8c + 8)
+          const int c = 4 * hh + c4;
+          const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
+          o[8 * c4 + 0] = e4m3x2_to_bf16x2(__byte_perm(v.x, 0, 0x1404));
+          o[8 * c4 + 1] = e4m3x2_to_bf16x2(__byte_perm(v.x, 0, 0x3424));
+          o[8 * c4 + 2] = e4m3x2_to_bf16x2(__byte_perm(v.y, 0, 0x1404));
+          o[8 * c4 + 3] = e4m3x2_to_bf16x2(__byte_perm(v.y, 0, 0x3424));
+          o[8 * c4 + 4] = e4m3x2_to_bf16x2(__byte_perm(v.z, 0, 0x1404));
+          o[8 * c4 + 5] = e4m3x2_to_bf16x2(__byte_perm(v.z, 0, 0x3424));
+          o[8 * c4 + 6] = e4m3x2_to_bf16x2(__byte_perm(v.w, 0, 0x1404));
+          o[8 * c4 + 7] = e4m3x2_to_bf16x2(__byte_perm(v.w, 0, 0x3424));
+        }
+        ptx::tmem_st_32x32b_x32(acol + 32 * hh, o);
       }
-      ptx::fence_proxy_async_smem();  // the tensor core reads these through the async proxy
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         ptx::mbar_arrive(&bars[kBarKFull + sk]);
@@ -566,7 +586,7 @@ __global__ void __launch_bounds__(MIXED ? kMixedThreads : kScoreThreads, 1)
     if (lane == 0) mma_role<H, DECODE>(a, smem, P, bars, abort, n_items, tmem_base);
     __syncwarp();
   } else if (MIXED && warp >= 10) {
-    convert_role<H, DECODE>(a, smem, P, bars, abort, n_items);
+    convert_role<H, DECODE>(a, smem, P, bars, abort, n_items, tmem_base);
   } else {
     epilogue_role<H, DECODE>(a, smem, P, bars, abort, n_items, tmem_base);
   }
