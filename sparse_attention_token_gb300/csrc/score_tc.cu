@@ -16,7 +16,8 @@
 //   warp 0      TMA producer: q tile (N x D) per item into a 2-deep ring, key tiles
 //               (128 x D, dense or gathered page by page through block_tables) into
 //               an nK-deep ring, per-item w / q_scale by cp.async, per-tile k_scale by
-//               cp.async (dense keys) or one bulk copy per page (paged keys).
+//               cp.async (dense keys) or a bulk copy per page (paged prefill); decode
+//               epilogue threads read their paged key scales from global memory.
 //   warp 1      TMEM allocator; lane 0 issues tcgen05.mma into two 256-column fp32
 //               accumulators (double buffered) and commits to mbarriers.
 //   warps 2..9  epilogue: tcgen05.ld, ReLU, head-weighted sum, k scale, causal mask,
@@ -218,15 +219,17 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
         const bool valid = needed && pg >= 0 && pg < a.num_pages;
         if (needed && !valid && at == 0) atomicOr(a.status, kStatusBadPage);
         const unsigned vmask = __ballot_sync(0xffffffffu, valid && at == 0);
+        // e4m3 key scales: decode epilogue threads read their own from global memory;
+        // prefill tiles take them by one bulk copy per page into ksbuf
+        const bool ks_bulk = a.k_fp8 && !DECODE;
         if (lane == 0) {
-          // page rows, plus (e4m3) the page's fp32 key scales
-          const uint32_t per_page = page_bytes + (a.k_fp8 ? static_cast<uint32_t>(PS) * 4u : 0u);
+          const uint32_t per_page = page_bytes + (ks_bulk ? static_cast<uint32_t>(PS) * 4u : 0u);
           ptx::mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(vmask)) * per_page);
         }
         __syncwarp();
         if (valid) {
           ptx::tma_load_3d(dst + at * kBlockM * 128 + j * PS * 128, tmap_k, full, at * box_k, 0, pg);
-          if (a.k_fp8 && at == 0)
+          if (ks_bulk && at == 0)
             ptx::bulk_load(ksbuf + s * kBlockM + j * PS, a.k_scale + static_cast<long long>(pg) * PS,
                            static_cast<uint32_t>(PS) * 4u, full);
         }
@@ -446,7 +449,22 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
       const int acc = nt & 1;
       const bool mine = DECODE ? (acc == half) : true;
       if (mine) {
-        if (a.k_fp8 && !warp_wait(&bars[kBarKFull + sk], (nk / nK) & 1, abort, a.status)) {
+        // paged e4m3 keys: this thread's key scale straight from global memory (page
+        // table, then the page's scale row), issued before the accumulator wait so the
+        // two dependent loads overlap it; dense e4m3 keys: the staged copy in ksbuf
+        float ks_g = 1.f;
+        const bool ks_smem = a.k_fp8 && !(DECODE && a.paged);
+        if (a.k_fp8 && !ks_smem) {
+          const long long key = static_cast<long long>(kt) * kBlockM + m;
+          const int lp = static_cast<int>(key / a.page_size);
+          const int pg = (lp < a.max_pages_per_seq && key <= I.pos0 + I.nrows - 1)
+                             ? __ldg(a.block_tables + static_cast<long long>(I.b) * a.max_pages_per_seq + lp)
+                             : -1;
+          ks_g = (pg >= 0 && pg < a.num_pages)
+                     ? __ldg(a.k_scale + static_cast<long long>(pg) * a.page_size + (key - static_cast<long long>(lp) * a.page_size))
+                     : 0.f;
+        }
+        if (ks_smem && !warp_wait(&bars[kBarKFull + sk], (nk / nK) & 1, abort, a.status)) {
           ok = false;
           break;
         }
@@ -500,8 +518,8 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&bars[kBarTEmpty + acc]);
-        float ks = 1.f;
-        if (a.k_fp8) {
+        float ks = ks_g;
+        if (ks_smem) {
           ks = ksbuf[sk * kBlockM + m];
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&bars[kBarKEmpty + sk]);
@@ -556,7 +574,8 @@ __global__ void __launch_bounds__(MIXED ? kMixedThreads : kScoreThreads, 1)
     for (int s = 0; s < a.num_k_stages; ++s) {
       // dense e4m3 key scales come by cp.async (32 lane arrivals); paged ones by bulk copy
       ptx::mbar_init(&bars[kBarKFull + s], MIXED ? 4 : 1 + ((a.k_fp8 && !a.paged) ? 32 : 0));
-      ptx::mbar_init(&bars[kBarKEmpty + s], 1 + (a.k_fp8 ? C::EPI_T_ARRIVALS : 0));
+      // the epilogue also releases a stage when it reads that stage's key scales from ksbuf
+      ptx::mbar_init(&bars[kBarKEmpty + s], 1 + ((a.k_fp8 && !(DECODE && a.paged)) ? C::EPI_T_ARRIVALS : 0));
       ptx::mbar_init(&bars[kBarK8Full + s], 1);
       ptx::mbar_init(&bars[kBarK8Empty + s], 4);
     }
