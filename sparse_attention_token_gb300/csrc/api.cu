@@ -143,8 +143,8 @@ bool make_map_paged(CUtensorMap* m, const void* base, bool fp8, int D, int page_
 
 // Deepest key-tile ring that fits in shared memory (>= 2), or 0.
 int pick_stages(const ScoreArgs& a) {
-  // mixed mode: each stage also holds 64 TMEM columns next to the two accumulators
-  const int top = a.mixed ? std::min(kMaxKStages, mixed_stage_limit(a.N)) : kMaxKStages;
+  // mixed mode: the ring in shared memory holds e4m3 tiles only (the widened ones live in TMEM)
+  const int top = a.mixed ? kMaxK8Stages : kMaxKStages;
   for (int s = top; s >= 2; --s)
     if (score_smem_bytes(a, s) <= kMaxSmem) return s;
   return 0;
@@ -269,6 +269,7 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
   s.status = status;
   s.num_k_stages = p.pair ? pick_stages_pair(s) : pick_stages(s);
   if (s.num_k_stages < 2) return DSA_ERR_UNSUPPORTED;
+  s.num_a_stages = s.mixed ? std::min(kMaxKStages, mixed_stage_limit(s.N)) : 0;
 
   CUtensorMap tq, tk;
   if (!make_map_2d(&tq, a->q, fp8, a->D, static_cast<long long>(a->total_q) * a->H, p.pair ? p.N / 2 : p.N))

@@ -22,6 +22,7 @@ constexpr int kBlockM = 128;             // keys per MMA tile (TMEM lanes)
 constexpr int kScoreThreads = 320;       // warp 0 TMA, warp 1 MMA/TMEM, warps 2..9 epilogue
 constexpr int kMixedThreads = 448;       // + warps 10..13 widening e4m3 keys to bf16
 constexpr int kMaxKStages = 8;
+constexpr int kMaxK8Stages = 12;       // e4m3 staging ring of the mixed decode kernel
 constexpr int kTmemCols = 512;           // two accumulators at column 0 and 256
 constexpr int kMaxN = 256;               // MMA N (queries x heads per tile)
 
@@ -39,7 +40,8 @@ struct ScoreArgs {
   int q_fp8, k_fp8;   // element type of q / keys (1 = e4m3, 0 = bf16)
   int mixed;          // bf16 q with e4m3 keys: keys are widened to bf16 in shared memory
   int H, D, NQ, N;    // N = NQ * H
-  int num_k_stages;
+  int num_k_stages;   // key ring depth (mixed mode: the e4m3 staging ring in shared memory)
+  int num_a_stages;   // mixed mode: ring of widened key tiles in TMEM
   // dense single sequence
   int T, S, q_pos0, n_dense_items;
   // paged varlen

@@ -38,7 +38,7 @@ namespace {
 struct SmemPlan {
   uint32_t q[2];
   uint32_t k[kMaxKStages];
-  uint32_t k8[kMaxKStages];  // e4m3 staging of the keys (mixed mode)
+  uint32_t k8[kMaxK8Stages];  // e4m3 staging of the keys (mixed mode)
   uint32_t wbuf, qsbuf, ksbuf, bars, misc, total;
 };
 
@@ -50,11 +50,11 @@ __host__ __device__ inline SmemPlan plan_smem(int N, int D, int q_fp8, int k_fp8
   const uint32_t kb = mixed ? 0u : static_cast<uint32_t>(kBlockM) * D * (k_fp8 ? 1 : 2);
   for (int i = 0; i < 2; ++i) { p.q[i] = off; off += qb; }
   for (int i = 0; i < kMaxKStages; ++i) { p.k[i] = off; if (i < nK) off += kb; }
-  for (int i = 0; i < kMaxKStages; ++i) { p.k8[i] = off; if (mixed && i < nK) off += static_cast<uint32_t>(kBlockM) * D; }
+  for (int i = 0; i < kMaxK8Stages; ++i) { p.k8[i] = off; if (mixed && i < nK) off += static_cast<uint32_t>(kBlockM) * D; }
   p.wbuf = off;  off += 2u * N * 4u;
   p.qsbuf = off; if (q_fp8) off += 2u * N * 4u;
-  p.ksbuf = off; if (k_fp8) off += static_cast<uint32_t>(nK) * kBlockM * 4u;
-  p.bars = off;  off += 48u * 8u;
+  p.ksbuf = off; if (k_fp8 && !mixed) off += static_cast<uint32_t>(nK) * kBlockM * 4u;  // mixed decode reads scales from global
+  p.bars = off;  off += 64u * 8u;
   p.misc = off;  off += 16u;
   p.total = off;
   return p;
@@ -70,10 +70,12 @@ __device__ __forceinline__ uint32_t mixed_a_col(int s, int N) {
 // Barrier slots inside the bars region.
 enum {
   kBarQFull = 0, kBarQEmpty = 2, kBarTFull = 4, kBarTEmpty = 6, kBarFold = 8,  // fold: 4 slots
+  // key ring; in mixed mode the ring of widened tiles in TMEM (full: converted, empty: MMAs done)
   kBarDone = 12, kBarKFull = 13, kBarKEmpty = 13 + kMaxKStages,
-  kBarK8Full = 13 + 2 * kMaxKStages,   // mixed: e4m3 key tile (and its scales) landed
-  kBarK8Empty = 13 + 3 * kMaxKStages   // mixed: e4m3 staging slot converted
+  kBarK8Full = 13 + 2 * kMaxKStages,                  // mixed: e4m3 key tile landed in shared memory
+  kBarK8Empty = 13 + 2 * kMaxKStages + kMaxK8Stages   // mixed: e4m3 staging slot converted
 };
+static_assert(kBarK8Empty + kMaxK8Stages <= 64, "barrier region");
 
 struct ItemInfo {
   int row0, pos0, kt0, kt1, b, nrows;
@@ -176,15 +178,15 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
       const int s = nk % nK;
       int good = 1;
       if (lane == 0) {
-        good = ptx::mbar_wait(&bars[kBarKEmpty + s], ((nk / nK) & 1) ^ 1, abort, a.status, kStatusTimeout);
-        if (good && a.mixed)
-          good = ptx::mbar_wait(&bars[kBarK8Empty + s], ((nk / nK) & 1) ^ 1, abort, a.status, kStatusTimeout);
+        // mixed: the staging slot is free once the converters have read it
+        good = ptx::mbar_wait(&bars[(a.mixed ? kBarK8Empty : kBarKEmpty) + s], ((nk / nK) & 1) ^ 1, abort, a.status,
+                              kStatusTimeout);
       }
       good = __shfl_sync(0xffffffffu, good, 0);
       if (!good) { ok = false; break; }
       // mixed: the e4m3 tile and its scales land in the staging slot; converters fill P.k
       uint64_t* full = a.mixed ? &bars[kBarK8Full + s] : &bars[kBarKFull + s];
-      uint8_t* dst = smem + (a.mixed ? P.k8[s] : P.k[s]);
+      uint8_t* dst = smem + (a.mixed ? P.k8[0] + s * (P.k8[1] - P.k8[0]) : P.k[0] + s * (P.k[1] - P.k[0]));
       // Each TMA instruction costs the issuing warp a fixed time however many lanes
       // issue it, so every copy of a tile goes out in one instruction, one lane per copy.
       if (!a.paged) {
@@ -264,7 +266,7 @@ __device__ __forceinline__ void mma_loop(const ScoreArgs& a, uint8_t* smem, cons
                                          volatile int* abort, int n_items, uint32_t tmem_base) {
   using C = Cfg<H, DECODE>;
   constexpr int N = C::N;
-  const int nK = a.num_k_stages;
+  const int nK = ATMEM ? a.num_a_stages : a.num_k_stages;
   const uint32_t idesc = ptx::idesc_f32acc(kBlockM, N, !F8);
   const uint32_t sbase = ptx::smem_u32(smem);
   const uint32_t k_stage_bytes = P.k[1] - P.k[0];
@@ -361,19 +363,23 @@ __device__ __forceinline__ void convert_role(const ScoreArgs& a, uint8_t* smem, 
   const int lane = threadIdx.x & 31;
   const int r = quarter * 32 + lane;
   const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-  const int nK = a.num_k_stages;
-  uint32_t sk = 0, kph = 0;
+  const int nK = a.num_k_stages;   // e4m3 staging ring (shared memory)
+  const int nA = a.num_a_stages;   // widened tiles (TMEM)
+  const uint32_t k8_stage = P.k8[1] - P.k8[0];
+  uint32_t sk = 0, kph = 0, sa = 0, aph = 0;
   bool ok = true;
   for (int it = 0; ok; ++it) {
     ItemInfo I;
     if (!fetch_item<C::NQ>(a, n_items, it, I)) break;
     for (int kt = I.kt0; kt < I.kt1; ++kt) {
-      if (!warp_wait(&bars[kBarK8Full + sk], kph, abort, a.status)) {
+      // the staged tile has landed, and the MMAs that read this TMEM slot last are done
+      if (!warp_wait(&bars[kBarK8Full + sk], kph, abort, a.status) ||
+          !warp_wait(&bars[kBarKEmpty + sa], aph ^ 1u, abort, a.status)) {
         ok = false;
         break;
       }
-      const uint8_t* row = smem + P.k8[sk] + r * 128;
-      const uint32_t acol = tmem_base + lane_addr + mixed_a_col(static_cast<int>(sk), C::N);
+      const uint8_t* row = smem + P.k8[0] + sk * k8_stage + r * 128;
+      const uint32_t acol = tmem_base + lane_addr + mixed_a_col(static_cast<int>(sa), C::N);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t o[32];
@@ -397,10 +403,11 @@ __device__ __forceinline__ void convert_role(const ScoreArgs& a, uint8_t* smem, 
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        ptx::mbar_arrive(&bars[kBarKFull + sk]);
+        ptx::mbar_arrive(&bars[kBarKFull + sa]);
         ptx::mbar_arrive(&bars[kBarK8Empty + sk]);
       }
       if (++sk == static_cast<uint32_t>(nK)) { sk = 0; kph ^= 1u; }
+      if (++sa == static_cast<uint32_t>(nA)) { sa = 0; aph ^= 1u; }
     }
   }
 }
@@ -571,13 +578,19 @@ __global__ void __launch_bounds__(MIXED ? kMixedThreads : kScoreThreads, 1)
       ptx::mbar_init(&bars[kBarFold + 2 * s + 1], 128);
     }
     ptx::mbar_init(&bars[kBarDone], 1);
-    for (int s = 0; s < a.num_k_stages; ++s) {
-      // dense e4m3 key scales come by cp.async (32 lane arrivals); paged ones by bulk copy
+    const int n_ring = MIXED ? a.num_a_stages : a.num_k_stages;
+    for (int s = 0; s < n_ring; ++s) {
+      // dense e4m3 key scales come by cp.async (32 lane arrivals); paged ones by bulk copy;
+      // mixed: the four converter warps fill a TMEM slot
       ptx::mbar_init(&bars[kBarKFull + s], MIXED ? 4 : 1 + ((a.k_fp8 && !a.paged) ? 32 : 0));
       // the epilogue also releases a stage when it reads that stage's key scales from ksbuf
       ptx::mbar_init(&bars[kBarKEmpty + s], 1 + ((a.k_fp8 && !(DECODE && a.paged)) ? C::EPI_T_ARRIVALS : 0));
-      ptx::mbar_init(&bars[kBarK8Full + s], 1);
-      ptx::mbar_init(&bars[kBarK8Empty + s], 4);
+    }
+    if (MIXED) {
+      for (int s = 0; s < a.num_k_stages; ++s) {
+        ptx::mbar_init(&bars[kBarK8Full + s], 1);
+        ptx::mbar_init(&bars[kBarK8Empty + s], 4);
+      }
     }
     *abort = 0;
     ptx::fence_mbar_init();
