@@ -385,11 +385,12 @@ __device__ void radix_sort_desc(uint32_t* ka, uint32_t* va, uint32_t* kb, uint32
 // plus the number of bucket-mates that beat it (higher key, or equal key and lower
 // index).  Writes out[slot] = index for slots < keep.  Returns false (writing
 // nothing) when some bucket holds more than kBucketLimit keys -- many equal or
-// clustered scores -- so the caller sorts with the radix sort instead.
+// clustered scores -- so the caller sorts with the radix sort instead.  bk and bi
+// are adjacent scratch arrays (bi == bk + n at least), used together as n 8-byte words.
 constexpr int kBucketLimit = 64;
 constexpr int kSortBuckets = 4096;
 
-__device__ bool bucket_rank_out(const uint32_t* ck, const uint32_t* ci, int n, int keep, uint32_t* bk,
+__device__ bool bucket_rank_out(uint32_t* ck, const uint32_t* ci, int n, int keep, uint32_t* bk,
                                 uint32_t* bi, uint32_t* cur, uint32_t* red, int32_t* out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
@@ -445,25 +446,31 @@ __device__ bool bucket_rank_out(const uint32_t* ck, const uint32_t* ci, int n, i
     run += c[j];
   }
   __syncthreads();
+  // key and complemented index in one word: a larger word is a better key, or the same
+  // key at a lower index, so ranking is one 8-byte load and one compare per element
+  uint64_t* bw = reinterpret_cast<uint64_t*>(bk);  // bk and bi: 2n adjacent words
   for (int i = tid; i < n; i += kThreads) {
     const uint32_t u = ck[i];
     const uint32_t pos = atomicAdd(&cur[hslot((u >> sh) - base)], 1u);
-    bk[pos] = u;
-    bi[pos] = ci[i];
+    bw[pos] = (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~ci[i]);
   }
   __syncthreads();
   // cur[b] is now the end of bucket b; bucket b starts where bucket b + 1 ends
   for (int p = tid; p < n; p += kThreads) {
-    const uint32_t u = bk[p], idx = bi[p];
-    const int b = static_cast<int>((u >> sh) - base);
+    const uint64_t x = bw[p];
+    const int b = static_cast<int>((static_cast<uint32_t>(x >> 32) >> sh) - base);
     const uint32_t q0 = b + 1 < nb ? cur[hslot(b + 1)] : 0u, q1 = cur[hslot(b)];
     uint32_t rank = q0;
-    for (uint32_t q = q0; q < q1; ++q) {
-      const uint32_t v = bk[q];
-      rank += (v > u || (v == u && bi[q] < idx)) ? 1u : 0u;
-    }
-    if (rank < static_cast<uint32_t>(keep)) out[rank] = static_cast<int32_t>(idx);
+    uint32_t q = q0;
+    for (; q + 4 <= q1; q += 4)
+      rank += (bw[q] > x ? 1u : 0u) + (bw[q + 1] > x ? 1u : 0u) + (bw[q + 2] > x ? 1u : 0u) +
+              (bw[q + 3] > x ? 1u : 0u);
+    for (; q < q1; ++q) rank += bw[q] > x ? 1u : 0u;
+    if (rank < static_cast<uint32_t>(keep)) ck[rank] = ~static_cast<uint32_t>(x);  // ck is free after the scatter
   }
+  __syncthreads();
+  // coalesced copy-out (scattered 4-byte global stores were a third of the sort's time)
+  for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(ck[i]);
   return true;
 }
 
@@ -664,7 +671,6 @@ __global__ void __launch_bounds__(kThreads, NB == 8 ? 3 : 2) topk_kernel(const T
 }
 
 // ---------------------------------------------------------------- long rows: a cluster of CTAs per row
-constexpr int kClusterCtas = 8;
 
 __device__ __forceinline__ uint32_t dsmem_ld(uint32_t addr) {
   uint32_t v;
@@ -690,41 +696,43 @@ __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Sum the kClusterCtas local histograms (m.hist of every CTA) into m.merged of every CTA:
-// CTA r adds up bins [r, r + 1) * kBins / kClusterCtas, then every CTA gathers the rest.
-__device__ void cluster_merge_hist(const TopkSmem& m, uint32_t rank) {
-  constexpr int kSlice = kBins / kClusterCtas;
-  cluster_barrier();  // every local histogram is complete
-  for (int b = rank * kSlice + threadIdx.x; b < static_cast<int>(rank + 1) * kSlice; b += kThreads) {
-    uint32_t s = 0;
-#pragma unroll
-    for (int j = 0; j < kClusterCtas; ++j) s += dsmem_ld(mapa(&m.hist[hslot(b)], j));
-    m.merged[hslot(b)] = s;
-  }
-  cluster_barrier();  // every slice is merged
-  for (int b = threadIdx.x; b < kBins; b += kThreads) {
-    const uint32_t owner = static_cast<uint32_t>(b / kSlice);
-    if (owner != rank) m.merged[hslot(b)] = dsmem_ld(mapa(&m.merged[hslot(b)], owner));
-  }
-  cluster_barrier();  // no CTA reads another's histograms after this
+__device__ __forceinline__ void red_add_cluster(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-template <int NB>
+// Sum the CL local histograms (m.hist of every CTA) into m.merged of every CTA: each CTA
+// adds its non-zero bins into every CTA's merged histogram with remote atomics (a row's
+// keys fill a few hundred of the 4096 bins), between two cluster barriers.  Every CTA
+// zeroes its own m.merged before the call, after its last read of the previous merge.
+template <int CL>
+__device__ void cluster_merge_hist(const TopkSmem& m, uint32_t rank) {
+  cluster_barrier();  // every local histogram complete, every merged histogram zeroed
+  for (int b = threadIdx.x; b < kBins; b += kThreads) {
+    const uint32_t c = m.hist[hslot(b)];
+    if (c != 0) {
+#pragma unroll
+      for (int j = 0; j < CL; ++j) red_add_cluster(mapa(&m.merged[hslot(b)], static_cast<uint32_t>(j)), c);
+    }
+  }
+  cluster_barrier();  // every contribution has landed
+}
+
+template <int NB, int CL>  // CL CTAs per row, each holding up to kWarps * NB * 128 keys in registers
 __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkArgs a, int cand_cap) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ uint32_t red[2 * kWarps];
   __shared__ uint32_t info[4];
-  __shared__ uint32_t counts[kClusterCtas];
+  __shared__ uint32_t counts[CL];
   const TopkSmem m = topk_smem(smem, cand_cap);
   const uint32_t rank = cluster_rank();
-  const RowInfo R = row_info(a, blockIdx.x / kClusterCtas);
+  const RowInfo R = row_info(a, blockIdx.x / CL);
   const int tid = threadIdx.x;
   if (rank == 0)
     for (int i = R.keep + tid; i < a.k_out; i += kThreads) R.out[i] = -1;
   if (R.keep == 0) return;  // the same decision in every CTA of the cluster
   const bool by_score = a.order == 0;
   // this CTA's contiguous part of the row
-  const long long part = ((R.n + kClusterCtas - 1) / kClusterCtas + 1023) & ~1023LL;
+  const long long part = ((R.n + CL - 1) / CL + 1023) & ~1023LL;
   const long long lo = min(R.n, static_cast<long long>(rank) * part);
   const long long len = min(R.n - lo, part);
   RegSeg<NB> rs;
@@ -736,11 +744,11 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkArg
   bool exact = take_all;
   bool fallback = false;  // tie-heavy row: the first CTA finishes it alone
   if (!take_all) {
-    for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = 0;
+    for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = m.merged[i] = 0;
     __syncthreads();
     seg_hist(rs, m.hist, 20, 4095u, 32, 0u);
     __syncthreads();
-    cluster_merge_hist(m, rank);
+    cluster_merge_hist<CL>(m, rank);
     find_bucket(m.merged, kBins, static_cast<uint32_t>(R.keep), red, info);
     d1 = info[0];
     const uint32_t above = info[1], in_b = info[2];
@@ -749,11 +757,11 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkArg
     exact = in_b == want;
     if (!exact && above + in_b > static_cast<uint32_t>(cand_cap)) {
       // one more level, cluster-wide: bits 8..19 inside bucket d1
-      for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = 0;
+      for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = m.merged[i] = 0;
       __syncthreads();
       seg_hist(rs, m.hist, 8, 4095u, 20, d1);
       __syncthreads();
-      cluster_merge_hist(m, rank);
+      cluster_merge_hist<CL>(m, rank);
       find_bucket(m.merged, kBins, want, red, info);
       const uint32_t d2 = info[0], above2 = info[1], in_b2 = info[2];
       const uint32_t pre = (d1 << 12) | d2;
@@ -794,10 +802,10 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkArg
   if (tid == 0) dsmem_st(mapa(&counts[rank], 0), ctotal);
   cluster_barrier();
   uint32_t cbase = 0, n_cand = 0;
-  if (tid < kClusterCtas) counts[tid] = rank == 0 ? counts[tid] : dsmem_ld(mapa(&counts[tid], 0));
+  if (tid < CL) counts[tid] = rank == 0 ? counts[tid] : dsmem_ld(mapa(&counts[tid], 0));
   __syncthreads();
 #pragma unroll
-  for (int j = 0; j < kClusterCtas; ++j) {
+  for (int j = 0; j < CL; ++j) {
     cbase += j < static_cast<int>(rank) ? counts[j] : 0u;
     n_cand += counts[j];
   }
@@ -902,18 +910,18 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
     return cudaGetLastError();
   };
   // rows longer than one CTA's registers hold, but within a cluster's: one cluster per row
-  auto go_cluster = [&](auto kern) -> cudaError_t {
+  auto go_cluster = [&](auto kern, int cl) -> cudaError_t {
     const size_t csmem = smem + static_cast<size_t>(kHistWords) * 4;  // + merged histogram
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(csmem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.n_rows) * kClusterCtas, 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(a.n_rows) * cl, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = csmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kClusterCtas;
+    attr[0].val.clusterDim.x = cl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -923,9 +931,11 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
     return cudaGetLastError();
   };
   if (max_row_len <= kWarps * 8 * 128) return go(topk_kernel<8>);
-  if (max_row_len <= kWarps * 16 * 128) return go(topk_kernel<16>);
-  if (max_row_len <= kClusterCtas * kWarps * 8 * 128) return go_cluster(topk_cluster_kernel<8>);
-  if (max_row_len <= kClusterCtas * kWarps * 16 * 128) return go_cluster(topk_cluster_kernel<16>);
+  // a cluster per row: 4 CTAs of 8192 or 16384 keys up to 65536 keys (few CTAs, few merge
+  // partners), then 8 of 16384
+  if (max_row_len <= 4 * kWarps * 8 * 128) return go_cluster(topk_cluster_kernel<8, 4>, 4);
+  if (max_row_len <= 4 * kWarps * 16 * 128) return go_cluster(topk_cluster_kernel<16, 4>, 4);
+  if (max_row_len <= 8 * kWarps * 16 * 128) return go_cluster(topk_cluster_kernel<16, 8>, 8);
   return go(topk_kernel<0>);
 }
 
