@@ -285,23 +285,20 @@ def _paged_on_device(B, lens, q_len, H, D, page, q_fp8, k_fp8, seed, dev):
                 block_tables=bt, max_seq_len=max(lens))
 
 
-def run_other_workloads(dev, stream, peaks):
+def _chunked_prefill_fp8(dev, stream, peaks, iters=3):
+    """8192 queries at 57344..65535 vs a 65536-key cache, e4m3 q and k (one dsa_indexer call)."""
+    import ctypes
     import sparse_attention_token_gb300 as dsa
-    out = {}
     bf16_peak = float(peaks["bf16_tflops"])
-    hbm = float(peaks["hbm_gbs"])
-    # chunked prefill: 8192 queries at 57344..65535 vs 65536 keys, e4m3 q and k
     c = _paged_on_device(1, [65536], 8192, 64, 128, 64, True, True, 4, dev)
     args, keep = dsa.make_indexer_args(c["q"], c["w"], c["k_cache"], c["cu_q_lens"], c["seq_lens"],
                                        c["block_tables"], max_seq_len=c["max_seq_len"], topk_limit=2048,
                                        q_scale=c["q_scale"], k_scale_cache=c["k_scale_cache"])
     L = dsa.lib()
-    import ctypes
-    call = lambda: L.dsa_indexer(ctypes.byref(args), stream.cuda_stream)
-    ms = _time_events(call, 3, stream)
+    ms = _time_events(lambda: L.dsa_indexer(ctypes.byref(args), stream.cuda_stream), iters, stream)
     pairs = sum(57344 + i + 1 for i in range(8192))
     flops = 2 * 64 * 128 * pairs
-    out["chunked_prefill_fp8"] = {
+    out = {
         "workload": "8192 queries at 57344..65535 vs a 65536-key paged cache (page 64), e4m3 q/k with fp32 scales, "
                     "H=64, D=128, index_topk=2048",
         "ms_per_step": ms, "scores_per_s": pairs / (ms / 1e3), "topk_rows_per_s": 8192 / (ms / 1e3),
@@ -309,22 +306,30 @@ def run_other_workloads(dev, stream, peaks):
         "peak": f"e4m3 dense = 2 x measured bf16 ({2 * bf16_peak:.0f} TFLOP/s, nominal ratio)"}
     del c, args, keep
     torch.cuda.empty_cache()
-    # decode: B=64 single queries, contexts U[4096, 65536], bf16 q against an e4m3 cache
+    return out
+
+
+def _decode_b64_fp8_cache(dev, stream, peaks, iters=10):
+    """Decode B=64, contexts U[4096, 65536], bf16 q against a paged e4m3 cache."""
+    import ctypes
+    import sparse_attention_token_gb300 as dsa
     import workloads
+    hbm = float(peaks["hbm_gbs"])
     lens = workloads.decode_lens(64, 4096, 65536, 0)
     c = _paged_on_device(64, lens, 1, 64, 128, 64, False, True, 5, dev)
     args, keep = dsa.make_indexer_args(c["q"], c["w"], c["k_cache"], c["cu_q_lens"], c["seq_lens"],
                                        c["block_tables"], max_seq_len=c["max_seq_len"], topk_limit=2048,
                                        k_scale_cache=c["k_scale_cache"])
+    L = dsa.lib()
     rc = L.dsa_indexer(ctypes.byref(args), stream.cuda_stream)
     if rc != 0:
         raise RuntimeError(f"dsa_indexer (bf16 q, e4m3 cache): {dsa.dsa_status_string(rc)}")
-    ms = _time_events(lambda: L.dsa_indexer(ctypes.byref(args), stream.cuda_stream), 10, stream)
+    ms = _time_events(lambda: L.dsa_indexer(ctypes.byref(args), stream.cuda_stream), iters, stream)
     keys = sum(lens)
     # algorithmic bytes: e4m3 keys + fp32 key scales + page ids + q + w + int32 top-k out
     dec_bytes = keys * (128 + 4) + sum((x + 63) // 64 for x in lens) * 4 + 64 * 64 * 128 * 2 + 64 * 64 * 4 \
         + 64 * 2048 * 4
-    out["decode_b64_fp8_cache"] = {
+    out = {
         "workload": "decode B=64, one query per sequence, contexts U[4096, 65536] (seeded), bf16 q, "
                     "paged e4m3 cache (page 64) with fp32 per-token scales, H=64, D=128, index_topk=2048",
         "ms_per_step": ms, "keys_per_s": keys / (ms / 1e3), "keys": keys,
@@ -334,7 +339,14 @@ def run_other_workloads(dev, stream, peaks):
                 "algorithmic bytes"}
     del c, args, keep
     torch.cuda.empty_cache()
-    # IndexShare: 12 layers [full, shared, shared] x 4, decode B=32 at 32768 keys, bf16 caches
+    return out
+
+
+def _indexshare_stack(dev, stream, peaks, iters=5):
+    """12 layers [full, shared, shared] x 4, decode B=32 at 32768 keys, bf16 caches."""
+    import ctypes
+    import sparse_attention_token_gb300 as dsa
+    hbm = float(peaks["hbm_gbs"])
     types = ["full", "shared", "shared"] * 4
     fulls, keeps = [], []
     for li in range(4):
@@ -351,12 +363,13 @@ def run_other_workloads(dev, stream, peaks):
             fi += 1
         else:
             layer_args.append(None)
-    stack_ms = _time_events(lambda: dsa.dsa_indexer_stack(types, layer_args, stream=stream), 5, stream)
+    L = dsa.lib()
+    stack_ms = _time_events(lambda: dsa.dsa_indexer_stack(types, layer_args, stream=stream), iters, stream)
     allfull_ms = _time_events(lambda: [L.dsa_indexer(ctypes.byref(fulls[i % 4]), stream.cuda_stream)
-                                       for i in range(12)], 5, stream)
+                                       for i in range(12)], iters, stream)
     keys = 32 * 32768
     bytes_full = keys * 128 * 2 + 32 * 64 * 128 * 2 + 32 * 64 * 4 * 2 + 32 * 2048 * 4
-    out["indexshare_stack"] = {
+    out = {
         "workload": "12 layers [full, shared, shared] x 4, decode B=32 at 32768 keys, bf16 paged caches "
                     "(one per full layer), H=64, D=128, index_topk=2048",
         "ms_stack": stack_ms, "ms_all_full": allfull_ms, "speedup_vs_all_full": allfull_ms / stack_ms,
@@ -367,6 +380,17 @@ def run_other_workloads(dev, stream, peaks):
     del keeps, fulls, layer_args
     torch.cuda.empty_cache()
     return out
+
+
+OTHER_WORKLOADS = {
+    "chunked_prefill_fp8": _chunked_prefill_fp8,
+    "decode_b64_fp8_cache": _decode_b64_fp8_cache,
+    "indexshare_stack": _indexshare_stack,
+}
+
+
+def run_other_workloads(dev, stream, peaks):
+    return {name: fn(dev, stream, peaks) for name, fn in OTHER_WORKLOADS.items()}
 
 
 def cpu_sample_rows(n_rows: int):
@@ -442,6 +466,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--only", choices=sorted(OTHER_WORKLOADS),
+                    help="time one of the other workloads alone (--steps calls) and print its line; "
+                         "for profiling it in isolation")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -457,6 +484,13 @@ def main():
     import __graft_entry__ as g
     if rank == 0:
         g.build()
+    if args.only:
+        if rank == 0:
+            peaks, _ = measured_peaks()
+            out = OTHER_WORKLOADS[args.only](torch.device("cuda", local_rank), torch.cuda.current_stream(), peaks,
+                                             iters=args.steps)
+            print(json.dumps({"only": args.only, **out}), flush=True)
+        return
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
         torch.distributed.barrier()
