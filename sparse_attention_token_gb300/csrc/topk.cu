@@ -387,6 +387,17 @@ __device__ void radix_sort_desc(uint32_t* ka, uint32_t* va, uint32_t* kb, uint32
 // nothing) when some bucket holds more than kBucketLimit keys -- many equal or
 // clustered scores -- so the caller sorts with the radix sort instead.  bk and bi
 // are adjacent scratch arrays (bi == bk + n at least), used together as n 8-byte words.
+// |value| bits of an order-preserving key (sign dropped).
+__device__ __forceinline__ uint32_t key_mag(uint32_t u) {
+  return (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : (~u & 0x7FFFFFFFu);
+}
+// Order-preserving key with magnitudes below floor_mag clamped to zero (monotone in u).
+__device__ __forceinline__ uint32_t bucket_key(uint32_t u, uint32_t floor_mag) {
+  const uint32_t m = key_mag(u);
+  const uint32_t c = m > floor_mag ? m - floor_mag : 0u;
+  return (u & 0x80000000u) ? 0x80000000u + c : 0x80000000u - c;
+}
+
 constexpr int kBucketLimit = 64;
 constexpr int kSortBuckets = 4096;
 
@@ -411,13 +422,20 @@ __device__ bool bucket_rank_out(uint32_t* ck, const uint32_t* ci, int n, int kee
     lo = min(lo, red[w]);
     hi = max(hi, red[kWarps + w]);
   }
+  // Buckets are equal-width in a compressed key: magnitudes more than 12 binades below
+  // the largest one are clamped to zero.  Key space is logarithmic across binades, so
+  // when the candidates straddle zero the raw range covers every exponent of both signs
+  // and a few buckets would get most keys; the compressed key is still monotone.
+  const uint32_t mbig = max(key_mag(lo), key_mag(hi));
+  const uint32_t floor_mag = (mbig >> 23) > 12u ? ((mbig >> 23) - 12u) << 23 : 0u;
+  const uint32_t clo = bucket_key(lo, floor_mag), chi = bucket_key(hi, floor_mag);
   int sh = 0;
-  while (((hi >> sh) - (lo >> sh)) >= static_cast<uint32_t>(kSortBuckets)) ++sh;
-  const uint32_t base = lo >> sh;
-  const int nb = static_cast<int>((hi >> sh) - base) + 1;
+  while (((chi >> sh) - (clo >> sh)) >= static_cast<uint32_t>(kSortBuckets)) ++sh;
+  const uint32_t base = clo >> sh;
+  const int nb = static_cast<int>((chi >> sh) - base) + 1;
   for (int b = tid; b < nb; b += kThreads) cur[hslot(b)] = 0;
   __syncthreads();
-  for (int i = tid; i < n; i += kThreads) atomicAdd(&cur[hslot((ck[i] >> sh) - base)], 1u);
+  for (int i = tid; i < n; i += kThreads) atomicAdd(&cur[hslot((bucket_key(ck[i], floor_mag) >> sh) - base)], 1u);
   __syncthreads();
   // descending exclusive scan: start[b] = keys in buckets above b; thread t owns 16 bins
   uint32_t c[16], sum = 0, mx = 0;
@@ -451,14 +469,14 @@ __device__ bool bucket_rank_out(uint32_t* ck, const uint32_t* ci, int n, int kee
   uint64_t* bw = reinterpret_cast<uint64_t*>(bk);  // bk and bi: 2n adjacent words
   for (int i = tid; i < n; i += kThreads) {
     const uint32_t u = ck[i];
-    const uint32_t pos = atomicAdd(&cur[hslot((u >> sh) - base)], 1u);
+    const uint32_t pos = atomicAdd(&cur[hslot((bucket_key(u, floor_mag) >> sh) - base)], 1u);
     bw[pos] = (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~ci[i]);
   }
   __syncthreads();
   // cur[b] is now the end of bucket b; bucket b starts where bucket b + 1 ends
   for (int p = tid; p < n; p += kThreads) {
     const uint64_t x = bw[p];
-    const int b = static_cast<int>((static_cast<uint32_t>(x >> 32) >> sh) - base);
+    const int b = static_cast<int>((bucket_key(static_cast<uint32_t>(x >> 32), floor_mag) >> sh) - base);
     const uint32_t q0 = b + 1 < nb ? cur[hslot(b + 1)] : 0u, q1 = cur[hslot(b)];
     uint32_t rank = q0;
     uint32_t q = q0;
