@@ -150,12 +150,28 @@ def test_topk_tie_storms_exact(S, limit, order):
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("S", [100, 2049, 8192, 16385, 65536])
-def test_topk_gaussian_exact(S):
+# row lengths on every kernel: one CTA (<= 8192 keys), clusters of 4 CTAs of 8192 and of
+# 16384 keys, clusters of 8, and the streaming kernel beyond 131072 keys
+@pytest.mark.parametrize("order", [0, 1])
+@pytest.mark.parametrize("S", [100, 2049, 8192, 16385, 40000, 65536, 100000, 140000])
+def test_topk_gaussian_exact(S, order):
     g = torch.Generator().manual_seed(S)
     T = 4
     sc = torch.randn((T, S), generator=g).numpy().astype(np.float32)
-    got, ref = _topk_on(sc, S - T, S, 2048, 2048, 0)
+    got, ref = _topk_on(sc, S - T, S, 2048, 2048, order)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("order", [0, 1])
+@pytest.mark.parametrize("S,step", [(3000, 0.05), (8192, 0.02), (30000, 0.01), (8192, 1e-6)])
+def test_topk_quantised_scores_exact(S, step, order):
+    # values on a grid: tens of equal keys per value, both signs, so the score-order sort
+    # meets buckets of 8..64 keys (and, for the coarse grids, more), plus near-zero values
+    g = torch.Generator().manual_seed(int(S / step) % 100003)
+    T = 5
+    sc = (torch.round(torch.randn((T, S), generator=g) / step) * step).numpy().astype(np.float32)
+    sc[4, ::3] *= 1e-30
+    got, ref = _topk_on(sc, S - T, S, 2048, 2048, order)
     assert np.array_equal(got, ref)
 
 
@@ -244,6 +260,18 @@ def test_mixed_decode_integer_exact(H):
                               k_dtype="fp8_e4m3", integer=True, seed=41 + H)
     got = run_paged(pc)
     ref, _, _ = oracle.paged(pc)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("page_size,order", [(16, 1), (32, 0), (128, 1)])
+def test_mixed_decode_pages_orders_padding(page_size, order):
+    # every page size (16..128 keys: 8..1 copies per tile), both orders, rows shorter than
+    # index_topk (-1 padding) and k_out wider than the limit
+    lens = [1, 7, 129, 500, 1000, 3000]
+    pc = workloads.paged_case(lens, [1] * len(lens), 64, 128, 600, page_size=page_size, k_out=640,
+                              q_dtype="bf16", k_dtype="fp8_e4m3", integer=True, seed=60 + page_size)
+    got = run_paged(pc, order=order)
+    ref, _, _ = oracle.paged(pc, order=order)
     assert np.array_equal(got, ref)
 
 
