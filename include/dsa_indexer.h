@@ -170,6 +170,38 @@ dsa_status dsa_indexer_workspace_size(const dsa_indexer_args* args, size_t* byte
 dsa_status dsa_indexer(const dsa_indexer_args* args, dsa_stream_t stream);
 
 /*
+ * dsa_indexer_dense_host -- dsa_indexer_scores + dsa_indexer_topk of one sequence whose
+ * inputs and output are in HOST memory, with the transfers overlapped with the kernels.
+ * The pages describe the indexer on device tensors; this entry point exists for callers
+ * that hold the step's inputs on the host (and is what an end-to-end measurement calls).
+ *
+ *   q_host [T, H, D], w_host [T, H], k_host [S, D] (+ q_scale_host [T, H], k_scale_host [S]
+ *   for e4m3): row-major host arrays, pinned (cudaHostAlloc / cudaHostRegister) for the
+ *   copies to overlap; pageable memory works but the copies then serialise.
+ *   topk_host [T, k_out]: written with the same rows dsa_indexer_topk returns.
+ *   chunk_rows: query rows per chunk (0 = max(512, T/16); raised so there are at most
+ *   256 chunks).
+ *   workspace: device memory of dsa_indexer_dense_host_workspace_size bytes, 256-byte
+ *   aligned, owned by the caller and not shared with overlapping work.
+ *
+ * The query rows travel in chunks (last rows first) on a library-owned copy stream;
+ * each chunk is scored and selected as soon as its rows land, alternately on `stream`
+ * and on a library-owned compute stream so consecutive chunks' kernels overlap; another
+ * library-owned stream copies the chunk's top-k rows back.  The call returns once everything is enqueued; `stream` waits
+ * for the last copy, so synchronising it makes topk_host final.  Same element types, H,
+ * D and errors as dsa_indexer_scores / dsa_indexer_topk; S = 0 is DSA_ERR_UNSUPPORTED.
+ * Concurrent calls from several host threads on one device are serialised internally.
+ */
+dsa_status dsa_indexer_dense_host_workspace_size(int T, int S, int H, int D, int q_dtype, int k_out,
+                                                 int chunk_rows, size_t* bytes);
+dsa_status dsa_indexer_dense_host(const void* q_host, int q_dtype, const float* q_scale_host,
+                                  const void* k_host, int k_dtype, const float* k_scale_host,
+                                  const float* w_host, int T, int S, int H, int D, int q_pos0,
+                                  int topk_limit, int k_out, int order, int chunk_rows,
+                                  int32_t* topk_host, void* workspace, size_t workspace_bytes,
+                                  dsa_stream_t stream);
+
+/*
  * dsa_indexer_static -- dsa_indexer for callers that cannot allocate device memory.
  * The pages have no counterpart of this entry point; it exists for library users.
  *

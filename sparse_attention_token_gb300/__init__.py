@@ -7,6 +7,7 @@ missing or a call fails, an exception is raised.
 
 Function names mirror the C ABI:
   dsa_indexer_scores, dsa_indexer_topk, dsa_indexer, dsa_indexer_workspace_size,
+  dsa_indexer_dense_host, dsa_indexer_dense_host_workspace_size,
   dsa_resolve_indexer_sources, dsa_indexer_stack, dsa_check_device_status,
   dsa_topk_width, dsa_status_string, dsa_version.
 Host helpers from the GLM5 TensorCast adaptation design ("Sparse MLA 配置兼容",
@@ -93,6 +94,10 @@ def lib():
         L.dsa_indexer_stack.argtypes = [I, P, P, P, P, P]
         L.dsa_check_device_status.restype = I
         L.dsa_check_device_status.argtypes = [P]
+        L.dsa_indexer_dense_host_workspace_size.restype = I
+        L.dsa_indexer_dense_host_workspace_size.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(S)]
+        L.dsa_indexer_dense_host.restype = I
+        L.dsa_indexer_dense_host.argtypes = [P, I, P, P, I, P, P, I, I, I, I, I, I, I, I, I, P, P, S, P]
         _LIB = L
     return _LIB
 
@@ -165,6 +170,58 @@ def dsa_indexer_scores(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, *, q_p
         _dev(w, "w", torch.float32), T, S, H, D, int(q_pos0), _dev(scores, "scores", torch.float32),
         int(scores.stride(0)), _stream_ptr(stream)), "dsa_indexer_scores")
     return scores
+
+
+def _host(t: Optional[torch.Tensor], name: str, dtype=None):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def dsa_indexer_dense_host_workspace_size(T: int, S: int, H: int, D: int, q_dtype: int, k_out: int,
+                                          chunk_rows: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().dsa_indexer_dense_host_workspace_size(T, S, H, D, q_dtype, k_out, chunk_rows, ctypes.byref(n)),
+           "dsa_indexer_dense_host_workspace_size")
+    return int(n.value)
+
+
+def dsa_indexer_dense_host(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, *, topk_limit: int,
+                           q_pos0: Optional[int] = None, k_out: Optional[int] = None, order: int = DSA_ORDER_SCORE,
+                           q_scale: Optional[torch.Tensor] = None, k_scale: Optional[torch.Tensor] = None,
+                           chunk_rows: int = 0, topk: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Scores + top-k of one sequence from HOST tensors q [T, H, D], k [S, D], w [T, H]
+    (pin them for overlapped copies) into a host int32 [T, k_out] tensor; the transfers
+    are chunked and overlapped with the kernels.  `workspace`: a CUDA uint8 tensor of at
+    least dsa_indexer_dense_host_workspace_size bytes (allocated when omitted).  The
+    result is final once `stream` (default: torch's current stream) is synchronised."""
+    T, H, D = q.shape
+    S = k.shape[0]
+    if q_pos0 is None:
+        q_pos0 = S - T
+    if k_out is None:
+        k_out = topk_limit
+    if topk is None:
+        topk = torch.empty((T, k_out), dtype=torch.int32, pin_memory=torch.cuda.is_available())
+    need = dsa_indexer_dense_host_workspace_size(T, S, H, D, _dtype_code(q), k_out, chunk_rows)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    if not workspace.is_cuda or workspace.dtype != torch.uint8:
+        raise TypeError("workspace must be a CUDA uint8 tensor")
+    _check(lib().dsa_indexer_dense_host(
+        _host(q, "q"), _dtype_code(q), _host(q_scale, "q_scale", torch.float32),
+        _host(k, "k"), _dtype_code(k), _host(k_scale, "k_scale", torch.float32),
+        _host(w, "w", torch.float32), T, S, H, D, int(q_pos0), int(topk_limit), int(k_out), int(order),
+        int(chunk_rows), _host(topk, "topk", torch.int32), workspace.data_ptr(), workspace.numel(),
+        _stream_ptr(stream)), "dsa_indexer_dense_host")
+    return topk
 
 
 def dsa_indexer_topk(scores: torch.Tensor, *, T: int, S: int, q_pos0: int, topk_limit: int,

@@ -189,3 +189,26 @@ def test_workload_shapes():
     st = workloads.indexshare_stack(B=2, ctx=256)
     assert st.indexer_types == workloads.INDEXSHARE_TYPES_12
     assert sum(l is not None for l in st.layers) == 4
+
+def test_dense_host_validation_happens_before_any_cuda_call(dsa):
+    L = dsa.lib()
+    n = dsa.dsa_indexer_dense_host_workspace_size(8192, 8192, 64, 128, dsa.DSA_BF16, 2048)
+    assert n >= 8192 * 64 * 128 * 2 + 8192 * 2048 * 4            # q and the top-k rows at least
+    assert dsa.dsa_indexer_dense_host_workspace_size(100, 100, 64, 128, dsa.DSA_BF16, 16, 7) > 0
+    with pytest.raises(dsa.DsaError):
+        dsa.dsa_indexer_dense_host_workspace_size(0, 10, 64, 128, dsa.DSA_BF16, 16)
+    fake = 1 << 20
+
+    def call(qd=0, kd=0, T=10, S=10, k_out=16, order=0, chunk=0, ptrs=True, ws_bytes=1 << 40, qs=None, ks=None):
+        p = fake if ptrs else None
+        return L.dsa_indexer_dense_host(p, qd, qs, p, kd, ks, p, T, S, 64, 128, 0, 16, k_out, order, chunk, p,
+                                        fake, ws_bytes, None)
+    assert call(ptrs=False) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert call(order=2) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert call(chunk=-1) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert call(k_out=5000) == dsa.DSA_ERR_UNSUPPORTED
+    assert call(qd=1, kd=0) == dsa.DSA_ERR_UNSUPPORTED
+    assert call(qd=1, kd=1) == dsa.DSA_ERR_INVALID_ARGUMENT      # e4m3 needs both scale arrays
+    assert call(S=0) == dsa.DSA_ERR_UNSUPPORTED
+    assert call(ws_bytes=16) == dsa.DSA_ERR_WORKSPACE
+    assert call(T=0) == dsa.DSA_OK                               # nothing to do

@@ -360,3 +360,29 @@ print("pair ok")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0 and "pair ok" in r.stdout, r.stdout + r.stderr
+
+
+# --------------------------------------------------- host-memory entry point (pipelined)
+
+@pytest.mark.parametrize("chunk_rows,order", [(0, 0), (700, 1), (3000, 0), (97, 0)])
+def test_dense_host_matches_oracle(chunk_rows, order):
+    # inputs and output in pinned host memory, chunked copies overlapped with the kernels
+    c = workloads.dense_case(3000, 3000, 64, 128, 200, integer=True, int_range=(-2, 2), seed=71)
+    q, k, w = c.q.pin_memory(), c.k.pin_memory(), c.w.pin_memory()
+    tk = dsa.dsa_indexer_dense_host(q, k, w, q_pos0=c.q_pos0, topk_limit=c.topk_limit, k_out=c.k_out,
+                                    order=order, chunk_rows=chunk_rows)
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_status() == dsa.DSA_OK
+    ref, _, _ = oracle_dense(c, order=order)
+    assert np.array_equal(tk.numpy(), ref)
+
+
+def test_dense_host_fp8_longer_keys_than_queries():
+    c = workloads.dense_case(900, 2500, 64, 128, 300, q_pos0=1600, dtype="fp8_e4m3", integer=True, seed=72)
+    pin = lambda t: None if t is None else t.pin_memory()
+    tk = dsa.dsa_indexer_dense_host(pin(c.q), pin(c.k), pin(c.w), q_pos0=c.q_pos0, topk_limit=c.topk_limit,
+                                    k_out=c.k_out, q_scale=pin(c.q_scale), k_scale=pin(c.k_scale), chunk_rows=256)
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_status() == dsa.DSA_OK
+    ref, _, _ = oracle_dense(c)
+    assert np.array_equal(tk.numpy(), ref)
