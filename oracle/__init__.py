@@ -55,6 +55,10 @@ def _load():
         lib.oracle_topk.restype = i32
         lib.oracle_topk.argtypes = [P, i64, i32, P, i32, i32, i32, P, i32]
         lib.oracle_max_threads.restype = i32
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_cache_append.restype = i32
+        lib.oracle_cache_append.argtypes = [P, i32, i32, P, i32, P, P, i64]
         _lib = lib
     return _lib
 
@@ -209,3 +213,41 @@ def stack(indexer_types: Sequence[str], layers, **kw):
         else:
             out.append(out[s])
     return src, out
+
+
+def e4m3_encode(values) -> np.ndarray:
+    """e4m3 codes (uint8) of fp32 values: nearest finite code, ties to the even code,
+    saturating at +-448, sign copied (see ``oracle_e4m3_encode``)."""
+    lib = _load()
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib.oracle_e4m3_encode(float(x)) for x in v], dtype=np.uint8)
+
+
+def cache_append(k_new: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                 k_scale_cache: Optional[torch.Tensor] = None):
+    """Copies of (k_cache, k_scale_cache) after writing the bf16 rows ``k_new [n, D]`` to
+    the slots ``slot_mapping [n]`` (page * page_size + row; negative = skip): a bf16
+    cache takes the rows as they are, an e4m3 cache takes them quantised with one
+    scale = amax / 448 per token (the GLM5 TensorCast adaptation design's FP8 key and
+    scale cache write).  Raises ValueError on a slot past the cache."""
+    lib = _load()
+    if k_new.dtype != torch.bfloat16:
+        raise TypeError("k_new must be bf16")
+    n, D = k_new.shape
+    kn = np.ascontiguousarray(k_new.contiguous().view(torch.int16).numpy())
+    sl = np.ascontiguousarray(slot_mapping.to(torch.int64).numpy())
+    fp8 = k_cache.dtype == torch.float8_e4m3fn
+    cache = k_cache.clone().contiguous()
+    cache_raw = np.ascontiguousarray(cache.view(torch.uint8 if fp8 else torch.int16).numpy())
+    scales = None
+    if fp8:
+        if k_scale_cache is None:
+            raise ValueError("an e4m3 cache needs its scale cache")
+        scales = np.ascontiguousarray(k_scale_cache.to(torch.float32).clone().numpy())
+    n_slots = cache.shape[0] * cache.shape[1]
+    rc = lib.oracle_cache_append(_ptr(kn), n, D, _ptr(sl), 1 if fp8 else 0, _ptr(cache_raw), _ptr(scales), n_slots)
+    if rc != 0:
+        raise ValueError("cache_append: slot outside the cache")
+    out = torch.from_numpy(cache_raw).view(k_cache.dtype).reshape(k_cache.shape)
+    return out, (torch.from_numpy(scales).reshape(k_scale_cache.shape) if fp8 else k_scale_cache)
+

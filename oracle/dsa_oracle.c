@@ -261,6 +261,64 @@ int oracle_paged(int q_dtype, int k_dtype, const void* q, const float* q_scale, 
     return failed ? -1 : 0;
 }
 
+/* ---- cache append -------------------------------------------------------
+ * The fused op takes the indexer cache as a mutable argument together with
+ * slot_mapping (GLM5 TensorCast adaptation design, "DSA Indexer 融合语义算子"), and
+ * its FP8 path writes the key cache and the scale cache after an activation
+ * quantisation ("FP8 key cache/scale cache 写入"; cost buckets 9 and 10).  The pages
+ * do not print the quantiser; the reading taken is one fp32 scale per token,
+ * scale = amax / 448 (amax = the largest |k| of the token's row; 1 for an all-zero
+ * row), and code = the e4m3 value nearest to k / scale.
+ *
+ * Encoding to e4m3 by its definition: the finite non-negative codes 0x00..0x7E are
+ * enumerated and the one whose value is nearest to |v| wins; of two equally near
+ * neighbours the one with an even code (mantissa lsb 0) wins; beyond 448 the
+ * nearest finite code is 448 itself (saturation).  The sign bit is copied, so -0.0
+ * becomes 0x80.  NaN becomes 0x7F. */
+uint8_t oracle_e4m3_encode(float v) {
+    if (v != v) return 0x7F;
+    const double a = fabs((double)v);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double d = fabs(oracle_e4m3_to_double((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(best | (signbit(v) ? 0x80 : 0));
+}
+
+/* k_new [n, D] bf16 rows go to cache slots slots[i] (slot = page * page_size + row;
+ * negative: the token is skipped).  bf16 cache: the row is copied.  e4m3 cache: the
+ * row is quantised as above, in fp32 arithmetic (amax of the decoded values, one
+ * division for the scale, one division per element), and the scale goes to
+ * scale_cache[slot].  Returns -1 (writing nothing further) at a slot >= n_slots. */
+int oracle_cache_append(const uint16_t* k_new, int n, int D, const int64_t* slots, int cache_dtype, void* cache,
+                        float* scale_cache, int64_t n_slots) {
+    for (int i = 0; i < n; ++i) {
+        const int64_t slot = slots[i];
+        if (slot < 0) continue;
+        if (slot >= n_slots) return -1;
+        const uint16_t* row = k_new + (int64_t)i * D;
+        if (cache_dtype == OR_BF16) {
+            memcpy((uint16_t*)cache + slot * D, row, (size_t)D * sizeof(uint16_t));
+            continue;
+        }
+        float amax = 0.0f;
+        for (int d = 0; d < D; ++d) {
+            const float x = (float)oracle_bf16_to_double(row[d]);
+            if (fabsf(x) > amax) amax = fabsf(x);
+        }
+        const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        uint8_t* out = (uint8_t*)cache + slot * D;
+        for (int d = 0; d < D; ++d) out[d] = oracle_e4m3_encode((float)oracle_bf16_to_double(row[d]) / scale);
+        scale_cache[slot] = scale;
+    }
+    return 0;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -305,3 +305,109 @@ def test_stack_shared_layers_forward_source_unchanged():
     assert src == [0, 0, 0, 3, 3]
     assert outs[1] is outs[0] and outs[2] is outs[0] and outs[4] is outs[3]
     assert not np.array_equal(outs[0], outs[3])
+
+
+# ---------------------------------------------------------------- cache append (encoder, quantiser)
+
+def test_e4m3_encode_matches_torch_rounding():
+    # every finite code, every midpoint between neighbours (ties), and random in-range
+    # values: torch's float8_e4m3fn cast rounds to nearest, ties to even
+    vals = torch.arange(127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    mids = (vals[:-1] + vals[1:]) / 2
+    g = torch.Generator().manual_seed(3)
+    rnd = (torch.rand(4000, generator=g, dtype=torch.float64) * 2 - 1) * 448 * torch.pow(
+        2.0, -torch.randint(0, 18, (4000,), generator=g).to(torch.float64))
+    x = torch.cat([vals, -vals, mids, -mids, rnd]).to(torch.float32)
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle.e4m3_encode(x.numpy())
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_encode_hand_values():
+    # derived by hand from the format: 448 = 1.75 * 2^8 (e=15, m=6); 224 = 1.75 * 2^7
+    # (e=14, m=6) with the sign; 1 = 2^0 (e=7); 2^-9 is the smallest subnormal; 2^-10 is
+    # half of it, a tie between codes 0 and 1 -> the even code 0; 0.05 = 1.6 * 2^-5 lies
+    # between 1.5 and 1.625 (m=4, 5) and is nearer 1.625; 500 saturates to 448
+    x = [448.0, -224.0, 1.0, 2.0 ** -9, 2.0 ** -10, 0.0, -0.0, 0.05, 500.0, -1e6]
+    assert oracle.e4m3_encode(x).tolist() == [0x7E, 0xF6, 0x38, 0x01, 0x00, 0x00, 0x80, 0x15, 0x7E, 0xFE]
+
+
+def _append_case(cache_dtype, seed=0, n=12, D=128, pages=5, PS=16):
+    g = torch.Generator().manual_seed(seed)
+    k_new = (torch.randn((n, D), generator=g) * torch.pow(2.0, torch.randint(-6, 6, (n, 1), generator=g))).to(
+        torch.bfloat16)
+    k_new[3] = 0                                          # all-zero row: scale 1, codes 0
+    slots = torch.randperm(pages * PS, generator=g)[:n].to(torch.int64)
+    slots[5] = -1                                         # padding token: skipped
+    if cache_dtype == "bf16":
+        cache = torch.randn((pages, PS, D), generator=g).to(torch.bfloat16)
+        return k_new, slots, cache, None
+    cache = torch.randint(0, 0x7E, (pages, PS, D), generator=g).to(torch.uint8).view(torch.float8_e4m3fn)
+    return k_new, slots, cache, torch.rand((pages, PS), generator=g) + 0.5
+
+
+def test_cache_append_bf16_copies_rows_and_leaves_the_rest():
+    k_new, slots, cache, _ = _append_case("bf16")
+    out, _ = oracle.cache_append(k_new, slots, cache)
+    flat, before = out.view(-1, 128), cache.view(-1, 128)
+    touched = set()
+    for i, s in enumerate(slots.tolist()):
+        if s >= 0:
+            assert torch.equal(flat[s].view(torch.int16), k_new[i].view(torch.int16))
+            touched.add(s)
+    for s in range(flat.shape[0]):
+        if s not in touched:
+            assert torch.equal(flat[s].view(torch.int16), before[s].view(torch.int16))
+
+
+def test_cache_append_e4m3_quantiser_properties():
+    k_new, slots, cache, scales = _append_case("fp8", seed=1)
+    out, sc = oracle.cache_append(k_new, slots, cache, scales)
+    flat, fsc = out.view(-1, 128), sc.view(-1)
+    codes = flat.view(torch.uint8)
+    for i, s in enumerate(slots.tolist()):
+        if s < 0:
+            continue
+        x = k_new[i].to(torch.float64)
+        amax = x.abs().max().item()
+        if amax == 0:
+            assert fsc[s].item() == 1.0 and codes[s].tolist() == [0] * 128
+            continue
+        # the scale is amax / 448 rounded once to fp32
+        assert fsc[s].item() == float(np.float32(np.float32(amax) / np.float32(448.0)))
+        dec = flat[s].to(torch.float64) * fsc[s].item()
+        # the amax element lands on +-448 and every element is within half an e4m3 step
+        # of its value (relative 1/16 for normals, 2^-10 * scale below 2^-6 * scale)
+        j = int(x.abs().argmax())
+        assert abs(flat[s].to(torch.float64)[j].item()) == 448.0
+        step = torch.maximum(x.abs() / 16, torch.full_like(x, 2.0 ** -10 * fsc[s].item()))
+        assert torch.all((dec - x).abs() <= step * 1.0001)
+        assert torch.all(torch.sign(dec) * torch.sign(x) >= 0)
+    # untouched slots keep their bytes and scales
+    touched = {s for s in slots.tolist() if s >= 0}
+    before = cache.view(-1, 128).view(torch.uint8)
+    for s in range(flat.shape[0]):
+        if s not in touched:
+            assert torch.equal(codes[s], before[s]) and fsc[s].item() == scales.view(-1)[s].item()
+
+
+def test_cache_append_e4m3_matches_torch_quantisation():
+    # library special case: torch's own per-row scale and cast give the same bytes
+    k_new, slots, cache, scales = _append_case("fp8", seed=2)
+    out, sc = oracle.cache_append(k_new, slots, cache, scales)
+    x = k_new.to(torch.float32)
+    amax = x.abs().amax(dim=1, keepdim=True)
+    s_ref = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    ref = (x / s_ref).to(torch.float8_e4m3fn).view(torch.uint8)
+    flat, fsc = out.view(-1, 128).view(torch.uint8), sc.view(-1)
+    for i, s in enumerate(slots.tolist()):
+        if s >= 0:
+            assert torch.equal(flat[s], ref[i])
+            assert fsc[s].item() == s_ref[i, 0].item()
+
+
+def test_cache_append_rejects_slot_past_the_cache():
+    k_new, slots, cache, _ = _append_case("bf16")
+    slots[0] = cache.shape[0] * cache.shape[1]
+    with pytest.raises(ValueError):
+        oracle.cache_append(k_new, slots, cache)
