@@ -136,7 +136,7 @@ typedef struct {
     int B;                       /* sequences                                        */
     int total_q;                 /* cu_q_lens[B] (host copy; rows of q, w, topk)     */
     int H, D;                    /* indexer heads, head dim                          */
-    int page_size;               /* tokens per page; 64 supported                    */
+    int page_size;               /* tokens per page: 16, 32, 64 or 128               */
     int num_pages;               /* pages in k_cache                                 */
     int max_pages_per_seq;       /* columns of block_tables                          */
     int max_seq_len;             /* host upper bound of seq_lens[b]                  */
@@ -146,14 +146,17 @@ typedef struct {
     const int32_t* cu_q_lens;    /* [B + 1], cu_q_lens[0] = 0, non-decreasing        */
     const int32_t* seq_lens;     /* [B], q_len_b <= seq_lens[b] <= max_seq_len       */
     const int32_t* block_tables; /* [B, max_pages_per_seq]                           */
-    const void* k_cache;         /* [num_pages, page_size, D]                        */
-    const float* k_scale_cache;  /* [num_pages, page_size] fp32 (FP8 k) or NULL      */
+    void* k_cache;               /* [num_pages, page_size, D] (written when k_new)   */
+    float* k_scale_cache;        /* [num_pages, page_size] fp32 (FP8 k) or NULL      */
     int topk_limit;              /* index_topk / topk_limit                          */
     int k_out;                   /* columns of topk, >= 1                            */
     int order;                   /* dsa_topk_order                                   */
     int32_t* topk;               /* out [total_q, k_out]                             */
     void* workspace;             /* device scratch, >= dsa_indexer_workspace_size    */
     size_t workspace_bytes;
+    const void* k_new;           /* NULL, or [total_q, D] bf16: this step's new keys, */
+                                 /* appended to the cache before scoring             */
+    const int64_t* slot_mapping; /* [total_q] with k_new: cache slot of each new key */
 } dsa_indexer_args;
 
 /* Bytes of device workspace dsa_indexer needs for these sizes (pointers may be NULL). */
@@ -168,6 +171,25 @@ dsa_status dsa_indexer_workspace_size(const dsa_indexer_args* args, size_t* byte
  * prefill batch the mix returns DSA_ERR_UNSUPPORTED.  The workspace must not be used
  * by another call that overlaps on the GPU. */
 dsa_status dsa_indexer(const dsa_indexer_args* args, dsa_stream_t stream);
+
+/*
+ * dsa_indexer_cache_append -- write this step's new indexer keys into the paged cache
+ * (GLM5 TensorCast adaptation design, "DSA Indexer 融合语义算子": the op's indexer cache
+ * is a mutable argument written through slot_mapping; its FP8 path writes the key
+ * cache and the scale cache after an activation quantisation, cost buckets 9 and 10).
+ *
+ *   k_new [n, D] bf16 device rows; slot_mapping [n] int64, slot = page * page_size + row
+ *   (negative: skip the token); k_cache [num_pages, page_size, D] of cache_dtype;
+ *   k_scale_cache [num_pages, page_size] fp32 (e4m3 cache only).
+ *   bf16 cache (D = 64 or 128): the row is copied.  e4m3 cache (D = 128): scale =
+ *   amax / 448 (fp32; 1 for an all-zero row), each element the e4m3 value nearest to
+ *   k / scale (ties to even, saturating at +-448), the scale stored beside the row.
+ * A slot past the cache is skipped and reported through dsa_check_device_status.
+ * The same append runs first inside dsa_indexer when dsa_indexer_args.k_new is set.
+ */
+dsa_status dsa_indexer_cache_append(const void* k_new, int n, int D, const int64_t* slot_mapping,
+                                    void* k_cache, int cache_dtype, float* k_scale_cache, int page_size,
+                                    int num_pages, dsa_stream_t stream);
 
 /*
  * dsa_indexer_dense_host -- dsa_indexer_scores + dsa_indexer_topk of one sequence whose

@@ -7,7 +7,7 @@ missing or a call fails, an exception is raised.
 
 Function names mirror the C ABI:
   dsa_indexer_scores, dsa_indexer_topk, dsa_indexer, dsa_indexer_workspace_size,
-  dsa_indexer_dense_host, dsa_indexer_dense_host_workspace_size,
+  dsa_indexer_dense_host, dsa_indexer_dense_host_workspace_size, dsa_indexer_cache_append,
   dsa_resolve_indexer_sources, dsa_indexer_stack, dsa_check_device_status,
   dsa_topk_width, dsa_status_string, dsa_version.
 Host helpers from the GLM5 TensorCast adaptation design ("Sparse MLA 配置兼容",
@@ -59,7 +59,7 @@ class dsa_indexer_args(ctypes.Structure):
         ("block_tables", ctypes.c_void_p), ("k_cache", ctypes.c_void_p),
         ("k_scale_cache", ctypes.c_void_p), ("topk_limit", ctypes.c_int), ("k_out", ctypes.c_int),
         ("order", ctypes.c_int), ("topk", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-        ("workspace_bytes", ctypes.c_size_t),
+        ("workspace_bytes", ctypes.c_size_t), ("k_new", ctypes.c_void_p), ("slot_mapping", ctypes.c_void_p),
     ]
 
 
@@ -94,6 +94,8 @@ def lib():
         L.dsa_indexer_stack.argtypes = [I, P, P, P, P, P]
         L.dsa_check_device_status.restype = I
         L.dsa_check_device_status.argtypes = [P]
+        L.dsa_indexer_cache_append.restype = I
+        L.dsa_indexer_cache_append.argtypes = [P, I, I, P, P, I, P, I, I, P]
         L.dsa_indexer_dense_host_workspace_size.restype = I
         L.dsa_indexer_dense_host_workspace_size.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(S)]
         L.dsa_indexer_dense_host.restype = I
@@ -240,7 +242,8 @@ def dsa_indexer_topk(scores: torch.Tensor, *, T: int, S: int, q_pos0: int, topk_
 
 def make_indexer_args(q, w, k_cache, cu_q_lens, seq_lens, block_tables, *, max_seq_len: int, topk_limit: int,
                       k_out: Optional[int] = None, q_scale=None, k_scale_cache=None, topk=None,
-                      workspace=None, order: int = DSA_ORDER_SCORE, total_q: Optional[int] = None):
+                      workspace=None, order: int = DSA_ORDER_SCORE, total_q: Optional[int] = None,
+                      k_new=None, slot_mapping=None):
     """Fill a dsa_indexer_args from tensors (allocating topk / workspace with torch if absent).
 
     Returns (args, keepalive) -- keep the second value alive while the call runs."""
@@ -272,7 +275,12 @@ def make_indexer_args(q, w, k_cache, cu_q_lens, seq_lens, block_tables, *, max_s
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
     a.workspace = _dev(workspace, "workspace", torch.uint8)
     a.workspace_bytes = workspace.numel()
-    return a, (q, w, k_cache, cu_q_lens, seq_lens, block_tables, q_scale, k_scale_cache, topk, workspace)
+    if (k_new is None) != (slot_mapping is None):
+        raise ValueError("k_new and slot_mapping go together")
+    a.k_new = _dev(k_new, "k_new", torch.bfloat16)
+    a.slot_mapping = _dev(slot_mapping, "slot_mapping", torch.int64)
+    return a, (q, w, k_cache, cu_q_lens, seq_lens, block_tables, q_scale, k_scale_cache, topk, workspace, k_new,
+               slot_mapping)
 
 
 def dsa_indexer_workspace_size(args: dsa_indexer_args) -> int:
@@ -283,13 +291,30 @@ def dsa_indexer_workspace_size(args: dsa_indexer_args) -> int:
 
 def dsa_indexer(q, w, k_cache, cu_q_lens, seq_lens, block_tables, *, max_seq_len: int, topk_limit: int,
                 k_out: Optional[int] = None, q_scale=None, k_scale_cache=None, topk=None, workspace=None,
-                order: int = DSA_ORDER_SCORE, stream=None) -> torch.Tensor:
-    """Fused paged indexer for a varlen batch; returns topk [total_q, k_out] int32."""
+                order: int = DSA_ORDER_SCORE, k_new=None, slot_mapping=None, stream=None) -> torch.Tensor:
+    """Fused paged indexer for a varlen batch; returns topk [total_q, k_out] int32.
+    With k_new [total_q, D] bf16 and slot_mapping [total_q] int64 the step's keys are
+    first written into k_cache (and k_scale_cache), in place."""
     a, keep = make_indexer_args(q, w, k_cache, cu_q_lens, seq_lens, block_tables, max_seq_len=max_seq_len,
                                 topk_limit=topk_limit, k_out=k_out, q_scale=q_scale,
-                                k_scale_cache=k_scale_cache, topk=topk, workspace=workspace, order=order)
+                                k_scale_cache=k_scale_cache, topk=topk, workspace=workspace, order=order,
+                                k_new=k_new, slot_mapping=slot_mapping)
     _check(lib().dsa_indexer(ctypes.byref(a), _stream_ptr(stream)), "dsa_indexer")
     return keep[8]
+
+
+def dsa_indexer_cache_append(k_new: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                             k_scale_cache: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Write new bf16 key rows k_new [n, D] into k_cache [num_pages, page_size, D] at the
+    slots slot_mapping [n] (int64, page * page_size + row; negative = skip), in place;
+    an e4m3 cache takes them quantised with one scale amax/448 per token into
+    k_scale_cache [num_pages, page_size]."""
+    n, D = k_new.shape
+    num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+    _check(lib().dsa_indexer_cache_append(
+        _dev(k_new, "k_new", torch.bfloat16), n, D, _dev(slot_mapping, "slot_mapping", torch.int64),
+        _dev(k_cache, "k_cache"), _dtype_code(k_cache), _dev(k_scale_cache, "k_scale_cache", torch.float32),
+        page_size, num_pages, _stream_ptr(stream)), "dsa_indexer_cache_append")
 
 
 def indexer_types_to_codes(indexer_types: Sequence) -> list:

@@ -241,6 +241,13 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
   if (a->total_q == 0 || a->B == 0) return DSA_OK;
   unsigned* status = device_status_ptr();
   if (!status) return DSA_ERR_CUDA;
+  if (a->k_new) {
+    // this step's keys go into the cache first, so the step's own queries see them
+    const cudaError_t e = launch_cache_append(a->k_new, a->total_q, a->D, a->slot_mapping, a->k_cache,
+                                              a->k_dtype == DSA_FP8_E4M3, a->k_scale_cache,
+                                              static_cast<long long>(a->num_pages) * a->page_size, status, st);
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+  }
   uint8_t* ws = static_cast<uint8_t*>(a->workspace);
   int* counts = reinterpret_cast<int*>(ws + p.off_counts);
   WorkItem* items = reinterpret_cast<WorkItem*>(ws + p.off_items);
@@ -438,6 +445,12 @@ static dsa_status validate_paged_pointers(const dsa_indexer_args* a, const Paged
     return DSA_ERR_INVALID_ARGUMENT;
   if (a->num_pages < 1 || a->max_pages_per_seq < 1) return DSA_ERR_INVALID_ARGUMENT;
   if (!a->workspace || a->workspace_bytes < p.total || !aligned16(a->workspace)) return DSA_ERR_WORKSPACE;
+  if (a->k_new) {
+    // append before scoring: bf16 rows, one slot each; e4m3 caches need their scales
+    if (!a->slot_mapping || !aligned16(a->k_new) || (reinterpret_cast<uintptr_t>(a->slot_mapping) & 7u) != 0)
+      return DSA_ERR_INVALID_ARGUMENT;
+    if (a->k_dtype == DSA_FP8_E4M3 && (a->D != 128 || !a->k_scale_cache)) return DSA_ERR_INVALID_ARGUMENT;
+  }
   return DSA_OK;
 }
 
@@ -447,6 +460,25 @@ dsa_status dsa_indexer(const dsa_indexer_args* args, dsa_stream_t stream) {
   if (st != DSA_OK) return st;
   if ((st = validate_paged_pointers(args, p)) != DSA_OK) return st;
   return run_paged(args, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dsa_status dsa_indexer_cache_append(const void* k_new, int n, int D, const int64_t* slot_mapping, void* k_cache,
+                                    int cache_dtype, float* k_scale_cache, int page_size, int num_pages,
+                                    dsa_stream_t stream) {
+  if (n < 0 || D <= 0 || page_size <= 0 || num_pages < 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (cache_dtype != DSA_BF16 && cache_dtype != DSA_FP8_E4M3) return DSA_ERR_INVALID_ARGUMENT;
+  if (cache_dtype == DSA_BF16 ? (D != 64 && D != 128) : D != 128) return DSA_ERR_UNSUPPORTED;
+  if (n == 0) return DSA_OK;
+  if (!k_new || !slot_mapping || !k_cache || (cache_dtype == DSA_FP8_E4M3 && !k_scale_cache))
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(k_new) || !aligned16(k_cache) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0 ||
+      (k_scale_cache && (reinterpret_cast<uintptr_t>(k_scale_cache) & 3u) != 0))
+    return DSA_ERR_INVALID_ARGUMENT;
+  unsigned* status = device_status_ptr();
+  if (!status) return DSA_ERR_CUDA;
+  return from_cuda(launch_cache_append(k_new, n, D, slot_mapping, k_cache, cache_dtype == DSA_FP8_E4M3,
+                                       k_scale_cache, static_cast<long long>(num_pages) * page_size, status,
+                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dsa_status dsa_resolve_indexer_sources(int L, const int32_t* types, int32_t* src) {

@@ -89,6 +89,10 @@ cudaError_t launch_score_pair(const ScoreArgs& a, const CUtensorMap* tmap_q, con
                               size_t smem_bytes, cudaStream_t st);
 size_t score_pair_smem_bytes(const ScoreArgs& a, int num_k_stages);
 cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st);
-unsigned* device_status_ptr();   // address of the status word on the current device
+unsigned* device_status_ptr();
+// New indexer keys through slot_mapping into the paged cache (bf16 copy or per-token
+// e4m3 quantisation with its scale); slots >= n_slots set kStatusBadPage.
+cudaError_t launch_cache_append(const void* k_new, int n, int D, const int64_t* slots, void* cache, bool fp8,
+                                float* scale_cache, long long n_slots, unsigned* status, cudaStream_t st);   // address of the status word on the current device
 
 }  // namespace dsa

@@ -212,3 +212,21 @@ def test_dense_host_validation_happens_before_any_cuda_call(dsa):
     assert call(S=0) == dsa.DSA_ERR_UNSUPPORTED
     assert call(ws_bytes=16) == dsa.DSA_ERR_WORKSPACE
     assert call(T=0) == dsa.DSA_OK                               # nothing to do
+
+
+def test_cache_append_validation_happens_before_any_cuda_call(dsa):
+    L = dsa.lib()
+    fake = 1 << 20
+
+    def call(n=4, D=128, dt=1, scales=True, ptrs=True, PS=64, pages=3):
+        p = fake if ptrs else None
+        return L.dsa_indexer_cache_append(p, n, D, p, p, dt, fake if scales else None, PS, pages, None)
+    assert call(n=0) == dsa.DSA_OK
+    assert call(n=-1) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert call(ptrs=False) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert call(scales=False) == dsa.DSA_ERR_INVALID_ARGUMENT   # e4m3 cache needs its scale cache
+    assert call(D=64) == dsa.DSA_ERR_UNSUPPORTED                 # e4m3 rows are D = 128
+    assert call(D=96, dt=0) == dsa.DSA_ERR_UNSUPPORTED
+    assert call(dt=5) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert call(PS=0) == dsa.DSA_ERR_INVALID_ARGUMENT
+

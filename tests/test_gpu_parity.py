@@ -386,3 +386,90 @@ def test_dense_host_fp8_longer_keys_than_queries():
     assert dsa.dsa_check_device_status() == dsa.DSA_OK
     ref, _, _ = oracle_dense(c)
     assert np.array_equal(tk.numpy(), ref)
+
+
+# --------------------------------------------------- cache append (the step's new keys)
+
+def _run_append(k_new, slots, cache, scales):
+    c_d = cache.clone().to(DEV)
+    s_d = None if scales is None else scales.clone().to(DEV)
+    dsa.dsa_indexer_cache_append(k_new.to(DEV), slots.to(DEV), c_d, s_d)
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_status() == dsa.DSA_OK
+    return c_d.cpu(), (None if s_d is None else s_d.cpu())
+
+
+def _same_bytes(a, b):
+    return torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("bf16", 128), ("fp8_e4m3", 128)])
+def test_cache_append_matches_oracle(dtype, D):
+    g = torch.Generator().manual_seed(D + (7 if dtype == "bf16" else 0))
+    n, pages, PS = 300, 12, 64
+    k_new = (torch.randn((n, D), generator=g) *
+             torch.pow(2.0, torch.randint(-8, 8, (n, 1), generator=g).float())).to(torch.bfloat16)
+    k_new[7] = 0
+    slots = torch.randperm(pages * PS, generator=g)[:n].to(torch.int64)
+    slots[::17] = -1
+    if dtype == "bf16":
+        cache, scales = torch.randn((pages, PS, D), generator=g).to(torch.bfloat16), None
+    else:
+        cache = torch.randint(0, 0x7E, (pages, PS, D), generator=g).to(torch.uint8).view(torch.float8_e4m3fn)
+        scales = torch.rand((pages, PS), generator=g) + 0.5
+    got_c, got_s = _run_append(k_new, slots, cache, scales)
+    ref_c, ref_s = oracle.cache_append(k_new, slots, cache, scales)
+    assert _same_bytes(got_c, ref_c)
+    if scales is not None:
+        assert torch.equal(got_s, ref_s)
+
+
+def test_cache_append_every_e4m3_code_and_tie():
+    # rows with amax 448 (scale exactly 1): every finite code, every midpoint between
+    # neighbouring codes (round-to-even ties), both signs, zeros, saturating values
+    vals = torch.arange(127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float32)
+    mids = (vals[:-1] + vals[1:]) / 2
+    pool = torch.cat([vals, -vals, mids, -mids, torch.tensor([0.0, -0.0, 460.0, -470.0])])
+    rows = []
+    for i in range(0, pool.numel(), 127):
+        part = pool[i:i + 127]
+        rows.append(torch.cat([torch.tensor([448.0]), part, torch.zeros(127 - part.numel())]))
+    k_new = torch.stack(rows).to(torch.bfloat16)
+    assert torch.equal(k_new.float()[:, 1:].flatten()[:pool.numel()], pool)  # exact in bf16
+    n = k_new.shape[0]
+    slots = torch.arange(n, dtype=torch.int64)
+    cache = torch.zeros((1, 64, 128), dtype=torch.uint8).view(torch.float8_e4m3fn)
+    scales = torch.zeros((1, 64))
+    got_c, got_s = _run_append(k_new, slots, cache, scales)
+    ref_c, ref_s = oracle.cache_append(k_new, slots, cache, scales)
+    assert _same_bytes(got_c, ref_c) and torch.equal(got_s, ref_s)
+
+
+@pytest.mark.parametrize("q_dtype,k_dtype,decode", [("bf16", "bf16", False), ("fp8_e4m3", "fp8_e4m3", False),
+                                                     ("bf16", "fp8_e4m3", True)])
+def test_indexer_appends_new_keys_before_scoring(q_dtype, k_dtype, decode):
+    # the step's own keys are written through slot_mapping first, so every query sees them
+    if decode:
+        lens, qlens = [1, 300, 1200, 77], [1, 1, 1, 1]
+    else:
+        lens, qlens = [900, 40, 1500, 300], [300, 40, 17, 1]
+    pc = workloads.paged_case(lens, qlens, 64, 128, 128, page_size=64, q_dtype=q_dtype, k_dtype=k_dtype,
+                              integer=True, seed=81)
+    k_new = workloads.new_keys(pc, seed=82, integer=True)
+    if k_dtype == "fp8_e4m3":
+        k_new[:, 5] = 448.0  # amax 448: scale exactly 1, every code exact, so scores stay exact
+    slots = workloads.new_token_slots(pc)
+    to = lambda t: None if t is None else t.to(DEV)
+    cache_d, scale_d = to(pc.k_cache.clone()), to(None if pc.k_scale_cache is None else pc.k_scale_cache.clone())
+    got = dsa.dsa_indexer(to(pc.q), to(pc.w), cache_d, to(pc.cu_q_lens), to(pc.seq_lens), to(pc.block_tables),
+                          max_seq_len=pc.max_seq_len, topk_limit=pc.topk_limit, q_scale=to(pc.q_scale),
+                          k_scale_cache=scale_d, k_new=to(k_new), slot_mapping=to(slots))
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_status() == dsa.DSA_OK
+    ref_c, ref_s = oracle.cache_append(k_new, slots, pc.k_cache, pc.k_scale_cache)
+    assert _same_bytes(cache_d.cpu(), ref_c)
+    if ref_s is not None:
+        assert torch.equal(scale_d.cpu(), ref_s)
+    pc.k_cache, pc.k_scale_cache = ref_c, ref_s
+    ref, _, _ = oracle.paged(pc)
+    assert np.array_equal(got.cpu().numpy(), ref)

@@ -308,3 +308,28 @@ def indexshare_stack(seed: int = 0, B: int = 32, ctx: int = 32768,
         else:
             layers.append(None)
     return StackCase(indexer_types=types, layers=layers)
+
+
+def new_token_slots(pc: PagedCase) -> torch.Tensor:
+    """Cache slot (page * page_size + row) of every query token of a paged case: query i
+    of sequence b is the token at position seq_len - q_len + i, the step's new key."""
+    slots = []
+    cu = pc.cu_q_lens.tolist()
+    for b in range(pc.B):
+        q_len, L = cu[b + 1] - cu[b], int(pc.seq_lens[b])
+        for i in range(q_len):
+            pos = L - q_len + i
+            slots.append(int(pc.block_tables[b, pos // pc.page_size]) * pc.page_size + pos % pc.page_size)
+    return torch.tensor(slots, dtype=torch.int64)
+
+
+def new_keys(pc: PagedCase, seed: int = 0, integer: bool = False) -> torch.Tensor:
+    """bf16 new key rows [total_q, D] for a paged case (N(0,1) scaled per row by a power of
+    two in [2^-6, 2^5], or integers in [-4, 4])."""
+    g = _gen(seed)
+    total_q = int(pc.cu_q_lens[-1])
+    if integer:
+        return randint_values((total_q, pc.D), -4, 4, g).to(torch.bfloat16)
+    x = gaussian((total_q, pc.D), g) * torch.pow(2.0, torch.randint(-6, 6, (total_q, 1), generator=g).float())
+    return x.to(torch.bfloat16)
+
