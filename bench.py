@@ -387,7 +387,30 @@ def _indexshare_stack(dev, stream, peaks, iters=5):
     return out
 
 
+def _cache_append_fp8(dev, stream, peaks, iters=20):
+    """65536 new bf16 keys (D=128) quantised into a paged e4m3 cache through slot_mapping."""
+    import sparse_attention_token_gb300 as dsa
+    hbm = float(peaks["hbm_gbs"])
+    g = torch.Generator(device=dev)
+    g.manual_seed(6)
+    n, PS = 65536, 64
+    pages = n // PS + 8
+    k_new = torch.randn((n, 128), generator=g, device=dev).to(torch.bfloat16)
+    slots = torch.randperm(pages * PS, generator=g, device=dev)[:n].to(torch.int64)
+    cache = torch.zeros((pages, PS, 128), dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
+    scales = torch.zeros((pages, PS), dtype=torch.float32, device=dev)
+    ms = _time_events(lambda: dsa.dsa_indexer_cache_append(k_new, slots, cache, scales, stream=stream), iters, stream)
+    nbytes = n * (128 * 2 + 8 + 128 + 4)  # bf16 row + slot read, codes + scale written
+    out = {"workload": "65536 new keys, bf16 D=128, quantised per token into a paged e4m3 cache (page 64)",
+           "ms_per_step": ms, "tokens_per_s": n / (ms / 1e3), "algorithmic_bytes": nbytes,
+           "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm}
+    del k_new, slots, cache, scales
+    torch.cuda.empty_cache()
+    return out
+
+
 OTHER_WORKLOADS = {
+    "cache_append_fp8": _cache_append_fp8,
     "chunked_prefill_fp8": _chunked_prefill_fp8,
     "decode_b64_fp8_cache": _decode_b64_fp8_cache,
     "indexshare_stack": _indexshare_stack,
