@@ -166,10 +166,14 @@ dsa_status dsa_indexer_workspace_size(const dsa_indexer_args* args, size_t* byte
  * BF16 q against an FP8-e4m3 cache (GLM5 TensorCast adaptation design, background
  * item 5: the indexer cache takes the FP8 dtype when attention is quantised).  That
  * mix is taken on decode batches (total_q <= B) with D = 128 and k_scale_cache set
- * (q_scale is ignored): the keys are widened to bf16 on chip, so every product is
- * exact; the two e4m3 NaN codes are not accepted there (they decode as 480).  On a
- * prefill batch the mix returns DSA_ERR_UNSUPPORTED.  The workspace must not be used
- * by another call that overlaps on the GPU. */
+ * (q_scale is ignored): each bf16 query row x is first rewritten as s x = hi + lo,
+ * two e4m3 rows with a power-of-two scale s (largest |s x| in [128, 256)), exact for
+ * every element within ~2^9 of the row's largest |x| and within 2^-17 of that largest
+ * value otherwise; the keys then meet both rows in FP8 MMAs whose two halves are added
+ * before the ReLU, and w is divided by s.  The two e4m3 NaN codes are not accepted in
+ * the cache.  On a prefill batch the mix returns DSA_ERR_UNSUPPORTED.  The workspace
+ * (which also holds the rewritten queries) must not be used by another call that
+ * overlaps on the GPU. */
 dsa_status dsa_indexer(const dsa_indexer_args* args, dsa_stream_t stream);
 
 /*

@@ -143,9 +143,7 @@ bool make_map_paged(CUtensorMap* m, const void* base, bool fp8, int D, int page_
 
 // Deepest key-tile ring that fits in shared memory (>= 2), or 0.
 int pick_stages(const ScoreArgs& a) {
-  // mixed mode: the ring in shared memory holds e4m3 tiles only (the widened ones live in TMEM)
-  const int top = a.mixed ? kMaxK8Stages : kMaxKStages;
-  for (int s = top; s >= 2; --s)
+  for (int s = kMaxKStages; s >= 2; --s)
     if (score_smem_bytes(a, s) <= kMaxSmem) return s;
   return 0;
 }
@@ -178,10 +176,10 @@ size_t score_pair_launch_smem(const ScoreArgs& a) {
 dsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
 struct PagedPlan {
-  bool decode, pair, mixed;
+  bool decode, pair, split;
   int NQ, N, KC, R, n_chunks, cap, tile_keys;
   long long ld;
-  size_t off_counts, off_items, off_scores, total;
+  size_t off_counts, off_items, off_scores, off_q8, off_w8, total;
 };
 
 dsa_status plan_paged(const dsa_indexer_args* a, PagedPlan* p) {
@@ -199,9 +197,10 @@ dsa_status plan_paged(const dsa_indexer_args* a, PagedPlan* p) {
   if (a->max_seq_len >= (1 << 16) * kBlockM) return DSA_ERR_UNSUPPORTED;  // key-tile ids are 16-bit
   if (a->max_seq_len > INT_MAX - 2 * kBlockM) return DSA_ERR_UNSUPPORTED;
   p->decode = a->total_q <= a->B;
-  p->mixed = a->q_dtype == DSA_BF16 && a->k_dtype == DSA_FP8_E4M3;
-  if (p->mixed) {
-    // bf16 queries against an e4m3 cache: keys are widened to bf16 on chip (decode shapes)
+  p->split = a->q_dtype == DSA_BF16 && a->k_dtype == DSA_FP8_E4M3;
+  if (p->split) {
+    // bf16 queries against an e4m3 cache (decode shapes): each query row is rewritten as an
+    // exact sum of two e4m3 rows and scored by FP8 MMAs
     if (!p->decode || a->D != 128) return DSA_ERR_UNSUPPORTED;
     if (!a->k_scale_cache) return DSA_ERR_INVALID_ARGUMENT;
   } else {
@@ -209,8 +208,8 @@ dsa_status plan_paged(const dsa_indexer_args* a, PagedPlan* p) {
     if (st != DSA_OK) return st;
   }
   const int ns = std::max(num_sms(), 1);
-  p->N = p->decode ? std::max(64, a->H) : 256;
-  p->NQ = p->N / a->H;
+  p->N = p->split ? std::max(64, 2 * a->H) : (p->decode ? std::max(64, a->H) : 256);
+  p->NQ = p->split ? 1 : p->N / a->H;
   p->pair = !p->decode && use_pair_mma();
   p->tile_keys = p->pair ? 2 * kBlockM : kBlockM;
   p->ld = (std::max(a->max_seq_len, 1) + 3) & ~3LL;
@@ -233,6 +232,11 @@ dsa_status plan_paged(const dsa_indexer_args* a, PagedPlan* p) {
   off += ((static_cast<size_t>(p->n_chunks) * p->cap * sizeof(WorkItem) + 255) / 256) * 256;
   p->off_scores = off;
   off += static_cast<size_t>(p->R) * static_cast<size_t>(p->ld) * 4;
+  off = (off + 255) / 256 * 256;
+  p->off_q8 = off;
+  if (p->split) off += (static_cast<size_t>(a->total_q) * 2 * a->H * a->D + 255) / 256 * 256;
+  p->off_w8 = off;
+  if (p->split) off += (static_cast<size_t>(a->total_q) * a->H * 4 + 255) / 256 * 256;
   p->total = off;
   return DSA_OK;
 }
@@ -258,7 +262,7 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
   s.paged = 1;
   s.q_fp8 = fp8;
   s.k_fp8 = a->k_dtype == DSA_FP8_E4M3;
-  s.mixed = p.mixed;
+  s.split = p.split;
   s.H = a->H;
   s.D = a->D;
   s.NQ = p.NQ;
@@ -276,11 +280,24 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
   s.status = status;
   s.num_k_stages = p.pair ? pick_stages_pair(s) : pick_stages(s);
   if (s.num_k_stages < 2) return DSA_ERR_UNSUPPORTED;
-  s.num_a_stages = s.mixed ? std::min(kMaxKStages, mixed_stage_limit(s.N)) : 0;
 
   CUtensorMap tq, tk;
-  if (!make_map_2d(&tq, a->q, fp8, a->D, static_cast<long long>(a->total_q) * a->H, p.pair ? p.N / 2 : p.N))
+  if (p.split) {
+    // hi/lo e4m3 rows of every query and the weights divided by the rows' scales
+    void* q8 = ws + p.off_q8;
+    float* w8 = reinterpret_cast<float*>(ws + p.off_w8);
+    if (launch_qsplit(a->q, a->w, static_cast<long long>(a->total_q) * a->H, a->H, q8, w8, st) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    s.q_fp8 = 1;
+    s.w = w8;
+    s.q_scale = nullptr;
+    s.num_k_stages = pick_stages(s);
+    if (s.num_k_stages < 2) return DSA_ERR_UNSUPPORTED;
+    if (!make_map_2d(&tq, q8, true, a->D, static_cast<long long>(a->total_q) * 2 * a->H, p.N)) return DSA_ERR_CUDA;
+  } else if (!make_map_2d(&tq, a->q, fp8, a->D, static_cast<long long>(a->total_q) * a->H,
+                          p.pair ? p.N / 2 : p.N)) {
     return DSA_ERR_CUDA;
+  }
   if (!make_map_paged(&tk, a->k_cache, s.k_fp8 != 0, a->D, a->page_size, std::max(a->num_pages, 1)))
     return DSA_ERR_CUDA;
 

@@ -20,9 +20,7 @@ enum : unsigned {
 
 constexpr int kBlockM = 128;             // keys per MMA tile (TMEM lanes)
 constexpr int kScoreThreads = 320;       // warp 0 TMA, warp 1 MMA/TMEM, warps 2..9 epilogue
-constexpr int kMixedThreads = 448;       // + warps 10..13 widening e4m3 keys to bf16
 constexpr int kMaxKStages = 8;
-constexpr int kMaxK8Stages = 12;       // e4m3 staging ring of the mixed decode kernel
 constexpr int kTmemCols = 512;           // two accumulators at column 0 and 256
 constexpr int kMaxN = 256;               // MMA N (queries x heads per tile)
 
@@ -38,10 +36,9 @@ struct WorkItem {
 struct ScoreArgs {
   int paged;          // 0: dense k[S, D]; 1: paged k_cache[num_pages, page_size, D]
   int q_fp8, k_fp8;   // element type of q / keys (1 = e4m3, 0 = bf16)
-  int mixed;          // bf16 q with e4m3 keys: keys are widened to bf16 in shared memory
+  int split;          // decode, bf16 q with e4m3 keys: q comes as 2H e4m3 rows (hi, lo) per query
   int H, D, NQ, N;    // N = NQ * H
-  int num_k_stages;   // key ring depth (mixed mode: the e4m3 staging ring in shared memory)
-  int num_a_stages;   // mixed mode: ring of widened key tiles in TMEM
+  int num_k_stages;   // key ring depth
   // dense single sequence
   int T, S, q_pos0, n_dense_items;
   // paged varlen
@@ -81,18 +78,19 @@ struct TopkArgs {
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
                          int grid, size_t smem_bytes, cudaStream_t st);
 size_t score_smem_bytes(const ScoreArgs& a, int num_k_stages);
-// Key stages the mixed (bf16 q, e4m3 keys) decode kernel can hold in TMEM beside its two
-// N-column accumulators: 64 columns per stage in the two 256-column halves.
-inline int mixed_stage_limit(int N) { return 2 * ((256 - N) / 64); }
 // Prefill (N = 256) on CTA pairs: grid = 2 x pairs, work items in 256-key tiles.
 cudaError_t launch_score_pair(const ScoreArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k, int grid,
                               size_t smem_bytes, cudaStream_t st);
 size_t score_pair_smem_bytes(const ScoreArgs& a, int num_k_stages);
 cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st);
-unsigned* device_status_ptr();
+unsigned* device_status_ptr();  // address of the status word on the current device
 // New indexer keys through slot_mapping into the paged cache (bf16 copy or per-token
 // e4m3 quantisation with its scale); slots >= n_slots set kStatusBadPage.
 cudaError_t launch_cache_append(const void* k_new, int n, int D, const int64_t* slots, void* cache, bool fp8,
-                                float* scale_cache, long long n_slots, unsigned* status, cudaStream_t st);   // address of the status word on the current device
+                                float* scale_cache, long long n_slots, unsigned* status, cudaStream_t st);
+// bf16 q rows [rows = total_q * H, 128] -> q8 [total_q, 2H, 128] e4m3 (hi rows, then lo
+// rows, per query) with a power-of-two scale s per row, and w8 = w / s.
+cudaError_t launch_qsplit(const void* q, const float* w, long long rows, int H, void* q8, float* w8,
+                          cudaStream_t st);
 
 }  // namespace dsa

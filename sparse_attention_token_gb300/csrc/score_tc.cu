@@ -38,44 +38,31 @@ namespace {
 struct SmemPlan {
   uint32_t q[2];
   uint32_t k[kMaxKStages];
-  uint32_t k8[kMaxK8Stages];  // e4m3 staging of the keys (mixed mode)
   uint32_t wbuf, qsbuf, ksbuf, bars, misc, total;
 };
 
-__host__ __device__ inline SmemPlan plan_smem(int N, int D, int q_fp8, int k_fp8, int nK, int mixed = 0) {
+__host__ __device__ inline SmemPlan plan_smem(int N, int D, int q_fp8, int k_fp8, int nK) {
   SmemPlan p{};
   uint32_t off = 0;
   const uint32_t qb = static_cast<uint32_t>(N) * D * (q_fp8 ? 1 : 2);
-  // mixed: the widened keys live in TMEM, only the e4m3 staging ring is in shared memory
-  const uint32_t kb = mixed ? 0u : static_cast<uint32_t>(kBlockM) * D * (k_fp8 ? 1 : 2);
+  const uint32_t kb = static_cast<uint32_t>(kBlockM) * D * (k_fp8 ? 1 : 2);
   for (int i = 0; i < 2; ++i) { p.q[i] = off; off += qb; }
   for (int i = 0; i < kMaxKStages; ++i) { p.k[i] = off; if (i < nK) off += kb; }
-  for (int i = 0; i < kMaxK8Stages; ++i) { p.k8[i] = off; if (mixed && i < nK) off += static_cast<uint32_t>(kBlockM) * D; }
   p.wbuf = off;  off += 2u * N * 4u;
   p.qsbuf = off; if (q_fp8) off += 2u * N * 4u;
-  p.ksbuf = off; if (k_fp8 && !mixed) off += static_cast<uint32_t>(nK) * kBlockM * 4u;  // mixed decode reads scales from global
-  p.bars = off;  off += 64u * 8u;
+  p.ksbuf = off; if (k_fp8) off += static_cast<uint32_t>(nK) * kBlockM * 4u;
+  p.bars = off;  off += 48u * 8u;
   p.misc = off;  off += 16u;
   p.total = off;
   return p;
 }
 
-// Mixed mode: TMEM column of key stage s widened to bf16 (128 lanes x 64 columns).  The
-// accumulators take columns [0, N) and [256, 256 + N); the stages fill the rest.
-__device__ __forceinline__ uint32_t mixed_a_col(int s, int N) {
-  const int per = (256 - N) / 64;
-  return static_cast<uint32_t>(s < per ? N + 64 * s : 256 + N + 64 * (s - per));
-}
-
 // Barrier slots inside the bars region.
 enum {
   kBarQFull = 0, kBarQEmpty = 2, kBarTFull = 4, kBarTEmpty = 6, kBarFold = 8,  // fold: 4 slots
-  // key ring; in mixed mode the ring of widened tiles in TMEM (full: converted, empty: MMAs done)
-  kBarDone = 12, kBarKFull = 13, kBarKEmpty = 13 + kMaxKStages,
-  kBarK8Full = 13 + 2 * kMaxKStages,                  // mixed: e4m3 key tile landed in shared memory
-  kBarK8Empty = 13 + 2 * kMaxKStages + kMaxK8Stages   // mixed: e4m3 staging slot converted
+  kBarDone = 12, kBarKFull = 13, kBarKEmpty = 13 + kMaxKStages, kBarEnd = 13 + 2 * kMaxKStages
 };
-static_assert(kBarK8Empty + kMaxK8Stages <= 64, "barrier region");
+static_assert(kBarEnd <= 48, "barrier region");
 
 struct ItemInfo {
   int row0, pos0, kt0, kt1, b, nrows;
@@ -108,21 +95,24 @@ __device__ __forceinline__ bool fetch_item(const ScoreArgs& a, int n_items, int 
   return true;
 }
 
-template <int H, bool DECODE>
+// SPLIT (decode, bf16 q against e4m3 keys): each query's H heads come as 2H e4m3 rows
+// (hi rows, then lo rows), one query per tile: N = max(64, 2H).
+template <int H, bool DECODE, bool SPLIT = false>
 struct Cfg {
-  static constexpr int N = DECODE ? (H >= 64 ? H : 64) : 256;
-  static constexpr int NQ = N / H;
+  static constexpr int N = SPLIT ? (2 * H >= 64 ? 2 * H : 64) : (DECODE ? (H >= 64 ? H : 64) : 256);
+  static constexpr int NQ = SPLIT ? 1 : N / H;
   static constexpr int NCOLS = DECODE ? N : N / 2;  // columns one epilogue thread reduces
-  static constexpr int QH = NCOLS / H;               // queries in those columns
+  static constexpr int QH = SPLIT ? 1 : NCOLS / H;   // queries in those columns
   static constexpr int EPI_T_ARRIVALS = DECODE ? 4 : 8;
+  static constexpr int QROWS = SPLIT ? 2 * H : H;    // q rows per query
 };
 
 // ------------------------------------------------------------------ producer (warp 0)
-template <int H, bool DECODE>
+template <int H, bool DECODE, bool SPLIT>
 __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensorMap* tmap_q,
                                               const CUtensorMap* tmap_k, uint8_t* smem, const SmemPlan& P,
                                               uint64_t* bars, volatile int* abort, int n_items) {
-  using C = Cfg<H, DECODE>;
+  using C = Cfg<H, DECODE, SPLIT>;
   constexpr int N = C::N;
   const int lane = threadIdx.x & 31;
   const int nK = a.num_k_stages;
@@ -151,12 +141,13 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
       if (!good) { ok = false; break; }
       const long long base = static_cast<long long>(I.row0) * H;
       const long long lim = static_cast<long long>(a.total_rows) * H;
-      for (int c = lane; c < N / 4; c += 32) {
+      // w (and q_scale) for the item's columns; SPLIT: the query's H weights (w / s)
+      for (int c = lane; c < (SPLIT ? H : N) / 4; c += 32) {
         const long long e = base + 4ll * c;
         const bool v = e + 4 <= lim;
         ptx::cp_async_16(wbuf + s * N + 4 * c, v ? static_cast<const void*>(a.w + e) : static_cast<const void*>(a.w),
                          v ? 16u : 0u);
-        if (a.q_fp8)
+        if (a.q_fp8 && !SPLIT)
           ptx::cp_async_16(qsbuf + s * N + 4 * c,
                            v ? static_cast<const void*>(a.q_scale + e) : static_cast<const void*>(a.q_scale),
                            v ? 16u : 0u);
@@ -166,7 +157,8 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
       __syncwarp();
       // one TMA instruction: lane `at` copies 128-byte atom column `at`
       if (lane < n_atoms_q)
-        ptx::tma_load_2d(smem + P.q[s] + lane * N * 128, tmap_q, &bars[kBarQFull + s], lane * box_q, I.row0 * H);
+        ptx::tma_load_2d(smem + P.q[s] + lane * N * 128, tmap_q, &bars[kBarQFull + s], lane * box_q,
+                         I.row0 * C::QROWS);
       ++nq;
     }
     // ---- key tiles
@@ -178,15 +170,12 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
       const int s = nk % nK;
       int good = 1;
       if (lane == 0) {
-        // mixed: the staging slot is free once the converters have read it
-        good = ptx::mbar_wait(&bars[(a.mixed ? kBarK8Empty : kBarKEmpty) + s], ((nk / nK) & 1) ^ 1, abort, a.status,
-                              kStatusTimeout);
+        good = ptx::mbar_wait(&bars[kBarKEmpty + s], ((nk / nK) & 1) ^ 1, abort, a.status, kStatusTimeout);
       }
       good = __shfl_sync(0xffffffffu, good, 0);
       if (!good) { ok = false; break; }
-      // mixed: the e4m3 tile and its scales land in the staging slot; converters fill P.k
-      uint64_t* full = a.mixed ? &bars[kBarK8Full + s] : &bars[kBarKFull + s];
-      uint8_t* dst = smem + (a.mixed ? P.k8[0] + s * (P.k8[1] - P.k8[0]) : P.k[0] + s * (P.k[1] - P.k[0]));
+      uint64_t* full = &bars[kBarKFull + s];
+      uint8_t* dst = smem + P.k[0] + s * (P.k[1] - P.k[0]);
       // Each TMA instruction costs the issuing warp a fixed time however many lanes
       // issue it, so every copy of a tile goes out in one instruction, one lane per copy.
       if (!a.paged) {
@@ -250,8 +239,7 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
     const int kk = nk < static_cast<uint32_t>(nK) ? static_cast<int>(nk) : nK;
     for (int i = 1; i <= kk; ++i) {
       const uint32_t u = nk - i;
-      ptx::mbar_wait_drain(&bars[(a.mixed ? kBarK8Full : kBarKFull) + (u % nK)], (u / nK) & 1, a.status, kStatusTimeout,
-                           200000000ull);
+      ptx::mbar_wait_drain(&bars[kBarKFull + (u % nK)], (u / nK) & 1, a.status, kStatusTimeout, 200000000ull);
     }
   }
 }
@@ -261,12 +249,12 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
 // everything in registers: stage index and phase advance incrementally, stage
 // addresses come from one multiply, and the per-step descriptors are the first
 // step's descriptors plus a compile-time offset in their 16-byte address field.
-template <int H, bool DECODE, bool F8, int NSTEPS, bool ATMEM = false>
+template <int H, bool DECODE, bool SPLIT, bool F8, int NSTEPS>
 __device__ __forceinline__ void mma_loop(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P, uint64_t* bars,
                                          volatile int* abort, int n_items, uint32_t tmem_base) {
-  using C = Cfg<H, DECODE>;
+  using C = Cfg<H, DECODE, SPLIT>;
   constexpr int N = C::N;
-  const int nK = ATMEM ? a.num_a_stages : a.num_k_stages;
+  const int nK = a.num_k_stages;
   const uint32_t idesc = ptx::idesc_f32acc(kBlockM, N, !F8);
   const uint32_t sbase = ptx::smem_u32(smem);
   const uint32_t k_stage_bytes = P.k[1] - P.k[0];
@@ -289,24 +277,14 @@ __device__ __forceinline__ void mma_loop(const ScoreArgs& a, uint8_t* smem, cons
       }
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
-      if constexpr (ATMEM) {
-        // keys widened into TMEM: step j takes columns [8j, 8j + 8) (16 bf16 of K)
-        const uint32_t a_tmem = tmem_base + mixed_a_col(static_cast<int>(sk), N);
+      const uint64_t adesc0 = ptx::sw128_kmajor_desc(k_base + sk * k_stage_bytes);
 #pragma unroll
-        for (int j = 0; j < NSTEPS; ++j) {
-          const uint64_t bd = bdesc0 + static_cast<uint64_t>(((j >> 2) * (N * 128) + (j & 3) * 32) >> 4);
-          ptx::mma_bf16_ts(d_tmem, a_tmem + 8 * j, bd, idesc, j > 0 ? 1u : 0u);
-        }
-      } else {
-        const uint64_t adesc0 = ptx::sw128_kmajor_desc(k_base + sk * k_stage_bytes);
-#pragma unroll
-        for (int j = 0; j < NSTEPS; ++j) {
-          // step j reads 32 bytes of K at atom (j / 4), byte (j % 4) * 32 of each row
-          const uint64_t ad = adesc0 + static_cast<uint64_t>(((j >> 2) * (kBlockM * 128) + (j & 3) * 32) >> 4);
-          const uint64_t bd = bdesc0 + static_cast<uint64_t>(((j >> 2) * (N * 128) + (j & 3) * 32) >> 4);
-          if (F8) ptx::mma_f8(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
-          else ptx::mma_bf16(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
-        }
+      for (int j = 0; j < NSTEPS; ++j) {
+        // step j reads 32 bytes of K at atom (j / 4), byte (j % 4) * 32 of each row
+        const uint64_t ad = adesc0 + static_cast<uint64_t>(((j >> 2) * (kBlockM * 128) + (j & 3) * 32) >> 4);
+        const uint64_t bd = bdesc0 + static_cast<uint64_t>(((j >> 2) * (N * 128) + (j & 3) * 32) >> 4);
+        if (F8) ptx::mma_f8(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
+        else ptx::mma_bf16(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
       }
       ptx::mma_commit(&bars[kBarKEmpty + sk]);
       ptx::mma_commit(&bars[kBarTFull + acc]);
@@ -322,14 +300,13 @@ __device__ __forceinline__ void mma_loop(const ScoreArgs& a, uint8_t* smem, cons
   ptx::mbar_wait_drain(&bars[kBarDone], 0, a.status, kStatusTimeout, 200000000ull);
 }
 
-template <int H, bool DECODE>
+template <int H, bool DECODE, bool SPLIT>
 __device__ __forceinline__ void mma_role(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P, uint64_t* bars,
                                          volatile int* abort, int n_items, uint32_t tmem_base) {
-  // 32 bytes of K per MMA: 16 bf16 or 32 e4m3 values; mixed mode multiplies bf16 by widened keys
-  if (a.q_fp8) mma_loop<H, DECODE, true, 4>(a, smem, P, bars, abort, n_items, tmem_base);
-  else if (DECODE && a.mixed) mma_loop<H, DECODE, false, 8, DECODE>(a, smem, P, bars, abort, n_items, tmem_base);
-  else if (a.D == 128) mma_loop<H, DECODE, false, 8>(a, smem, P, bars, abort, n_items, tmem_base);
-  else mma_loop<H, DECODE, false, 4>(a, smem, P, bars, abort, n_items, tmem_base);
+  // 32 bytes of K per MMA: 16 bf16 or 32 e4m3 values (SPLIT: e4m3 queries, N = 2H)
+  if (SPLIT || a.q_fp8) mma_loop<H, DECODE, SPLIT, true, 4>(a, smem, P, bars, abort, n_items, tmem_base);
+  else if (a.D == 128) mma_loop<H, DECODE, SPLIT, false, 8>(a, smem, P, bars, abort, n_items, tmem_base);
+  else mma_loop<H, DECODE, SPLIT, false, 4>(a, smem, P, bars, abort, n_items, tmem_base);
 }
 
 // Every lane waits (each observes the barrier itself); the outcome is made uniform
@@ -339,85 +316,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-// ------------------------------------------------------------------ key widening (mixed mode, warps 10..13)
-// Two e4m3 codes -> two bf16, exactly (every e4m3 value, subnormals included, is a
-// bf16 value).  `t` holds the codes in bits 15..8 and 31..24.  Moving the code's
-// exponent and mantissa bits under bf16's exponent/mantissa boundary gives a bf16
-// whose exponent is biased by 127 instead of 7 (an e4m3 subnormal lands on a bf16
-// subnormal with the same mantissa); one multiply by 2^120 removes the bias gap.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t t) {
-  const uint32_t v = (t & 0x80008000u) | ((t >> 4) & 0x07F007F0u);
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x7B807B80u));  // 0x7B80 = 2^120
-  return r;
-}
-
-// Widen every staged e4m3 key tile (128 rows x D=128 bytes, 128-byte swizzle) to bf16
-// straight into TMEM, where the MMA reads it as its A operand.  Warp w owns TMEM lanes
-// [32 (w % 4), 32 (w % 4) + 32): lane l converts key row 32 (w % 4) + l, 64 columns.
-template <int H, bool DECODE>
-__device__ __forceinline__ void convert_role(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P, uint64_t* bars,
-                                             volatile int* abort, int n_items, uint32_t tmem_base) {
-  using C = Cfg<H, DECODE>;
-  const int quarter = (threadIdx.x >> 5) & 3;
-  const int lane = threadIdx.x & 31;
-  const int r = quarter * 32 + lane;
-  const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-  const int nK = a.num_k_stages;   // e4m3 staging ring (shared memory)
-  const int nA = a.num_a_stages;   // widened tiles (TMEM)
-  const uint32_t k8_stage = P.k8[1] - P.k8[0];
-  uint32_t sk = 0, kph = 0, sa = 0, aph = 0;
-  bool ok = true;
-  for (int it = 0; ok; ++it) {
-    ItemInfo I;
-    if (!fetch_item<C::NQ>(a, n_items, it, I)) break;
-    for (int kt = I.kt0; kt < I.kt1; ++kt) {
-      // the staged tile has landed, and the MMAs that read this TMEM slot last are done
-      if (!warp_wait(&bars[kBarK8Full + sk], kph, abort, a.status) ||
-          !warp_wait(&bars[kBarKEmpty + sa], aph ^ 1u, abort, a.status)) {
-        ok = false;
-        break;
-      }
-      const uint8_t* row = smem + P.k8[0] + sk * k8_stage + r * 128;
-      const uint32_t acol = tmem_base + lane_addr + mixed_a_col(static_cast<int>(sa), C::N);
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t o[32];
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          // logical 16-byte chunk c = e4m3 elements [16c, 16c + 16) -> columns [8c, 8c + 8)
-          const int c = 4 * hh + c4;
-          const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
-          o[8 * c4 + 0] = e4m3x2_to_bf16x2(__byte_perm(v.x, 0, 0x1404));
-          o[8 * c4 + 1] = e4m3x2_to_bf16x2(__byte_perm(v.x, 0, 0x3424));
-          o[8 * c4 + 2] = e4m3x2_to_bf16x2(__byte_perm(v.y, 0, 0x1404));
-          o[8 * c4 + 3] = e4m3x2_to_bf16x2(__byte_perm(v.y, 0, 0x3424));
-          o[8 * c4 + 4] = e4m3x2_to_bf16x2(__byte_perm(v.z, 0, 0x1404));
-          o[8 * c4 + 5] = e4m3x2_to_bf16x2(__byte_perm(v.z, 0, 0x3424));
-          o[8 * c4 + 6] = e4m3x2_to_bf16x2(__byte_perm(v.w, 0, 0x1404));
-          o[8 * c4 + 7] = e4m3x2_to_bf16x2(__byte_perm(v.w, 0, 0x3424));
-        }
-        ptx::tmem_st_32x32b_x32(acol + 32 * hh, o);
-      }
-      ptx::tmem_st_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(&bars[kBarKFull + sa]);
-        ptx::mbar_arrive(&bars[kBarK8Empty + sk]);
-      }
-      if (++sk == static_cast<uint32_t>(nK)) { sk = 0; kph ^= 1u; }
-      if (++sa == static_cast<uint32_t>(nA)) { sa = 0; aph ^= 1u; }
-    }
-  }
-}
-
 // ------------------------------------------------------------------ epilogue (warps 2..9)
-template <int H, bool DECODE>
+template <int H, bool DECODE, bool SPLIT>
 __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P,
                                               uint64_t* bars, volatile int* abort, int n_items,
                                               uint32_t tmem_base) {
-  using C = Cfg<H, DECODE>;
+  using C = Cfg<H, DECODE, SPLIT>;
   constexpr int N = C::N;
   constexpr int NCOLS = C::NCOLS;
   constexpr int QH = C::QH;
@@ -443,7 +347,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
     const int sq = nq & 1;
     if (!warp_wait(&bars[kBarQFull + sq], (nq >> 1) & 1, abort, a.status)) break;
     float* wq = wbuf + sq * N;
-    if (a.q_fp8) {
+    if (a.q_fp8 && !SPLIT) {
       // fold the q scale into w once per item (in place, each thread one column)
       const int c = DECODE ? fold_t : col0 + fold_t;
       if (!DECODE || fold_t < N) wq[c] *= qsbuf[sq * N + c];
@@ -480,6 +384,44 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
           break;
         }
         ptx::tc_fence_after();
+        const uint32_t tcol = tmem_base + lane_addr + static_cast<uint32_t>(acc * 256 + col0);
+        float accq[QH];
+        if constexpr (SPLIT) {
+          // head h: the hi part at column h, the lo part at column H + h; their sum is the
+          // exact bf16 product up to fp32 rounding, and the ReLU takes the sum
+          float2 part[4];
+#pragma unroll
+          for (int p = 0; p < 4; ++p) part[p] = make_float2(0.f, 0.f);
+          uint32_t xa[32], xb[32];
+          if constexpr (H >= 32) {
+#pragma unroll
+            for (int j = 0; j < H / 32; ++j) {
+              ptx::tmem_ld_32x32b_x32(tcol + 32 * j, xa);
+              ptx::tmem_ld_32x32b_x32(tcol + H + 32 * j, xb);
+              ptx::tmem_ld_wait_regs(xa);  // waits for both loads; the second ties xb's registers
+              ptx::tmem_ld_wait_regs(xb);
+              const float2* w2 = reinterpret_cast<const float2*>(wq + 32 * j);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float r0 = fmaxf(__uint_as_float(xa[2 * i]) + __uint_as_float(xb[2 * i]), 0.f);
+                const float r1 = fmaxf(__uint_as_float(xa[2 * i + 1]) + __uint_as_float(xb[2 * i + 1]), 0.f);
+                ptx::ffma2(part[i & 3], w2[i], make_float2(r0, r1));
+              }
+            }
+          } else {
+            ptx::tmem_ld_32x32b_x32(tcol, xa);
+            ptx::tmem_ld_wait_regs(xa);
+            const float2* w2 = reinterpret_cast<const float2*>(wq);
+#pragma unroll
+            for (int i = 0; i < H / 2; ++i) {
+              const float r0 = fmaxf(__uint_as_float(xa[2 * i]) + __uint_as_float(xa[H + 2 * i]), 0.f);
+              const float r1 = fmaxf(__uint_as_float(xa[2 * i + 1]) + __uint_as_float(xa[H + 2 * i + 1]), 0.f);
+              ptx::ffma2(part[i & 3], w2[i], make_float2(r0, r1));
+            }
+          }
+          accq[0] = (part[0].x + part[0].y) + (part[1].x + part[1].y) + (part[2].x + part[2].y) +
+                    (part[3].x + part[3].y);
+        } else {
         // NP packed (f32x2) partial sums per query: independent FMA chains
         constexpr int NP = (32 / (2 * QH)) > 4 ? 4 : ((32 / (2 * QH)) < 1 ? 1 : (32 / (2 * QH)));
         float2 part[QH][NP];
@@ -487,7 +429,6 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
         for (int j = 0; j < QH; ++j)
 #pragma unroll
           for (int p = 0; p < NP; ++p) part[j][p] = make_float2(0.f, 0.f);
-        const uint32_t tcol = tmem_base + lane_addr + static_cast<uint32_t>(acc * 256 + col0);
         uint32_t xa[32], xb[32];
         ptx::tmem_ld_32x32b_x32(tcol, xa);
         ptx::tmem_ld_wait_regs(xa);
@@ -514,13 +455,13 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
             for (int i = 0; i < 32; ++i) xa[i] = xb[i];
           }
         }
-        float accq[QH];
 #pragma unroll
         for (int j = 0; j < QH; ++j) {
           float t = 0.f;
 #pragma unroll
           for (int p = 0; p < NP; ++p) t += part[j][p].x + part[j][p].y;
           accq[j] = t;
+        }
         }
         ptx::tc_fence_before();
         __syncwarp();
@@ -552,18 +493,18 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
   }
 }
 
-template <int H, bool DECODE, bool MIXED>
-__global__ void __launch_bounds__(MIXED ? kMixedThreads : kScoreThreads, 1)
+template <int H, bool DECODE, bool SPLIT>
+__global__ void __launch_bounds__(kScoreThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                  const ScoreArgs a) {
-  using C = Cfg<H, DECODE>;
+  using C = Cfg<H, DECODE, SPLIT>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if ((ptx::smem_u32(smem) & 1023u) != 0) {
     if (threadIdx.x == 0) atomicOr(a.status, kStatusSmemAlign);
     return;
   }
-  const SmemPlan P = plan_smem(C::N, a.D, a.q_fp8, a.k_fp8, a.num_k_stages, MIXED ? 1 : 0);
+  const SmemPlan P = plan_smem(C::N, a.D, SPLIT ? 1 : a.q_fp8, a.k_fp8, a.num_k_stages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + P.misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + P.misc + 4);
@@ -578,19 +519,11 @@ __global__ void __launch_bounds__(MIXED ? kMixedThreads : kScoreThreads, 1)
       ptx::mbar_init(&bars[kBarFold + 2 * s + 1], 128);
     }
     ptx::mbar_init(&bars[kBarDone], 1);
-    const int n_ring = MIXED ? a.num_a_stages : a.num_k_stages;
-    for (int s = 0; s < n_ring; ++s) {
-      // dense e4m3 key scales come by cp.async (32 lane arrivals); paged ones by bulk copy;
-      // mixed: the four converter warps fill a TMEM slot
-      ptx::mbar_init(&bars[kBarKFull + s], MIXED ? 4 : 1 + ((a.k_fp8 && !a.paged) ? 32 : 0));
+    for (int s = 0; s < a.num_k_stages; ++s) {
+      // dense e4m3 key scales come by cp.async (32 lane arrivals); paged ones by bulk copy
+      ptx::mbar_init(&bars[kBarKFull + s], 1 + ((a.k_fp8 && !a.paged) ? 32 : 0));
       // the epilogue also releases a stage when it reads that stage's key scales from ksbuf
       ptx::mbar_init(&bars[kBarKEmpty + s], 1 + ((a.k_fp8 && !(DECODE && a.paged)) ? C::EPI_T_ARRIVALS : 0));
-    }
-    if (MIXED) {
-      for (int s = 0; s < a.num_k_stages; ++s) {
-        ptx::mbar_init(&bars[kBarK8Full + s], 1);
-        ptx::mbar_init(&bars[kBarK8Empty + s], 4);
-      }
     }
     *abort = 0;
     ptx::fence_mbar_init();
@@ -613,14 +546,12 @@ __global__ void __launch_bounds__(MIXED ? kMixedThreads : kScoreThreads, 1)
     // the two accumulators assume the allocation starts at column 0
     if (threadIdx.x == 0) atomicOr(a.status, kStatusTmemAlloc);
   } else if (warp == 0) {
-    producer_role<H, DECODE>(a, &tmap_q, &tmap_k, smem, P, bars, abort, n_items);
+    producer_role<H, DECODE, SPLIT>(a, &tmap_q, &tmap_k, smem, P, bars, abort, n_items);
   } else if (warp == 1) {
-    if (lane == 0) mma_role<H, DECODE>(a, smem, P, bars, abort, n_items, tmem_base);
+    if (lane == 0) mma_role<H, DECODE, SPLIT>(a, smem, P, bars, abort, n_items, tmem_base);
     __syncwarp();
-  } else if (MIXED && warp >= 10) {
-    convert_role<H, DECODE>(a, smem, P, bars, abort, n_items, tmem_base);
   } else {
-    epilogue_role<H, DECODE>(a, smem, P, bars, abort, n_items, tmem_base);
+    epilogue_role<H, DECODE, SPLIT>(a, smem, P, bars, abort, n_items, tmem_base);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -630,28 +561,28 @@ __global__ void __launch_bounds__(MIXED ? kMixedThreads : kScoreThreads, 1)
   }
 }
 
-template <int H, bool DECODE, bool MIXED>
+template <int H, bool DECODE, bool SPLIT>
 cudaError_t launch_t(const ScoreArgs& a, const CUtensorMap* tq, const CUtensorMap* tk, int grid, size_t smem,
                      cudaStream_t st) {
-  auto kern = score_kernel<H, DECODE, MIXED>;
+  auto kern = score_kernel<H, DECODE, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, MIXED ? kMixedThreads : kScoreThreads, smem, st>>>(*tq, *tk, a);
+  kern<<<grid, kScoreThreads, smem, st>>>(*tq, *tk, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t score_smem_bytes(const ScoreArgs& a, int num_k_stages) {
-  return plan_smem(a.N, a.D, a.q_fp8, a.k_fp8, num_k_stages, a.mixed).total;
+  return plan_smem(a.N, a.D, a.split ? 1 : a.q_fp8, a.k_fp8, num_k_stages).total;
 }
 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k, int grid,
                          size_t smem_bytes, cudaStream_t st) {
-  const bool dec = a.N != 256;
+  const bool dec = a.split || a.N != 256;
 #define DSA_CASE(HH)                                                                        \
   case HH:                                                                                  \
-    return dec ? (a.mixed ? launch_t<HH, true, true>(a, tmap_q, tmap_k, grid, smem_bytes, st)          \
+    return dec ? (a.split ? launch_t<HH, true, true>(a, tmap_q, tmap_k, grid, smem_bytes, st)          \
                           : launch_t<HH, true, false>(a, tmap_q, tmap_k, grid, smem_bytes, st))        \
                : launch_t<HH, false, false>(a, tmap_q, tmap_k, grid, smem_bytes, st);
   switch (a.H) {
