@@ -20,7 +20,7 @@ enum : unsigned {
 
 constexpr int kBlockM = 128;             // keys per MMA tile (TMEM lanes)
 constexpr int kScoreThreads = 320;       // warp 0 TMA, warp 1 MMA/TMEM, warps 2..9 epilogue
-constexpr int kMaxKStages = 8;
+constexpr int kMaxKStages = 12;
 constexpr int kTmemCols = 512;           // two accumulators at column 0 and 256
 constexpr int kMaxN = 256;               // MMA N (queries x heads per tile)
 

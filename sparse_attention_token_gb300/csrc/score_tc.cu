@@ -11,13 +11,15 @@
 // (each query's H heads are H consecutive TMEM columns), K = D.  A TMEM lane then
 // holds every head of one (key, query) pair, so the head reduction is in-thread.
 //
-// Warp roles (320 threads, 448 with the key converters; one CTA per SM, persistent
-// over work items):
+// Warp roles (one CTA per SM, persistent over work items; 320 threads, 352 for decode):
 //   warp 0      TMA producer: q tile (N x D) per item into a 2-deep ring, key tiles
 //               (128 x D, dense or gathered page by page through block_tables) into
 //               an nK-deep ring, per-item w / q_scale by cp.async, per-tile k_scale by
 //               cp.async (dense keys) or a bulk copy per page (paged prefill); decode
 //               epilogue threads read their paged key scales from global memory.
+//   warp 10     decode only: a second key producer.  Warp 0 takes the even key tiles,
+//               warp 10 the odd ones (each owns alternate stages of an even ring), so
+//               the address work and TMA issue of one overlap the other's.
 //   warp 1      TMEM allocator; lane 0 issues tcgen05.mma into two 256-column fp32
 //               accumulators (double buffered) and commits to mbarriers.
 //   warps 2..9  epilogue: tcgen05.ld, ReLU, head-weighted sum, k scale, causal mask,
@@ -51,7 +53,7 @@ __host__ __device__ inline SmemPlan plan_smem(int N, int D, int q_fp8, int k_fp8
   p.wbuf = off;  off += 2u * N * 4u;
   p.qsbuf = off; if (q_fp8) off += 2u * N * 4u;
   p.ksbuf = off; if (k_fp8) off += static_cast<uint32_t>(nK) * kBlockM * 4u;
-  p.bars = off;  off += 48u * 8u;
+  p.bars = off;  off += 64u * 8u;
   p.misc = off;  off += 16u;
   p.total = off;
   return p;
@@ -62,7 +64,7 @@ enum {
   kBarQFull = 0, kBarQEmpty = 2, kBarTFull = 4, kBarTEmpty = 6, kBarFold = 8,  // fold: 4 slots
   kBarDone = 12, kBarKFull = 13, kBarKEmpty = 13 + kMaxKStages, kBarEnd = 13 + 2 * kMaxKStages
 };
-static_assert(kBarEnd <= 48, "barrier region");
+static_assert(kBarEnd <= 64, "barrier region");
 
 struct ItemInfo {
   int row0, pos0, kt0, kt1, b, nrows;
@@ -104,14 +106,18 @@ struct Cfg {
   static constexpr int NCOLS = DECODE ? N : N / 2;  // columns one epilogue thread reduces
   static constexpr int QH = SPLIT ? 1 : NCOLS / H;   // queries in those columns
   static constexpr int EPI_T_ARRIVALS = DECODE ? 4 : 8;
-  static constexpr int QROWS = SPLIT ? 2 * H : H;    // q rows per query
+  static constexpr int QROWS = SPLIT ? 2 * H : H;
+  // decode tiles are short (16 or 32 KB) and HBM-bound: a second producer warp (warp 10)
+  // takes every other key tile, which needs an even ring
+  static constexpr int NPROD = DECODE ? 2 : 1;
+  static constexpr int THREADS = kScoreThreads + 32 * (NPROD - 1);    // q rows per query
 };
 
 // ------------------------------------------------------------------ producer (warp 0)
 template <int H, bool DECODE, bool SPLIT>
 __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensorMap* tmap_q,
                                               const CUtensorMap* tmap_k, uint8_t* smem, const SmemPlan& P,
-                                              uint64_t* bars, volatile int* abort, int n_items) {
+                                              uint64_t* bars, volatile int* abort, int n_items, int pw) {
   using C = Cfg<H, DECODE, SPLIT>;
   constexpr int N = C::N;
   const int lane = threadIdx.x & 31;
@@ -132,8 +138,8 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
   for (int it = 0; ok; ++it) {
     ItemInfo I;
     if (!fetch_item<C::NQ>(a, n_items, it, I)) break;
-    // ---- q tile, w and q_scale of this item
-    {
+    // ---- q tile, w and q_scale of this item (first producer)
+    if (pw == 0) {
       const int s = nq & 1;
       int good = 1;
       if (lane == 0) good = ptx::mbar_wait(&bars[kBarQEmpty + s], ((nq >> 1) & 1) ^ 1, abort, a.status, kStatusTimeout);
@@ -167,6 +173,10 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
     int pg_win = -1;
     const int pos_last = I.pos0 + I.nrows - 1;
     for (int kt = I.kt0; kt < I.kt1; ++kt) {
+      if (C::NPROD == 2 && (nk & 1u) != static_cast<uint32_t>(pw)) {
+        ++nk;  // the other producer's tile (and stage)
+        continue;
+      }
       const int s = nk % nK;
       int good = 1;
       if (lane == 0) {
@@ -239,6 +249,7 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
     const int kk = nk < static_cast<uint32_t>(nK) ? static_cast<int>(nk) : nK;
     for (int i = 1; i <= kk; ++i) {
       const uint32_t u = nk - i;
+      if (C::NPROD == 2 && (u & 1u) != static_cast<uint32_t>(pw)) continue;  // the other producer's copy
       ptx::mbar_wait_drain(&bars[kBarKFull + (u % nK)], (u / nK) & 1, a.status, kStatusTimeout, 200000000ull);
     }
   }
@@ -494,7 +505,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
 }
 
 template <int H, bool DECODE, bool SPLIT>
-__global__ void __launch_bounds__(kScoreThreads, 1)
+__global__ void __launch_bounds__(Cfg<H, DECODE, SPLIT>::THREADS, 1)
     score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                  const ScoreArgs a) {
   using C = Cfg<H, DECODE, SPLIT>;
@@ -546,7 +557,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     // the two accumulators assume the allocation starts at column 0
     if (threadIdx.x == 0) atomicOr(a.status, kStatusTmemAlloc);
   } else if (warp == 0) {
-    producer_role<H, DECODE, SPLIT>(a, &tmap_q, &tmap_k, smem, P, bars, abort, n_items);
+    producer_role<H, DECODE, SPLIT>(a, &tmap_q, &tmap_k, smem, P, bars, abort, n_items, 0);
+  } else if (C::NPROD == 2 && warp == 10) {
+    producer_role<H, DECODE, SPLIT>(a, &tmap_q, &tmap_k, smem, P, bars, abort, n_items, 1);
   } else if (warp == 1) {
     if (lane == 0) mma_role<H, DECODE, SPLIT>(a, smem, P, bars, abort, n_items, tmem_base);
     __syncwarp();
@@ -567,7 +580,8 @@ cudaError_t launch_t(const ScoreArgs& a, const CUtensorMap* tq, const CUtensorMa
   auto kern = score_kernel<H, DECODE, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, kScoreThreads, smem, st>>>(*tq, *tk, a);
+  if (Cfg<H, DECODE, SPLIT>::NPROD == 2 && (a.num_k_stages & 1)) return cudaErrorInvalidValue;
+  kern<<<grid, Cfg<H, DECODE, SPLIT>::THREADS, smem, st>>>(*tq, *tk, a);
   return cudaGetLastError();
 }
 

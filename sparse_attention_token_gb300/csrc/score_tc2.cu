@@ -48,7 +48,7 @@ __host__ __device__ inline Plan2 plan2(int D, int q_fp8, int k_fp8, int nK) {
   p.wbuf = off;  off += 2u * kN2 * 4u;
   p.qsbuf = off; if (q_fp8) off += 2u * kN2 * 4u;
   p.ksbuf = off; if (k_fp8) off += static_cast<uint32_t>(nK) * kBlockM * 4u;
-  p.bars = off;  off += 48u * 8u;
+  p.bars = off;  off += 64u * 8u;
   p.misc = off;  off += 16u;
   p.total = off;
   return p;
@@ -66,6 +66,7 @@ enum {
   bKEmpty = 15 + kMaxKStages,   // [nK] each CTA: MMA commit (+ 8 epilogue warps for FP8 keys)
   bKSFull = 15 + 2 * kMaxKStages  // [nK] each CTA: 32 cp.async arrivals (k scales)
 };
+static_assert(15 + 3 * kMaxKStages <= 64, "barrier slots exceed the bars region");
 
 struct Item2 {
   int row0, pos0, kt0, kt1, b, nrows;
