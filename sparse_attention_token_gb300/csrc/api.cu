@@ -73,6 +73,128 @@ __global__ void prep_items_kernel(const int32_t* cu_q_lens, const int32_t* seq_l
   }
 }
 
+// Exclusive prefix sum of one int per thread over the whole block (blockDim a multiple
+// of 32, at most 1024); *total gets the block's sum.  Every thread must call it.
+__device__ int block_scan_excl(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int before = warp > 0 ? warp_sums[warp - 1] : 0;
+  *total = warp_sums[nw - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+constexpr int kPrepThreads = 1024;
+
+// Balanced work lists for launches that split long key ranges (few query blocks, e.g.
+// decode): the query blocks' key tiles, laid end to end, are cut into one equal share
+// (+-1 tile) per CTA of the score grid, and each share into items at query-block
+// boundaries.  CTA c's items go to items[c * per_cta ...] and their number to
+// cta_counts[c].  One block of kPrepThreads; dynamic shared memory holds q_max query
+// blocks (16 bytes each) and q_max + 1 prefix sums.
+__global__ void __launch_bounds__(kPrepThreads) prep_balanced_kernel(
+    const int32_t* cu_q_lens, const int32_t* seq_lens, int B, int NQ, int G, int per_cta, int q_max,
+    int max_seq_len, int max_pages_per_seq, int page_size, int tile_keys, WorkItem* items, int* cta_counts,
+    unsigned* status) {
+  extern __shared__ int4 blk[];  // row0, pos0, b | nrows << 24, key tiles
+  int* pre = reinterpret_cast<int*>(blk + q_max);
+  __shared__ int warp_sums[32];
+  __shared__ int s_over;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_over = 0;
+  __syncthreads();
+  int nq = 0;
+  for (int b0 = 0; b0 < B; b0 += blockDim.x) {
+    const int b = b0 + tid;
+    int nb = 0, cu0 = 0, q_len = 0, L = 0;
+    if (b < B) {
+      cu0 = cu_q_lens[b];
+      q_len = cu_q_lens[b + 1] - cu0;
+      L = seq_lens[b];
+      if (q_len > 0) {
+        if (L > max_seq_len || q_len > L || cu0 < 0 ||
+            static_cast<long long>(L) > static_cast<long long>(max_pages_per_seq) * page_size)
+          atomicOr(status, kStatusUncovered);
+        else
+          nb = (q_len + NQ - 1) / NQ;
+      }
+    }
+    int tot;
+    const int off = nq + block_scan_excl(nb, warp_sums, &tot);
+    for (int j = 0; j < nb; ++j) {
+      const int q = off + j;
+      if (q >= q_max) {
+        s_over = 1;
+        break;
+      }
+      const int row0 = cu0 + j * NQ, nrows = min(NQ, cu0 + q_len - row0);
+      const int pos0 = L - q_len + j * NQ;
+      blk[q] = make_int4(row0, pos0, b | (nrows << 24), (pos0 + nrows - 1 + tile_keys) / tile_keys);
+    }
+    nq += tot;
+  }
+  __syncthreads();
+  if (s_over) {
+    for (int c = tid; c < G; c += blockDim.x) cta_counts[c] = 0;
+    if (tid == 0) atomicOr(status, kStatusUncovered);
+    return;
+  }
+  int carry = 0;
+  for (int q0 = 0; q0 < nq; q0 += blockDim.x) {
+    const int q = q0 + tid;
+    int tot;
+    const int off = carry + block_scan_excl(q < nq ? blk[q].w : 0, warp_sums, &tot);
+    if (q < nq) pre[q] = off;
+    carry += tot;
+  }
+  if (tid == 0) pre[nq] = carry;
+  __syncthreads();
+  const long long W = carry;
+  for (int c = tid; c < G; c += blockDim.x) {
+    const int lo = static_cast<int>(W * c / G), hi = static_cast<int>(W * (c + 1) / G);
+    int n = 0;
+    if (lo < hi) {
+      int l = 0, r = nq - 1;  // first block whose tiles reach past lo
+      while (l < r) {
+        const int m = (l + r) >> 1;
+        if (pre[m + 1] > lo) r = m;
+        else l = m + 1;
+      }
+      for (int j = l; j < nq && pre[j] < hi; ++j) {
+        if (n >= per_cta) {
+          atomicOr(status, kStatusUncovered);
+          break;
+        }
+        const int4 q = blk[j];
+        WorkItem w;
+        w.row0 = q.x;
+        w.pos0 = q.y;
+        w.kt = (max(lo, pre[j]) - pre[j]) | ((min(hi, pre[j + 1]) - pre[j]) << 16);
+        w.bn = q.z;
+        items[static_cast<long long>(c) * per_cta + n++] = w;
+      }
+    }
+    cta_counts[c] = n;
+  }
+}
+
 // ---------------------------------------------------------------- helpers
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -179,7 +301,9 @@ dsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR
 
 struct PagedPlan {
   bool decode, pair, split;
+  bool balanced;  // one chunk of split key ranges: per-CTA balanced lists (prep_balanced_kernel)
   int NQ, N, KC, R, n_chunks, cap, tile_keys;
+  int G, per_cta, q_max;
   long long ld;
   size_t off_counts, off_items, off_scores, off_q8, off_w8, total;
 };
@@ -224,12 +348,17 @@ dsa_status plan_paged(const dsa_indexer_args* a, PagedPlan* p) {
   p->KC = qb_per_chunk < 2LL * ns ? (p->pair ? 8 : 16) : 0;
   const long long kt_max = (a->max_seq_len + p->tile_keys - 1) / p->tile_keys;
   const long long per_qb = p->KC > 0 ? (kt_max + p->KC - 1) / p->KC : 1;
-  const long long cap = qb_per_chunk * std::max<long long>(per_qb, 1);
+  long long cap = qb_per_chunk * std::max<long long>(per_qb, 1);
+  p->balanced = p->KC > 0 && !p->pair && p->n_chunks == 1;
+  p->G = ns;
+  p->q_max = static_cast<int>(qb_per_chunk);
+  p->per_cta = p->q_max + 1;  // a CTA's share meets at most every query block
+  if (p->balanced) cap = static_cast<long long>(p->G) * p->per_cta;
   if (cap > INT_MAX / 2) return DSA_ERR_UNSUPPORTED;
   p->cap = static_cast<int>(cap);
   size_t off = 0;
   p->off_counts = off;
-  off += ((static_cast<size_t>(p->n_chunks) * 4 + 255) / 256) * 256;
+  off += ((static_cast<size_t>(std::max(p->n_chunks, p->balanced ? p->G : 0)) * 4 + 255) / 256) * 256;
   p->off_items = off;
   off += ((static_cast<size_t>(p->n_chunks) * p->cap * sizeof(WorkItem) + 255) / 256) * 256;
   p->off_scores = off;
@@ -303,11 +432,20 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
   if (!make_map_paged(&tk, a->k_cache, s.k_fp8 != 0, a->D, a->page_size, std::max(a->num_pages, 1)))
     return DSA_ERR_CUDA;
 
-  cudaError_t e = cudaMemsetAsync(counts, 0, static_cast<size_t>(p.n_chunks) * 4, st);
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
-  prep_items_kernel<<<a->B, 128, 0, st>>>(a->cu_q_lens, a->seq_lens, p.NQ, p.KC, p.R, p.cap, p.n_chunks,
-                                          a->max_seq_len, a->max_pages_per_seq, a->page_size, p.tile_keys, items,
-                                          counts, status);
+  cudaError_t e;
+  if (p.balanced) {
+    const size_t prep_smem = static_cast<size_t>(p.q_max) * 16 + (static_cast<size_t>(p.q_max) + 1) * 4;
+    prep_balanced_kernel<<<1, kPrepThreads, prep_smem, st>>>(a->cu_q_lens, a->seq_lens, a->B, p.NQ, p.G, p.per_cta,
+                                                             p.q_max, a->max_seq_len, a->max_pages_per_seq,
+                                                             a->page_size, p.tile_keys, items, counts, status);
+    s.cta_counts = counts;
+    s.per_cta = p.per_cta;
+  } else {
+    if ((e = cudaMemsetAsync(counts, 0, static_cast<size_t>(p.n_chunks) * 4, st)) != cudaSuccess) return DSA_ERR_CUDA;
+    prep_items_kernel<<<a->B, 128, 0, st>>>(a->cu_q_lens, a->seq_lens, p.NQ, p.KC, p.R, p.cap, p.n_chunks,
+                                            a->max_seq_len, a->max_pages_per_seq, a->page_size, p.tile_keys, items,
+                                            counts, status);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return DSA_ERR_CUDA;
   const int ns = std::max(num_sms(), 1);
   const size_t smem = p.pair ? score_pair_launch_smem(s) : score_launch_smem(s);
@@ -317,7 +455,7 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
     s.items_cap = p.cap;
     s.row_base = c * p.R;
     e = p.pair ? launch_score_pair(s, &tq, &tk, std::max(2, ns & ~1), smem, st)
-               : launch_score(s, &tq, &tk, ns, smem, st);
+               : launch_score(s, &tq, &tk, p.balanced ? p.G : ns, smem, st);
     if (e != cudaSuccess) return DSA_ERR_CUDA;
     TopkArgs t{};
     t.scores = scores;

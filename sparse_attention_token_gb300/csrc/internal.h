@@ -47,6 +47,10 @@ struct ScoreArgs {
   const WorkItem* items;
   const int* n_items;
   int items_cap;      // capacity of the items segment (clamps *n_items)
+  // balanced lists (per_cta > 0): CTA c runs items[c * per_cta + i], i < cta_counts[c],
+  // instead of the strided walk over n_items
+  const int* cta_counts;
+  int per_cta;
   int row_base;       // global query row stored in scores row 0
   int total_rows;     // rows of q / w (bounds for cp.async of w and q_scale)
   // common

@@ -73,8 +73,16 @@ struct ItemInfo {
 template <int NQ>
 __device__ __forceinline__ bool fetch_item(const ScoreArgs& a, int n_items, int it, ItemInfo& I) {
   const long long G = gridDim.x, c = blockIdx.x;
-  const long long idx = static_cast<long long>(it) * G + ((it & 1) ? (G - 1 - c) : c);
-  if (idx >= n_items) return false;
+  long long idx;
+  if (a.per_cta > 0) {
+    // balanced list: this CTA's own items, in order
+    if (it >= min(__ldg(a.cta_counts + c), a.per_cta)) return false;
+    idx = c * a.per_cta + it;
+  } else {
+    // strided walk, alternating direction so CTAs share the tail of the list
+    idx = static_cast<long long>(it) * G + ((it & 1) ? (G - 1 - c) : c);
+    if (idx >= n_items) return false;
+  }
   if (!a.paged) {
     // query blocks in decreasing order of causal work
     const int qb = a.n_dense_items - 1 - static_cast<int>(idx);

@@ -215,6 +215,31 @@ def test_paged_decode_heads(H):
     assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("H,k_dtype", [(16, "bf16"), (64, "bf16"), (32, "fp8_e4m3")])
+def test_paged_decode_balanced_lists(H, k_dtype):
+    # decode-shaped batches (total_q <= B) run on balanced per-CTA work lists: each CTA's
+    # equal share of key tiles crosses query blocks and sequences; sequences without a
+    # query, several queries per sequence (one block of NQ, or split e4m3 rows per query)
+    lens = [(i * 997) % 4999 + 1 for i in range(45)] + [1, 2, 127, 128, 129]
+    qlens = [min([1, 0, 2, 1, 0, 1][i % 6], L) for i, L in enumerate(lens)]
+    assert sum(qlens) <= len(lens)
+    pc = workloads.paged_case(lens, qlens, H, 128, 300, page_size=32, integer=True, seed=70 + H,
+                              q_dtype="bf16", k_dtype=k_dtype)
+    for order in (0, 1):
+        got = run_paged(pc, order=order)
+        ref, _, _ = oracle.paged(pc, order=order)
+        assert np.array_equal(got, ref)
+
+
+def test_paged_decode_balanced_many_short():
+    # 120 short sequences (1..300 keys): most CTAs' shares are one or two tiles
+    lens = [(i * 37) % 300 + 1 for i in range(120)]
+    pc = workloads.paged_case(lens, [1] * len(lens), 64, 128, 64, page_size=16, integer=True, seed=77)
+    got = run_paged(pc)
+    ref, _, _ = oracle.paged(pc)
+    assert np.array_equal(got, ref)
+
+
 def test_paged_varlen_prefill_integer_exact():
     lens, qlens = [900, 40, 1500, 300], [300, 40, 17, 1]
     pc = workloads.paged_case(lens, qlens, 64, 128, 128, page_size=64, integer=True, seed=11)
