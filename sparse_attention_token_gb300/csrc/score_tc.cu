@@ -15,8 +15,8 @@
 //   warp 0      TMA producer: q tile (N x D) per item into a 2-deep ring, key tiles
 //               (128 x D, dense or gathered page by page through block_tables) into
 //               an nK-deep ring, per-item w / q_scale by cp.async, per-tile k_scale by
-//               cp.async (dense keys) or a bulk copy per page (paged prefill); decode
-//               epilogue threads read their paged key scales from global memory.
+//               cp.async (dense keys and decode tiles, 16 bytes per lane) or a bulk
+//               copy per page (paged prefill).
 //   warp 10     decode only: a second key producer.  Warp 0 takes the even key tiles,
 //               warp 10 the odd ones (each owns alternate stages of an even ring), so
 //               the address work and TMA issue of one overlap the other's.
@@ -228,8 +228,18 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
         const bool valid = needed && pg >= 0 && pg < a.num_pages;
         if (needed && !valid && at == 0) atomicOr(a.status, kStatusBadPage);
         const unsigned vmask = __ballot_sync(0xffffffffu, valid && at == 0);
-        // e4m3 key scales: decode epilogue threads read their own from global memory;
-        // prefill tiles take them by one bulk copy per page into ksbuf
+        // e4m3 key scales into ksbuf: decode tiles by cp.async, 16 bytes (4 keys of one
+        // page) per lane, so the copy engine only sees the key boxes; prefill tiles by one
+        // bulk copy per page
+        if (DECODE && a.k_fp8) {
+          const int js = (4 * lane) / PS;  // page of this lane's 4 keys within the tile
+          const int pgs = __shfl_sync(0xffffffffu, pg_win, (lp0 - win0 + js) & 31);
+          const bool vs = static_cast<long long>(kt) * kBlockM + 4 * lane <= pos_last && pgs >= 0 &&
+                          pgs < a.num_pages;
+          const float* src = vs ? a.k_scale + static_cast<long long>(pgs) * PS + (4 * lane - js * PS) : a.k_scale;
+          ptx::cp_async_16(ksbuf + s * kBlockM + 4 * lane, src, vs ? 16u : 0u);
+          ptx::cp_async_mbar_arrive_noinc(full);
+        }
         const bool ks_bulk = a.k_fp8 && !DECODE;
         if (lane == 0) {
           const uint32_t per_page = page_bytes + (ks_bulk ? static_cast<uint32_t>(PS) * 4u : 0u);
@@ -379,24 +389,17 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
       const int acc = nt & 1;
       const bool mine = DECODE ? (acc == half) : true;
       if (mine) {
-        // paged e4m3 keys: this thread's key scale straight from global memory (page
-        // table, then the page's scale row), issued before the accumulator wait so the
-        // two dependent loads overlap it; dense e4m3 keys: the staged copy in ksbuf
-        float ks_g = 1.f;
-        const bool ks_smem = a.k_fp8 && !(DECODE && a.paged);
-        if (a.k_fp8 && !ks_smem) {
-          const long long key = static_cast<long long>(kt) * kBlockM + m;
-          const int lp = static_cast<int>(key / a.page_size);
-          const int pg = (lp < a.max_pages_per_seq && key <= I.pos0 + I.nrows - 1)
-                             ? __ldg(a.block_tables + static_cast<long long>(I.b) * a.max_pages_per_seq + lp)
-                             : -1;
-          ks_g = (pg >= 0 && pg < a.num_pages)
-                     ? __ldg(a.k_scale + static_cast<long long>(pg) * a.page_size + (key - static_cast<long long>(lp) * a.page_size))
-                     : 0.f;
-        }
-        if (ks_smem && !warp_wait(&bars[kBarKFull + sk], (nk / nK) & 1, abort, a.status)) {
-          ok = false;
-          break;
+        // e4m3 keys: take this key's scale and release the stage's scale slot before the
+        // accumulator wait, so the ring turns over as soon as the MMA is done with it
+        float ks = 1.f;
+        if (a.k_fp8) {
+          if (!warp_wait(&bars[kBarKFull + sk], (nk / nK) & 1, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          ks = ksbuf[sk * kBlockM + m];
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&bars[kBarKEmpty + sk]);
         }
         if (!warp_wait(&bars[kBarTFull + acc], (nt >> 1) & 1, abort, a.status)) {
           ok = false;
@@ -485,12 +488,6 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&bars[kBarTEmpty + acc]);
-        float ks = ks_g;
-        if (ks_smem) {
-          ks = ksbuf[sk * kBlockM + m];
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&bars[kBarKEmpty + sk]);
-        }
         const int s = kt * kBlockM + m;
         const bool key_ok = a.paged || s < a.S;
 #pragma unroll
@@ -539,10 +536,11 @@ __global__ void __launch_bounds__(Cfg<H, DECODE, SPLIT>::THREADS, 1)
     }
     ptx::mbar_init(&bars[kBarDone], 1);
     for (int s = 0; s < a.num_k_stages; ++s) {
-      // dense e4m3 key scales come by cp.async (32 lane arrivals); paged ones by bulk copy
-      ptx::mbar_init(&bars[kBarKFull + s], 1 + ((a.k_fp8 && !a.paged) ? 32 : 0));
+      // e4m3 key scales of dense and decode tiles come by cp.async (32 lane arrivals);
+      // those of paged prefill tiles by bulk copy
+      ptx::mbar_init(&bars[kBarKFull + s], 1 + ((a.k_fp8 && (!a.paged || DECODE)) ? 32 : 0));
       // the epilogue also releases a stage when it reads that stage's key scales from ksbuf
-      ptx::mbar_init(&bars[kBarKEmpty + s], 1 + ((a.k_fp8 && !(DECODE && a.paged)) ? C::EPI_T_ARRIVALS : 0));
+      ptx::mbar_init(&bars[kBarKEmpty + s], 1 + (a.k_fp8 ? C::EPI_T_ARRIVALS : 0));
     }
     *abort = 0;
     ptx::fence_mbar_init();
