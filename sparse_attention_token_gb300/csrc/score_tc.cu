@@ -15,8 +15,7 @@
 //   warp 0      TMA producer: q tile (N x D) per item into a 2-deep ring, key tiles
 //               (128 x D, dense or gathered page by page through block_tables) into
 //               an nK-deep ring, per-item w / q_scale by cp.async, per-tile k_scale by
-//               cp.async (dense keys and decode tiles, 16 bytes per lane) or a bulk
-//               copy per page (paged prefill).
+//               cp.async (dense keys) or a bulk copy per page (paged keys).
 //   warp 10     decode only: a second key producer.  Warp 0 takes the even key tiles,
 //               warp 10 the odd ones (each owns alternate stages of an even ring), so
 //               the address work and TMA issue of one overlap the other's.
@@ -228,19 +227,9 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
         const bool valid = needed && pg >= 0 && pg < a.num_pages;
         if (needed && !valid && at == 0) atomicOr(a.status, kStatusBadPage);
         const unsigned vmask = __ballot_sync(0xffffffffu, valid && at == 0);
-        // e4m3 key scales into ksbuf: decode tiles by cp.async, 16 bytes (4 keys of one
-        // page) per lane, so the copy engine only sees the key boxes; prefill tiles by one
-        // bulk copy per page
-        if (DECODE && a.k_fp8) {
-          const int js = (4 * lane) / PS;  // page of this lane's 4 keys within the tile
-          const int pgs = __shfl_sync(0xffffffffu, pg_win, (lp0 - win0 + js) & 31);
-          const bool vs = static_cast<long long>(kt) * kBlockM + 4 * lane <= pos_last && pgs >= 0 &&
-                          pgs < a.num_pages;
-          const float* src = vs ? a.k_scale + static_cast<long long>(pgs) * PS + (4 * lane - js * PS) : a.k_scale;
-          ptx::cp_async_16(ksbuf + s * kBlockM + 4 * lane, src, vs ? 16u : 0u);
-          ptx::cp_async_mbar_arrive_noinc(full);
-        }
-        const bool ks_bulk = a.k_fp8 && !DECODE;
+        // e4m3 key scales into ksbuf: one bulk copy of the page's scale row per page, on
+        // the same barrier as the page's keys
+        const bool ks_bulk = a.k_fp8;
         if (lane == 0) {
           const uint32_t per_page = page_bytes + (ks_bulk ? static_cast<uint32_t>(PS) * 4u : 0u);
           ptx::mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(vmask)) * per_page);
@@ -536,9 +525,9 @@ __global__ void __launch_bounds__(Cfg<H, DECODE, SPLIT>::THREADS, 1)
     }
     ptx::mbar_init(&bars[kBarDone], 1);
     for (int s = 0; s < a.num_k_stages; ++s) {
-      // e4m3 key scales of dense and decode tiles come by cp.async (32 lane arrivals);
-      // those of paged prefill tiles by bulk copy
-      ptx::mbar_init(&bars[kBarKFull + s], 1 + ((a.k_fp8 && (!a.paged || DECODE)) ? 32 : 0));
+      // e4m3 key scales of dense tiles come by cp.async (32 lane arrivals), those of
+      // paged tiles by one bulk copy per page
+      ptx::mbar_init(&bars[kBarKFull + s], 1 + ((a.k_fp8 && !a.paged) ? 32 : 0));
       // the epilogue also releases a stage when it reads that stage's key scales from ksbuf
       ptx::mbar_init(&bars[kBarKEmpty + s], 1 + (a.k_fp8 ? C::EPI_T_ARRIVALS : 0));
     }
