@@ -301,7 +301,9 @@ def test_mixed_decode_pages_orders_padding(page_size, order):
 
 
 def test_mixed_decode_gaussian_tolerance():
-    # bf16 x e4m3 products are exact in fp32: only the accumulation order differs
+    # each bf16 query row is split into e4m3 hi + lo rows: exact for elements within ~2^9
+    # of the row's largest, else off by at most 2^-17 of it; the products are exact and
+    # the fp32 accumulation order differs: far inside the bf16 bound
     lens = [4096, 5000, 300, 1, 7777]
     pc = workloads.paged_case(lens, [1] * len(lens), 64, 128, 2048, page_size=64, q_dtype="bf16",
                               k_dtype="fp8_e4m3", w_std=1 / 8, seed=45)
