@@ -411,3 +411,96 @@ def test_cache_append_rejects_slot_past_the_cache():
     slots[0] = cache.shape[0] * cache.shape[1]
     with pytest.raises(ValueError):
         oracle.cache_append(k_new, slots, cache)
+
+
+# ---------------------------------------------------------------- indexer front-end (oracle/frontend.py)
+
+from oracle import frontend  # noqa: E402
+
+
+def test_frontend_hadamard_is_orthogonal_with_sign_entries():
+    # Sylvester order: H[i, j] = (-1)^popcount(i & j) / sqrt(D); H H^T = I
+    for D in (2, 8, 128):
+        Hm = frontend.hadamard(D)
+        assert np.allclose(Hm @ Hm.T, np.eye(D), atol=1e-12)
+        i, j = np.meshgrid(np.arange(D), np.arange(D), indexing="ij")
+        signs = np.vectorize(lambda a: (-1) ** bin(a).count("1"))(i & j)
+        assert np.array_equal(Hm * np.sqrt(D), signs.astype(np.float64))
+    # the rotation of a basis vector is one column of +-1/sqrt(D); norms are kept
+    e = np.zeros((1, 128)); e[0, 5] = 1.0
+    r = frontend.rotate_activation(e)
+    assert np.allclose(np.abs(r), 1 / np.sqrt(128))
+    x = np.random.default_rng(0).standard_normal((3, 128))
+    assert np.allclose(np.linalg.norm(frontend.rotate_activation(x), axis=1), np.linalg.norm(x, axis=1))
+
+
+def test_frontend_rope_identity_quarter_turn_and_norms():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((2, 3, 16))
+    for inter in (False, True):
+        ones, zeros = np.ones((2, 4)), np.zeros((2, 4))
+        assert np.array_equal(frontend.rope(x, ones, zeros, 8, inter), x)      # angle 0
+        y = frontend.rope(x, zeros, ones, 8, inter)                              # angle 90 degrees
+        if inter:
+            assert np.allclose(y[..., 0:8:2], -x[..., 1:8:2]) and np.allclose(y[..., 1:8:2], x[..., 0:8:2])
+        else:
+            assert np.allclose(y[..., :4], -x[..., 4:8]) and np.allclose(y[..., 4:8], x[..., :4])
+        assert np.array_equal(y[..., 8:], x[..., 8:])                          # values past rope_dim untouched
+        th = rng.uniform(0, 6.3, (2, 4))
+        z = frontend.rope(x, np.cos(th), np.sin(th), 8, inter)
+        assert np.allclose(np.linalg.norm(z, axis=-1), np.linalg.norm(x, axis=-1))
+
+
+def test_frontend_layer_norm_hand_worked():
+    # x = [1, 2, 3, 4]: mean 2.5, biased variance 1.25, eps 0 -> (x - 2.5) / sqrt(1.25)
+    y = frontend.layer_norm(np.array([[1.0, 2.0, 3.0, 4.0]]), np.ones(4), None, 0.0)
+    assert np.allclose(y, [[-1.5 / np.sqrt(1.25), -0.5 / np.sqrt(1.25), 0.5 / np.sqrt(1.25), 1.5 / np.sqrt(1.25)]])
+    y2 = frontend.layer_norm(np.array([[1.0, 2.0, 3.0, 4.0]]), np.array([2.0, 2.0, 2.0, 2.0]), np.full(4, 0.5), 0.0)
+    assert np.allclose(y2, 2 * y + 0.5)
+    x = np.random.default_rng(2).standard_normal((5, 128)) * 3 + 1
+    z = frontend.layer_norm(x, np.ones(128), None, 1e-6)
+    assert np.allclose(z.mean(axis=1), 0, atol=1e-12) and np.allclose(z.var(axis=1), 1, atol=1e-5)
+
+
+def test_frontend_linear_brute_force():
+    rng = np.random.default_rng(3)
+    x, Wm = rng.integers(-3, 4, (3, 5)).astype(np.float64), rng.integers(-3, 4, (4, 5)).astype(np.float64)
+    ref = [[sum(x[t, k] * Wm[n, k] for k in range(5)) for n in range(4)] for t in range(3)]
+    assert np.array_equal(frontend.linear(x, Wm), np.array(ref))
+
+
+def test_frontend_quantize_rows_bound_and_zero_row():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((4, 128))
+    x[2] = 0.0
+    codes, scale = frontend.quantize_rows(x)
+    assert scale[2] == 1.0 and np.all(codes[2] == 0)
+    dq = frontend.dequantize(codes, scale)
+    # e4m3 keeps 3 mantissa bits: error at most half a unit in the last place (2^-4 relative),
+    # and the row's largest magnitude maps to 448 exactly
+    assert np.all(np.abs(dq - x) <= np.abs(x) * 2.0 ** -4 + scale[:, None] * 2.0 ** -10)
+    for r in (0, 1, 3):
+        assert np.isclose(np.abs(dq[r]).max(), np.abs(x[r]).max(), rtol=1e-6)
+
+
+def test_frontend_prepare_composition():
+    # the pipeline's pieces in order: k is a normalised row rotated by RoPE (and Hadamard),
+    # so its norm is the layer norm's (sqrt(D) for a unit weight); w is the plain projection
+    g = torch.Generator().manual_seed(5)
+    T, Dm, R, H, D, r = 3, 64, 32, 2, 128, 64
+    hid = torch.randn((T, Dm), generator=g).to(torch.bfloat16)
+    qa = torch.randn((T, R), generator=g).to(torch.bfloat16)
+    wq = (torch.randn((H * D, R), generator=g) / 8).to(torch.bfloat16)
+    wk = (torch.randn((D, Dm), generator=g) / 8).to(torch.bfloat16)
+    wp = (torch.randn((H, Dm), generator=g) / 8).to(torch.bfloat16)
+    th = torch.rand((T, r // 2), generator=g) * 6
+    for fp8 in (False, True):
+        out = frontend.prepare(hid, qa, torch.cos(th), torch.sin(th), wq, wk, wp, torch.ones(D), None, H=H, D=D,
+                               rope_dim=r, interleaved=False, eps=1e-6, fp8=fp8)
+        assert np.allclose(np.linalg.norm(out["k"], axis=1), np.sqrt(D), rtol=1e-6)
+        assert np.allclose(out["w"], frontend.to_f64(hid) @ frontend.to_f64(wp).T)
+        q0 = (frontend.to_f64(qa) @ frontend.to_f64(wq).T).reshape(T, H, D)
+        assert np.allclose(np.linalg.norm(out["q"], axis=-1), np.linalg.norm(q0, axis=-1))
+        if fp8:
+            assert out["q_codes"].shape == (T, H, D) and out["q_scale"].shape == (T, H)
+            assert out["k_codes"].shape == (T, D) and out["k_scale"].shape == (T,)
