@@ -196,6 +196,66 @@ dsa_status dsa_indexer_cache_append(const void* k_new, int n, int D, const int64
                                     int num_pages, dsa_stream_t stream);
 
 /*
+ * dsa_indexer_prepare -- the indexer front-end: this step's q, k and head weights from
+ * the layer's activations (GLM5 TensorCast adaptation design, "DSA Indexer 融合语义算子":
+ * the op's inputs hidden_states, qa_normed, RoPE cos / sin, wq_b, wk, weights_proj,
+ * k_norm weight, indexer cache, slot_mapping; performance-model buckets 1-5, 9, 10).
+ *
+ *   q  = RoPE(qa_normed @ wq_b^T), one row of D per head          [T, H, D]
+ *   k  = RoPE(layer_norm(hidden @ wk^T) * k_norm_weight + bias)    [T, D]
+ *   w  = hidden @ weights_proj^T                                   [T, H] fp32 -> w_out
+ * e4m3 cache: q and k are then rotated by the Walsh-Hadamard transform (Sylvester order,
+ * times D^-1/2) and quantised per row: scale = amax / 448 (1 for an all-zero row), codes
+ * the e4m3 value nearest to x / scale; q -> q_out (e4m3) and q_scale_out [T, H]; k and
+ * its scale -> the cache slot.  bf16 cache: q -> q_out (bf16), k -> the cache slot (bf16).
+ * The outputs feed dsa_indexer (q, q_scale, w; the cache now holds this step's keys).
+ *
+ * Readings (the page gives no formulas): projection weights are [out, in] row-major
+ * (x @ W^T); k_norm is a layer norm with the biased variance and eps k_norm_eps, times
+ * the weight, plus k_norm_bias when not NULL; RoPE turns pair i of the first rope_dim
+ * values -- (i, i + rope_dim/2), or (2i, 2i+1) when rope_interleaved -- by the angle with
+ * cosine rope_cos[t, i] and sine rope_sin[t, i]: (a, b) -> (a cos - b sin, a sin + b cos).
+ *
+ * All pointers are device memory, 16-byte aligned (slot_mapping 8-byte).  hidden
+ * [T, hidden_dim] and qa_normed [T, q_rank] bf16; wq_b [H*D, q_rank], wk [D, hidden_dim],
+ * weights_proj [H, hidden_dim] bf16; rope_cos / rope_sin [T, rope_dim/2] fp32;
+ * k_norm_weight [D] fp32, k_norm_bias [D] fp32 or NULL.  D = 128; H a power of two up to
+ * 128; rope_dim even, at most D, a multiple of 8 unless interleaved; hidden_dim and
+ * q_rank multiples of 8.  The three projections run as bf16 GEMMs with fp32 results and
+ * fp32 accumulation (cuBLAS, one library handle per device, created on first use); the
+ * rest runs in the library's kernels.  workspace: dsa_indexer_prepare_workspace_size
+ * bytes of device memory (fp32 q and k before the row kernels), not shared with
+ * overlapping work.  Slots past the cache are skipped and reported through
+ * dsa_check_device_status; negative slots are skipped.
+ */
+typedef struct {
+  int T, hidden_dim, q_rank, H, D, rope_dim, rope_interleaved;
+  const void* hidden;
+  const void* qa_normed;
+  const float* rope_cos;
+  const float* rope_sin;
+  const void* wq_b;
+  const void* wk;
+  const void* weights_proj;
+  const float* k_norm_weight;
+  const float* k_norm_bias;
+  float k_norm_eps;
+  int cache_dtype;           /* DSA_BF16 or DSA_FP8_E4M3 */
+  const int64_t* slot_mapping;
+  void* k_cache;             /* [num_pages, page_size, D] */
+  float* k_scale_cache;      /* [num_pages, page_size] (e4m3 cache) */
+  int page_size, num_pages;
+  void* q_out;               /* [T, H, D] bf16 or e4m3 */
+  float* q_scale_out;        /* [T, H] (e4m3 cache) */
+  float* w_out;              /* [T, H] */
+  void* workspace;
+  size_t workspace_bytes;
+} dsa_indexer_prepare_args;
+
+dsa_status dsa_indexer_prepare_workspace_size(const dsa_indexer_prepare_args* args, size_t* bytes);
+dsa_status dsa_indexer_prepare(const dsa_indexer_prepare_args* args, dsa_stream_t stream);
+
+/*
  * dsa_indexer_dense_host -- dsa_indexer_scores + dsa_indexer_topk of one sequence whose
  * inputs and output are in HOST memory, with the transfers overlapped with the kernels.
  * The pages describe the indexer on device tensors; this entry point exists for callers

@@ -63,6 +63,20 @@ class dsa_indexer_args(ctypes.Structure):
     ]
 
 
+class dsa_indexer_prepare_args(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int), ("hidden_dim", ctypes.c_int), ("q_rank", ctypes.c_int), ("H", ctypes.c_int),
+        ("D", ctypes.c_int), ("rope_dim", ctypes.c_int), ("rope_interleaved", ctypes.c_int),
+        ("hidden", ctypes.c_void_p), ("qa_normed", ctypes.c_void_p), ("rope_cos", ctypes.c_void_p),
+        ("rope_sin", ctypes.c_void_p), ("wq_b", ctypes.c_void_p), ("wk", ctypes.c_void_p),
+        ("weights_proj", ctypes.c_void_p), ("k_norm_weight", ctypes.c_void_p), ("k_norm_bias", ctypes.c_void_p),
+        ("k_norm_eps", ctypes.c_float), ("cache_dtype", ctypes.c_int), ("slot_mapping", ctypes.c_void_p),
+        ("k_cache", ctypes.c_void_p), ("k_scale_cache", ctypes.c_void_p), ("page_size", ctypes.c_int),
+        ("num_pages", ctypes.c_int), ("q_out", ctypes.c_void_p), ("q_scale_out", ctypes.c_void_p),
+        ("w_out", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
 _LIB = None
 
 
@@ -94,6 +108,10 @@ def lib():
         L.dsa_indexer_stack.argtypes = [I, P, P, P, P, P]
         L.dsa_check_device_status.restype = I
         L.dsa_check_device_status.argtypes = [P]
+        L.dsa_indexer_prepare_workspace_size.restype = I
+        L.dsa_indexer_prepare_workspace_size.argtypes = [ctypes.POINTER(dsa_indexer_prepare_args), ctypes.POINTER(S)]
+        L.dsa_indexer_prepare.restype = I
+        L.dsa_indexer_prepare.argtypes = [ctypes.POINTER(dsa_indexer_prepare_args), P]
         L.dsa_indexer_cache_append.restype = I
         L.dsa_indexer_cache_append.argtypes = [P, I, I, P, P, I, P, I, I, P]
         L.dsa_indexer_dense_host_workspace_size.restype = I
@@ -315,6 +333,75 @@ def dsa_indexer_cache_append(k_new: torch.Tensor, slot_mapping: torch.Tensor, k_
         _dev(k_new, "k_new", torch.bfloat16), n, D, _dev(slot_mapping, "slot_mapping", torch.int64),
         _dev(k_cache, "k_cache"), _dtype_code(k_cache), _dev(k_scale_cache, "k_scale_cache", torch.float32),
         page_size, num_pages, _stream_ptr(stream)), "dsa_indexer_cache_append")
+
+
+def make_prepare_args(hidden: torch.Tensor, qa_normed: torch.Tensor, rope_cos: Optional[torch.Tensor],
+                      rope_sin: Optional[torch.Tensor], wq_b: torch.Tensor, wk: torch.Tensor,
+                      weights_proj: torch.Tensor, k_norm_weight: torch.Tensor, k_cache: torch.Tensor,
+                      slot_mapping: torch.Tensor, *, H: int, rope_dim: int, rope_interleaved: bool = False,
+                      k_norm_bias: Optional[torch.Tensor] = None, k_norm_eps: float = 1e-6,
+                      k_scale_cache: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """(args, keepalive, (q, q_scale, w)) for dsa_indexer_prepare: allocates the outputs
+    (q [T, H, D] in the cache's element type, q_scale [T, H] for an e4m3 cache, w [T, H])
+    and, unless given, the workspace."""
+    T, hidden_dim = hidden.shape
+    q_rank = qa_normed.shape[1]
+    D = wk.shape[0]
+    fp8 = k_cache.dtype == torch.float8_e4m3fn
+    dev = hidden.device
+    q = torch.empty((T, H, D), dtype=k_cache.dtype, device=dev)
+    q_scale = torch.empty((T, H), dtype=torch.float32, device=dev) if fp8 else None
+    w = torch.empty((T, H), dtype=torch.float32, device=dev)
+    a = dsa_indexer_prepare_args()
+    a.T, a.hidden_dim, a.q_rank, a.H, a.D = T, hidden_dim, q_rank, H, D
+    a.rope_dim, a.rope_interleaved = rope_dim, 1 if rope_interleaved else 0
+    a.hidden = _dev(hidden, "hidden", torch.bfloat16)
+    a.qa_normed = _dev(qa_normed, "qa_normed", torch.bfloat16)
+    a.rope_cos = _dev(rope_cos, "rope_cos", torch.float32)
+    a.rope_sin = _dev(rope_sin, "rope_sin", torch.float32)
+    a.wq_b = _dev(wq_b, "wq_b", torch.bfloat16)
+    a.wk = _dev(wk, "wk", torch.bfloat16)
+    a.weights_proj = _dev(weights_proj, "weights_proj", torch.bfloat16)
+    a.k_norm_weight = _dev(k_norm_weight, "k_norm_weight", torch.float32)
+    a.k_norm_bias = _dev(k_norm_bias, "k_norm_bias", torch.float32)
+    a.k_norm_eps = float(k_norm_eps)
+    a.cache_dtype = _dtype_code(k_cache)
+    a.slot_mapping = _dev(slot_mapping, "slot_mapping", torch.int64)
+    a.k_cache = _dev(k_cache, "k_cache")
+    a.k_scale_cache = _dev(k_scale_cache, "k_scale_cache", torch.float32)
+    a.page_size, a.num_pages = k_cache.shape[1], k_cache.shape[0]
+    a.q_out, a.q_scale_out, a.w_out = q.data_ptr(), _dev(q_scale, "q_scale"), w.data_ptr()
+    if workspace is None:
+        n = ctypes.c_size_t(0)
+        _check(lib().dsa_indexer_prepare_workspace_size(ctypes.byref(a), ctypes.byref(n)),
+               "dsa_indexer_prepare_workspace_size")
+        workspace = torch.empty(max(int(n.value), 1), dtype=torch.uint8, device=dev)
+    a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    keep = [hidden, qa_normed, rope_cos, rope_sin, wq_b, wk, weights_proj, k_norm_weight, k_norm_bias, k_cache,
+            slot_mapping, k_scale_cache, q, q_scale, w, workspace]
+    return a, keep, (q, q_scale, w)
+
+
+def dsa_indexer_prepare(hidden: torch.Tensor, qa_normed: torch.Tensor, rope_cos: Optional[torch.Tensor],
+                        rope_sin: Optional[torch.Tensor], wq_b: torch.Tensor, wk: torch.Tensor,
+                        weights_proj: torch.Tensor, k_norm_weight: torch.Tensor, k_cache: torch.Tensor,
+                        slot_mapping: torch.Tensor, *, H: int, rope_dim: int, rope_interleaved: bool = False,
+                        k_norm_bias: Optional[torch.Tensor] = None, k_norm_eps: float = 1e-6,
+                        k_scale_cache: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                        stream=None):
+    """The indexer front-end through the C ABI: returns (q, q_scale, w) for dsa_indexer
+    and writes this step's keys (and on an e4m3 cache their scales) through slot_mapping."""
+    a, keep, out = make_prepare_args(hidden, qa_normed, rope_cos, rope_sin, wq_b, wk, weights_proj, k_norm_weight,
+                                     k_cache, slot_mapping, H=H, rope_dim=rope_dim, rope_interleaved=rope_interleaved,
+                                     k_norm_bias=k_norm_bias, k_norm_eps=k_norm_eps, k_scale_cache=k_scale_cache,
+                                     workspace=workspace)
+    _check(lib().dsa_indexer_prepare(ctypes.byref(a), _stream_ptr(stream)), "dsa_indexer_prepare")
+    if stream is not None:  # memory freed here must not be reused ahead of that stream's kernels
+        for t in keep:
+            if isinstance(t, torch.Tensor):
+                t.record_stream(stream)
+    del keep
+    return out
 
 
 def indexer_types_to_codes(indexer_types: Sequence) -> list:

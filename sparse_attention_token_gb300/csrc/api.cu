@@ -638,6 +638,77 @@ dsa_status dsa_indexer_cache_append(const void* k_new, int n, int D, const int64
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+struct PrepPlan {
+  size_t off_q, off_k, total;
+};
+
+dsa_status plan_prepare(const dsa_indexer_prepare_args* a, PrepPlan* p) {
+  if (!a) return DSA_ERR_INVALID_ARGUMENT;
+  if (a->T < 0 || a->hidden_dim <= 0 || a->q_rank <= 0 || a->H <= 0 || a->D <= 0 || a->page_size <= 0 ||
+      a->num_pages < 0 || a->rope_dim < 0 || a->rope_dim > a->D || (a->rope_dim & 1) || !(a->k_norm_eps >= 0.f))
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (a->cache_dtype != DSA_BF16 && a->cache_dtype != DSA_FP8_E4M3) return DSA_ERR_INVALID_ARGUMENT;
+  if (a->D != 128 || !supported_h(a->H) || (a->hidden_dim & 7) || (a->q_rank & 7)) return DSA_ERR_UNSUPPORTED;
+  if (!a->rope_interleaved && (a->rope_dim & 7)) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(a->T) * a->H > INT_MAX) return DSA_ERR_UNSUPPORTED;
+  p->off_q = 0;
+  const size_t qb = static_cast<size_t>(a->T) * a->H * a->D * 4;
+  p->off_k = (qb + 255) / 256 * 256;
+  p->total = p->off_k + (static_cast<size_t>(a->T) * a->D * 4 + 255) / 256 * 256;
+  return DSA_OK;
+}
+}  // namespace
+
+dsa_status dsa_indexer_prepare_workspace_size(const dsa_indexer_prepare_args* a, size_t* bytes) {
+  if (!bytes) return DSA_ERR_INVALID_ARGUMENT;
+  PrepPlan p;
+  const dsa_status st = plan_prepare(a, &p);
+  if (st != DSA_OK) return st;
+  *bytes = p.total;
+  return DSA_OK;
+}
+
+dsa_status dsa_indexer_prepare(const dsa_indexer_prepare_args* a, dsa_stream_t stream) {
+  PrepPlan p;
+  dsa_status st = plan_prepare(a, &p);
+  if (st != DSA_OK) return st;
+  if (a->T == 0) return DSA_OK;
+  const bool fp8 = a->cache_dtype == DSA_FP8_E4M3;
+  if (!a->hidden || !a->qa_normed || !a->wq_b || !a->wk || !a->weights_proj || !a->k_norm_weight ||
+      !a->slot_mapping || !a->k_cache || !a->q_out || !a->w_out ||
+      (a->rope_dim > 0 && (!a->rope_cos || !a->rope_sin)) || (fp8 && (!a->k_scale_cache || !a->q_scale_out)))
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(a->hidden) || !aligned16(a->qa_normed) || !aligned16(a->wq_b) || !aligned16(a->wk) ||
+      !aligned16(a->weights_proj) || !aligned16(a->k_norm_weight) || (a->k_norm_bias && !aligned16(a->k_norm_bias)) ||
+      (a->rope_cos && !aligned16(a->rope_cos)) || (a->rope_sin && !aligned16(a->rope_sin)) ||
+      !aligned16(a->k_cache) || (a->k_scale_cache && (reinterpret_cast<uintptr_t>(a->k_scale_cache) & 3u) != 0) ||
+      !aligned16(a->q_out) || (a->q_scale_out && (reinterpret_cast<uintptr_t>(a->q_scale_out) & 3u) != 0) ||
+      !aligned16(a->w_out) || (reinterpret_cast<uintptr_t>(a->slot_mapping) & 7u) != 0)
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (!a->workspace || a->workspace_bytes < p.total || !aligned16(a->workspace)) return DSA_ERR_WORKSPACE;
+  unsigned* status = device_status_ptr();
+  if (!status) return DSA_ERR_CUDA;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+  float* Qf = reinterpret_cast<float*>(ws + p.off_q);
+  float* Kf = reinterpret_cast<float*>(ws + p.off_k);
+  cudaError_t e;
+  if ((e = gemm_bf16_nt(a->qa_normed, a->wq_b, Qf, a->T, a->H * a->D, a->q_rank, s)) != cudaSuccess ||
+      (e = gemm_bf16_nt(a->hidden, a->wk, Kf, a->T, a->D, a->hidden_dim, s)) != cudaSuccess ||
+      (e = gemm_bf16_nt(a->hidden, a->weights_proj, a->w_out, a->T, a->H, a->hidden_dim, s)) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if ((e = launch_frontend_q(Qf, static_cast<long long>(a->T) * a->H, a->H, a->rope_cos, a->rope_sin, a->rope_dim,
+                             a->rope_interleaved != 0, fp8, a->q_out, a->q_scale_out, s)) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if ((e = launch_frontend_k(Kf, a->T, a->rope_cos, a->rope_sin, a->rope_dim, a->rope_interleaved != 0,
+                             a->k_norm_weight, a->k_norm_bias, a->k_norm_eps, fp8, a->slot_mapping, a->k_cache,
+                             a->k_scale_cache, static_cast<long long>(a->num_pages) * a->page_size, status, s)) !=
+      cudaSuccess)
+    return DSA_ERR_CUDA;
+  return DSA_OK;
+}
+
 dsa_status dsa_resolve_indexer_sources(int L, const int32_t* types, int32_t* src) {
   if (L < 0 || (L > 0 && (!types || !src))) return DSA_ERR_INVALID_ARGUMENT;
   int last_full = -1;

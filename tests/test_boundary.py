@@ -230,3 +230,40 @@ def test_cache_append_validation_happens_before_any_cuda_call(dsa):
     assert call(dt=5) == dsa.DSA_ERR_INVALID_ARGUMENT
     assert call(PS=0) == dsa.DSA_ERR_INVALID_ARGUMENT
 
+
+
+def _prepare_args(dsa, **over):
+    a = dsa.dsa_indexer_prepare_args()
+    fake = 1 << 20
+    a.T, a.hidden_dim, a.q_rank, a.H, a.D, a.rope_dim, a.rope_interleaved = 16, 256, 128, 64, 128, 64, 0
+    for f in ("hidden", "qa_normed", "rope_cos", "rope_sin", "wq_b", "wk", "weights_proj", "k_norm_weight",
+              "slot_mapping", "k_cache", "k_scale_cache", "q_out", "q_scale_out", "w_out", "workspace"):
+        setattr(a, f, fake)
+    a.k_norm_eps, a.cache_dtype, a.page_size, a.num_pages, a.workspace_bytes = 1e-6, 1, 64, 4, 1 << 30
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_prepare_workspace_size_and_validation_without_cuda(dsa):
+    import ctypes
+    L = dsa.lib()
+    n = ctypes.c_size_t(0)
+    a = _prepare_args(dsa)
+    assert L.dsa_indexer_prepare_workspace_size(ctypes.byref(a), ctypes.byref(n)) == dsa.DSA_OK
+    # fp32 q [T, H, D] and k [T, D] before the row kernels, each 256-byte rounded
+    assert n.value == 16 * 64 * 128 * 4 + 16 * 128 * 4
+
+    def st(**over):
+        return L.dsa_indexer_prepare(ctypes.byref(_prepare_args(dsa, **over)), None)
+    assert st(T=0) == dsa.DSA_OK                                  # nothing to do, no launch
+    assert st(D=64) == dsa.DSA_ERR_UNSUPPORTED                    # rows of 128 (Hadamard, lane quads)
+    assert st(H=48) == dsa.DSA_ERR_UNSUPPORTED
+    assert st(hidden_dim=100) == dsa.DSA_ERR_UNSUPPORTED          # rows of 16-byte multiples
+    assert st(rope_dim=63) == dsa.DSA_ERR_INVALID_ARGUMENT        # pairs
+    assert st(rope_dim=130) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert st(rope_dim=60) == dsa.DSA_ERR_UNSUPPORTED             # half-split pairs need rope_dim % 8 == 0
+    assert st(cache_dtype=7) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert st(T=-1) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert st(k_norm_eps=-1.0) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert L.dsa_indexer_prepare_workspace_size(None, ctypes.byref(n)) == dsa.DSA_ERR_INVALID_ARGUMENT

@@ -333,3 +333,56 @@ def new_keys(pc: PagedCase, seed: int = 0, integer: bool = False) -> torch.Tenso
     x = gaussian((total_q, pc.D), g) * torch.pow(2.0, torch.randint(-6, 6, (total_q, 1), generator=g).float())
     return x.to(torch.bfloat16)
 
+
+
+@dataclass
+class FrontendCase:
+    """Inputs of the indexer front-end (the fused op's hidden_states, qa_normed, RoPE
+    cos / sin, wq_b, wk, weights_proj, k_norm weight, cache and slot_mapping)."""
+    hidden: torch.Tensor          # [T, hidden_dim] bf16
+    qa_normed: torch.Tensor       # [T, q_rank] bf16
+    rope_cos: torch.Tensor        # [T, rope_dim / 2] fp32
+    rope_sin: torch.Tensor
+    wq_b: torch.Tensor            # [H * D, q_rank] bf16
+    wk: torch.Tensor              # [D, hidden_dim] bf16
+    weights_proj: torch.Tensor    # [H, hidden_dim] bf16
+    k_norm_weight: torch.Tensor   # [D] fp32
+    k_norm_bias: Optional[torch.Tensor]
+    k_cache: torch.Tensor         # [num_pages, page_size, D] bf16 or e4m3 (zeros)
+    k_scale_cache: Optional[torch.Tensor]
+    slot_mapping: torch.Tensor    # [T] int64
+    H: int
+    D: int
+    rope_dim: int
+
+
+def frontend_case(T: int, hidden_dim: int, q_rank: int, H: int, D: int = 128, rope_dim: int = 64, *,
+                  fp8: bool = False, bias: bool = False, page_size: int = 64, num_pages: Optional[int] = None,
+                  pos0: int = 0, seed: int = 0, pad_every: int = 0) -> FrontendCase:
+    """Seeded front-end inputs: activations N(0, 1) in bf16 (qa_normed is the output of a
+    norm, so unit scale), projection weights N(0, 1)/sqrt(in_features) in bf16 (unit-scale
+    outputs), k_norm weight 1 + N(0, 0.1), RoPE tables of positions pos0 .. pos0 + T - 1 with
+    frequencies 10000^(-2i / rope_dim), slots a seeded permutation of the cache's slots
+    (every pad_every-th token padded with -1 when pad_every > 0)."""
+    g = _gen(seed)
+    if num_pages is None:
+        num_pages = (T + page_size - 1) // page_size + 2
+    hidden = torch.randn((T, hidden_dim), generator=g).to(torch.bfloat16)
+    qa = torch.randn((T, q_rank), generator=g).to(torch.bfloat16)
+    wq_b = (torch.randn((H * D, q_rank), generator=g) / math.sqrt(q_rank)).to(torch.bfloat16)
+    wk = (torch.randn((D, hidden_dim), generator=g) / math.sqrt(hidden_dim)).to(torch.bfloat16)
+    wp = (torch.randn((H, hidden_dim), generator=g) / math.sqrt(hidden_dim)).to(torch.bfloat16)
+    knw = (1.0 + 0.1 * torch.randn((D,), generator=g)).to(torch.float32)
+    knb = (0.1 * torch.randn((D,), generator=g)).to(torch.float32) if bias else None
+    half = rope_dim // 2
+    pos = torch.arange(pos0, pos0 + T, dtype=torch.float64)[:, None]
+    freq = 10000.0 ** (-2.0 * torch.arange(half, dtype=torch.float64) / max(rope_dim, 1))
+    ang = pos * freq[None, :]
+    cos, sin = torch.cos(ang).to(torch.float32).contiguous(), torch.sin(ang).to(torch.float32).contiguous()
+    slots = torch.randperm(num_pages * page_size, generator=g)[:T].to(torch.int64)
+    if pad_every > 0:
+        slots[::pad_every] = -1
+    dt = torch.float8_e4m3fn if fp8 else torch.bfloat16
+    cache = torch.zeros((num_pages, page_size, D), dtype=torch.float32).to(dt)
+    scales = torch.zeros((num_pages, page_size), dtype=torch.float32) if fp8 else None
+    return FrontendCase(hidden, qa, cos, sin, wq_b, wk, wp, knw, knb, cache, scales, slots, H, D, rope_dim)
