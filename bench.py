@@ -409,7 +409,38 @@ def _cache_append_fp8(dev, stream, peaks, iters=20):
     return out
 
 
+def _frontend_fp8(dev, stream, peaks, iters=20):
+    """dsa_indexer_prepare on an e4m3 cache: 8192 prefill tokens and 64 decode tokens."""
+    import ctypes
+    import sparse_attention_token_gb300 as dsa
+    import workloads
+    bf16_peak, hbm = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
+    Dm, R, H, D, r = 6144, 2048, 64, 128, 64
+    out = {"workload": f"indexer front-end, e4m3 cache: hidden {Dm}, q_rank {R}, H={H}, D={D}, rope_dim={r} "
+                       "(projection sizes assumed; the pages give none), synthetic N(0,1) activations"}
+    for name, T in (("prefill_8k", 8192), ("decode_64", 64)):
+        c = workloads.frontend_case(T, Dm, R, H, D, rope_dim=r, fp8=True, seed=7)
+        to = lambda t: None if t is None else t.to(dev)
+        a, keep, _ = dsa.make_prepare_args(to(c.hidden), to(c.qa_normed), to(c.rope_cos), to(c.rope_sin), to(c.wq_b),
+                                           to(c.wk), to(c.weights_proj), to(c.k_norm_weight), to(c.k_cache),
+                                           to(c.slot_mapping), H=H, rope_dim=r, k_scale_cache=to(c.k_scale_cache))
+        L = dsa.lib()
+        fn = lambda: L.dsa_indexer_prepare(ctypes.byref(a), stream.cuda_stream)
+        if fn() != 0:
+            raise RuntimeError("dsa_indexer_prepare failed")
+        ms = _time_events(fn, iters, stream)
+        flops = 2.0 * T * (R * H * D + Dm * D + Dm * H)
+        wbytes = 2.0 * (H * D * R + D * Dm + H * Dm)
+        out[name] = {"tokens": T, "ms_per_step": ms, "gemm_tflops": flops / (ms / 1e3) / 1e12,
+                     "tc_frac": flops / (ms / 1e3) / 1e12 / bf16_peak,
+                     "weight_bytes_hbm_frac": wbytes / (ms / 1e3) / 1e9 / hbm}
+        del a, keep, c
+        torch.cuda.empty_cache()
+    return out
+
+
 OTHER_WORKLOADS = {
+    "frontend_fp8": _frontend_fp8,
     "cache_append_fp8": _cache_append_fp8,
     "chunked_prefill_fp8": _chunked_prefill_fp8,
     "decode_b64_fp8_cache": _decode_b64_fp8_cache,
