@@ -15,6 +15,7 @@
 
 #include "dsa_indexer.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dsa {
 
@@ -118,6 +119,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_balanced_kernel(
   __shared__ int warp_sums[32];
   __shared__ int s_over;
   const int tid = threadIdx.x;
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   if (tid == 0) s_over = 0;
   __syncthreads();
   int nq = 0;
@@ -435,9 +438,10 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
   cudaError_t e;
   if (p.balanced) {
     const size_t prep_smem = static_cast<size_t>(p.q_max) * 16 + (static_cast<size_t>(p.q_max) + 1) * 4;
-    prep_balanced_kernel<<<1, kPrepThreads, prep_smem, st>>>(a->cu_q_lens, a->seq_lens, a->B, p.NQ, p.G, p.per_cta,
-                                                             p.q_max, a->max_seq_len, a->max_pages_per_seq,
-                                                             a->page_size, p.tile_keys, items, counts, status);
+    if ((e = launch_pdl(prep_balanced_kernel, dim3(1), dim3(kPrepThreads), prep_smem, st, a->cu_q_lens, a->seq_lens,
+                        a->B, p.NQ, p.G, p.per_cta, p.q_max, a->max_seq_len, a->max_pages_per_seq, a->page_size,
+                        p.tile_keys, items, counts, status)) != cudaSuccess)
+      return DSA_ERR_CUDA;
     s.cta_counts = counts;
     s.per_cta = p.per_cta;
   } else {

@@ -19,6 +19,7 @@
 #include <vector>
 
 #include "dsa_indexer.h"
+#include "internal.h"
 
 namespace {
 
@@ -164,6 +165,9 @@ dsa_status dsa_indexer_dense_host(const void* q_host, int q_dtype, const float* 
   // per chunk: score and select, alternating between the caller's stream and a second
   // compute stream so that one chunk's kernels fill the SMs another chunk's tail leaves
   // idle; then copy the chunk's rows back
+  // plain launches here: a programmatic dependent grid waiting on one compute stream
+  // would hold SM space that the other stream's chunk is meant to fill
+  dsa::PdlOffScope no_pdl;
   for (int j = 0; j < L.n_chunks; ++j) {
     const cudaStream_t cs = (j & 1) ? c.comp : st;
     const dsa_stream_t cs_h = reinterpret_cast<dsa_stream_t>(cs);

@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 namespace dsa {
 
 // Bits of the device status word (library-owned __device__ variable).
@@ -77,6 +79,38 @@ struct TopkArgs {
   int topk_limit, k_out, order;
   int32_t* topk;
 };
+
+// Programmatic dependent launch may be switched off for the calling host thread: the
+// host-memory pipeline runs chunks on two streams, and a dependent grid's CTAs waiting
+// on one stream would hold SM space the other stream's kernels could use.
+inline bool& pdl_off() {
+  static thread_local bool off = false;
+  return off;
+}
+struct PdlOffScope {
+  bool prev;
+  PdlOffScope() : prev(pdl_off()) { pdl_off() = true; }
+  ~PdlOffScope() { pdl_off() = prev; }
+};
+
+// Launch with programmatic stream serialisation: the kernel may be scheduled while the
+// previous kernel on the stream drains, runs its prologue, and waits (grid_dep_wait)
+// before it touches global memory that kernel may write.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl_off() ? 0 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Host launchers (return a cudaError_t).
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,

@@ -160,6 +160,12 @@ __device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t 
 }
 // The mbarrier gets one arrival when all of this thread's earlier cp.async complete
 // (the arrival is part of the barrier's expected count).
+// Programmatic dependent launch: wait until the grid this one depends on has finished
+// and its memory is visible (a no-op when the kernel was launched without the
+// attribute); and let this grid's dependents launch (their CTAs wait in turn).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }

@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dsa {
 namespace {
@@ -42,6 +43,8 @@ __device__ __forceinline__ float2 from_e4m3x2(uint16_t c) {
 __global__ void __launch_bounds__(kSplitWarps * 32) qsplit_kernel(const uint2* __restrict__ q, const float* __restrict__ w,
                                                                   long long rows, int H, uint32_t* __restrict__ q8,
                                                                   float* __restrict__ w8) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int lane = threadIdx.x & 31;
   const long long r = static_cast<long long>(blockIdx.x) * kSplitWarps + (threadIdx.x >> 5);  // (t, h) row
   if (r >= rows) return;
@@ -72,9 +75,9 @@ cudaError_t launch_qsplit(const void* q, const float* w, long long rows, int H, 
                           cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const long long blocks = (rows + kSplitWarps - 1) / kSplitWarps;
-  qsplit_kernel<<<static_cast<unsigned>(blocks), kSplitWarps * 32, 0, st>>>(
-      static_cast<const uint2*>(q), w, rows, H, static_cast<uint32_t*>(q8), w8);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(qsplit_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kSplitWarps * 32), 0, st,
+                                   static_cast<const uint2*>(q), w, rows, H, static_cast<uint32_t*>(q8), w8);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace dsa

@@ -546,6 +546,10 @@ __global__ void __launch_bounds__(Cfg<H, DECODE, SPLIT>::THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // the prologue above overlaps the previous kernel's tail; its outputs (work lists,
+  // split queries, the scores buffer it read) are safe to use from here on
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int n_items = a.paged ? min(*a.n_items, a.items_cap) : a.n_dense_items;
 
   if ((tmem_base & 0xFFFFu) != 0) {
@@ -576,7 +580,8 @@ cudaError_t launch_t(const ScoreArgs& a, const CUtensorMap* tq, const CUtensorMa
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (Cfg<H, DECODE, SPLIT>::NPROD == 2 && (a.num_k_stages & 1)) return cudaErrorInvalidValue;
-  kern<<<grid, Cfg<H, DECODE, SPLIT>::THREADS, smem, st>>>(*tq, *tk, a);
+  e = launch_pdl(kern, dim3(grid), dim3(Cfg<H, DECODE, SPLIT>::THREADS), smem, st, *tq, *tk, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -22,6 +22,7 @@
 #include <type_traits>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dsa {
 
@@ -675,6 +676,8 @@ __device__ void row_topk(const RS& rs, long long n, int keep, bool by_score, int
 
 template <int NB>  // NB > 0: rows up to kWarps * NB * 128 keys held in registers; 0: any length
 __global__ void __launch_bounds__(kThreads, NB == 8 ? 3 : 2) topk_kernel(const TopkArgs a, int cand_cap) {
+  ptx::grid_dep_wait();  // the scores come from the previous kernel on the stream
+  ptx::grid_dep_launch();
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ uint32_t red[2 * kWarps];
   __shared__ uint32_t info[4];
@@ -737,6 +740,8 @@ __device__ void cluster_merge_hist(const TopkSmem& m, uint32_t rank) {
 
 template <int NB, int CL>  // CL CTAs per row, each holding up to kWarps * NB * 128 keys in registers
 __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkArgs a, int cand_cap) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ uint32_t red[2 * kWarps];
   __shared__ uint32_t info[4];
@@ -924,7 +929,8 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kern<<<a.n_rows, kThreads, smem, st>>>(a, cap);
+    e = launch_pdl(kern, dim3(static_cast<unsigned>(a.n_rows)), dim3(kThreads), smem, st, a, cap);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   };
   // rows longer than one CTA's registers hold, but within a cluster's: one cluster per row
@@ -937,13 +943,15 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = csmem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_off() ? 1 : 2;
     e = cudaLaunchKernelEx(&cfg, kern, a, cap);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
