@@ -693,24 +693,37 @@ dsa_status dsa_indexer_prepare(const dsa_indexer_prepare_args* a, dsa_stream_t s
   if (!a->workspace || a->workspace_bytes < p.total || !aligned16(a->workspace)) return DSA_ERR_WORKSPACE;
   unsigned* status = device_status_ptr();
   if (!status) return DSA_ERR_CUDA;
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(a->workspace);
-  float* Qf = reinterpret_cast<float*>(ws + p.off_q);
-  float* Kf = reinterpret_cast<float*>(ws + p.off_k);
-  cudaError_t e;
-  if ((e = gemm_bf16_nt(a->qa_normed, a->wq_b, Qf, a->T, a->H * a->D, a->q_rank, s)) != cudaSuccess ||
-      (e = gemm_bf16_nt(a->hidden, a->wk, Kf, a->T, a->D, a->hidden_dim, s)) != cudaSuccess ||
-      (e = gemm_bf16_nt(a->hidden, a->weights_proj, a->w_out, a->T, a->H, a->hidden_dim, s)) != cudaSuccess)
-    return DSA_ERR_CUDA;
-  if ((e = launch_frontend_q(Qf, static_cast<long long>(a->T) * a->H, a->H, a->rope_cos, a->rope_sin, a->rope_dim,
-                             a->rope_interleaved != 0, fp8, a->q_out, a->q_scale_out, s)) != cudaSuccess)
-    return DSA_ERR_CUDA;
-  if ((e = launch_frontend_k(Kf, a->T, a->rope_cos, a->rope_sin, a->rope_dim, a->rope_interleaved != 0,
-                             a->k_norm_weight, a->k_norm_bias, a->k_norm_eps, fp8, a->slot_mapping, a->k_cache,
-                             a->k_scale_cache, static_cast<long long>(a->num_pages) * a->page_size, status, s)) !=
-      cudaSuccess)
-    return DSA_ERR_CUDA;
-  return DSA_OK;
+  PrepareLaunch L{};
+  L.T = a->T;
+  L.hidden_dim = a->hidden_dim;
+  L.q_rank = a->q_rank;
+  L.H = a->H;
+  L.D = a->D;
+  L.rope_dim = a->rope_dim;
+  L.interleaved = a->rope_interleaved != 0;
+  L.fp8 = fp8;
+  L.hidden = a->hidden;
+  L.qa_normed = a->qa_normed;
+  L.wq_b = a->wq_b;
+  L.wk = a->wk;
+  L.weights_proj = a->weights_proj;
+  L.cosb = a->rope_cos;
+  L.sinb = a->rope_sin;
+  L.ln_w = a->k_norm_weight;
+  L.ln_b = a->k_norm_bias;
+  L.eps = a->k_norm_eps;
+  L.slots = a->slot_mapping;
+  L.cache = a->k_cache;
+  L.scale_cache = a->k_scale_cache;
+  L.n_slots = static_cast<long long>(a->num_pages) * a->page_size;
+  L.q_out = a->q_out;
+  L.q_scale = a->q_scale_out;
+  L.w_out = a->w_out;
+  L.Qf = reinterpret_cast<float*>(ws + p.off_q);
+  L.Kf = reinterpret_cast<float*>(ws + p.off_k);
+  L.status = status;
+  return from_cuda(launch_prepare(L, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dsa_status dsa_resolve_indexer_sources(int L, const int32_t* types, int32_t* src) {

@@ -5,7 +5,8 @@
 // hidden_states, qa_normed, RoPE cos / sin, wq_b, wk, weights_proj, k_norm weight,
 // indexer cache, slot_mapping) and its performance-model buckets 1-5, 9 and 10:
 //   1-3  q = qa_normed @ wq_b^T, k = hidden @ wk^T, w = hidden @ weights_proj^T: plain
-//        bf16 GEMMs with fp32 results (cuBLAS, fp32 accumulation);
+//        bf16 GEMMs with fp32 results (cuBLAS, fp32 accumulation), the three chains on
+//        the caller's stream and two library-owned streams;
 //   4    RoPE on the first rope_dim values of every q head and of k;
 //   5    FP8 cache only: the Walsh-Hadamard rotation (Sylvester order, times D^-1/2) of
 //        q and k, then per-row e4m3 quantisation (scale = amax / 448);
@@ -186,23 +187,38 @@ __global__ void __launch_bounds__(kFrontWarps * 32) frontend_k_kernel(
   }
 }
 
-std::mutex g_blas_mu;
-cublasHandle_t g_blas[64] = {};
+// Per device: three cuBLAS handles (one per stream the front-end uses, so no two
+// concurrent GEMMs share a handle's workspace), two library-owned streams and the
+// fork / join events.  Created on first use; calls on one device are serialised.
+struct FrontCtx {
+  bool ready = false;
+  cublasHandle_t blas[3] = {};
+  cudaStream_t side[2] = {};
+  cudaEvent_t fork = nullptr, join[2] = {};
+};
+std::mutex g_front_mu;
+FrontCtx g_front[64];
 
-}  // namespace
+bool front_ctx_init(FrontCtx& c) {
+  if (c.ready) return true;
+  for (auto& h : c.blas)
+    if (!h && cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) return false;
+  for (auto& st : c.side)
+    if (!st && cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return false;
+  const unsigned f = cudaEventDisableTiming;
+  if (!c.fork && cudaEventCreateWithFlags(&c.fork, f) != cudaSuccess) return false;
+  for (auto& e : c.join)
+    if (!e && cudaEventCreateWithFlags(&e, f) != cudaSuccess) return false;
+  c.ready = true;
+  return true;
+}
 
 // C[M, N] = A[M, K] (bf16, row-major) times W[N, K]^T (bf16, row-major), fp32 result
 // and accumulation.  Row-major C is column-major C^T = W A^T: one GEMM with W
-// transposed.  One library handle per device, created on first use.
-cudaError_t gemm_bf16_nt(const void* A, const void* W, float* C, int M, int N, int K, cudaStream_t st) {
+// transposed.
+cudaError_t gemm_bf16_nt(cublasHandle_t h, const void* A, const void* W, float* C, int M, int N, int K,
+                         cudaStream_t st) {
   if (M <= 0 || N <= 0) return cudaSuccess;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_blas_mu);
-  if (!g_blas[dev] && cublasCreate(&g_blas[dev]) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
-  cublasHandle_t h = g_blas[dev];
   if (cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
   const float alpha = 1.f, beta = 0.f;
   const cublasStatus_t s = cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, N, M, K, &alpha, W, CUDA_R_16BF, K, A,
@@ -211,6 +227,9 @@ cudaError_t gemm_bf16_nt(const void* A, const void* W, float* C, int M, int N, i
   return s == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
 }
 
+}  // namespace
+
+namespace {
 cudaError_t launch_frontend_q(const float* Qf, long long rows, int H, const float* cosb, const float* sinb,
                               int rope_dim, bool interleaved, bool fp8, void* q_out, float* q_scale,
                               cudaStream_t st) {
@@ -231,6 +250,43 @@ cudaError_t launch_frontend_k(const float* Kf, int T, const float* cosb, const f
                                                          ln_b, eps, fp8 ? 1 : 0, slots, cache, scale_cache, n_slots,
                                                          status);
   return cudaGetLastError();
+}
+}  // namespace
+
+// The three chains are independent until the end: q (GEMM, row kernel) on the caller's
+// stream, k (GEMM, row kernel, cache write) and w (GEMM) on two library-owned streams
+// forked from it and joined back, so the small k and w GEMMs overlap the q GEMM.
+cudaError_t launch_prepare(const PrepareLaunch& p, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_front_mu);
+  FrontCtx& c = g_front[dev];
+  if (!front_ctx_init(c)) return cudaErrorUnknown;
+  const bool fp8 = p.fp8;
+  if ((e = cudaEventRecord(c.fork, st)) != cudaSuccess) return e;
+  for (auto s2 : c.side)
+    if ((e = cudaStreamWaitEvent(s2, c.fork, 0)) != cudaSuccess) return e;
+  // k: projection, layer norm, RoPE, (rotation, quantisation), cache write
+  if ((e = gemm_bf16_nt(c.blas[1], p.hidden, p.wk, p.Kf, p.T, p.D, p.hidden_dim, c.side[0])) != cudaSuccess ||
+      (e = launch_frontend_k(p.Kf, p.T, p.cosb, p.sinb, p.rope_dim, p.interleaved, p.ln_w, p.ln_b, p.eps, fp8,
+                             p.slots, p.cache, p.scale_cache, p.n_slots, p.status, c.side[0])) != cudaSuccess ||
+      (e = cudaEventRecord(c.join[0], c.side[0])) != cudaSuccess)
+    return e;
+  // w: the head-weight projection straight into the output
+  if ((e = gemm_bf16_nt(c.blas[2], p.hidden, p.weights_proj, p.w_out, p.T, p.H, p.hidden_dim, c.side[1])) !=
+          cudaSuccess ||
+      (e = cudaEventRecord(c.join[1], c.side[1])) != cudaSuccess)
+    return e;
+  // q: projection, RoPE, (rotation, quantisation)
+  if ((e = gemm_bf16_nt(c.blas[0], p.qa_normed, p.wq_b, p.Qf, p.T, p.H * p.D, p.q_rank, st)) != cudaSuccess ||
+      (e = launch_frontend_q(p.Qf, static_cast<long long>(p.T) * p.H, p.H, p.cosb, p.sinb, p.rope_dim,
+                             p.interleaved, fp8, p.q_out, p.q_scale, st)) != cudaSuccess)
+    return e;
+  for (auto j : c.join)
+    if ((e = cudaStreamWaitEvent(st, j, 0)) != cudaSuccess) return e;
+  return cudaSuccess;
 }
 
 }  // namespace dsa

@@ -126,16 +126,23 @@ unsigned* device_status_ptr();  // address of the status word on the current dev
 // e4m3 quantisation with its scale); slots >= n_slots set kStatusBadPage.
 cudaError_t launch_cache_append(const void* k_new, int n, int D, const int64_t* slots, void* cache, bool fp8,
                                 float* scale_cache, long long n_slots, unsigned* status, cudaStream_t st);
-// Indexer front-end (frontend.cu): C[M, N] = A[M, K] W[N, K]^T in bf16 with fp32 results
-// (cuBLAS), and the q / k row kernels (RoPE, layer norm, Hadamard, quantisation).
-cudaError_t gemm_bf16_nt(const void* A, const void* W, float* C, int M, int N, int K, cudaStream_t st);
-cudaError_t launch_frontend_q(const float* Qf, long long rows, int H, const float* cosb, const float* sinb,
-                              int rope_dim, bool interleaved, bool fp8, void* q_out, float* q_scale,
-                              cudaStream_t st);
-cudaError_t launch_frontend_k(const float* Kf, int T, const float* cosb, const float* sinb, int rope_dim,
-                              bool interleaved, const float* ln_w, const float* ln_b, float eps, bool fp8,
-                              const int64_t* slots, void* cache, float* scale_cache, long long n_slots,
-                              unsigned* status, cudaStream_t st);
+// Indexer front-end (frontend.cu): projections (cuBLAS bf16 GEMMs, fp32 results) and the
+// q / k row kernels (RoPE, layer norm, Hadamard, quantisation, cache write).
+struct PrepareLaunch {
+  int T, hidden_dim, q_rank, H, D, rope_dim;
+  bool interleaved, fp8;
+  const void *hidden, *qa_normed, *wq_b, *wk, *weights_proj;
+  const float *cosb, *sinb, *ln_w, *ln_b;
+  float eps;
+  const int64_t* slots;
+  void* cache;
+  float* scale_cache;
+  long long n_slots;
+  void* q_out;
+  float *q_scale, *w_out, *Qf, *Kf;
+  unsigned* status;
+};
+cudaError_t launch_prepare(const PrepareLaunch& p, cudaStream_t st);
 // bf16 q rows [rows = total_q * H, 128] -> q8 [total_q, 2H, 128] e4m3 (hi rows, then lo
 // rows, per query) with a power-of-two scale s per row, and w8 = w / s.
 cudaError_t launch_qsplit(const void* q, const float* w, long long rows, int H, void* q8, float* w8,
