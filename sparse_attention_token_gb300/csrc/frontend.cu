@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kFrontWarps * 32) frontend_q_kernel(const floa
   const int lane = threadIdx.x & 31;
   const long long r = static_cast<long long>(blockIdx.x) * kFrontWarps + (threadIdx.x >> 5);
   if (r >= rows) return;
-  const long long t = r / H;
+  const long long t = r >> (31 - __clz(H));  // H is a power of two: no 64-bit division
   const float4 v = reinterpret_cast<const float4*>(Qf + r * 128)[lane];
   float x[4] = {v.x, v.y, v.z, v.w};
   const long long half = rope_dim / 2;

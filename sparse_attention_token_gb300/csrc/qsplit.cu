@@ -48,8 +48,9 @@ __global__ void __launch_bounds__(kSplitWarps * 32) qsplit_kernel(const uint2* _
   const int lane = threadIdx.x & 31;
   const long long r = static_cast<long long>(blockIdx.x) * kSplitWarps + (threadIdx.x >> 5);  // (t, h) row
   if (r >= rows) return;
-  const long long t = r / H;
-  const int h = static_cast<int>(r - t * H);
+  const int lg = 31 - __clz(H);  // H is a power of two: no 64-bit division
+  const long long t = r >> lg;
+  const int h = static_cast<int>(r - (t << lg));
   const uint2 raw = q[r * 32 + lane];  // elements 4 lane .. 4 lane + 3 of the row (D = 128)
   const float x0 = __uint_as_float(raw.x << 16), x1 = __uint_as_float(raw.x & 0xFFFF0000u);
   const float x2 = __uint_as_float(raw.y << 16), x3 = __uint_as_float(raw.y & 0xFFFF0000u);
