@@ -935,7 +935,11 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
   };
   // rows longer than one CTA's registers hold, but within a cluster's: one cluster per row
   auto go_cluster = [&](auto kern, int cl) -> cudaError_t {
-    const size_t csmem = smem + static_cast<size_t>(kHistWords) * 4;  // + merged histogram
+    // long rows: room for the kept keys plus a wide threshold bucket, so the second
+    // histogram level (a cluster-wide pass and merge) is rarely needed
+    const int ccap = max_cap;
+    const size_t csmem = (static_cast<size_t>(kHistWords) + 4 * static_cast<size_t>(ccap)) * 4 +
+                         static_cast<size_t>(kHistWords) * 4;  // + merged histogram
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(csmem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
@@ -952,7 +956,7 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_off() ? 1 : 2;
-    e = cudaLaunchKernelEx(&cfg, kern, a, cap);
+    e = cudaLaunchKernelEx(&cfg, kern, a, ccap);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   };
