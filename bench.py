@@ -229,14 +229,24 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     h2d = q_h.numel() * q_h.element_size() + k_h.numel() * k_h.element_size() + w_h.numel() * w_h.element_size()
     d2h = topk_h.numel() * topk_h.element_size()
 
-    # ---- max over ranks
-    vals = torch.tensor([total_ms, score_ms, topk_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
-    total_ms, score_ms, topk_ms, e2e_ms = vals.tolist()
+    total_ms, score_ms, topk_ms, e2e_ms = max_over_ranks([total_ms, score_ms, topk_ms, e2e_ms], world, dev)
     return dict(total_ms=total_ms, score_ms=score_ms, topk_ms=topk_ms, e2e_ms=e2e_ms, clocks=clocks,
                 h2d=h2d, d2h=d2h, status=status, case=case, e2e_steps=e2e_steps)
 
+
+
+def max_over_ranks(values, world: int, device) -> list:
+    """Each timing's maximum over the ranks (the slowest replica sets the job's time)."""
+    vals = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
+    return vals.tolist()
+
+
+def job_rate(units_per_rank: float, world: int, ms_per_step_max: float) -> float:
+    """Whole-job throughput: the units every rank processed in one step, over the
+    slowest rank's step time (weak scaling: each rank holds the same workload)."""
+    return units_per_rank * world / (ms_per_step_max / 1e3)
 
 
 # ----------------------------------------------------------------------------- other workloads
@@ -571,7 +581,7 @@ def main():
         achieved = FLOPS / score_s / 1e12
         peak = float(peaks["bf16_tflops"])
         ms = r["total_ms"] / args.steps
-        value = PAIRS * world / (ms / 1e3)
+        value = job_rate(PAIRS, world, ms)
         traffic = recorded_traffic()
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -581,14 +591,14 @@ def main():
             "config": {"workload": WORKLOAD, "T": T, "S": S, "H": H, "D": D, "index_topk": TOPK,
                        "parallelism": f"replicas x{world} (independent sequences)",
                        "l2": "no flush: each step reads q (134 MB) and writes + reads 134 MB of scores, > 129 MB L2"},
-            "topk_rows_per_s": T * world / (ms / 1e3),
+            "topk_rows_per_s": job_rate(T, world, ms),
             "tc_frac_step": (FLOPS / (ms / 1e3) / 1e12) / peak,
             "kernel_ms": {"score": r["score_ms"], "topk": r["topk_ms"]},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "score_kernel<64,false> (tcgen05 q.k + fused ReLU/head-sum epilogue)",
                          "peak_kind": f"{peak_kind} bf16 dense burst"},
-            "e2e": {"value": PAIRS * world / (r["e2e_ms"] / 1e3), "unit": UNIT,
+            "e2e": {"value": job_rate(PAIRS, world, r["e2e_ms"]), "unit": UNIT,
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"]},
             "gpu_launches": 2 * args.steps,
             "clocks": r["clocks"],
