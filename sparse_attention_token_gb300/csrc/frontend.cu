@@ -86,11 +86,13 @@ __device__ __forceinline__ void hadamard_row(float (&x)[4], int lane) {
   x[3] = b - d;
 #pragma unroll
   for (int bit = 1; bit < 32; bit <<= 1) {
-    const bool hi = (lane & bit) != 0;
+    // the lane holding the upper value of a pair keeps p - x, the other x + p: one
+    // fma with a +-1 factor (exact: a single rounding of the sum either way)
+    const float sgn = (lane & bit) ? -1.f : 1.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float p = __shfl_xor_sync(0xffffffffu, x[j], bit);
-      x[j] = hi ? p - x[j] : x[j] + p;
+      x[j] = fmaf(sgn, x[j], p);
     }
   }
   const float s = 0.08838834764831845f;  // 128^-1/2 rounded to fp32
