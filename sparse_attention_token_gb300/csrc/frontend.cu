@@ -271,24 +271,25 @@ cudaError_t launch_prepare(const PrepareLaunch& p, cudaStream_t st) {
   for (auto s2 : c.side)
     if ((e = cudaStreamWaitEvent(s2, c.fork, 0)) != cudaSuccess) return e;
   // k: projection, layer norm, RoPE, (rotation, quantisation), cache write
-  if ((e = gemm_bf16_nt(c.blas[1], p.hidden, p.wk, p.Kf, p.T, p.D, p.hidden_dim, c.side[0])) != cudaSuccess ||
-      (e = launch_frontend_k(p.Kf, p.T, p.cosb, p.sinb, p.rope_dim, p.interleaved, p.ln_w, p.ln_b, p.eps, fp8,
-                             p.slots, p.cache, p.scale_cache, p.n_slots, p.status, c.side[0])) != cudaSuccess ||
-      (e = cudaEventRecord(c.join[0], c.side[0])) != cudaSuccess)
-    return e;
+  cudaError_t ek = gemm_bf16_nt(c.blas[1], p.hidden, p.wk, p.Kf, p.T, p.D, p.hidden_dim, c.side[0]);
+  if (ek == cudaSuccess)
+    ek = launch_frontend_k(p.Kf, p.T, p.cosb, p.sinb, p.rope_dim, p.interleaved, p.ln_w, p.ln_b, p.eps, fp8,
+                           p.slots, p.cache, p.scale_cache, p.n_slots, p.status, c.side[0]);
   // w: the head-weight projection straight into the output
-  if ((e = gemm_bf16_nt(c.blas[2], p.hidden, p.weights_proj, p.w_out, p.T, p.H, p.hidden_dim, c.side[1])) !=
-          cudaSuccess ||
-      (e = cudaEventRecord(c.join[1], c.side[1])) != cudaSuccess)
-    return e;
+  const cudaError_t ew = gemm_bf16_nt(c.blas[2], p.hidden, p.weights_proj, p.w_out, p.T, p.H, p.hidden_dim,
+                                      c.side[1]);
   // q: projection, RoPE, (rotation, quantisation)
-  if ((e = gemm_bf16_nt(c.blas[0], p.qa_normed, p.wq_b, p.Qf, p.T, p.H * p.D, p.q_rank, st)) != cudaSuccess ||
-      (e = launch_frontend_q(p.Qf, static_cast<long long>(p.T) * p.H, p.H, p.cosb, p.sinb, p.rope_dim,
-                             p.interleaved, fp8, p.q_out, p.q_scale, st)) != cudaSuccess)
-    return e;
-  for (auto j : c.join)
-    if ((e = cudaStreamWaitEvent(st, j, 0)) != cudaSuccess) return e;
-  return cudaSuccess;
+  cudaError_t eq = gemm_bf16_nt(c.blas[0], p.qa_normed, p.wq_b, p.Qf, p.T, p.H * p.D, p.q_rank, st);
+  if (eq == cudaSuccess)
+    eq = launch_frontend_q(p.Qf, static_cast<long long>(p.T) * p.H, p.H, p.cosb, p.sinb, p.rope_dim,
+                           p.interleaved, fp8, p.q_out, p.q_scale, st);
+  // join the side streams back into the caller's stream whatever happened above, so no
+  // work of this call is left unordered with the caller's later work
+  for (int i = 0; i < 2; ++i) {
+    if ((e = cudaEventRecord(c.join[i], c.side[i])) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(st, c.join[i], 0)) != cudaSuccess) return e;
+  }
+  return eq != cudaSuccess ? eq : (ek != cudaSuccess ? ek : ew);
 }
 
 }  // namespace dsa
