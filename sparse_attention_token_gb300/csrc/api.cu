@@ -16,6 +16,7 @@
 #include "dsa_indexer.h"
 #include "internal.h"
 #include "ptx.cuh"
+#include "qsplit.cuh"
 
 namespace dsa {
 
@@ -114,7 +115,7 @@ constexpr int kPrepThreads = 1024;
 // boundaries.  CTA c's items go to items[c * per_cta ...] and their number to
 // cta_counts[c].  One block of kPrepThreads; dynamic shared memory holds q_max query
 // blocks (16 bytes each) and q_max + 1 prefix sums.
-__global__ void __launch_bounds__(kPrepThreads) prep_balanced_kernel(
+__device__ __forceinline__ void prep_balanced_body(
     const int32_t* cu_q_lens, const int32_t* seq_lens, int B, int NQ, int G, int per_cta, int q_max,
     int max_seq_len, int max_pages_per_seq, int page_size, int tile_keys, WorkItem* items, int* cta_counts,
     unsigned* status) {
@@ -123,8 +124,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_balanced_kernel(
   __shared__ int warp_sums[32];
   __shared__ int s_over;
   const int tid = threadIdx.x;
-  ptx::grid_dep_wait();
-  ptx::grid_dep_launch();
   if (tid == 0) s_over = 0;
   __syncthreads();
   int nq = 0;
@@ -200,6 +199,34 @@ __global__ void __launch_bounds__(kPrepThreads) prep_balanced_kernel(
     }
     cta_counts[c] = n;
   }
+}
+
+__global__ void __launch_bounds__(kPrepThreads) prep_balanced_kernel(
+    const int32_t* cu_q_lens, const int32_t* seq_lens, int B, int NQ, int G, int per_cta, int q_max,
+    int max_seq_len, int max_pages_per_seq, int page_size, int tile_keys, WorkItem* items, int* cta_counts,
+    unsigned* status) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  prep_balanced_body(cu_q_lens, seq_lens, B, NQ, G, per_cta, q_max, max_seq_len, max_pages_per_seq, page_size,
+                     tile_keys, items, cta_counts, status);
+}
+
+// Decode against an e4m3 cache needs both the balanced lists and the split query rows;
+// neither reads the other's output, so one launch runs both: block 0 builds the lists,
+// blocks 1.. split 32 query rows each.
+__global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
+    const int32_t* cu_q_lens, const int32_t* seq_lens, int B, int NQ, int G, int per_cta, int q_max,
+    int max_seq_len, int max_pages_per_seq, int page_size, int tile_keys, WorkItem* items, int* cta_counts,
+    unsigned* status, const uint2* q, const float* w, long long rows, int H, uint32_t* q8, float* w8) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  if (blockIdx.x == 0) {
+    prep_balanced_body(cu_q_lens, seq_lens, B, NQ, G, per_cta, q_max, max_seq_len, max_pages_per_seq, page_size,
+                       tile_keys, items, cta_counts, status);
+    return;
+  }
+  const long long r = static_cast<long long>(blockIdx.x - 1) * (kPrepThreads / 32) + (threadIdx.x >> 5);
+  if (r < rows) split_row(q, w, r, H, q8, w8, threadIdx.x & 31);
 }
 
 // ---------------------------------------------------------------- helpers
@@ -420,12 +447,13 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
   if (s.num_k_stages < 2) return DSA_ERR_UNSUPPORTED;
 
   CUtensorMap tq, tk;
+  void* q8 = ws + p.off_q8;
+  float* w8 = reinterpret_cast<float*>(ws + p.off_w8);
+  const long long split_rows = static_cast<long long>(a->total_q) * a->H;
   if (p.split) {
-    // hi/lo e4m3 rows of every query and the weights divided by the rows' scales
-    void* q8 = ws + p.off_q8;
-    float* w8 = reinterpret_cast<float*>(ws + p.off_w8);
-    if (launch_qsplit(a->q, a->w, static_cast<long long>(a->total_q) * a->H, a->H, q8, w8, st) != cudaSuccess)
-      return DSA_ERR_CUDA;
+    // hi/lo e4m3 rows of every query and the weights divided by the rows' scales (with
+    // balanced lists, in the same launch as the lists, below)
+    if (!p.balanced && launch_qsplit(a->q, a->w, split_rows, a->H, q8, w8, st) != cudaSuccess) return DSA_ERR_CUDA;
     s.q_fp8 = 1;
     s.w = w8;
     s.q_scale = nullptr;
@@ -442,10 +470,18 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
   cudaError_t e;
   if (p.balanced) {
     const size_t prep_smem = static_cast<size_t>(p.q_max) * 16 + (static_cast<size_t>(p.q_max) + 1) * 4;
-    if ((e = launch_pdl(prep_balanced_kernel, dim3(1), dim3(kPrepThreads), prep_smem, st, a->cu_q_lens, a->seq_lens,
-                        a->B, p.NQ, p.G, p.per_cta, p.q_max, a->max_seq_len, a->max_pages_per_seq, a->page_size,
-                        p.tile_keys, items, counts, status)) != cudaSuccess)
-      return DSA_ERR_CUDA;
+    if (p.split) {
+      const long long nb = 1 + (split_rows + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
+      e = launch_pdl(decode_prep_kernel, dim3(static_cast<unsigned>(nb)), dim3(kPrepThreads), prep_smem, st,
+                     a->cu_q_lens, a->seq_lens, a->B, p.NQ, p.G, p.per_cta, p.q_max, a->max_seq_len,
+                     a->max_pages_per_seq, a->page_size, p.tile_keys, items, counts, status,
+                     static_cast<const uint2*>(a->q), a->w, split_rows, a->H, static_cast<uint32_t*>(q8), w8);
+    } else {
+      e = launch_pdl(prep_balanced_kernel, dim3(1), dim3(kPrepThreads), prep_smem, st, a->cu_q_lens, a->seq_lens,
+                     a->B, p.NQ, p.G, p.per_cta, p.q_max, a->max_seq_len, a->max_pages_per_seq, a->page_size,
+                     p.tile_keys, items, counts, status);
+    }
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
     s.cta_counts = counts;
     s.per_cta = p.per_cta;
   } else {
