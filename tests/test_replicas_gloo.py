@@ -37,7 +37,7 @@ def _rank_main(rank: int, world: int, port: int, out):
 
 def test_max_over_ranks_two_gloo_ranks():
     world = 2
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:   # no fork of this (threaded) process
         out = mgr.dict()
         mp.start_processes(_rank_main, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
         res = dict(out)
