@@ -113,7 +113,9 @@ def test_workspace_size_and_paged_validation(dsa):
         with pytest.raises(dsa.DsaError):
             dsa.dsa_indexer_workspace_size(_args(dsa, **bad))
     # bf16 queries with an e4m3 cache: decode shapes only, and the key scales are required
-    assert dsa.dsa_indexer_workspace_size(_args(dsa, q_dtype=0, k_dtype=1, k_scale_cache=1 << 20)) >= n
+    n_split = dsa.dsa_indexer_workspace_size(_args(dsa, q_dtype=0, k_dtype=1, k_scale_cache=1 << 20))
+    # ... plus the split query rows q8 [total_q, 2H, D] e4m3 and their weights w8 [total_q, H]
+    assert n_split - n >= 2 * (2 * 64) * 128 + 2 * 64 * 4
     with pytest.raises(dsa.DsaError):
         dsa.dsa_indexer_workspace_size(_args(dsa, q_dtype=0, k_dtype=1))
     with pytest.raises(dsa.DsaError):
