@@ -504,3 +504,73 @@ def test_frontend_prepare_composition():
         if fp8:
             assert out["q_codes"].shape == (T, H, D) and out["q_scale"].shape == (T, H)
             assert out["k_codes"].shape == (T, D) and out["k_scale"].shape == (T,)
+
+
+# ---------------------------------------------------------------- sparse MLA over top-k (oracle/sparse_mla.py)
+
+from oracle import sparse_mla as smla  # noqa: E402
+
+
+def _smla(c, topk=None, q_nope=None, q_rope=None):
+    return smla.sparse_mla(c.q_nope if q_nope is None else q_nope, c.q_rope if q_rope is None else q_rope,
+                           c.cache_c, c.cache_r, c.block_tables, c.cu_q_lens, c.topk if topk is None else topk,
+                           page_size=c.page_size, scale=c.scale)
+
+
+def _latent_rows(c, b, positions):
+    cc, cr = frontend.to_f64(c.cache_c), frontend.to_f64(c.cache_r)
+    return smla.gather_latent(cc, cr, c.block_tables[b].numpy(), c.page_size, np.asarray(positions))
+
+
+def test_sparse_mla_single_key_returns_its_latent_row():
+    c = workloads.sparse_mla_case([100, 40], [3, 1], 4, 8, kv_rank=32, rope_dim=8, page_size=16, seed=1)
+    tk = torch.full_like(c.topk, -1)
+    tk[:, 3] = torch.tensor([5, 0, 97, 39], dtype=torch.int32)          # one key per token, anywhere in the row
+    out = _smla(c, topk=tk)
+    rows = [(0, 5), (0, 0), (0, 97), (1, 39)]
+    for t, (b, s) in enumerate(rows):
+        lat, _ = _latent_rows(c, b, [s])
+        assert np.allclose(out[t], np.broadcast_to(lat[0], out[t].shape), atol=1e-12)
+
+
+def test_sparse_mla_equal_logits_average_the_selection():
+    c = workloads.sparse_mla_case([64], [2], 3, 10, kv_rank=16, rope_dim=8, page_size=16, seed=2)
+    zq, zr = torch.zeros_like(c.q_nope), torch.zeros_like(c.q_rope)
+    out = _smla(c, q_nope=zq, q_rope=zr)
+    for t in range(2):
+        sel = c.topk[t][c.topk[t] >= 0].numpy()
+        lat, _ = _latent_rows(c, 0, sel)
+        assert np.allclose(out[t], lat.mean(axis=0)[None, :], atol=1e-12)
+
+
+def test_sparse_mla_order_and_padding_do_not_matter():
+    c = workloads.sparse_mla_case([300, 90], [2, 2], 4, 24, kv_rank=32, rope_dim=8, page_size=32, seed=3)
+    base = _smla(c)
+    g = torch.Generator().manual_seed(9)
+    tk = torch.full((c.topk.shape[0], 40), -1, dtype=torch.int32)
+    for t in range(c.topk.shape[0]):
+        sel = c.topk[t][c.topk[t] >= 0]
+        slots = torch.randperm(40, generator=g)[:sel.numel()]
+        tk[t, slots] = sel[torch.randperm(sel.numel(), generator=g)]
+    assert np.allclose(_smla(c, topk=tk), base, atol=1e-12)
+    empty = torch.full_like(c.topk, -1)
+    assert np.array_equal(_smla(c, topk=empty), np.zeros_like(base))
+
+
+def test_sparse_mla_all_causal_keys_equals_dense_attention():
+    # selecting every visible key reduces to dense causal attention: torch's
+    # scaled_dot_product_attention on q = [q_nope, q_rope], k = [c_kv, k_rope], v = c_kv
+    L, ql, H, R, rd, P = 96, 5, 3, 16, 8, 16
+    c = workloads.sparse_mla_case([L], [ql], H, L, kv_rank=R, rope_dim=rd, page_size=P, seed=4)
+    tk = torch.full((ql, L), -1, dtype=torch.int32)
+    for i in range(ql):
+        pos = L - ql + i
+        tk[i, :pos + 1] = torch.arange(pos + 1, dtype=torch.int32)
+    out = _smla(c, topk=tk)
+    lat, rope = _latent_rows(c, 0, np.arange(L))
+    q = torch.cat([c.q_nope.to(torch.float64), c.q_rope.to(torch.float64)], dim=-1).transpose(0, 1)  # [H, ql, R+rd]
+    k = torch.from_numpy(np.concatenate([lat, rope], axis=-1))[None].expand(H, L, R + rd)
+    v = torch.from_numpy(lat)[None].expand(H, L, R)
+    mask = torch.arange(L)[None, :] <= (L - ql + torch.arange(ql))[:, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=c.scale)
+    assert np.allclose(out, ref.transpose(0, 1).numpy(), atol=1e-10)

@@ -386,3 +386,57 @@ def frontend_case(T: int, hidden_dim: int, q_rank: int, H: int, D: int = 128, ro
     cache = torch.zeros((num_pages, page_size, D), dtype=torch.float32).to(dt)
     scales = torch.zeros((num_pages, page_size), dtype=torch.float32) if fp8 else None
     return FrontendCase(hidden, qa, cos, sin, wq_b, wk, wp, knw, knb, cache, scales, slots, H, D, rope_dim)
+
+
+@dataclass
+class SparseMlaCase:
+    """Inputs of sparse MLA over top-k: absorbed queries, a paged latent cache and each
+    query token's selected logical key positions."""
+    q_nope: torch.Tensor        # [total_q, H, kv_rank] bf16
+    q_rope: torch.Tensor        # [total_q, H, rope_dim] bf16
+    cache_c: torch.Tensor       # [num_pages, page_size, kv_rank] bf16
+    cache_r: torch.Tensor       # [num_pages, page_size, rope_dim] bf16
+    block_tables: torch.Tensor  # [B, max_pages] int32
+    cu_q_lens: torch.Tensor     # [B + 1] int32
+    seq_lens: torch.Tensor      # [B] int32
+    topk: torch.Tensor          # [total_q, k] int32, -1 = none
+    page_size: int
+    scale: float
+
+
+def sparse_mla_case(seq_lens, q_lens, H: int, k: int, *, kv_rank: int = 512, rope_dim: int = 64,
+                    page_size: int = 64, seed: int = 0) -> SparseMlaCase:
+    """Seeded sparse-MLA inputs: N(0,1) bf16 queries and latent rows, pages in a seeded
+    permutation, and for query i of a sequence of length L with q_len new tokens (position
+    L - q_len + i) a seeded draw of min(k, position + 1) distinct visible positions in
+    random order, -1 padded to k.  scale = (kv_rank + rope_dim)^-1/2."""
+    g = _gen(seed)
+    seq_lens = [int(x) for x in seq_lens]
+    q_lens = [int(x) for x in q_lens]
+    B = len(seq_lens)
+    pages_per_seq = [(L + page_size - 1) // page_size for L in seq_lens]
+    num_pages = sum(pages_per_seq) + 1
+    perm = torch.randperm(num_pages, generator=g).to(torch.int32)
+    bt = torch.full((B, max(1, max(pages_per_seq))), -1, dtype=torch.int32)
+    cur = 0
+    for b, npg in enumerate(pages_per_seq):
+        bt[b, :npg] = perm[cur:cur + npg]
+        cur += npg
+    total_q = sum(q_lens)
+    cu = [0]
+    for ql in q_lens:
+        cu.append(cu[-1] + ql)
+    q_nope = torch.randn((total_q, H, kv_rank), generator=g).to(torch.bfloat16)
+    q_rope = torch.randn((total_q, H, rope_dim), generator=g).to(torch.bfloat16)
+    cache_c = torch.randn((num_pages, page_size, kv_rank), generator=g).to(torch.bfloat16)
+    cache_r = torch.randn((num_pages, page_size, rope_dim), generator=g).to(torch.bfloat16)
+    topk = torch.full((total_q, k), -1, dtype=torch.int32)
+    for b in range(B):
+        for i in range(q_lens[b]):
+            pos = seq_lens[b] - q_lens[b] + i
+            n = min(k, pos + 1)
+            sel = torch.randperm(pos + 1, generator=g)[:n].to(torch.int32)
+            topk[cu[b] + i, :n] = sel
+    return SparseMlaCase(q_nope, q_rope, cache_c, cache_r, bt, torch.tensor(cu, dtype=torch.int32),
+                         torch.tensor(seq_lens, dtype=torch.int32), topk, page_size,
+                         1.0 / math.sqrt(kv_rank + rope_dim))
