@@ -14,6 +14,12 @@ Contents:
     (GLM5 TensorCast adaptation design, section "GLM-5.2 IndexShare").
   * ``brute``: an exact rational-arithmetic brute force for tiny inputs,
     used to pin the C oracle.
+  * ``e4m3_encode`` / ``cache_append``: the FP8 key-cache write (per-token
+    amax/448 quantisation through slot_mapping).
+  * ``frontend`` (numpy, fp64): the indexer front-end -- projections, k layer
+    norm, RoPE, Hadamard rotation, per-row e4m3 quantisation.
+  * ``sparse_mla`` (numpy, fp64): absorbed latent attention over each token's
+    selected keys (the consumer of the top-k).
 
 Every function in this package is pinned by ``tests/test_oracle_pins.py``
 (hand-worked example, library special cases, invariants, brute force).
