@@ -348,6 +348,22 @@ def make_prepare_args(hidden: torch.Tensor, qa_normed: torch.Tensor, rope_cos: O
     q_rank = qa_normed.shape[1]
     D = wk.shape[0]
     fp8 = k_cache.dtype == torch.float8_e4m3fn
+    # the C ABI sees only pointers and sizes: every tensor's shape is checked here
+    want = {"qa_normed": (qa_normed, (T, q_rank)), "wq_b": (wq_b, (H * D, q_rank)), "wk": (wk, (D, hidden_dim)),
+            "weights_proj": (weights_proj, (H, hidden_dim)), "k_norm_weight": (k_norm_weight, (D,)),
+            "slot_mapping": (slot_mapping, (T,))}
+    if k_norm_bias is not None:
+        want["k_norm_bias"] = (k_norm_bias, (D,))
+    if rope_dim > 0:
+        want["rope_cos"] = (rope_cos, (T, rope_dim // 2))
+        want["rope_sin"] = (rope_sin, (T, rope_dim // 2))
+    if k_cache.dim() != 3 or k_cache.shape[2] != D:
+        raise ValueError(f"k_cache must be [num_pages, page_size, {D}], got {tuple(k_cache.shape)}")
+    if fp8:
+        want["k_scale_cache"] = (k_scale_cache, tuple(k_cache.shape[:2]))
+    for name, (t, shape) in want.items():
+        if t is None or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}, got {None if t is None else tuple(t.shape)}")
     dev = hidden.device
     q = torch.empty((T, H, D), dtype=k_cache.dtype, device=dev)
     q_scale = torch.empty((T, H), dtype=torch.float32, device=dev) if fp8 else None

@@ -269,3 +269,24 @@ def test_prepare_workspace_size_and_validation_without_cuda(dsa):
     assert st(T=-1) == dsa.DSA_ERR_INVALID_ARGUMENT
     assert st(k_norm_eps=-1.0) == dsa.DSA_ERR_INVALID_ARGUMENT
     assert L.dsa_indexer_prepare_workspace_size(None, ctypes.byref(n)) == dsa.DSA_ERR_INVALID_ARGUMENT
+
+
+def test_prepare_binding_checks_shapes_before_anything_else(dsa):
+    import workloads
+    c = workloads.frontend_case(5, 64, 32, 4, rope_dim=16, fp8=True, page_size=16)
+    base = dict(hidden=c.hidden, qa_normed=c.qa_normed, rope_cos=c.rope_cos, rope_sin=c.rope_sin, wq_b=c.wq_b,
+                wk=c.wk, weights_proj=c.weights_proj, k_norm_weight=c.k_norm_weight, k_cache=c.k_cache,
+                slot_mapping=c.slot_mapping)
+
+    def call(**over):
+        kw = dict(base, **over)
+        return dsa.make_prepare_args(kw.pop("hidden"), kw.pop("qa_normed"), kw.pop("rope_cos"), kw.pop("rope_sin"),
+                                     kw.pop("wq_b"), kw.pop("wk"), kw.pop("weights_proj"), kw.pop("k_norm_weight"),
+                                     kw.pop("k_cache"), kw.pop("slot_mapping"), H=4, rope_dim=16,
+                                     k_scale_cache=kw.pop("k_scale_cache", c.k_scale_cache))
+    for bad in [dict(rope_cos=c.rope_cos[:, :4]), dict(wq_b=c.wq_b[:100]), dict(slot_mapping=c.slot_mapping[:3]),
+                dict(k_scale_cache=None), dict(qa_normed=c.qa_normed[:4]), dict(wk=c.wk[:64])]:
+        with pytest.raises(ValueError, match="shape|must be"):
+            call(**bad)
+    with pytest.raises(ValueError, match="CUDA"):   # right shapes: the next check is the device
+        call()
