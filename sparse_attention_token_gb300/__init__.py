@@ -265,6 +265,9 @@ def make_indexer_args(q, w, k_cache, cu_q_lens, seq_lens, block_tables, *, max_s
     """Fill a dsa_indexer_args from tensors (allocating topk / workspace with torch if absent).
 
     Returns (args, keepalive) -- keep the second value alive while the call runs."""
+    if q.dim() != 3 or k_cache.dim() != 3 or seq_lens.dim() != 1 or block_tables.dim() != 2:
+        raise ValueError("q [total_q, H, D], k_cache [num_pages, page_size, D], seq_lens [B] and "
+                         "block_tables [B, max_pages] expected")
     total_q = q.shape[0] if total_q is None else total_q
     H, D = q.shape[1], q.shape[2]
     B = seq_lens.shape[0]
@@ -273,6 +276,16 @@ def make_indexer_args(q, w, k_cache, cu_q_lens, seq_lens, block_tables, *, max_s
         k_out = topk_limit
     if topk is None:
         topk = torch.empty((total_q, k_out), dtype=torch.int32, device=q.device)
+    # the C ABI sees only pointers and sizes: every tensor's shape is checked here
+    want = {"w": (w, (q.shape[0], H)), "q_scale": (q_scale, (q.shape[0], H)),
+            "k_scale_cache": (k_scale_cache, (num_pages, page_size)), "cu_q_lens": (cu_q_lens, (B + 1,)),
+            "block_tables": (block_tables, (B, block_tables.shape[1])), "topk": (topk, (total_q, k_out)),
+            "k_new": (k_new, (total_q, D)), "slot_mapping": (slot_mapping, (total_q,))}
+    for name, (t, shape) in want.items():
+        if t is not None and tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+    if k_cache.shape[2] != D or q.shape[0] < total_q:
+        raise ValueError(f"k_cache rows must have D = {D} values and q at least {total_q} rows")
     a = dsa_indexer_args()
     a.q_dtype, a.k_dtype = _dtype_code(q), _dtype_code(k_cache)
     a.B, a.total_q, a.H, a.D = B, total_q, H, D

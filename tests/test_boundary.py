@@ -290,3 +290,24 @@ def test_prepare_binding_checks_shapes_before_anything_else(dsa):
             call(**bad)
     with pytest.raises(ValueError, match="CUDA"):   # right shapes: the next check is the device
         call()
+
+
+def test_indexer_binding_checks_shapes_before_anything_else(dsa):
+    import torch
+    pc = workloads.paged_case([300, 70], [2, 1], 64, 128, 32, page_size=64, integer=True, seed=3)
+
+    def call(**over):
+        kw = dict(q=pc.q, w=pc.w, k_cache=pc.k_cache, cu_q_lens=pc.cu_q_lens, seq_lens=pc.seq_lens,
+                  block_tables=pc.block_tables)
+        kw.update(over)
+        extra = {k: kw.pop(k) for k in ("q_scale", "k_scale_cache", "topk", "k_new", "slot_mapping") if k in kw}
+        return dsa.make_indexer_args(kw["q"], kw["w"], kw["k_cache"], kw["cu_q_lens"], kw["seq_lens"],
+                                     kw["block_tables"], max_seq_len=pc.max_seq_len, topk_limit=32, **extra)
+    for bad in [dict(w=pc.w[:2]), dict(cu_q_lens=pc.cu_q_lens[:2]), dict(block_tables=pc.block_tables[:1]),
+                dict(topk=torch.empty((3, 16), dtype=torch.int32)), dict(k_cache=pc.k_cache[:, :, :64]),
+                dict(k_new=torch.zeros((3, 64), dtype=torch.bfloat16), slot_mapping=torch.zeros(3, dtype=torch.int64)),
+                dict(q=pc.q[0])]:
+        with pytest.raises(ValueError):
+            call(**bad)
+    with pytest.raises(ValueError, match="CUDA"):   # right shapes: the next check is the device
+        call()
