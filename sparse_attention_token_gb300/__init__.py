@@ -168,6 +168,17 @@ def _stream_ptr(stream) -> Optional[int]:
     return stream.cuda_stream
 
 
+def _expect(checks) -> None:
+    """Raise ValueError unless every (tensor or None, name, shape) matches; a shape entry
+    of None accepts any size in that dimension.  The C ABI sees only pointers and sizes."""
+    for t, name, shape in checks:
+        if t is None:
+            continue
+        ok = t.dim() == len(shape) and all(w is None or t.shape[i] == w for i, w in enumerate(shape))
+        if not ok:
+            raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
 def dsa_indexer_scores(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, *, q_pos0: Optional[int] = None,
                        q_scale: Optional[torch.Tensor] = None, k_scale: Optional[torch.Tensor] = None,
                        scores: Optional[torch.Tensor] = None, ld: Optional[int] = None,
@@ -184,6 +195,10 @@ def dsa_indexer_scores(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, *, q_p
         ld = (S + 3) // 4 * 4
     if scores is None:
         scores = torch.full((T, ld), fill, dtype=torch.float32, device=q.device)
+    _expect([(k, "k", (S, D)), (w, "w", (T, H)), (q_scale, "q_scale", (T, H)), (k_scale, "k_scale", (S,)),
+             (scores, "scores", (T, None))])
+    if scores.shape[1] < S:
+        raise ValueError(f"scores needs at least S = {S} columns, got {scores.shape[1]}")
     _check(lib().dsa_indexer_scores(
         _dev(q, "q"), _dtype_code(q), _dev(q_scale, "q_scale", torch.float32),
         _dev(k, "k"), _dtype_code(k), _dev(k_scale, "k_scale", torch.float32),
@@ -230,6 +245,8 @@ def dsa_indexer_dense_host(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, *,
         k_out = topk_limit
     if topk is None:
         topk = torch.empty((T, k_out), dtype=torch.int32, pin_memory=torch.cuda.is_available())
+    _expect([(k, "k", (S, D)), (w, "w", (T, H)), (q_scale, "q_scale", (T, H)), (k_scale, "k_scale", (S,)),
+             (topk, "topk", (T, k_out))])
     need = dsa_indexer_dense_host_workspace_size(T, S, H, D, _dtype_code(q), k_out, chunk_rows)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
@@ -252,6 +269,9 @@ def dsa_indexer_topk(scores: torch.Tensor, *, T: int, S: int, q_pos0: int, topk_
         k_out = topk_limit
     if topk is None:
         topk = torch.empty((T, k_out), dtype=torch.int32, device=scores.device)
+    _expect([(scores, "scores", (None, None)), (topk, "topk", (T, k_out))])
+    if scores.shape[0] < T or scores.shape[1] < S:
+        raise ValueError(f"scores must hold at least [{T}, {S}], got {tuple(scores.shape)}")
     _check(lib().dsa_indexer_topk(_dev(scores, "scores", torch.float32), int(scores.stride(0)), T, S,
                                   int(q_pos0), int(topk_limit), int(k_out), int(order),
                                   _dev(topk, "topk", torch.int32), _stream_ptr(stream)), "dsa_indexer_topk")
@@ -342,6 +362,8 @@ def dsa_indexer_cache_append(k_new: torch.Tensor, slot_mapping: torch.Tensor, k_
     k_scale_cache [num_pages, page_size]."""
     n, D = k_new.shape
     num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+    _expect([(slot_mapping, "slot_mapping", (n,)), (k_cache, "k_cache", (None, None, D)),
+             (k_scale_cache, "k_scale_cache", (num_pages, page_size))])
     _check(lib().dsa_indexer_cache_append(
         _dev(k_new, "k_new", torch.bfloat16), n, D, _dev(slot_mapping, "slot_mapping", torch.int64),
         _dev(k_cache, "k_cache"), _dtype_code(k_cache), _dev(k_scale_cache, "k_scale_cache", torch.float32),

@@ -311,3 +311,23 @@ def test_indexer_binding_checks_shapes_before_anything_else(dsa):
             call(**bad)
     with pytest.raises(ValueError, match="CUDA"):   # right shapes: the next check is the device
         call()
+
+
+def test_dense_bindings_check_shapes(dsa):
+    import torch
+    q = torch.zeros((4, 8, 64), dtype=torch.bfloat16)
+    k = torch.zeros((16, 64), dtype=torch.bfloat16)
+    w = torch.zeros((4, 8))
+    with pytest.raises(ValueError, match="w must have shape"):
+        dsa.dsa_indexer_scores(q, k, w[:3])
+    with pytest.raises(ValueError, match="k must have shape"):
+        dsa.dsa_indexer_scores(q, k[:, :32], w)
+    with pytest.raises(ValueError, match="S = 16 columns"):
+        dsa.dsa_indexer_scores(q, k, w, scores=torch.zeros((4, 12)))
+    with pytest.raises(ValueError, match="topk must have shape"):
+        dsa.dsa_indexer_topk(torch.zeros((4, 16)), T=4, S=16, q_pos0=12, topk_limit=4, topk=torch.zeros((4, 3), dtype=torch.int32))
+    with pytest.raises(ValueError, match="at least"):
+        dsa.dsa_indexer_topk(torch.zeros((3, 16)), T=4, S=16, q_pos0=12, topk_limit=4)
+    with pytest.raises(ValueError, match="slot_mapping must have shape"):
+        dsa.dsa_indexer_cache_append(torch.zeros((5, 128), dtype=torch.bfloat16), torch.zeros(4, dtype=torch.int64),
+                                     torch.zeros((2, 16, 128), dtype=torch.bfloat16))
