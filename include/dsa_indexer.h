@@ -19,7 +19,11 @@
  *  - Pointers named q, k, k_cache, w, scales, scores, topk, cu_q_lens,
  *    seq_lens, block_tables and workspace are DEVICE pointers, owned by the
  *    caller; the library keeps none of them after returning and allocates no
- *    device memory.  Pointers named types / src / full_args / topk_out are host.
+ *    device memory per call.  Held for the process lifetime once first used on a
+ *    device: the fixed scratch array of dsa_indexer_static, the streams and events
+ *    of dsa_indexer_dense_host, and the streams, events and three cuBLAS handles
+ *    (with the workspaces cuBLAS keeps) of dsa_indexer_prepare.  Pointers named
+ *    types / src / full_args / topk_out are host.
  *  - All work is enqueued on `stream` (NULL = legacy default stream) and is
  *    asynchronous; nothing synchronises except dsa_check_device_status.
  *  - Host-side validation happens before any launch; a failing call launches
