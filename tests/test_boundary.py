@@ -331,3 +331,21 @@ def test_dense_bindings_check_shapes(dsa):
     with pytest.raises(ValueError, match="slot_mapping must have shape"):
         dsa.dsa_indexer_cache_append(torch.zeros((5, 128), dtype=torch.bfloat16), torch.zeros(4, dtype=torch.int64),
                                      torch.zeros((2, 16, 128), dtype=torch.bfloat16))
+
+
+def test_seeded_workloads_repeat_byte_for_byte():
+    import torch
+    a = workloads.paged_case([300, 70], [2, 1], 64, 128, 32, page_size=64, q_dtype="bf16", k_dtype="fp8_e4m3",
+                             seed=5)
+    b = workloads.paged_case([300, 70], [2, 1], 64, 128, 32, page_size=64, q_dtype="bf16", k_dtype="fp8_e4m3",
+                             seed=5)
+    for name in ("q", "w", "k_cache", "k_scale_cache", "block_tables", "cu_q_lens", "seq_lens"):
+        x, y = getattr(a, name), getattr(b, name)
+        assert torch.equal(x.view(torch.uint8) if x.dtype == torch.float8_e4m3fn else x,
+                           y.view(torch.uint8) if y.dtype == torch.float8_e4m3fn else y), name
+    f1 = workloads.frontend_case(7, 64, 32, 4, fp8=True, seed=3)
+    f2 = workloads.frontend_case(7, 64, 32, 4, fp8=True, seed=3)
+    assert torch.equal(f1.hidden, f2.hidden) and torch.equal(f1.slot_mapping, f2.slot_mapping)
+    s1 = workloads.sparse_mla_case([50], [2], 2, 8, kv_rank=16, rope_dim=8, page_size=16, seed=4)
+    s2 = workloads.sparse_mla_case([50], [2], 2, 8, kv_rank=16, rope_dim=8, page_size=16, seed=4)
+    assert torch.equal(s1.topk, s2.topk) and torch.equal(s1.cache_c, s2.cache_c)
