@@ -574,3 +574,68 @@ def test_sparse_mla_all_causal_keys_equals_dense_attention():
     mask = torch.arange(L)[None, :] <= (L - ql + torch.arange(ql))[:, None]
     ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=c.scale)
     assert np.allclose(out, ref.transpose(0, 1).numpy(), atol=1e-10)
+
+
+FRONTEND_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "frontend_hand_worked.json")
+
+
+def _frontend_golden_inputs():
+    with open(FRONTEND_GOLDEN) as f:
+        g = json.load(f)
+    bf = lambda v: torch.tensor(v, dtype=torch.float32).to(torch.bfloat16)
+    ins = dict(hidden=bf(g["hidden"]), qa_normed=bf(g["qa_normed"]), wq_b=bf(g["wq_b"]), wk=bf(g["wk"]),
+               weights_proj=bf(g["weights_proj"]), k_norm_weight=torch.tensor(g["k_norm_weight"], dtype=torch.float32),
+               rope_cos=torch.tensor(g["cos"], dtype=torch.float64), rope_sin=torch.tensor(g["sin"], dtype=torch.float64))
+    return g, ins
+
+
+def _frontend_golden_expected(g, kind):
+    e = g[kind]
+    return np.array(e["q"], dtype=np.float64), np.array(e["k_times_sqrt6"], dtype=np.float64) / np.sqrt(6.0), \
+        np.array(e["w"], dtype=np.float64)
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp8"])
+def test_frontend_prepare_hand_worked(kind):
+    """The front-end's step order (projections, k layer norm, RoPE, then on FP8 the rotation and the
+    row scales) against values worked by hand."""
+    g, ins = _frontend_golden_inputs()
+    out = frontend.prepare(ins["hidden"], ins["qa_normed"], ins["rope_cos"], ins["rope_sin"], ins["wq_b"], ins["wk"],
+                           ins["weights_proj"], ins["k_norm_weight"], None, H=g["H"], D=g["D"], rope_dim=g["rope_dim"],
+                           interleaved=False, eps=g["eps"], fp8=(kind == "fp8"))
+    q, k, w = _frontend_golden_expected(g, kind)
+    assert np.allclose(out["q"], q, rtol=0, atol=1e-12)
+    assert np.allclose(out["k"], k, rtol=0, atol=1e-12)
+    assert np.allclose(out["w"], w, rtol=0, atol=1e-12)
+    if kind == "fp8":
+        # the scales are fp32 (amax taken to fp32, divided by 448 in fp32)
+        assert np.allclose(out["q_scale"], g["fp8"]["q_scale"], rtol=1e-6, atol=0)
+        assert np.allclose(out["k_scale"], np.array(g["fp8"]["k_scale_times_sqrt6"]) / np.sqrt(6.0), rtol=1e-6, atol=0)
+
+
+def test_frontend_hand_worked_values_tell_the_plausible_mistakes_apart():
+    """Each misordering of the front-end's steps, built from the oracle's own pieces, misses the
+    hand-worked values: the golden case would catch it in prepare."""
+    g, ins = _frontend_golden_inputs()
+    f64 = frontend.to_f64
+    H, D, r = g["H"], g["D"], g["rope_dim"]
+    cos, sin = f64(ins["rope_cos"]), f64(ins["rope_sin"])
+    ln = lambda x: frontend.layer_norm(x, f64(ins["k_norm_weight"]), None, g["eps"])
+    rp = lambda x, c=cos, s=sin: frontend.rope(x, c, s, r, False)
+    q0 = frontend.linear(f64(ins["qa_normed"]), f64(ins["wq_b"])).reshape(1, H, D)
+    k0 = frontend.linear(f64(ins["hidden"]), f64(ins["wk"]))
+    rot = frontend.rotate_activation
+    mistakes = {
+        "no RoPE": (q0, ln(k0), "bf16"),
+        "cos and sin swapped": (rp(q0, sin, cos), rp(ln(k0), sin, cos), "bf16"),
+        "layer norm after RoPE": (rp(q0), ln(rp(k0)), "bf16"),
+        "rotation before RoPE": (rp(rot(q0)), rp(rot(ln(k0))), "fp8"),
+        "projections transposed": (rp((f64(ins["qa_normed"]) @ f64(ins["wq_b"])).reshape(1, H, D)),
+                                   rp(ln(f64(ins["hidden"]) @ f64(ins["wk"]))), "bf16"),
+    }
+    for name, (q, k, kind) in mistakes.items():
+        eq, ek, _ = _frontend_golden_expected(g, kind)
+        assert not (np.allclose(q, eq, atol=1e-6) and np.allclose(k, ek, atol=1e-6)), name
+    # and the right order, built from the same pieces, meets them
+    eq, ek, _ = _frontend_golden_expected(g, "fp8")
+    assert np.allclose(rot(rp(q0)), eq, atol=1e-12) and np.allclose(rot(rp(ln(k0))), ek, atol=1e-12)
