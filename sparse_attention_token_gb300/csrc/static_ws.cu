@@ -11,7 +11,8 @@
 // process exits.
 //
 // In host code the array's name only stands for it: the device address is looked
-// up once per device, with that device current, by the first call made on it.
+// up per device, with that device current, by the first call made on it (and by
+// later calls for as long as that lookup has not succeeded).
 #include <mutex>
 
 #include "dsa_indexer.h"
@@ -21,29 +22,29 @@ namespace {
 constexpr size_t kStaticBytes = DSA_STATIC_WORKSPACE_BYTES;
 constexpr int kMaxDevices = 128;
 
-// The scratch itself.  Calls share it and it keeps the last call's contents; the
-// work-list counters, the only part that must start at zero, are cleared by every
-// call (dsa_indexer zeroes them on the stream before its first kernel).
+// The scratch itself.  Calls share it and it keeps the last call's contents.  The
+// work-list counters, the only part that must start at zero, are reset by every
+// call: zeroed on the stream before the score kernel, or, for balanced per-CTA work
+// lists (decode shapes), written in full (every CTA's count) by the list-building
+// kernel.
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
 
-struct DeviceScratch {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
-};
-DeviceScratch g_scratch[kMaxDevices];
+// Per device: the array's device address once a lookup has succeeded.  A failed
+// lookup is not kept, so an error that an earlier, unrelated asynchronous launch left
+// behind does not disable the entry point for the rest of the process.
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set up once per device).
+// Device address of the scratch array on the current device.
 void* scratch_on_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  DeviceScratch& s = g_scratch[dev];
-  std::call_once(s.once, [&s]() {
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
-    s.err = cudaGetSymbolAddress(&p, g_static_scratch);
-    s.ptr = s.err == cudaSuccess ? p : nullptr;
-  });
-  return s.err == cudaSuccess ? s.ptr : nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) == cudaSuccess) g_scratch_ptr[dev] = p;
+  }
+  return g_scratch_ptr[dev];
 }
 
 }  // namespace
