@@ -307,8 +307,13 @@ dsa_status dsa_indexer_dense_host(const void* q_host, int q_dtype, const float* 
  *  - A problem whose dsa_indexer_workspace_size exceeds DSA_STATIC_WORKSPACE_BYTES
  *    returns DSA_ERR_WORKSPACE before anything is launched (use dsa_indexer with a
  *    caller workspace for it).
- *  - The first call on a device looks up the array's device address with that device
- *    current; make that first call before any stream capture.
+ *  - The array is placed on a device when the library's device code is loaded there,
+ *    which under CUDA's default lazy module loading can be during the first call into
+ *    the library on that device, and the first dsa_indexer_static call on a device
+ *    looks up the array's device address with that device current.  So make one call
+ *    into the library (this one, or any other) on each device before reserving most of
+ *    its memory, and make the first dsa_indexer_static call there before any stream
+ *    capture.  A failed lookup returns DSA_ERR_CUDA and is tried again by the next call.
  *  - All calls on a device share the array and it keeps the last call's contents; each
  *    call clears the part that must start at zero (the work-list counters).  Calls that
  *    overlap on the GPU (other streams, other host threads) race on the array: serialise them.
@@ -342,6 +347,20 @@ dsa_status dsa_indexer_stack(int L, const int32_t* types, const dsa_indexer_args
 /* Synchronise `stream`, then report and clear the device status word of the current
  * device: DSA_OK, DSA_ERR_DEVICE_CHECK or DSA_ERR_TIMEOUT (or DSA_ERR_CUDA). */
 dsa_status dsa_check_device_status(dsa_stream_t stream);
+
+/*
+ * dsa_test_arm_score_timeout -- failure-path test hook; the pages have no counterpart.
+ * Every wait inside the library's kernels is bounded: a wait that runs out records
+ * DSA_ERR_TIMEOUT in the device status word and makes the kernel stop, wait (bounded)
+ * for its own copies and tensor-core work in flight, free its tensor memory and
+ * return, so the device stays usable.  This call arms the next score-kernel launch
+ * made by the calling host thread (by any entry point) so that its MMA-issuing thread
+ * first waits on an internal barrier that nothing ever completes, for at most
+ * limit_ns nanoseconds; that launch then takes the path above and its outputs are
+ * unspecified.  The arming is used up by that one launch; limit_ns = 0 disarms.
+ * Returns DSA_OK.
+ */
+dsa_status dsa_test_arm_score_timeout(unsigned long long limit_ns);
 
 #ifdef __cplusplus
 }

@@ -118,6 +118,8 @@ def lib():
         L.dsa_indexer_dense_host_workspace_size.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(S)]
         L.dsa_indexer_dense_host.restype = I
         L.dsa_indexer_dense_host.argtypes = [P, I, P, P, I, P, P, I, I, I, I, I, I, I, I, I, P, P, S, P]
+        L.dsa_test_arm_score_timeout.restype = I
+        L.dsa_test_arm_score_timeout.argtypes = [ctypes.c_ulonglong]
         _LIB = L
     return _LIB
 
@@ -500,6 +502,13 @@ def dsa_indexer_stack(indexer_types: Sequence, full_layer_args: Sequence, stream
                                  _stream_ptr(stream))
     _check(st, "dsa_indexer_stack")
     return [outs[i] for i in range(L)], list(src[:L])
+
+
+def dsa_test_arm_score_timeout(limit_ns: int) -> None:
+    """Failure-path test hook: the next score-kernel launch of this host thread first
+    waits up to limit_ns on a barrier nothing completes, then records DSA_ERR_TIMEOUT,
+    drains and returns (its outputs are unspecified).  0 disarms."""
+    _check(lib().dsa_test_arm_score_timeout(int(limit_ns)), "dsa_test_arm_score_timeout")
 
 
 def dsa_check_device_status(stream=None) -> int:

@@ -814,6 +814,11 @@ dsa_status dsa_indexer_stack(int L, const int32_t* types, const dsa_indexer_args
   return st;
 }
 
+dsa_status dsa_test_arm_score_timeout(unsigned long long limit_ns) {
+  armed_probe_wait_ns() = limit_ns;
+  return DSA_OK;
+}
+
 dsa_status dsa_check_device_status(dsa_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
   unsigned v = 0, zero = 0;

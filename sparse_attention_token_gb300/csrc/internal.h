@@ -62,6 +62,9 @@ struct ScoreArgs {
   float* scores;
   long long ld;
   unsigned* status;   // device status word
+  // failure-path test hook (0 = off): the MMA issuer first waits this many ns on a
+  // barrier nothing arrives at, so the kernel takes its timeout-and-drain path
+  unsigned long long probe_wait_ns;
 };
 
 struct TopkArgs {
@@ -110,6 +113,13 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   cfg.attrs = at;
   cfg.numAttrs = pdl_off() ? 0 : 1;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Failure-path test hook: the next score launch of the calling host thread gets this
+// probe_wait_ns (set by dsa_test_arm_score_timeout, consumed by launch_score).
+inline unsigned long long& armed_probe_wait_ns() {
+  static thread_local unsigned long long ns = 0;
+  return ns;
 }
 
 // Host launchers (return a cudaError_t).

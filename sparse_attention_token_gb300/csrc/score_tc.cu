@@ -61,7 +61,8 @@ __host__ __device__ inline SmemPlan plan_smem(int N, int D, int q_fp8, int k_fp8
 // Barrier slots inside the bars region.
 enum {
   kBarQFull = 0, kBarQEmpty = 2, kBarTFull = 4, kBarTEmpty = 6, kBarFold = 8,  // fold: 4 slots
-  kBarDone = 12, kBarKFull = 13, kBarKEmpty = 13 + kMaxKStages, kBarEnd = 13 + 2 * kMaxKStages
+  kBarDone = 12, kBarKFull = 13, kBarKEmpty = 13 + kMaxKStages, kBarProbe = 13 + 2 * kMaxKStages,
+  kBarEnd = kBarProbe + 1
 };
 static_assert(kBarEnd <= 64, "barrier region");
 
@@ -279,7 +280,10 @@ __device__ __forceinline__ void mma_loop(const ScoreArgs& a, uint8_t* smem, cons
   const uint32_t k_base = sbase + P.k[0];
   uint32_t nq = 0, nt = 0;
   uint32_t sk = 0, kphase = 0;  // key ring slot and its phase parity
-  bool ok = true;
+  // test hook: a wait that nothing ends, bounded by probe_wait_ns, so the kernel records
+  // a timeout and every role leaves its loop and drains
+  bool ok = a.probe_wait_ns == 0 ||
+            ptx::mbar_wait(&bars[kBarProbe], 0, abort, a.status, kStatusTimeout, a.probe_wait_ns);
   for (int it = 0; ok; ++it) {
     ItemInfo I;
     if (!fetch_item<C::NQ>(a, n_items, it, I)) break;
@@ -524,6 +528,7 @@ __global__ void __launch_bounds__(Cfg<H, DECODE, SPLIT>::THREADS, 1)
       ptx::mbar_init(&bars[kBarFold + 2 * s + 1], 128);
     }
     ptx::mbar_init(&bars[kBarDone], 1);
+    ptx::mbar_init(&bars[kBarProbe], 1);
     for (int s = 0; s < a.num_k_stages; ++s) {
       // e4m3 key scales of dense tiles come by cp.async (32 lane arrivals), those of
       // paged tiles by one bulk copy per page
@@ -591,8 +596,11 @@ size_t score_smem_bytes(const ScoreArgs& a, int num_k_stages) {
   return plan_smem(a.N, a.D, a.split ? 1 : a.q_fp8, a.k_fp8, num_k_stages).total;
 }
 
-cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k, int grid,
+cudaError_t launch_score(const ScoreArgs& args, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k, int grid,
                          size_t smem_bytes, cudaStream_t st) {
+  ScoreArgs a = args;
+  a.probe_wait_ns = armed_probe_wait_ns();
+  armed_probe_wait_ns() = 0;
   const bool dec = a.split || a.N != 256;
 #define DSA_CASE(HH)                                                                        \
   case HH:                                                                                  \
