@@ -101,3 +101,46 @@ def test_decode_b64_bf16_q_fp8_cache_full_size_sampled_rows():
     for i, r in enumerate(rows):
         n = int(lens[r])
         check_topk_row(tk[r], rt[i], rs[i, :n], RTOL["bf16"] * rb[i, :n], n, pc.topk_limit, True)
+
+
+def test_indexshare_stack_full_size_bf16_decode():
+    """The IndexShare workload at its full size: 12 layers [full, shared, shared] x 4, decode
+    B=32 at 32768 keys, bf16 paged caches.  Each full layer's sampled rows are checked
+    against the oracle and every row's width and uniqueness; each shared layer's output is
+    its source layer's buffer, bytes and all."""
+    sc = workloads.indexshare_stack()
+    to = lambda t: None if t is None else t.cuda()
+    args, keep = [], []
+    for pc in sc.layers:
+        if pc is None:
+            args.append(None)
+            continue
+        a, kk = dsa.make_indexer_args(to(pc.q), to(pc.w), to(pc.k_cache), to(pc.cu_q_lens), to(pc.seq_lens),
+                                      to(pc.block_tables), max_seq_len=pc.max_seq_len, topk_limit=pc.topk_limit)
+        args.append(a)
+        keep.append(kk)
+    ptrs, src = dsa.dsa_indexer_stack(sc.indexer_types, args)
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_status() == dsa.DSA_OK
+    assert src == [0, 0, 0, 3, 3, 3, 6, 6, 6, 9, 9, 9]
+    outs = {}
+    fi = 0
+    for l, pc in enumerate(sc.layers):
+        if pc is None:
+            continue
+        out = keep[fi][8]
+        fi += 1
+        assert ptrs[l] == out.data_ptr()
+        outs[l] = out.cpu().numpy()
+        tk = outs[l]
+        assert tk.shape == (32, 2048) and np.all(tk >= 0) and np.all(tk < 32768)
+        assert all(len(np.unique(r)) == 2048 for r in tk)
+        rows = sample_rows(pc.B, 4, n=4, seed=10 + l)
+        rt, rs, rb = oracle.paged(pc, rows=rows, want_scores=True, want_bound=True)
+        for i, r in enumerate(rows):
+            check_topk_row(tk[r], rt[i], rs[i, :32768], RTOL["bf16"] * rb[i, :32768], 32768, 2048, True)
+    # a shared layer's entry is its source layer's buffer: the same memory, the same bytes
+    by_ptr = {kk[8].data_ptr(): kk[8] for kk in keep}
+    for l, s in enumerate(src):
+        assert ptrs[l] == ptrs[s]
+        assert np.array_equal(by_ptr[ptrs[l]].cpu().numpy(), outs[s])
