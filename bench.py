@@ -86,6 +86,47 @@ def recorded_traffic():
         return None
 
 
+def measure_tensor_peaks(dev, n: int = 8192, reps: int = 10):
+    """Dense tensor-core throughput of this GPU measured in this run: bf16 torch.matmul and
+    e4m3 torch._scaled_mm (per-tensor scales, bf16 out) at n^3, best of `reps` (CUDA events).
+    The e4m3 figure is the roofline peak of the FP8 score kernel."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    a = torch.randn((n, n), generator=g, device=dev).to(torch.bfloat16)
+    b = torch.randn((n, n), generator=g, device=dev).to(torch.bfloat16)
+    out = {}
+
+    def best(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        t = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            t.append(e0.elapsed_time(e1))
+        return 2.0 * n ** 3 / (min(t) / 1e3) / 1e12
+
+    out["bf16_tflops"] = best(lambda: torch.matmul(a, b))
+    a8 = a.to(torch.float8_e4m3fn)
+    b8 = b.to(torch.float8_e4m3fn).t().contiguous().t()   # column-major second operand
+    one = torch.ones((), dtype=torch.float32, device=dev)
+    try:
+        out["e4m3_tflops"] = best(lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one,
+                                                           out_dtype=torch.bfloat16))
+    except Exception as exc:  # noqa: BLE001 -- reported, not hidden
+        out["e4m3_tflops"] = None
+        out["e4m3_error"] = str(exc).splitlines()[0][:200]
+    out["how"] = (f"{n}^3, best of {reps}, CUDA events: torch.matmul bf16; torch._scaled_mm e4m3 x e4m3 "
+                  "with per-tensor fp32 scales, bf16 out")
+    del a, b, a8, b8
+    torch.cuda.empty_cache()
+    return out
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
 
@@ -104,7 +145,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+                 "-lms", "20", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -117,6 +158,22 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0: float, t1: float):
+        rows = self._rows()
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        inside = [r for r in rows if t0 - 0.02 <= r[0] <= t1 + 0.02]
+        window = "timed region"
+        if not inside:
+            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
+            window = "nearest samples (timed region shorter than the sampling period)"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+    def _rows(self):
+        if getattr(self, "_cache", None) is not None:
+            return self._cache
         rows = []
         if self.path and os.path.exists(self.path):
             for line in open(self.path):
@@ -130,17 +187,8 @@ class ClockSampler:
                 except Exception:
                     continue
             os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
-        window = "timed region"
-        if not inside:
-            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
-            window = "nearest samples (timed region shorter than the sampling period)"
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
-                "reasons": reasons, "samples": len(inside), "window": window}
+        self._cache = rows
+        return rows
 
 
 def make_inputs(seed: int = 0):
@@ -224,8 +272,13 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    t_wall2 = time.time()
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
+    # the timed region is short next to the sampling period: also report the samples
+    # over the timed region and the end-to-end loop that follows it
+    clocks_e2e = sampler.summary(t_wall0, t_wall2)
+    clocks["timed_and_e2e"] = {k: clocks_e2e[k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")}
     h2d = q_h.numel() * q_h.element_size() + k_h.numel() * k_h.element_size() + w_h.numel() * w_h.element_size()
     d2h = topk_h.numel() * topk_h.element_size()
 
@@ -305,6 +358,7 @@ def _chunked_prefill_fp8(dev, stream, peaks, iters=3):
     import ctypes
     import sparse_attention_token_gb300 as dsa
     bf16_peak = float(peaks["bf16_tflops"])
+    e4m3_peak = peaks.get("e4m3_tflops")
     c = _paged_on_device(1, [65536], 8192, 64, 128, 64, True, True, 4, dev)
     args, keep = dsa.make_indexer_args(c["q"], c["w"], c["k_cache"], c["cu_q_lens"], c["seq_lens"],
                                        c["block_tables"], max_seq_len=c["max_seq_len"], topk_limit=2048,
@@ -317,8 +371,13 @@ def _chunked_prefill_fp8(dev, stream, peaks, iters=3):
         "workload": "8192 queries at 57344..65535 vs a 65536-key paged cache (page 64), e4m3 q/k with fp32 scales, "
                     "H=64, D=128, index_topk=2048",
         "ms_per_step": ms, "scores_per_s": pairs / (ms / 1e3), "topk_rows_per_s": 8192 / (ms / 1e3),
-        "tc_frac_step": flops / (ms / 1e3) / 1e12 / (2 * bf16_peak),
-        "peak": f"e4m3 dense = 2 x measured bf16 ({2 * bf16_peak:.0f} TFLOP/s, nominal ratio)"}
+        "tflops_step": flops / (ms / 1e3) / 1e12}
+    if e4m3_peak:
+        out["tc_frac_step"] = out["tflops_step"] / e4m3_peak
+        out["peak"] = f"e4m3 dense measured in this run (torch._scaled_mm 8192^3): {e4m3_peak:.0f} TFLOP/s"
+    else:
+        out["tc_frac_step"] = out["tflops_step"] / (2 * bf16_peak)
+        out["peak"] = f"e4m3 dense = 2 x measured bf16 ({2 * bf16_peak:.0f} TFLOP/s, nominal ratio)"
     del c, args, keep
     torch.cuda.empty_cache()
     return out
@@ -565,6 +624,9 @@ def main():
     if args.only:
         if rank == 0:
             peaks, _ = measured_peaks()
+            if args.only == "chunked_prefill_fp8":
+                peaks = dict(peaks)
+                peaks["e4m3_tflops"] = measure_tensor_peaks(torch.device("cuda", local_rank)).get("e4m3_tflops")
             out = OTHER_WORKLOADS[args.only](torch.device("cuda", local_rank), torch.cuda.current_stream(), peaks,
                                              iters=args.steps)
             print(json.dumps({"only": args.only, **out}), flush=True)
@@ -605,8 +667,13 @@ def main():
             "device_status": r["status"],
         }
         if not args.no_extra:
-            line["workloads"] = run_other_workloads(torch.device("cuda", local_rank),
-                                                    torch.cuda.current_stream(), peaks)
+            dev = torch.device("cuda", local_rank)
+            tp = measure_tensor_peaks(dev)
+            line["tensor_peaks_this_run"] = tp
+            wl_peaks = dict(peaks)
+            if tp.get("e4m3_tflops"):
+                wl_peaks["e4m3_tflops"] = tp["e4m3_tflops"]
+            line["workloads"] = run_other_workloads(dev, torch.cuda.current_stream(), wl_peaks)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(r["case"])
         print(json.dumps(line), flush=True)
