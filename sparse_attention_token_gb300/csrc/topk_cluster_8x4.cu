@@ -1,0 +1,8 @@
+// topk_cluster_8x4.cu -- the cluster top-k for clusters of 4 CTAs of up to 8192 keys.
+#include "topk_kernels.cuh"
+
+namespace dsa {
+cudaError_t launch_topk_cluster_8_4(const TopkArgs& a, int ccap, size_t csmem, cudaStream_t st) {
+  return launch_cluster_rows<8, 4>(a, ccap, csmem, st);
+}
+}  // namespace dsa

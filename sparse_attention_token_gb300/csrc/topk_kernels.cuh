@@ -1,0 +1,949 @@
+#pragma once
+// topk_kernels.cuh -- per-row top-k of indexer scores (GLM5 TensorCast adaptation design,
+// "性能模型设计" bucket 8, top-k selection; output width min(topk_limit, n_visible)).
+//
+// One CTA of 256 threads per row.  Scores become order-preserving unsigned keys
+// (larger score -> larger key; -0.0 folded onto +0.0).  The best `keep` keys under
+// (score desc, index asc) are found as follows.
+//   1. One pass over the row builds a histogram of the top 12 key bits; a suffix
+//      scan finds the bucket b where the running count reaches `keep`.
+//   2. Fast path (the keys in buckets >= b fit the candidate buffer): an
+//      order-preserving compaction (each warp owns a contiguous segment of the row;
+//      ballots and warp prefix sums, no block-wide scans) copies every key of
+//      bucket >= b with its index, in index order.
+//        score order: a stable LSD radix sort (8-bit digits, descending, digits that
+//        never change skipped) of the candidates; the first `keep` are the answer
+//        (ties keep ascending index because the input was in index order);
+//        index order: the exact threshold inside bucket b is refined on the
+//        candidates alone, then one ordered pass writes the selected indices.
+//   3. Slow path (a huge threshold bucket, e.g. many equal scores): the exact
+//      threshold key T and `need` (how many keys equal to T to keep, lowest index
+//      first) are refined over the whole row with two more histogram passes, then
+//      the ordered compaction keeps exactly `keep` keys, sorted as above.
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kBins = 4096;            // top 12 key bits
+constexpr int kMaxRounds = 16;         // sort: candidates per warp / 32
+constexpr int kHistWords = kBins + kBins / 16;  // histogram with one pad word per 16 bins
+constexpr int kSortBits = 9;           // radix sort digit width
+constexpr int kSortBins = 1 << kSortBits;
+
+// Histogram slot of bin b: one pad word after every 16 bins, so a thread reading 16
+// consecutive bins while its neighbours read the next 16 hits distinct banks.
+__device__ __forceinline__ int hslot(uint32_t b) { return static_cast<int>(b + (b >> 4)); }
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;  // -0.0 compares equal to +0.0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive prefix sum over the block in thread order; *total gets the block sum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) red[warp] = x;
+  __syncthreads();
+  uint32_t before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t r = red[w];
+    before += w < warp ? r : 0u;
+    tot += r;
+  }
+  *total = tot;
+  __syncthreads();  // red is reused by the next call
+  return before + x - v;
+}
+
+// Warp-inclusive prefix sum.
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
+// Bucket where the running count from the top reaches `want` (nbins = 16 * kThreads
+// or 256).  out = {bucket, keys above it, keys in it}.  Thread t scans the bins
+// nbins - per*(t+1) .. nbins - per*t - 1, highest first.
+__device__ __forceinline__ void find_bucket(const uint32_t* hist, int nbins, uint32_t want, uint32_t* red,
+                                            uint32_t* out) {
+  const int per = nbins / kThreads;  // 16 or 1
+  const int hi = nbins - per * static_cast<int>(threadIdx.x);
+  uint32_t c[16];
+  uint32_t s = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    c[j] = j < per ? hist[hslot(static_cast<uint32_t>(hi - 1 - j))] : 0u;
+    s += c[j];
+  }
+  uint32_t tot;
+  uint32_t run = block_excl_scan(s, red, &tot);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j < per && run < want && run + c[j] >= want) {
+      out[0] = static_cast<uint32_t>(hi - 1 - j);
+      out[1] = run;
+      out[2] = c[j];
+    }
+    run += c[j];
+  }
+  __syncthreads();
+}
+
+// Four consecutive keys of the row starting at i (cnt of them valid, the rest 0).
+__device__ __forceinline__ int load4(const float* p, long long n, long long i, uint32_t (&u)[4]) {
+  const long long rem = n - i;
+  if (rem >= 4) {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(p + i));
+    u[0] = order_key(f.x); u[1] = order_key(f.y); u[2] = order_key(f.z); u[3] = order_key(f.w);
+    return 4;
+  }
+  const int c = rem > 0 ? static_cast<int>(rem) : 0;
+  for (int j = 0; j < 4; ++j) u[j] = j < c ? order_key(__ldg(p + i + j)) : 0u;
+  return c;
+}
+
+// A row is split into kWarps contiguous segments, one per warp; a segment is read
+// in blocks of 128 keys (lane l holds keys 4l..4l+3 of the block), so the order
+// (segment, block, lane, element) is the key-index order.
+__device__ __forceinline__ long long seg_len(long long n) { return ((n + kWarps - 1) / kWarps + 127) & ~127LL; }
+
+// Segment read from global memory on every pass (any row length).  visit() walks the
+// segment in batches of kBatch blocks whose loads are all issued before any is used,
+// so a pass over a long row costs a few memory latencies, not one per block.
+struct GlobalSeg {
+  static constexpr int kBatch = 16;
+  const float* p;
+  long long s0, s1;
+  int nb;
+  __device__ void init(const float* row, long long n) {
+    const long long seg = seg_len(n);
+    p = row;
+    s0 = (threadIdx.x >> 5) * seg;
+    s1 = min(n, s0 + seg);
+    nb = s1 > s0 ? static_cast<int>((s1 - s0 + 127) / 128) : 0;
+  }
+  // f(u[4], first index, valid count) for every block of this lane, in index order.
+  template <class F>
+  __device__ __forceinline__ void visit(F f) const {
+    const int lane = threadIdx.x & 31;
+    for (int j0 = 0; j0 < nb; j0 += kBatch) {
+      uint32_t u[kBatch][4];
+      int c[kBatch];
+#pragma unroll
+      for (int jj = 0; jj < kBatch; ++jj) {
+        const long long i = s0 + 128LL * (j0 + jj) + 4 * lane;
+        c[jj] = (j0 + jj < nb && i < s1) ? load4(p, s1, i, u[jj]) : 0;
+      }
+#pragma unroll
+      for (int jj = 0; jj < kBatch; ++jj) {
+        if (j0 + jj < nb) f(u[jj], s0 + 128LL * (j0 + jj) + 4 * lane, c[jj]);
+      }
+    }
+  }
+};
+
+// Segment held in registers, loaded once with every load in flight (rows up to
+// kWarps * NB * 128 keys).
+template <int NB>
+struct RegSeg {
+  uint32_t v[NB][4];
+  int c[NB];
+  long long s0;
+  int nb;
+  __device__ void init(const float* row, long long n) {
+    const long long seg = seg_len(n);
+    s0 = (threadIdx.x >> 5) * seg;
+    const long long s1 = min(n, s0 + seg);
+    nb = s1 > s0 ? static_cast<int>((s1 - s0 + 127) / 128) : 0;
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const long long i = s0 + 128LL * j + 4 * (threadIdx.x & 31);
+      c[j] = (j < nb && i < s1) ? load4(row, s1, i, v[j]) : 0;
+      if (c[j] == 0) v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0u;
+    }
+  }
+  template <class F>
+  __device__ __forceinline__ void visit(F f) const {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      if (j < nb) {
+        uint32_t u[4] = {v[j][0], v[j][1], v[j][2], v[j][3]};
+        f(u, s0 + 128LL * j + 4 * lane, c[j]);
+      }
+    }
+  }
+};
+
+// hist[(u >> shift) & mask] += 1 for every key of the row with (u >> pshift) == pre
+// (pshift = 32: every key).
+template <class RS>
+__device__ __forceinline__ void seg_hist(const RS& rs, uint32_t* hist, int shift, uint32_t mask, int pshift,
+                                         uint32_t pre) {
+  rs.visit([&](const uint32_t (&u)[4], long long, int c) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < c && (pshift >= 32 || (u[e] >> pshift) == pre)) atomicAdd(&hist[hslot((u[e] >> shift) & mask)], 1u);
+  });
+}
+
+// Order-preserving compaction: key u (index i) is kept iff
+//   u > T, or u == T and it is among the first `need` keys equal to T (index order),
+// and kept keys are written to (ck, ci) in index order.  Returns the number kept.
+template <class RS>
+__device__ uint32_t seg_compact(const RS& rs, uint32_t T, uint32_t need, uint32_t* ck, uint32_t* ci,
+                                uint32_t* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool ties = need != 0 && need != 0xFFFFFFFFu;
+  uint32_t eq_before = 0;
+  if (ties) {
+    uint32_t ce = 0;
+    rs.visit([&](const uint32_t (&u)[4], long long, int c) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ce += (e < c && u[e] == T) ? 1u : 0u;
+    });
+    ce = __reduce_add_sync(0xffffffffu, ce);
+    if (lane == 0) red[warp] = ce;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) eq_before += w < warp ? red[w] : 0u;
+    __syncthreads();
+  }
+  // pass 1: kept keys per warp
+  uint32_t kept = 0;
+  {
+    uint32_t run = eq_before;
+    rs.visit([&](const uint32_t (&u)[4], long long, int c) {
+      uint32_t e4 = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) e4 += (e < c && u[e] == T) ? 1u : 0u;
+      const uint32_t ie = ties ? warp_incl_scan(e4) : e4;
+      uint32_t r = run + ie - e4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (e < c) {
+          if (u[e] > T) ++kept;
+          else if (u[e] == T) { kept += r < need ? 1u : 0u; ++r; }
+        }
+      }
+      if (ties) run += __shfl_sync(0xffffffffu, ie, 31);
+    });
+  }
+  kept = __reduce_add_sync(0xffffffffu, kept);
+  if (lane == 0) red[warp] = kept;
+  __syncthreads();
+  uint32_t base = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t r = red[w];
+    base += w < warp ? r : 0u;
+    total += r;
+  }
+  __syncthreads();
+  // pass 2: write
+  {
+    uint32_t run = eq_before;
+    rs.visit([&](const uint32_t (&u)[4], long long i, int c) {
+      uint32_t e4 = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) e4 += (e < c && u[e] == T) ? 1u : 0u;
+      const uint32_t ie = ties ? warp_incl_scan(e4) : e4;
+      uint32_t r = run + ie - e4;
+      uint32_t m = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (e < c) {
+          if (u[e] > T) m |= 1u << e;
+          else if (u[e] == T) { if (r < need) m |= 1u << e; ++r; }
+        }
+      }
+      const uint32_t k = __popc(m);
+      const uint32_t incl = warp_incl_scan(k);
+      uint32_t pos = base + incl - k;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if ((m >> e) & 1u) {
+          ck[pos] = u[e];
+          ci[pos] = static_cast<uint32_t>(i + e);
+          ++pos;
+        }
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+      if (ties) run += __shfl_sync(0xffffffffu, ie, 31);
+    });
+  }
+  __syncthreads();
+  return total;
+}
+
+// Stable LSD radix sort of n (key, value) pairs by key, descending.  Only the bits
+// below the highest bit in which the keys differ are sorted, kSortBits per pass (keys
+// of one row's candidates usually differ in their low ~25 bits: 3 passes).
+// n <= kWarps * 32 * kMaxRounds.  The sorted buffers come back in sk_out / sv_out.
+__device__ void radix_sort_desc(uint32_t* ka, uint32_t* va, uint32_t* kb, uint32_t* vb, int n, uint32_t* cnt,
+                                uint32_t* red, uint32_t** sk_out, uint32_t** sv_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t diff = 0;
+  if (n > 0) {
+    const uint32_t k0 = ka[0];
+    for (int i = tid; i < n; i += kThreads) diff |= ka[i] ^ k0;
+  }
+  diff = __reduce_or_sync(0xffffffffu, diff);
+  if (lane == 0) red[warp] = diff;
+  __syncthreads();
+  diff = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) diff |= red[w];
+  __syncthreads();
+  const int nbits = 32 - __clz(diff);  // 0 when all keys are equal
+
+  const int CH = (((n + kWarps - 1) / kWarps) + 31) & ~31;  // keys per warp, multiple of 32
+  const int rounds = CH / 32;
+  uint32_t *sk = ka, *sv = va, *dk = kb, *dv = vb;
+  for (int sh = 0; sh < nbits; sh += kSortBits) {
+    for (int i = tid; i < kWarps * kSortBins; i += kThreads) cnt[i] = 0;
+    __syncthreads();
+    uint32_t offs[kMaxRounds];
+    uint32_t digs[kMaxRounds];
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+      const int e = warp * CH + r * 32 + lane;
+      digs[r] = (r < rounds && e < n) ? (kSortBins - 1) - ((sk[e] >> sh) & (kSortBins - 1)) : kSortBins;
+    }
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+      offs[r] = 0;
+      if (r < rounds) {
+        const uint32_t d = digs[r];
+        const bool valid = d < kSortBins;
+        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        const uint32_t rank = __popc(peers & ((1u << lane) - 1u));
+        const uint32_t before = valid ? cnt[warp * kSortBins + d] : 0u;
+        __syncwarp();
+        if (valid && rank == 0) cnt[warp * kSortBins + d] = before + __popc(peers);
+        __syncwarp();
+        offs[r] = before + rank;
+      }
+    }
+    __syncthreads();
+    {
+      // exclusive scan in (digit, warp) order: thread t owns digits 2t and 2t+1 for all warps
+      uint32_t v[2][kWarps], s = 0;
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) { v[q][w] = cnt[w * kSortBins + 2 * tid + q]; s += v[q][w]; }
+      uint32_t tot;
+      uint32_t ex = block_excl_scan(s, red, &tot);
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) { cnt[w * kSortBins + 2 * tid + q] = ex; ex += v[q][w]; }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+      if (r < rounds) {
+        const int e = warp * CH + r * 32 + lane;
+        if (e < n) {
+          const uint32_t dest = cnt[warp * kSortBins + digs[r]] + offs[r];
+          dk[dest] = sk[e];
+          dv[dest] = sv[e];
+        }
+      }
+    }
+    __syncthreads();
+    uint32_t* t;
+    t = sk; sk = dk; dk = t;
+    t = sv; sv = dv; dv = t;
+  }
+  *sk_out = sk;
+  *sv_out = sv;
+}
+
+// Score order by buckets: the candidates' keys usually span a narrow range, so one
+// counting pass over at most 4096 equal-width buckets between their minimum and
+// maximum leaves a few keys per bucket; each key's final slot is its bucket's start
+// plus the number of bucket-mates that beat it (higher key, or equal key and lower
+// index).  Writes out[slot] = index for slots < keep.  Returns false (writing
+// nothing) when some bucket holds more than kBucketLimit keys -- many equal or
+// clustered scores -- so the caller sorts with the radix sort instead.  bk and bi
+// are adjacent scratch arrays (bi == bk + n at least), used together as n 8-byte words.
+// |value| bits of an order-preserving key (sign dropped).
+__device__ __forceinline__ uint32_t key_mag(uint32_t u) {
+  return (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : (~u & 0x7FFFFFFFu);
+}
+// Order-preserving key with magnitudes below floor_mag clamped to zero (monotone in u).
+__device__ __forceinline__ uint32_t bucket_key(uint32_t u, uint32_t floor_mag) {
+  const uint32_t m = key_mag(u);
+  const uint32_t c = m > floor_mag ? m - floor_mag : 0u;
+  return (u & 0x80000000u) ? 0x80000000u + c : 0x80000000u - c;
+}
+
+constexpr int kBucketLimit = 64;
+constexpr int kSortBuckets = 4096;
+
+__device__ bool bucket_rank_out(uint32_t* ck, const uint32_t* ci, int n, int keep, uint32_t* bk,
+                                uint32_t* bi, uint32_t* cur, uint32_t* red, int32_t* out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  for (int i = tid; i < n; i += kThreads) {
+    const uint32_t u = ck[i];
+    lo = min(lo, u);
+    hi = max(hi, u);
+  }
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) {
+    red[warp] = lo;
+    red[kWarps + warp] = hi;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    lo = min(lo, red[w]);
+    hi = max(hi, red[kWarps + w]);
+  }
+  // Buckets are equal-width in a compressed key: magnitudes more than 12 binades below
+  // the largest one are clamped to zero.  Key space is logarithmic across binades, so
+  // when the candidates straddle zero the raw range covers every exponent of both signs
+  // and a few buckets would get most keys; the compressed key is still monotone.
+  const uint32_t mbig = max(key_mag(lo), key_mag(hi));
+  const uint32_t floor_mag = (mbig >> 23) > 12u ? ((mbig >> 23) - 12u) << 23 : 0u;
+  const uint32_t clo = bucket_key(lo, floor_mag), chi = bucket_key(hi, floor_mag);
+  int sh = 0;
+  while (((chi >> sh) - (clo >> sh)) >= static_cast<uint32_t>(kSortBuckets)) ++sh;
+  const uint32_t base = clo >> sh;
+  const int nb = static_cast<int>((chi >> sh) - base) + 1;
+  for (int b = tid; b < nb; b += kThreads) cur[hslot(b)] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += kThreads) atomicAdd(&cur[hslot((bucket_key(ck[i], floor_mag) >> sh) - base)], 1u);
+  __syncthreads();
+  // descending exclusive scan: start[b] = keys in buckets above b; thread t owns 16 bins
+  uint32_t c[16], sum = 0, mx = 0;
+  const int b_hi = nb - 16 * tid;  // bins b_hi-1 .. b_hi-16, highest first
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int b = b_hi - 1 - j;
+    c[j] = b >= 0 ? cur[hslot(b)] : 0u;
+    sum += c[j];
+    mx = max(mx, c[j]);
+  }
+  uint32_t tot;
+  uint32_t run = block_excl_scan(sum, red, &tot);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  mx = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) mx = max(mx, red[w]);
+  __syncthreads();  // red is free again before any caller reuses it
+  if (mx > static_cast<uint32_t>(kBucketLimit)) return false;  // uniform across the block
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int b = b_hi - 1 - j;
+    if (b >= 0) cur[hslot(b)] = run;
+    run += c[j];
+  }
+  __syncthreads();
+  // key and complemented index in one word: a larger word is a better key, or the same
+  // key at a lower index, so ranking is one 8-byte load and one compare per element
+  uint64_t* bw = reinterpret_cast<uint64_t*>(bk);  // bk and bi: 2n adjacent words
+  for (int i = tid; i < n; i += kThreads) {
+    const uint32_t u = ck[i];
+    const uint32_t pos = atomicAdd(&cur[hslot((bucket_key(u, floor_mag) >> sh) - base)], 1u);
+    bw[pos] = (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~ci[i]);
+  }
+  __syncthreads();
+  // cur[b] is now the end of bucket b; bucket b starts where bucket b + 1 ends
+  for (int p = tid; p < n; p += kThreads) {
+    const uint64_t x = bw[p];
+    const int b = static_cast<int>((bucket_key(static_cast<uint32_t>(x >> 32), floor_mag) >> sh) - base);
+    const uint32_t q0 = b + 1 < nb ? cur[hslot(b + 1)] : 0u, q1 = cur[hslot(b)];
+    uint32_t rank = q0;
+    uint32_t q = q0;
+    for (; q + 4 <= q1; q += 4)
+      rank += (bw[q] > x ? 1u : 0u) + (bw[q + 1] > x ? 1u : 0u) + (bw[q + 2] > x ? 1u : 0u) +
+              (bw[q + 3] > x ? 1u : 0u);
+    for (; q < q1; ++q) rank += bw[q] > x ? 1u : 0u;
+    if (rank < static_cast<uint32_t>(keep)) ck[rank] = ~static_cast<uint32_t>(x);  // ck is free after the scatter
+  }
+  __syncthreads();
+  // coalesced copy-out (scattered 4-byte global stores were a third of the sort's time)
+  for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(ck[i]);
+  return true;
+}
+
+// Exact threshold among the keys of 12-bit bucket d1, of which `want` are still to
+// be taken: two histogram passes (the next 12 bits, then the last 8) over the keys
+// that `feed(hist, shift, mask, pshift, pre)` counts.  T = the threshold key,
+// need = how many keys equal to T to take (lowest index first).
+template <class Feed>
+__device__ void refine_threshold(Feed feed, uint32_t d1, uint32_t want, uint32_t* hist, uint32_t* red,
+                                 uint32_t* info, uint32_t* T_out, uint32_t* need_out) {
+  for (int i = threadIdx.x; i < kHistWords; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  feed(hist, 8, 4095u, 20, d1);
+  __syncthreads();
+  find_bucket(hist, kBins, want, red, info);
+  const uint32_t d2 = info[0];
+  want -= info[1];
+  const uint32_t pre = (d1 << 12) | d2;  // top 24 bits of the threshold
+  for (int i = threadIdx.x; i < kHistWords; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  feed(hist, 0, 255u, 8, pre);
+  __syncthreads();
+  find_bucket(hist, 256, want, red, info);
+  *T_out = (pre << 8) | info[0];
+  *need_out = want - info[1];
+}
+
+// Shared-memory layout of every top-k kernel (dynamic part).
+struct TopkSmem {
+  uint32_t* hist;   // kHistWords counters, later sort counters
+  uint32_t* ck;     // candidates: keys
+  uint32_t* ci;     //             indices
+  uint32_t* tk;     // sort scratch
+  uint32_t* ti;
+  uint32_t* merged; // cluster kernel: the row's merged histogram
+};
+
+__device__ __forceinline__ TopkSmem topk_smem(uint8_t* smem, int cand_cap) {
+  TopkSmem m;
+  m.hist = reinterpret_cast<uint32_t*>(smem);
+  m.ck = m.hist + kHistWords;
+  m.ci = m.ck + cand_cap;
+  m.tk = m.ci + cand_cap;
+  m.ti = m.tk + cand_cap;
+  m.merged = m.ti + cand_cap;
+  return m;
+}
+
+struct RowInfo {
+  long long n;
+  const float* src;
+  int32_t* out;
+  int keep;
+};
+
+__device__ __forceinline__ RowInfo row_info(const TopkArgs& a, int r_local) {
+  RowInfo R;
+  if (!a.paged) {
+    const int t = r_local;
+    long long v = static_cast<long long>(a.q_pos0) + t + 1;
+    if (v > a.S) v = a.S;
+    R.n = v > 0 ? v : 0;
+    R.src = a.scores + static_cast<long long>(t) * a.ld;
+    R.out = a.topk + static_cast<long long>(t) * a.k_out;
+  } else {
+    const int r = a.row_base + r_local;
+    int lo = 0, hi = a.B;  // last b with cu_q_lens[b] <= r
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (a.cu_q_lens[mid] <= r) lo = mid; else hi = mid;
+    }
+    const int b = lo;
+    const int q_len = a.cu_q_lens[b + 1] - a.cu_q_lens[b];
+    const long long pos = static_cast<long long>(a.seq_lens[b]) - q_len + (r - a.cu_q_lens[b]);
+    R.n = pos + 1 > 0 ? pos + 1 : 0;
+    R.src = a.scores + static_cast<long long>(r_local) * a.ld;
+    R.out = a.topk + static_cast<long long>(r) * a.k_out;
+  }
+  if (R.n > a.max_n) R.n = a.max_n;
+  long long keep_ll = R.n;
+  if (keep_ll > a.topk_limit) keep_ll = a.topk_limit;
+  if (keep_ll > a.k_out) keep_ll = a.k_out;
+  R.keep = static_cast<int>(keep_ll);
+  return R;
+}
+
+// Final output from candidates (ck, ci) in index order:
+//   exact    -- the candidates are exactly the kept keys;
+//   otherwise every key of 12-bit bucket >= d1 (`want` still to take from bucket d1).
+__device__ void finish_row(const TopkSmem& m, uint32_t n_cand, bool exact, uint32_t d1, uint32_t want, int keep,
+                           bool by_score, int32_t* out, uint32_t* red, uint32_t* info) {
+  const int tid = threadIdx.x;
+  if (by_score) {
+    if (bucket_rank_out(m.ck, m.ci, static_cast<int>(n_cand), keep, m.tk, m.ti, m.hist, red, out)) return;
+    uint32_t *sk, *sv;
+    radix_sort_desc(m.ck, m.ci, m.tk, m.ti, static_cast<int>(n_cand), m.hist, red, &sk, &sv);
+    for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(sv[i]);
+    return;
+  }
+  if (exact) {
+    for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(m.ci[i]);
+    return;
+  }
+  uint32_t T, need;
+  const uint32_t nc = n_cand;
+  const uint32_t* ckp = m.ck;
+  auto feed_cand = [&](uint32_t* h, int shift, uint32_t mask, int pshift, uint32_t pre) {
+    for (uint32_t i = tid; i < nc; i += kThreads) {
+      const uint32_t u = ckp[i];
+      if ((u >> pshift) == pre) atomicAdd(&h[hslot((u >> shift) & mask)], 1u);
+    }
+  };
+  refine_threshold(feed_cand, d1, want, m.hist, red, info, &T, &need);
+  const int lane = tid & 31, warp = tid >> 5;
+  const uint32_t per = ((n_cand + kWarps - 1) / kWarps + 31) & ~31u;
+  const uint32_t c0 = warp * per, c1 = min(n_cand, c0 + per);
+  uint32_t cgt = 0, ceq = 0;
+  for (uint32_t i = c0 + lane; i < c1; i += 32) {
+    cgt += m.ck[i] > T ? 1u : 0u;
+    ceq += m.ck[i] == T ? 1u : 0u;
+  }
+  cgt = __reduce_add_sync(0xffffffffu, cgt);
+  ceq = __reduce_add_sync(0xffffffffu, ceq);
+  if (lane == 0) red[warp] = cgt;
+  __syncthreads();
+  uint32_t gbase = 0;
+  for (int w = 0; w < warp; ++w) gbase += red[w];
+  __syncthreads();
+  if (lane == 0) red[warp] = ceq;
+  __syncthreads();
+  uint32_t ebase = 0;
+  for (int w = 0; w < warp; ++w) ebase += red[w];
+  for (uint32_t i0 = c0; i0 < c1; i0 += 32) {
+    const uint32_t i = i0 + lane;
+    const bool valid = i < c1;
+    const uint32_t u = valid ? m.ck[i] : 0u;
+    const bool gt = valid && u > T, eq = valid && u == T;
+    const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+    const uint32_t lt = (1u << lane) - 1u;
+    const uint32_t g = gbase + __popc(bg & lt), e = ebase + __popc(be & lt);
+    if (gt) out[g + (e < need ? e : need)] = static_cast<int32_t>(m.ci[i]);
+    else if (eq && e < need) out[g + e] = static_cast<int32_t>(m.ci[i]);
+    gbase += __popc(bg);
+    ebase += __popc(be);
+  }
+}
+
+// The whole top-k of one row by one CTA, reading the row through RS.
+template <class RS>
+__device__ void row_topk(const RS& rs, long long n, int keep, bool by_score, int32_t* out, int cand_cap,
+                         const TopkSmem& m, uint32_t* red, uint32_t* info) {
+  const int tid = threadIdx.x;
+  uint32_t n_cand;
+  bool exact = true;
+  uint32_t d1 = 0, want = 0;
+  if (n <= keep) {
+    n_cand = seg_compact(rs, 0u, 0xFFFFFFFFu, m.ck, m.ci, red);  // every key
+  } else {
+    for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = 0;
+    __syncthreads();
+    seg_hist(rs, m.hist, 20, 4095u, 32, 0u);
+    __syncthreads();
+    find_bucket(m.hist, kBins, static_cast<uint32_t>(keep), red, info);
+    d1 = info[0];
+    const uint32_t above = info[1], in_b = info[2];
+    want = static_cast<uint32_t>(keep) - above;
+    if (in_b == want) {
+      n_cand = seg_compact(rs, (d1 << 20) - 1u, 0u, m.ck, m.ci, red);  // the whole bucket is kept
+    } else if (above + in_b <= static_cast<uint32_t>(cand_cap)) {
+      n_cand = seg_compact(rs, (d1 << 20) - 1u, 0u, m.ck, m.ci, red);  // every key of buckets >= d1
+      exact = false;
+    } else {
+      // huge threshold bucket: exact threshold over the row, exactly `keep` keys
+      uint32_t T, need;
+      auto feed_row = [&](uint32_t* h, int shift, uint32_t mask, int pshift, uint32_t pre) {
+        seg_hist(rs, h, shift, mask, pshift, pre);
+      };
+      refine_threshold(feed_row, d1, want, m.hist, red, info, &T, &need);
+      n_cand = seg_compact(rs, T, need, m.ck, m.ci, red);
+    }
+  }
+  finish_row(m, n_cand, exact, d1, want, keep, by_score, out, red, info);
+}
+
+template <int NB>  // NB > 0: rows up to kWarps * NB * 128 keys held in registers; 0: any length
+__global__ void __launch_bounds__(kThreads, NB == 8 ? 3 : 2) topk_kernel(const TopkArgs a, int cand_cap) {
+  ptx::grid_dep_wait();  // the scores come from the previous kernel on the stream
+  ptx::grid_dep_launch();
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ uint32_t red[2 * kWarps];
+  __shared__ uint32_t info[4];
+  const TopkSmem m = topk_smem(smem, cand_cap);
+  const RowInfo R = row_info(a, blockIdx.x);
+  for (int i = R.keep + threadIdx.x; i < a.k_out; i += kThreads) R.out[i] = -1;
+  if (R.keep == 0) return;
+  using RS = typename std::conditional<NB == 0, GlobalSeg, RegSeg<(NB > 0 ? NB : 1)>>::type;
+  RS rs;
+  rs.init(R.src, R.n);
+  row_topk(rs, R.n, R.keep, a.order == 0, R.out, cand_cap, m, red, info);
+}
+
+// ---------------------------------------------------------------- long rows: a cluster of CTAs per row
+
+__device__ __forceinline__ uint32_t dsmem_ld(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t mapa(const void* p, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(d)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void red_add_cluster(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Sum the CL local histograms (m.hist of every CTA) into m.merged of every CTA: each CTA
+// adds its non-zero bins into every CTA's merged histogram with remote atomics (a row's
+// keys fill a few hundred of the 4096 bins), between two cluster barriers.  Every CTA
+// zeroes its own m.merged before the call, after its last read of the previous merge.
+template <int CL>
+__device__ void cluster_merge_hist(const TopkSmem& m, uint32_t rank) {
+  cluster_barrier();  // every local histogram complete, every merged histogram zeroed
+  for (int b = threadIdx.x; b < kBins; b += kThreads) {
+    const uint32_t c = m.hist[hslot(b)];
+    if (c != 0) {
+#pragma unroll
+      for (int j = 0; j < CL; ++j) red_add_cluster(mapa(&m.merged[hslot(b)], static_cast<uint32_t>(j)), c);
+    }
+  }
+  cluster_barrier();  // every contribution has landed
+}
+
+template <int NB, int CL>  // CL CTAs per row, each holding up to kWarps * NB * 128 keys in registers
+__global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkArgs a, int cand_cap) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ uint32_t red[2 * kWarps];
+  __shared__ uint32_t info[4];
+  __shared__ uint32_t counts[CL];
+  const TopkSmem m = topk_smem(smem, cand_cap);
+  const uint32_t rank = cluster_rank();
+  const RowInfo R = row_info(a, blockIdx.x / CL);
+  const int tid = threadIdx.x;
+  if (rank == 0)
+    for (int i = R.keep + tid; i < a.k_out; i += kThreads) R.out[i] = -1;
+  if (R.keep == 0) return;  // the same decision in every CTA of the cluster
+  const bool by_score = a.order == 0;
+  // this CTA's contiguous part of the row
+  const long long part = ((R.n + CL - 1) / CL + 1023) & ~1023LL;
+  const long long lo = min(R.n, static_cast<long long>(rank) * part);
+  const long long len = min(R.n - lo, part);
+  RegSeg<NB> rs;
+  rs.init(R.src + lo, len);
+
+  const bool take_all = R.n <= R.keep;
+  uint32_t T = 0;         // candidates: keys > T (every key when take_all)
+  uint32_t d1 = 0, want = 0;
+  bool exact = take_all;
+  bool fallback = false;  // tie-heavy row: the first CTA finishes it alone
+  if (!take_all) {
+    for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = m.merged[i] = 0;
+    __syncthreads();
+    seg_hist(rs, m.hist, 20, 4095u, 32, 0u);
+    __syncthreads();
+    cluster_merge_hist<CL>(m, rank);
+    find_bucket(m.merged, kBins, static_cast<uint32_t>(R.keep), red, info);
+    d1 = info[0];
+    const uint32_t above = info[1], in_b = info[2];
+    want = static_cast<uint32_t>(R.keep) - above;
+    T = (d1 << 20) - 1u;
+    exact = in_b == want;
+    if (!exact && above + in_b > static_cast<uint32_t>(cand_cap)) {
+      // one more level, cluster-wide: bits 8..19 inside bucket d1
+      for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = m.merged[i] = 0;
+      __syncthreads();
+      seg_hist(rs, m.hist, 8, 4095u, 20, d1);
+      __syncthreads();
+      cluster_merge_hist<CL>(m, rank);
+      find_bucket(m.merged, kBins, want, red, info);
+      const uint32_t d2 = info[0], above2 = info[1], in_b2 = info[2];
+      const uint32_t pre = (d1 << 12) | d2;
+      T = (pre << 8) - 1u;  // candidates: top 24 bits >= pre
+      want -= above2;
+      exact = in_b2 == want;
+      if (!exact) {
+        // the threshold sits inside 24-bit bucket pre: keep that level for the refinement
+        if (above + above2 + in_b2 > static_cast<uint32_t>(cand_cap)) fallback = true;
+        d1 = pre;  // finish_row refines inside (top 24 bits == pre) below
+      }
+    }
+  }
+  if (fallback) {
+    cluster_barrier();
+    if (rank != 0) return;
+    GlobalSeg gs;
+    gs.init(R.src, R.n);
+    row_topk(gs, R.n, R.keep, by_score, R.out, cand_cap, m, red, info);
+    return;
+  }
+  // candidates of this CTA, counted, then written in index order into CTA 0's buffers
+  uint32_t cnt = 0;
+  rs.visit([&](const uint32_t (&u)[4], long long, int c) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cnt += (e < c && (take_all || u[e] > T)) ? 1u : 0u;
+  });
+  cnt = __reduce_add_sync(0xffffffffu, cnt);
+  const int lane = tid & 31, warp = tid >> 5;
+  if (lane == 0) red[warp] = cnt;
+  __syncthreads();
+  uint32_t wbase = 0, ctotal = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    wbase += w < warp ? red[w] : 0u;
+    ctotal += red[w];
+  }
+  if (tid == 0) dsmem_st(mapa(&counts[rank], 0), ctotal);
+  cluster_barrier();
+  uint32_t cbase = 0, n_cand = 0;
+  if (tid < CL) counts[tid] = rank == 0 ? counts[tid] : dsmem_ld(mapa(&counts[tid], 0));
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < CL; ++j) {
+    cbase += j < static_cast<int>(rank) ? counts[j] : 0u;
+    n_cand += counts[j];
+  }
+  const bool overflow = n_cand > static_cast<uint32_t>(cand_cap);  // same in every CTA
+  if (!overflow) {
+    const uint32_t ck0 = mapa(m.ck, 0), ci0 = mapa(m.ci, 0);
+    uint32_t base = cbase + wbase;
+    rs.visit([&](const uint32_t (&u)[4], long long i, int c) {
+      uint32_t msk = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) msk |= ((e < c && (take_all || u[e] > T)) ? 1u : 0u) << e;
+      const uint32_t k = __popc(msk);
+      const uint32_t incl = warp_incl_scan(k);
+      uint32_t pos = base + incl - k;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if ((msk >> e) & 1u) {
+          dsmem_st(ck0 + 4u * pos, u[e]);
+          dsmem_st(ci0 + 4u * pos, static_cast<uint32_t>(lo + i + e));
+          ++pos;
+        }
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    });
+  }
+  cluster_barrier();  // CTA 0 holds every candidate; nobody touches its memory after this
+  if (rank != 0) return;
+  if (overflow) {
+    GlobalSeg gs;
+    gs.init(R.src, R.n);
+    row_topk(gs, R.n, R.keep, by_score, R.out, cand_cap, m, red, info);
+    return;
+  }
+  if (!by_score && !exact && (d1 >> 12) != 0) {
+    // index order with a 24-bit threshold prefix: refine the last 8 bits on the candidates
+    uint32_t need;
+    const uint32_t nc = n_cand, pre = d1;
+    const uint32_t* ckp = m.ck;
+    for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = 0;
+    __syncthreads();
+    for (uint32_t i = tid; i < nc; i += kThreads)
+      if ((ckp[i] >> 8) == pre) atomicAdd(&m.hist[hslot(ckp[i] & 255u)], 1u);
+    __syncthreads();
+    find_bucket(m.hist, 256, want, red, info);
+    const uint32_t Tx = (pre << 8) | info[0];
+    need = want - info[1];
+    // keep key > Tx and the first `need` keys == Tx (candidates are in index order)
+    const uint32_t per = ((nc + kWarps - 1) / kWarps + 31) & ~31u;
+    const uint32_t c0 = warp * per, c1 = min(nc, c0 + per);
+    uint32_t cgt = 0, ceq = 0;
+    for (uint32_t i = c0 + lane; i < c1; i += 32) {
+      cgt += ckp[i] > Tx ? 1u : 0u;
+      ceq += ckp[i] == Tx ? 1u : 0u;
+    }
+    cgt = __reduce_add_sync(0xffffffffu, cgt);
+    ceq = __reduce_add_sync(0xffffffffu, ceq);
+    if (lane == 0) red[warp] = cgt;
+    __syncthreads();
+    uint32_t gb = 0;
+    for (int w = 0; w < warp; ++w) gb += red[w];
+    __syncthreads();
+    if (lane == 0) red[warp] = ceq;
+    __syncthreads();
+    uint32_t eb = 0;
+    for (int w = 0; w < warp; ++w) eb += red[w];
+    for (uint32_t i0 = c0; i0 < c1; i0 += 32) {
+      const uint32_t i = i0 + lane;
+      const bool valid = i < c1;
+      const uint32_t u = valid ? ckp[i] : 0u;
+      const bool gt = valid && u > Tx, eq = valid && u == Tx;
+      const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+      const uint32_t lt = (1u << lane) - 1u;
+      const uint32_t g = gb + __popc(bg & lt), e = eb + __popc(be & lt);
+      if (gt) R.out[g + (e < need ? e : need)] = static_cast<int32_t>(m.ci[i]);
+      else if (eq && e < need) R.out[g + e] = static_cast<int32_t>(m.ci[i]);
+      gb += __popc(bg);
+      eb += __popc(be);
+    }
+    return;
+  }
+  finish_row(m, n_cand, exact, d1, want, R.keep, by_score, R.out, red, info);
+}
+
+
+// cluster launch of topk_cluster_kernel<NB, CL>: one cluster of CL CTAs per row
+template <int NB, int CL>
+cudaError_t launch_cluster_rows(const TopkArgs& a, int ccap, size_t csmem, cudaStream_t st) {
+  auto kern = topk_cluster_kernel<NB, CL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(csmem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.n_rows) * CL, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = csmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_off() ? 1 : 2;
+  e = cudaLaunchKernelEx(&cfg, kern, a, ccap);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// one translation unit per cluster shape (they compile in parallel)
+cudaError_t launch_topk_cluster_8_4(const TopkArgs& a, int ccap, size_t csmem, cudaStream_t st);
+cudaError_t launch_topk_cluster_16_4(const TopkArgs& a, int ccap, size_t csmem, cudaStream_t st);
+cudaError_t launch_topk_cluster_16_8(const TopkArgs& a, int ccap, size_t csmem, cudaStream_t st);
+
+}  // namespace dsa
