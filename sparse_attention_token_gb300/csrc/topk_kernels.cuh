@@ -167,20 +167,26 @@ struct GlobalSeg {
 template <int NB>
 struct RegSeg {
   uint32_t v[NB][4];
-  int c[NB];
   long long s0;
+  int len;  // keys of this warp's segment
   int nb;
   __device__ void init(const float* row, long long n) {
     const long long seg = seg_len(n);
     s0 = (threadIdx.x >> 5) * seg;
     const long long s1 = min(n, s0 + seg);
-    nb = s1 > s0 ? static_cast<int>((s1 - s0 + 127) / 128) : 0;
+    len = s1 > s0 ? static_cast<int>(s1 - s0) : 0;
+    nb = (len + 127) / 128;
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
       const long long i = s0 + 128LL * j + 4 * (threadIdx.x & 31);
-      c[j] = (j < nb && i < s1) ? load4(row, s1, i, v[j]) : 0;
-      if (c[j] == 0) v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0u;
+      const int c = (j < nb && i < s1) ? load4(row, s1, i, v[j]) : 0;
+      if (c == 0) v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0u;
     }
+  }
+  // valid keys of block j for this lane (recomputed instead of held in registers)
+  __device__ __forceinline__ int count(int j) const {
+    const int r = len - 128 * j - 4 * static_cast<int>(threadIdx.x & 31);
+    return r < 0 ? 0 : (r > 4 ? 4 : r);
   }
   template <class F>
   __device__ __forceinline__ void visit(F f) const {
@@ -189,7 +195,7 @@ struct RegSeg {
     for (int j = 0; j < NB; ++j) {
       if (j < nb) {
         uint32_t u[4] = {v[j][0], v[j][1], v[j][2], v[j][3]};
-        f(u, s0 + 128LL * j + 4 * lane, c[j]);
+        f(u, s0 + 128LL * j + 4 * lane, count(j));
       }
     }
   }
@@ -539,6 +545,124 @@ __device__ __forceinline__ TopkSmem topk_smem(uint8_t* smem, int cand_cap) {
   return m;
 }
 
+// Score of an order-preserving key (inverse of order_key; -0.0 comes back as +0.0).
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Bucket of a score on a linear grid of kBins equal-width buckets between the row's
+// smallest score lo and its largest: floor((x - lo) * scale), at most kBins - 1.  Every
+// step is a correctly rounded IEEE operation (no contraction), so the bucket is a
+// non-decreasing function of x and the same key always lands in the same bucket.
+__device__ __forceinline__ uint32_t lin_bucket(uint32_t k, float lo, float scale) {
+  const float f = __fmul_rn(__fsub_rn(key_value(k), lo), scale);
+  const int b = __float2int_rz(f);
+  return static_cast<uint32_t>(b < kBins - 1 ? b : kBins - 1);
+}
+
+// Score-order top-k of a row held in registers, in one histogram: the keys are counted
+// in linear buckets between the row's extremes (Gaussian-like rows leave a few keys per
+// bucket around the threshold), a descending scan gives the threshold bucket and every
+// bucket's start, the keys of the buckets at and above the threshold go straight from
+// registers to their bucket's slots, and each one's final rank is its bucket's start
+// plus the bucket-mates that beat it (higher key, or the same key at a lower index).
+// Returns false, having written nothing, when a bucket at or above the threshold holds
+// more than kBucketLimit keys, the candidates overflow the buffers, or the row's scores
+// are all equal; the caller then takes the general path.
+template <int NB>
+__device__ bool linear_bucket_topk(const RegSeg<NB>& rs, long long n, int keep, int32_t* out, int cand_cap,
+                                   const TopkSmem& m, uint32_t* red, uint32_t* info) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the row's extreme keys
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  rs.visit([&](const uint32_t (&u)[4], long long, int c) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < c) { kmin = min(kmin, u[e]); kmax = max(kmax, u[e]); }
+  });
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) { red[warp] = kmin; red[kWarps + warp] = kmax; }
+  for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) { kmin = min(kmin, red[w]); kmax = max(kmax, red[kWarps + w]); }
+  const float lo = key_value(kmin), hi = key_value(kmax);
+  const float width = __fsub_rn(hi, lo);
+  const float scale = __fdiv_rn(static_cast<float>(kBins), width);
+  // all-equal rows, and ranges whose width or scale is not a positive finite number
+  if (!(width > 0.f) || !(scale > 0.f) || isinf(width) || isinf(scale)) return false;  // uniform: same inputs
+  rs.visit([&](const uint32_t (&u)[4], long long, int c) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < c) atomicAdd(&m.hist[hslot(lin_bucket(u[e], lo, scale))], 1u);
+  });
+  __syncthreads();
+  // descending exclusive scan: thread t owns bins 4095 - 16t .. 4080 - 16t, highest first.
+  // The threshold bucket d1 is where the running count from the top reaches keep; the
+  // buckets at and above it are exactly those that start below keep.
+  const uint32_t want = static_cast<uint32_t>(keep);
+  const int b_hi = kBins - 16 * tid;
+  uint32_t sum = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) sum += m.hist[hslot(static_cast<uint32_t>(b_hi - 1 - j))];
+  uint32_t tot;
+  uint32_t r = block_excl_scan(sum, red, &tot);
+  uint32_t mx = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t b = static_cast<uint32_t>(b_hi - 1 - j);
+    const uint32_t cj = m.hist[hslot(b)];
+    if (r < want) {
+      mx = max(mx, cj);
+      if (r + cj >= want) {
+        info[0] = b;       // d1
+        info[1] = r + cj;  // candidates: every key of the buckets >= d1
+      }
+    }
+    m.hist[hslot(b)] = r;  // start of bucket b (each thread rewrites only its own bins)
+    r += cj;
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  const uint32_t d1 = info[0], n_cand = info[1];
+  mx = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) mx = max(mx, red[w]);
+  // bw (n_cand 8-byte words) lives in tk and ti, 2 * cand_cap adjacent words
+  if (mx > static_cast<uint32_t>(kBucketLimit) || n_cand > static_cast<uint32_t>(cand_cap)) return false;
+  // scatter the candidates: key and complemented index in one word, so a larger word is a
+  // better key or the same key at a lower index
+  uint64_t* bw = reinterpret_cast<uint64_t*>(m.tk);
+  rs.visit([&](const uint32_t (&u)[4], long long i, int c4) {
+    const uint32_t i0 = static_cast<uint32_t>(i);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (e < c4) {
+        const uint32_t b = lin_bucket(u[e], lo, scale);
+        if (b >= d1) {
+          const uint32_t pos = atomicAdd(&m.hist[hslot(b)], 1u);
+          reinterpret_cast<uint2*>(bw)[pos] = make_uint2(~(i0 + e), u[e]);
+        }
+      }
+    }
+  });
+  __syncthreads();
+  // hist[b] is now the end of bucket b; bucket b starts where bucket b + 1 ends
+  for (uint32_t p = tid; p < n_cand; p += kThreads) {
+    const uint64_t x = bw[p];
+    const uint32_t b = lin_bucket(static_cast<uint32_t>(x >> 32), lo, scale);
+    const uint32_t q0 = b + 1 < static_cast<uint32_t>(kBins) ? m.hist[hslot(b + 1)] : 0u, q1 = m.hist[hslot(b)];
+    uint32_t rank = q0;
+    for (uint32_t q = q0; q < q1; ++q) rank += bw[q] > x ? 1u : 0u;
+    if (rank < want) m.ck[rank] = ~static_cast<uint32_t>(x);
+  }
+  __syncthreads();
+  for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(m.ck[i]);
+  return true;
+}
+
 struct RowInfo {
   long long n;
   const float* src;
@@ -689,6 +813,10 @@ __global__ void __launch_bounds__(kThreads, NB == 8 ? 3 : 2) topk_kernel(const T
   using RS = typename std::conditional<NB == 0, GlobalSeg, RegSeg<(NB > 0 ? NB : 1)>>::type;
   RS rs;
   rs.init(R.src, R.n);
+  if constexpr (NB > 0) {
+    if (a.order == 0 && linear_bucket_topk(rs, R.n, R.keep, R.out, cand_cap, m, red, info)) return;
+    __syncthreads();  // the general path reuses the shared buffers
+  }
   row_topk(rs, R.n, R.keep, a.order == 0, R.out, cand_cap, m, red, info);
 }
 
