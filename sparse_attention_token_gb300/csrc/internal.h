@@ -81,6 +81,9 @@ struct TopkArgs {
   long long max_n;     // no row reads more than this many entries
   int topk_limit, k_out, order;
   int32_t* topk;
+  // single-CTA rows: CTA i prefetches into L2 the row of CTA i + prefetch_ahead (about one
+  // wave of resident CTAs later); 0 = no prefetch
+  int prefetch_ahead;
 };
 
 // Programmatic dependent launch may be switched off for the calling host thread: the

@@ -18,7 +18,14 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    e = launch_pdl(kern, dim3(static_cast<unsigned>(a.n_rows)), dim3(kThreads), smem, st, a, cap);
+    TopkArgs b = a;
+    b.prefetch_ahead = 0;
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) == cudaSuccess)
+      b.prefetch_ahead = sms * per_sm;
+    e = launch_pdl(kern, dim3(static_cast<unsigned>(a.n_rows)), dim3(kThreads), smem, st, b, cap);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   };

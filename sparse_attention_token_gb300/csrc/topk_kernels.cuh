@@ -808,6 +808,13 @@ __global__ void __launch_bounds__(kThreads, NB == 8 ? 3 : 2) topk_kernel(const T
   __shared__ uint32_t info[4];
   const TopkSmem m = topk_smem(smem, cand_cap);
   const RowInfo R = row_info(a, blockIdx.x);
+  if (a.prefetch_ahead > 0 && threadIdx.x == 32 && blockIdx.x + a.prefetch_ahead < a.n_rows) {
+    // the row a later CTA on this part of the GPU will read: into L2 while this one works
+    const RowInfo P = row_info(a, blockIdx.x + a.prefetch_ahead);
+    const long long bytes = ((P.n + 3) & ~3LL) * 4;  // whole 16-byte units inside the row's ld
+    if (bytes > 0 && (reinterpret_cast<uintptr_t>(P.src) & 15u) == 0)
+      ptx::bulk_prefetch_l2(P.src, static_cast<uint32_t>(bytes));
+  }
   for (int i = R.keep + threadIdx.x; i < a.k_out; i += kThreads) R.out[i] = -1;
   if (R.keep == 0) return;
   using RS = typename std::conditional<NB == 0, GlobalSeg, RegSeg<(NB > 0 ? NB : 1)>>::type;
