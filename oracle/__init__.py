@@ -20,6 +20,8 @@ Contents:
     norm, RoPE, Hadamard rotation, per-row e4m3 quantisation.
   * ``sparse_mla`` (numpy, fp64): absorbed latent attention over each token's
     selected keys (the consumer of the top-k).
+  * ``sharded``: the key-sharded top-k -- each shard's best (score, index)
+    candidates, and the exact merge of the gathered candidates.
 
 Every function in this package is pinned by ``tests/test_oracle_pins.py``
 (hand-worked example, library special cases, invariants, brute force).

@@ -639,3 +639,63 @@ def test_frontend_hand_worked_values_tell_the_plausible_mistakes_apart():
     # and the right order, built from the same pieces, meets them
     eq, ek, _ = _frontend_golden_expected(g, "fp8")
     assert np.allclose(rot(rp(q0)), eq, atol=1e-12) and np.allclose(rot(rp(ln(k0))), ek, atol=1e-12)
+
+
+# ---------------------------------------------------------------- key-sharded top-k (oracle/sharded.py)
+
+from oracle import sharded  # noqa: E402
+
+
+def _sharded_case(seed, T=40, S=70, topk=12, q_pos0=30):
+    c = workloads.dense_case(T, S, 4, 64, topk, q_pos0=q_pos0, integer=True, int_range=(-1, 1),
+                             w_int_range=(-1, 1), seed=seed)
+    rt, rs, _ = oracle.dense(c.q, c.k, c.w, T=T, S=S, H=4, D=64, q_pos0=q_pos0, topk_limit=topk, k_out=topk + 3,
+                             want_scores=True)
+    n_vis = np.minimum(q_pos0 + np.arange(T) + 1, S)
+    return c, rt, rs, n_vis
+
+
+@pytest.mark.parametrize("bounds", [[0, 70], [0, 17, 40, 70], [0, 1, 2, 69, 70], [0, 35, 70]])
+@pytest.mark.parametrize("order", [oracle.ORDER_SCORE, oracle.ORDER_INDEX])
+def test_sharded_merge_equals_the_full_row_topk(bounds, order):
+    """Merging every shard's best k (score, index) candidates gives the C oracle's own
+    full-row top-k, bit for bit, with small-integer scores full of ties across shard
+    boundaries and rows that see none of some shards."""
+    topk = 12
+    c, rt, rs, n_vis = _sharded_case(seed=70 + len(bounds))
+    ref = oracle.dense(c.q, c.k, c.w, T=c.T, S=c.S, H=4, D=64, q_pos0=c.q_pos0, topk_limit=topk, k_out=topk + 3,
+                       order=order)[0]
+    cands = [sharded.shard_candidates(rs, n_vis, b0, b1 - b0, topk) for b0, b1 in zip(bounds[:-1], bounds[1:])]
+    cs = np.stack([x[0] for x in cands])
+    ci = np.stack([x[1] for x in cands])
+    got = sharded.merge_candidates(cs, ci, topk, topk + 3, order)
+    assert np.array_equal(got, ref)
+    # the shards' order in the gather does not matter
+    perm = np.random.default_rng(1).permutation(len(cands))
+    assert np.array_equal(sharded.merge_candidates(cs[perm], ci[perm], topk, topk + 3, order), ref)
+
+
+def test_shard_candidates_brute_force_ranks():
+    """Each shard candidate list against rank counting: key s of the shard sits at position
+    #{s' in the shard, visible: o[s'] > o[s], or o[s'] == o[s] and s' < s} when that is < k."""
+    c, rt, rs, n_vis = _sharded_case(seed=75, T=12, S=30, topk=5, q_pos0=5)
+    b0, L, k = 7, 11, 5
+    cs, ci = sharded.shard_candidates(rs, n_vis, b0, L, k)
+    for t in range(12):
+        vis = [s for s in range(b0, b0 + L) if s < n_vis[t]]
+        want = [-1] * k
+        for s in vis:
+            r = sum(1 for s2 in vis if rs[t, s2] > rs[t, s] or (rs[t, s2] == rs[t, s] and s2 < s))
+            if r < k:
+                want[r] = s
+        assert ci[t].tolist() == want
+        for i, s in enumerate(want):
+            assert (cs[t, i] == rs[t, s]) if s >= 0 else cs[t, i] == -np.inf
+
+
+def test_sharded_merge_treats_signed_zeros_as_equal():
+    # one shard holds +0.0 at key 9, the other -0.0 at key 3: equal scores, the lower index first
+    cs = np.array([[[0.0, -1.0]], [[-0.0, -np.inf]]])
+    ci = np.array([[[9, 4]], [[3, -1]]], dtype=np.int32)
+    assert sharded.merge_candidates(cs, ci, 3, 4).tolist() == [[3, 9, 4, -1]]
+    assert sharded.merge_candidates(cs, ci, 2, 2, sharded.ORDER_INDEX).tolist() == [[3, 9]]
