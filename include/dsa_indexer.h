@@ -292,6 +292,52 @@ dsa_status dsa_indexer_dense_host(const void* q_host, int q_dtype, const float* 
                                   dsa_stream_t stream);
 
 /*
+ * Key-sharded top-k (GLM5 LoRA blog, section 3.1, 训练侧: context parallelism; a top-k
+ * taken per shard of a long sequence matches the full-sequence top-k only 68 % of the
+ * time, gathering the shards' indexer results 99.97 %).  The exact form: every shard of
+ * keys keeps its best min(k, visible) keys as (score, global index) candidates in
+ * (score desc, index asc) order; the caller gathers the candidates of all shards (for
+ * shards on several devices, one all-gather of [T, k_cand] indices and scores per
+ * shard); dsa_indexer_merge_candidates keeps the best of their union under the same
+ * order, which equals the top-k of the whole row.
+ *
+ * dsa_indexer_shard_candidates -- one shard's candidates.
+ *   q, q_scale, w, H, D, dtypes   as dsa_indexer_scores; query t at position q_pos0 + t
+ *   k_shard [S, D], k_scale [S]   the shard's keys: global key positions
+ *                                 key_offset .. key_offset + S - 1 (query t sees global key
+ *                                 g when g <= q_pos0 + t)
+ *   k_cand                        candidates per row, 1..DSA_MAX_TOPK (use the top-k width)
+ *   cand_idx [T, k_cand] int32    out: global key indices, then -1
+ *   cand_scores [T, k_cand] fp32  out: their scores, then -inf
+ *   workspace                     16-byte aligned device scratch of at least
+ *                                 dsa_indexer_shard_candidates_workspace_size(T, S) bytes
+ *                                 (the shard's fp32 score rows), caller-owned
+ * q_pos0 >= 0, key_offset >= 0.  Same element types, H, D and errors as
+ * dsa_indexer_scores; a missing or small workspace is DSA_ERR_WORKSPACE.
+ */
+dsa_status dsa_indexer_shard_candidates_workspace_size(int T, int S, size_t* bytes);
+dsa_status dsa_indexer_shard_candidates(const void* q, int q_dtype, const float* q_scale, const void* k_shard,
+                                        int k_dtype, const float* k_scale, const float* w, int T, int S, int H,
+                                        int D, int q_pos0, int key_offset, int k_cand, int32_t* cand_idx,
+                                        float* cand_scores, void* workspace, size_t workspace_bytes,
+                                        dsa_stream_t stream);
+
+/*
+ * dsa_indexer_merge_candidates -- the top-k of the union of n_shards candidate lists.
+ *   cand_scores [n_shards, T, k_cand] fp32, cand_idx [n_shards, T, k_cand] int32: list j
+ *   of row t holds shard j's candidates as written by dsa_indexer_shard_candidates
+ *   (valid entries first, in (score desc, index asc) order, then index -1); the shards'
+ *   key ranges must not overlap.
+ *   topk [T, k_out] int32 out: min(topk_limit, valid candidates) indices in `order`,
+ *   then -1.
+ * 1 <= n_shards <= 32, n_shards * k_cand <= 16384, 1 <= k_out <= DSA_MAX_TOPK.  Ties go
+ * to the lower key index; -0.0 and +0.0 are equal.
+ */
+dsa_status dsa_indexer_merge_candidates(const float* cand_scores, const int32_t* cand_idx, int n_shards, int T,
+                                        int k_cand, int topk_limit, int k_out, int order, int32_t* topk,
+                                        dsa_stream_t stream);
+
+/*
  * dsa_indexer_static -- dsa_indexer for callers that cannot allocate device memory.
  * The pages have no counterpart of this entry point; it exists for library users.
  *

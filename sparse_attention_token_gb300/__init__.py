@@ -118,6 +118,12 @@ def lib():
         L.dsa_indexer_dense_host_workspace_size.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(S)]
         L.dsa_indexer_dense_host.restype = I
         L.dsa_indexer_dense_host.argtypes = [P, I, P, P, I, P, P, I, I, I, I, I, I, I, I, I, P, P, S, P]
+        L.dsa_indexer_shard_candidates_workspace_size.restype = I
+        L.dsa_indexer_shard_candidates_workspace_size.argtypes = [I, I, ctypes.POINTER(S)]
+        L.dsa_indexer_shard_candidates.restype = I
+        L.dsa_indexer_shard_candidates.argtypes = [P, I, P, P, I, P, P, I, I, I, I, I, I, I, P, P, P, S, P]
+        L.dsa_indexer_merge_candidates.restype = I
+        L.dsa_indexer_merge_candidates.argtypes = [P, P, I, I, I, I, I, I, P, P]
         L.dsa_test_arm_score_timeout.restype = I
         L.dsa_test_arm_score_timeout.argtypes = [ctypes.c_ulonglong]
         _LIB = L
@@ -502,6 +508,79 @@ def dsa_indexer_stack(indexer_types: Sequence, full_layer_args: Sequence, stream
                                  _stream_ptr(stream))
     _check(st, "dsa_indexer_stack")
     return [outs[i] for i in range(L)], list(src[:L])
+
+
+# ---- key-sharded top-k (GLM5 LoRA blog, section 3.1: context parallelism) ---------------
+
+def dsa_indexer_shard_candidates(q: torch.Tensor, k_shard: torch.Tensor, w: torch.Tensor, *, q_pos0: int,
+                                 key_offset: int, k_cand: int, q_scale: Optional[torch.Tensor] = None,
+                                 k_scale: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                                 stream=None):
+    """One key shard's candidates: (cand_idx [T, k_cand] int32 global indices then -1,
+    cand_scores [T, k_cand] fp32 then -inf) for keys key_offset .. key_offset + S - 1."""
+    T, H, D = q.shape
+    S = k_shard.shape[0]
+    _expect([(k_shard, "k_shard", (S, D)), (w, "w", (T, H)), (q_scale, "q_scale", (T, H)),
+             (k_scale, "k_scale", (S,))])
+    nbytes = ctypes.c_size_t(0)
+    _check(lib().dsa_indexer_shard_candidates_workspace_size(T, S, ctypes.byref(nbytes)),
+           "dsa_indexer_shard_candidates_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(max(nbytes.value, 16), dtype=torch.uint8, device=q.device)
+    cand_idx = torch.empty((T, k_cand), dtype=torch.int32, device=q.device)
+    cand_scores = torch.empty((T, k_cand), dtype=torch.float32, device=q.device)
+    _check(lib().dsa_indexer_shard_candidates(
+        _dev(q, "q"), _dtype_code(q), _dev(q_scale, "q_scale", torch.float32), _dev(k_shard, "k_shard"),
+        _dtype_code(k_shard), _dev(k_scale, "k_scale", torch.float32), _dev(w, "w", torch.float32), T, S, H, D,
+        int(q_pos0), int(key_offset), int(k_cand), cand_idx.data_ptr(), cand_scores.data_ptr(),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+        "dsa_indexer_shard_candidates")
+    return cand_idx, cand_scores
+
+
+def dsa_indexer_merge_candidates(cand_scores: torch.Tensor, cand_idx: torch.Tensor, *, topk_limit: int,
+                                 k_out: Optional[int] = None, order: int = DSA_ORDER_SCORE,
+                                 topk: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Top-k [T, k_out] of the union of the shards' candidates [n_shards, T, k_cand]."""
+    n_shards, T, k_cand = cand_idx.shape
+    k_out = topk_limit if k_out is None else k_out
+    _expect([(cand_scores, "cand_scores", (n_shards, T, k_cand))])
+    if topk is None:
+        topk = torch.empty((T, k_out), dtype=torch.int32, device=cand_idx.device)
+    _expect([(topk, "topk", (T, k_out))])
+    _check(lib().dsa_indexer_merge_candidates(
+        _dev(cand_scores, "cand_scores", torch.float32), _dev(cand_idx, "cand_idx", torch.int32), n_shards, T,
+        k_cand, int(topk_limit), int(k_out), int(order), _dev(topk, "topk", torch.int32), _stream_ptr(stream)),
+        "dsa_indexer_merge_candidates")
+    return topk
+
+
+def gather_shard_candidates(cand_idx: torch.Tensor, cand_scores: torch.Tensor, group=None):
+    """The candidates of every rank of `group`, stacked in rank order: ([world, T, k] int32,
+    [world, T, k] fp32).  One all-gather of indices and one of scores (torch.distributed;
+    NCCL for device tensors, gloo for host tensors)."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    idx = [torch.empty_like(cand_idx) for _ in range(world)]
+    sc = [torch.empty_like(cand_scores) for _ in range(world)]
+    dist.all_gather(idx, cand_idx.contiguous(), group=group)
+    dist.all_gather(sc, cand_scores.contiguous(), group=group)
+    return torch.stack(idx), torch.stack(sc)
+
+
+def dsa_indexer_key_sharded(q: torch.Tensor, k_shard: torch.Tensor, w: torch.Tensor, *, q_pos0: int,
+                            key_offset: int, topk_limit: int, k_out: Optional[int] = None,
+                            order: int = DSA_ORDER_SCORE, q_scale: Optional[torch.Tensor] = None,
+                            k_scale: Optional[torch.Tensor] = None, group=None, stream=None) -> torch.Tensor:
+    """Top-k over a sequence whose keys are split over the ranks of `group` (each rank holds
+    the queries and its own contiguous key shard): local candidates, one all-gather, merge."""
+    k_out = topk_limit if k_out is None else k_out
+    ci, cs = dsa_indexer_shard_candidates(q, k_shard, w, q_pos0=q_pos0, key_offset=key_offset,
+                                          k_cand=min(topk_limit, k_out), q_scale=q_scale, k_scale=k_scale,
+                                          stream=stream)
+    all_idx, all_sc = gather_shard_candidates(ci, cs, group)
+    return dsa_indexer_merge_candidates(all_sc, all_idx, topk_limit=topk_limit, k_out=k_out, order=order,
+                                        stream=stream)
 
 
 def dsa_test_arm_score_timeout(limit_ns: int) -> None:

@@ -550,7 +550,29 @@ int dsa_topk_width(int topk_limit, int64_t active_seq_len) {
 dsa_status dsa_indexer_scores(const void* q, int q_dtype, const float* q_scale, const void* k, int k_dtype,
                               const float* k_scale, const float* w, int T, int S, int H, int D, int q_pos0,
                               float* scores, int64_t ld_scores, dsa_stream_t stream) {
-  if (T < 0 || S < 0 || q_pos0 < 0 || H <= 0 || D <= 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (q_pos0 < 0) return DSA_ERR_INVALID_ARGUMENT;
+  return dense_scores(q, q_dtype, q_scale, k, k_dtype, k_scale, w, T, S, H, D, q_pos0, scores, ld_scores,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+dsa_status dsa_indexer_topk(const float* scores, int64_t ld_scores, int T, int S, int q_pos0, int topk_limit,
+                            int k_out, int order, int32_t* topk, dsa_stream_t stream) {
+  if (q_pos0 < 0) return DSA_ERR_INVALID_ARGUMENT;
+  return dense_topk(scores, ld_scores, T, S, q_pos0, topk_limit, k_out, order, topk,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace dsa {
+
+// Dense scoring of T queries (query t at position q_pos0 + t) against keys 0..S-1.  q_pos0
+// may be negative: the key-sharded entry points score a shard whose first key sits after
+// some queries (those rows see none of its keys).
+dsa_status dense_scores(const void* q, int q_dtype, const float* q_scale, const void* k, int k_dtype,
+                        const float* k_scale, const float* w, int T, int S, int H, int D, int q_pos0,
+                        float* scores, int64_t ld_scores, cudaStream_t stream) {
+  if (T < 0 || S < 0 || H <= 0 || D <= 0) return DSA_ERR_INVALID_ARGUMENT;
   if (T == 0 || S == 0) return DSA_OK;
   if (!q || !k || !w || !scores) return DSA_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(k) || !aligned16(w) || !aligned16(scores) || (q_scale && !aligned16(q_scale)) ||
@@ -596,16 +618,17 @@ dsa_status dsa_indexer_scores(const void* q, int q_dtype, const float* q_scale, 
   const int ns = std::max(num_sms(), 1);
   if (pair) {
     const int pairs = std::max(1, std::min(ns / 2, a.n_dense_items));
-    return from_cuda(launch_score_pair(a, &tq, &tk, 2 * pairs, score_pair_launch_smem(a),
-                                       reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_score_pair(a, &tq, &tk, 2 * pairs, score_pair_launch_smem(a), stream));
   }
   const int grid = std::min(ns, a.n_dense_items);
-  return from_cuda(launch_score(a, &tq, &tk, grid, score_launch_smem(a), reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_score(a, &tq, &tk, grid, score_launch_smem(a), stream));
 }
 
-dsa_status dsa_indexer_topk(const float* scores, int64_t ld_scores, int T, int S, int q_pos0, int topk_limit,
-                            int k_out, int order, int32_t* topk, dsa_stream_t stream) {
-  if (T < 0 || S < 0 || q_pos0 < 0 || topk_limit < 1 || k_out < 1) return DSA_ERR_INVALID_ARGUMENT;
+// Top-k of dense score rows: row t sees entries 0 .. min(q_pos0 + t, S - 1) (none when
+// q_pos0 + t < 0).
+dsa_status dense_topk(const float* scores, int64_t ld_scores, int T, int S, int q_pos0, int topk_limit, int k_out,
+                      int order, int32_t* topk, cudaStream_t stream) {
+  if (T < 0 || S < 0 || topk_limit < 1 || k_out < 1) return DSA_ERR_INVALID_ARGUMENT;
   if (order != DSA_ORDER_SCORE && order != DSA_ORDER_INDEX) return DSA_ERR_INVALID_ARGUMENT;
   if (k_out > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
   if (T == 0) return DSA_OK;
@@ -624,9 +647,12 @@ dsa_status dsa_indexer_topk(const float* scores, int64_t ld_scores, int T, int S
   t.order = order;
   t.topk = topk;
   const long long longest = std::min<long long>(S, static_cast<long long>(q_pos0) + T);
-  return from_cuda(launch_topk(t, static_cast<int>(std::max<long long>(longest, 1)),
-                               reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_topk(t, static_cast<int>(std::max<long long>(longest, 1)), stream));
 }
+
+}  // namespace dsa
+
+extern "C" {
 
 dsa_status dsa_indexer_workspace_size(const dsa_indexer_args* args, size_t* bytes) {
   if (!bytes) return DSA_ERR_INVALID_ARGUMENT;

@@ -9,6 +9,8 @@
 
 #include <utility>
 
+#include "dsa_indexer.h"
+
 namespace dsa {
 
 // Bits of the device status word (library-owned __device__ variable).
@@ -156,6 +158,13 @@ struct PrepareLaunch {
   unsigned* status;
 };
 cudaError_t launch_prepare(const PrepareLaunch& p, cudaStream_t st);
+// Dense scoring and top-k of one sequence (the bodies of dsa_indexer_scores and
+// dsa_indexer_topk, with q_pos0 allowed to be negative: rows before the first key see none).
+dsa_status dense_scores(const void* q, int q_dtype, const float* q_scale, const void* k, int k_dtype,
+                        const float* k_scale, const float* w, int T, int S, int H, int D, int q_pos0, float* scores,
+                        int64_t ld_scores, cudaStream_t stream);
+dsa_status dense_topk(const float* scores, int64_t ld_scores, int T, int S, int q_pos0, int topk_limit, int k_out,
+               int order, int32_t* topk, cudaStream_t stream);
 // bf16 q rows [rows = total_q * H, 128] -> q8 [total_q, 2H, 128] e4m3 (hi rows, then lo
 // rows, per query) with a power-of-two scale s per row, and w8 = w / s.
 cudaError_t launch_qsplit(const void* q, const float* w, long long rows, int H, void* q8, float* w8,

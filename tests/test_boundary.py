@@ -349,3 +349,45 @@ def test_seeded_workloads_repeat_byte_for_byte():
     s1 = workloads.sparse_mla_case([50], [2], 2, 8, kv_rank=16, rope_dim=8, page_size=16, seed=4)
     s2 = workloads.sparse_mla_case([50], [2], 2, 8, kv_rank=16, rope_dim=8, page_size=16, seed=4)
     assert torch.equal(s1.topk, s2.topk) and torch.equal(s1.cache_c, s2.cache_c)
+
+
+def test_sharded_validation(dsa):
+    L = dsa.lib()
+    fake = 1 << 20  # never dereferenced: every call below fails validation first
+    import ctypes
+    n = ctypes.c_size_t(0)
+    assert L.dsa_indexer_shard_candidates_workspace_size(10, 13, ctypes.byref(n)) == dsa.DSA_OK
+    assert n.value == 10 * 16 * 4                                     # rows of ceil4(S) fp32 scores
+    assert L.dsa_indexer_shard_candidates_workspace_size(-1, 13, ctypes.byref(n)) == dsa.DSA_ERR_INVALID_ARGUMENT
+
+    def shard(**kw):
+        a = dict(q=fake, qd=0, qs=None, k=fake, kd=0, ks=None, w=fake, T=4, S=8, H=64, D=128, p0=4, off=8, kc=4,
+                 ci=fake, cs=fake, ws=fake, wsb=4 * 8 * 4, st=None)
+        a.update(kw)
+        return L.dsa_indexer_shard_candidates(a["q"], a["qd"], a["qs"], a["k"], a["kd"], a["ks"], a["w"], a["T"],
+                                              a["S"], a["H"], a["D"], a["p0"], a["off"], a["kc"], a["ci"], a["cs"],
+                                              a["ws"], a["wsb"], a["st"])
+    assert shard(off=-1) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert shard(p0=-1) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert shard(kc=0) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert shard(kc=5000) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert shard(ci=None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert shard(ws=None) == dsa.DSA_ERR_WORKSPACE
+    assert shard(wsb=16) == dsa.DSA_ERR_WORKSPACE
+    assert shard(ws=fake + 4) == dsa.DSA_ERR_WORKSPACE
+    assert shard(H=48) == dsa.DSA_ERR_UNSUPPORTED
+    assert shard(T=0) == dsa.DSA_OK
+
+    def merge(**kw):
+        a = dict(cs=fake, ci=fake, n=2, T=4, kc=8, lim=8, ko=8, order=0, out=fake, st=None)
+        a.update(kw)
+        return L.dsa_indexer_merge_candidates(a["cs"], a["ci"], a["n"], a["T"], a["kc"], a["lim"], a["ko"],
+                                              a["order"], a["out"], a["st"])
+    assert merge(n=0) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert merge(n=33) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert merge(lim=0) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert merge(order=3) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert merge(ko=5000) == dsa.DSA_ERR_UNSUPPORTED
+    assert merge(n=3, kc=8192) == dsa.DSA_ERR_UNSUPPORTED              # more than 16384 per row
+    assert merge(out=None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert merge(T=0) == dsa.DSA_OK
