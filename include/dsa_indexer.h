@@ -21,8 +21,8 @@
  *    caller; the library keeps none of them after returning and allocates no
  *    device memory per call.  Held for the process lifetime once first used on a
  *    device: the fixed scratch array of dsa_indexer_static, the streams and events
- *    of dsa_indexer_dense_host, and the streams, events and three cuBLAS handles
- *    (with the workspaces cuBLAS keeps) of dsa_indexer_prepare.  Pointers named
+ *    of dsa_indexer_dense_host, and the streams and events of dsa_indexer_prepare.
+ *    Pointers named
  *    types / src / full_args / topk_out are host.
  *  - All work is enqueued on `stream` (NULL = legacy default stream) and is
  *    asynchronous; nothing synchronises except dsa_check_device_status.
@@ -225,10 +225,12 @@ dsa_status dsa_indexer_cache_append(const void* k_new, int n, int D, const int64
  * weights_proj [H, hidden_dim] bf16; rope_cos / rope_sin [T, rope_dim/2] fp32;
  * k_norm_weight [D] fp32, k_norm_bias [D] fp32 or NULL.  D = 128; H a power of two up to
  * 128; rope_dim even, at most D, a multiple of 8 unless interleaved; hidden_dim and
- * q_rank multiples of 8.  The three projections run as bf16 GEMMs with fp32 results and
- * fp32 accumulation (cuBLAS, one library handle per device, created on first use); the
- * rest runs in the library's kernels.  workspace: dsa_indexer_prepare_workspace_size
- * bytes of device memory (fp32 q and k before the row kernels), not shared with
+ * q_rank multiples of 8.  The three projections run on the tensor cores as bf16
+ * products with fp32 accumulation, in the library's kernels like everything else; with
+ * 512 tokens or more and rope_dim 0, 64 or 128 the q projection finishes its rows
+ * (RoPE, rotation, quantisation) in its own epilogue.  workspace:
+ * dsa_indexer_prepare_workspace_size bytes of device memory (the fp32 partial sums of
+ * the projections that are not finished in their epilogue), not shared with
  * overlapping work.  Slots past the cache are skipped and reported through
  * dsa_check_device_status; negative slots are skipped.
  */

@@ -709,11 +709,7 @@ dsa_status dsa_indexer_cache_append(const void* k_new, int n, int D, const int64
 }
 
 namespace {
-struct PrepPlan {
-  size_t off_q, off_k, total;
-};
-
-dsa_status plan_prepare(const dsa_indexer_prepare_args* a, PrepPlan* p) {
+dsa_status plan_prepare(const dsa_indexer_prepare_args* a, PreparePlan* p) {
   if (!a) return DSA_ERR_INVALID_ARGUMENT;
   if (a->T < 0 || a->hidden_dim <= 0 || a->q_rank <= 0 || a->H <= 0 || a->D <= 0 || a->page_size <= 0 ||
       a->num_pages < 0 || a->rope_dim < 0 || a->rope_dim > a->D || (a->rope_dim & 1) || !(a->k_norm_eps >= 0.f))
@@ -722,17 +718,14 @@ dsa_status plan_prepare(const dsa_indexer_prepare_args* a, PrepPlan* p) {
   if (a->D != 128 || !supported_h(a->H) || (a->hidden_dim & 7) || (a->q_rank & 7)) return DSA_ERR_UNSUPPORTED;
   if (!a->rope_interleaved && (a->rope_dim & 7)) return DSA_ERR_UNSUPPORTED;
   if (static_cast<long long>(a->T) * a->H > INT_MAX) return DSA_ERR_UNSUPPORTED;
-  p->off_q = 0;
-  const size_t qb = static_cast<size_t>(a->T) * a->H * a->D * 4;
-  p->off_k = (qb + 255) / 256 * 256;
-  p->total = p->off_k + (static_cast<size_t>(a->T) * a->D * 4 + 255) / 256 * 256;
+  *p = plan_prepare_launch(a->T, a->hidden_dim, a->q_rank, a->H, a->D, a->rope_dim);
   return DSA_OK;
 }
 }  // namespace
 
 dsa_status dsa_indexer_prepare_workspace_size(const dsa_indexer_prepare_args* a, size_t* bytes) {
   if (!bytes) return DSA_ERR_INVALID_ARGUMENT;
-  PrepPlan p;
+  PreparePlan p;
   const dsa_status st = plan_prepare(a, &p);
   if (st != DSA_OK) return st;
   *bytes = p.total;
@@ -740,7 +733,7 @@ dsa_status dsa_indexer_prepare_workspace_size(const dsa_indexer_prepare_args* a,
 }
 
 dsa_status dsa_indexer_prepare(const dsa_indexer_prepare_args* a, dsa_stream_t stream) {
-  PrepPlan p;
+  PreparePlan p;
   dsa_status st = plan_prepare(a, &p);
   if (st != DSA_OK) return st;
   if (a->T == 0) return DSA_OK;
@@ -788,7 +781,9 @@ dsa_status dsa_indexer_prepare(const dsa_indexer_prepare_args* a, dsa_stream_t s
   L.w_out = a->w_out;
   L.Qf = reinterpret_cast<float*>(ws + p.off_q);
   L.Kf = reinterpret_cast<float*>(ws + p.off_k);
+  L.Wp = reinterpret_cast<float*>(ws + p.off_w);
   L.status = status;
+  L.plan = p;
   return from_cuda(launch_prepare(L, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -4,9 +4,12 @@
 // GLM5 TensorCast adaptation design, "DSA Indexer 融合语义算子" (the op's inputs:
 // hidden_states, qa_normed, RoPE cos / sin, wq_b, wk, weights_proj, k_norm weight,
 // indexer cache, slot_mapping) and its performance-model buckets 1-5, 9 and 10:
-//   1-3  q = qa_normed @ wq_b^T, k = hidden @ wk^T, w = hidden @ weights_proj^T: plain
-//        bf16 GEMMs with fp32 results (cuBLAS, fp32 accumulation), the three chains on
-//        the caller's stream and two library-owned streams;
+//   1-3  q = qa_normed @ wq_b^T, k = hidden @ wk^T, w = hidden @ weights_proj^T: bf16
+//        products with fp32 accumulation on the tensor cores (proj_gemm.cu), the three
+//        chains on the caller's stream and two library-owned streams; with enough tokens
+//        the q projection finishes its rows (RoPE, rotation, quantisation) in its own
+//        epilogue, otherwise it writes fp32 rows (split over K when the tokens are few)
+//        for the q row kernel below;
 //   4    RoPE on the first rope_dim values of every q head and of k;
 //   5    FP8 cache only: the Walsh-Hadamard rotation (Sylvester order, times D^-1/2) of
 //        q and k, then per-row e4m3 quantisation (scale = amax / 448);
@@ -15,14 +18,15 @@
 // optional bias).  One warp per row of D = 128 values: lane l holds values 4l..4l+3,
 // so the Hadamard butterflies with distance 1 and 2 stay in the thread and the other
 // five use shuffles; RoPE's half-split pairs are one shuffle of a value quad away.
-#include <cublas_v2.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "dsa_indexer.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dsa {
 namespace {
@@ -117,7 +121,8 @@ __device__ __forceinline__ uint2 to_bf16x4(const float (&x)[4]) {
 }
 
 // q rows: Qf [T * H, 128] fp32 -> q_out (bf16 or e4m3 with q_scale).
-__global__ void __launch_bounds__(kFrontWarps * 32) frontend_q_kernel(const float* __restrict__ Qf, long long rows,
+__global__ void __launch_bounds__(kFrontWarps * 32) frontend_q_kernel(const float* __restrict__ Qf, int planes,
+                                                                      long long rows,
                                                                       int H, const float* __restrict__ cosb,
                                                                       const float* __restrict__ sinb, int rope_dim,
                                                                       int interleaved, int fp8, void* q_out,
@@ -126,8 +131,13 @@ __global__ void __launch_bounds__(kFrontWarps * 32) frontend_q_kernel(const floa
   const long long r = static_cast<long long>(blockIdx.x) * kFrontWarps + (threadIdx.x >> 5);
   if (r >= rows) return;
   const long long t = r >> (31 - __clz(H));  // H is a power of two: no 64-bit division
-  const float4 v = reinterpret_cast<const float4*>(Qf + r * 128)[lane];
-  float x[4] = {v.x, v.y, v.z, v.w};
+  ptx::grid_dep_wait();  // Qf comes from the projection kernel before this one
+  ptx::grid_dep_launch();
+  float x[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int pl = 0; pl < planes; ++pl) {  // the K splits' partial sums, in order
+    const float4 v = reinterpret_cast<const float4*>(Qf + (pl * rows + r) * 128)[lane];
+    x[0] += v.x; x[1] += v.y; x[2] += v.z; x[3] += v.w;
+  }
   const long long half = rope_dim / 2;
   rope_row(x, cosb + t * half, sinb + t * half, rope_dim, interleaved != 0, lane);
   if (fp8) {
@@ -143,12 +153,14 @@ __global__ void __launch_bounds__(kFrontWarps * 32) frontend_q_kernel(const floa
 
 // k rows: Kf [T, 128] fp32 -> layer norm, RoPE, (Hadamard, quantisation) -> cache slot.
 __global__ void __launch_bounds__(kFrontWarps * 32) frontend_k_kernel(
-    const float* __restrict__ Kf, int T, const float* __restrict__ cosb, const float* __restrict__ sinb,
+    const float* __restrict__ Kf, int planes, int T, const float* __restrict__ cosb, const float* __restrict__ sinb,
     int rope_dim, int interleaved, const float* __restrict__ ln_w, const float* __restrict__ ln_b, float eps,
     int fp8, const int64_t* __restrict__ slots, void* cache, float* __restrict__ scale_cache, long long n_slots,
     unsigned* status) {
   const int lane = threadIdx.x & 31;
   const long long t = static_cast<long long>(blockIdx.x) * kFrontWarps + (threadIdx.x >> 5);
+  ptx::grid_dep_wait();  // Kf comes from the projection kernel before this one
+  ptx::grid_dep_launch();
   if (t >= T) return;
   const long long slot = slots[t];
   if (slot < 0) return;  // padding token
@@ -156,8 +168,11 @@ __global__ void __launch_bounds__(kFrontWarps * 32) frontend_k_kernel(
     if (lane == 0) atomicOr(status, kStatusBadPage);
     return;
   }
-  const float4 v = reinterpret_cast<const float4*>(Kf + t * 128)[lane];
-  float x[4] = {v.x, v.y, v.z, v.w};
+  float x[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int pl = 0; pl < planes; ++pl) {  // the K splits' partial sums, in order
+    const float4 v = reinterpret_cast<const float4*>(Kf + (pl * static_cast<long long>(T) + t) * 128)[lane];
+    x[0] += v.x; x[1] += v.y; x[2] += v.z; x[3] += v.w;
+  }
   const float mean = warp_sum((x[0] + x[1]) + (x[2] + x[3])) * 0.0078125f;  // / 128, exact
   float d2 = 0.f;
 #pragma unroll
@@ -189,12 +204,22 @@ __global__ void __launch_bounds__(kFrontWarps * 32) frontend_k_kernel(
   }
 }
 
-// Per device: three cuBLAS handles (one per stream the front-end uses, so no two
-// concurrent GEMMs share a handle's workspace), two library-owned streams and the
-// fork / join events.  Created on first use; calls on one device are serialised.
+// w [n] = the sum of `planes` partial planes of n values, in order.
+__global__ void sum_planes_kernel(const float* __restrict__ P, int planes, long long n, float* __restrict__ out) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float s = 0.f;
+    for (int pl = 0; pl < planes; ++pl) s += P[pl * n + i];
+    out[i] = s;
+  }
+}
+
+// Per device: two library-owned streams and the fork / join events.  Created on first
+// use; calls on one device are serialised.
 struct FrontCtx {
   bool ready = false;
-  cublasHandle_t blas[3] = {};
   cudaStream_t side[2] = {};
   cudaEvent_t fork = nullptr, join[2] = {};
 };
@@ -203,8 +228,6 @@ FrontCtx g_front[64];
 
 bool front_ctx_init(FrontCtx& c) {
   if (c.ready) return true;
-  for (auto& h : c.blas)
-    if (!h && cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) return false;
   for (auto& st : c.side)
     if (!st && cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return false;
   const unsigned f = cudaEventDisableTiming;
@@ -215,49 +238,53 @@ bool front_ctx_init(FrontCtx& c) {
   return true;
 }
 
-// C[M, N] = A[M, K] (bf16, row-major) times W[N, K]^T (bf16, row-major), fp32 result
-// and accumulation.  Row-major C is column-major C^T = W A^T: one GEMM with W
-// transposed.
-cudaError_t gemm_bf16_nt(cublasHandle_t h, const void* A, const void* W, float* C, int M, int N, int K,
-                         cudaStream_t st) {
-  if (M <= 0 || N <= 0) return cudaSuccess;
-  if (cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
-  const float alpha = 1.f, beta = 0.f;
-  const cublasStatus_t s = cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, N, M, K, &alpha, W, CUDA_R_16BF, K, A,
-                                        CUDA_R_16BF, K, &beta, C, CUDA_R_32F, N, CUBLAS_COMPUTE_32F,
-                                        CUBLAS_GEMM_DEFAULT);
-  return s == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
-}
-
 }  // namespace
 
 namespace {
-cudaError_t launch_frontend_q(const float* Qf, long long rows, int H, const float* cosb, const float* sinb,
-                              int rope_dim, bool interleaved, bool fp8, void* q_out, float* q_scale,
-                              cudaStream_t st) {
+cudaError_t launch_frontend_q(const float* Qf, int planes, long long rows, int H, const float* cosb,
+                              const float* sinb, int rope_dim, bool interleaved, bool fp8, void* q_out,
+                              float* q_scale, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const long long blocks = (rows + kFrontWarps - 1) / kFrontWarps;
-  frontend_q_kernel<<<static_cast<unsigned>(blocks), kFrontWarps * 32, 0, st>>>(
-      Qf, rows, H, cosb, sinb, rope_dim, interleaved ? 1 : 0, fp8 ? 1 : 0, q_out, q_scale);
-  return cudaGetLastError();
+  return launch_pdl(frontend_q_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kFrontWarps * 32), 0, st, Qf,
+                    planes, rows, H, cosb, sinb, rope_dim, interleaved ? 1 : 0, fp8 ? 1 : 0, q_out, q_scale);
 }
 
-cudaError_t launch_frontend_k(const float* Kf, int T, const float* cosb, const float* sinb, int rope_dim,
-                              bool interleaved, const float* ln_w, const float* ln_b, float eps, bool fp8,
-                              const int64_t* slots, void* cache, float* scale_cache, long long n_slots,
+cudaError_t launch_frontend_k(const float* Kf, int planes, int T, const float* cosb, const float* sinb,
+                              int rope_dim, bool interleaved, const float* ln_w, const float* ln_b, float eps,
+                              bool fp8, const int64_t* slots, void* cache, float* scale_cache, long long n_slots,
                               unsigned* status, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   const int blocks = (T + kFrontWarps - 1) / kFrontWarps;
-  frontend_k_kernel<<<blocks, kFrontWarps * 32, 0, st>>>(Kf, T, cosb, sinb, rope_dim, interleaved ? 1 : 0, ln_w,
-                                                         ln_b, eps, fp8 ? 1 : 0, slots, cache, scale_cache, n_slots,
-                                                         status);
-  return cudaGetLastError();
+  return launch_pdl(frontend_k_kernel, dim3(blocks), dim3(kFrontWarps * 32), 0, st, Kf, planes, T, cosb, sinb,
+                    rope_dim, interleaved ? 1 : 0, ln_w, ln_b, eps, fp8 ? 1 : 0, slots, cache, scale_cache, n_slots,
+                    status);
 }
 }  // namespace
 
-// The three chains are independent until the end: q (GEMM, row kernel) on the caller's
-// stream, k (GEMM, row kernel, cache write) and w (GEMM) on two library-owned streams
-// forked from it and joined back, so the small k and w GEMMs overlap the q GEMM.
+// The fused q projection needs enough token tiles to fill the GPU; below this many
+// tokens the projection is split over K instead and the q row kernel finishes the rows.
+constexpr int kFusedQMinTokens = 512;
+
+PreparePlan plan_prepare_launch(int T, int hidden_dim, int q_rank, int H, int D, int rope_dim) {
+  PreparePlan p{};
+  const size_t Tz = static_cast<size_t>(T > 0 ? T : 0);
+  p.q_fused = T >= kFusedQMinTokens && proj_q_fused_supported(H, rope_dim);
+  p.q_splits = p.q_fused ? 1 : proj_splits(T, H * D, q_rank);
+  p.k_splits = proj_splits(T, D, hidden_dim);
+  p.w_splits = proj_splits(T, H, hidden_dim);
+  auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+  p.off_q = 0;
+  p.off_k = p.off_q + (p.q_fused ? 0 : up(static_cast<size_t>(p.q_splits) * Tz * H * D * 4));
+  p.off_w = p.off_k + up(static_cast<size_t>(p.k_splits) * Tz * D * 4);
+  p.total = p.off_w + (p.w_splits > 1 ? up(static_cast<size_t>(p.w_splits) * Tz * H * 4) : 0);
+  return p;
+}
+
+// The three chains are independent until the end: q (projection and its rows) on the
+// caller's stream, k (projection, row kernel, cache write) and w (projection) on two
+// library-owned streams forked from it and joined back, so the small k and w projections
+// overlap the q projection.
 cudaError_t launch_prepare(const PrepareLaunch& p, cudaStream_t st) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -267,22 +294,39 @@ cudaError_t launch_prepare(const PrepareLaunch& p, cudaStream_t st) {
   FrontCtx& c = g_front[dev];
   if (!front_ctx_init(c)) return cudaErrorUnknown;
   const bool fp8 = p.fp8;
+  const PreparePlan& P = p.plan;
   if ((e = cudaEventRecord(c.fork, st)) != cudaSuccess) return e;
   for (auto s2 : c.side)
     if ((e = cudaStreamWaitEvent(s2, c.fork, 0)) != cudaSuccess) return e;
+  // q: projection with the rows finished in its epilogue, or fp32 planes and the row kernel
+  cudaError_t eq;
+  if (P.q_fused) {
+    eq = launch_proj_q(p.qa_normed, p.wq_b, p.T, p.H, p.q_rank, p.cosb, p.sinb, p.rope_dim, p.interleaved, fp8,
+                       p.q_out, p.q_scale, p.status, st);
+  } else {
+    eq = launch_proj_f32(p.qa_normed, p.wq_b, p.T, p.H * p.D, p.q_rank, P.q_splits, p.Qf, p.status, st);
+    if (eq == cudaSuccess)
+      eq = launch_frontend_q(p.Qf, P.q_splits, static_cast<long long>(p.T) * p.H, p.H, p.cosb, p.sinb, p.rope_dim,
+                             p.interleaved, fp8, p.q_out, p.q_scale, st);
+  }
   // k: projection, layer norm, RoPE, (rotation, quantisation), cache write
-  cudaError_t ek = gemm_bf16_nt(c.blas[1], p.hidden, p.wk, p.Kf, p.T, p.D, p.hidden_dim, c.side[0]);
+  cudaError_t ek = launch_proj_f32(p.hidden, p.wk, p.T, p.D, p.hidden_dim, P.k_splits, p.Kf, p.status, c.side[0]);
   if (ek == cudaSuccess)
-    ek = launch_frontend_k(p.Kf, p.T, p.cosb, p.sinb, p.rope_dim, p.interleaved, p.ln_w, p.ln_b, p.eps, fp8,
-                           p.slots, p.cache, p.scale_cache, p.n_slots, p.status, c.side[0]);
-  // w: the head-weight projection straight into the output
-  const cudaError_t ew = gemm_bf16_nt(c.blas[2], p.hidden, p.weights_proj, p.w_out, p.T, p.H, p.hidden_dim,
-                                      c.side[1]);
-  // q: projection, RoPE, (rotation, quantisation)
-  cudaError_t eq = gemm_bf16_nt(c.blas[0], p.qa_normed, p.wq_b, p.Qf, p.T, p.H * p.D, p.q_rank, st);
-  if (eq == cudaSuccess)
-    eq = launch_frontend_q(p.Qf, static_cast<long long>(p.T) * p.H, p.H, p.cosb, p.sinb, p.rope_dim,
-                           p.interleaved, fp8, p.q_out, p.q_scale, st);
+    ek = launch_frontend_k(p.Kf, P.k_splits, p.T, p.cosb, p.sinb, p.rope_dim, p.interleaved, p.ln_w, p.ln_b, p.eps,
+                           fp8, p.slots, p.cache, p.scale_cache, p.n_slots, p.status, c.side[0]);
+  // w: the head-weight projection, straight into the output or as planes then their sum
+  cudaError_t ew;
+  if (P.w_splits == 1) {
+    ew = launch_proj_f32(p.hidden, p.weights_proj, p.T, p.H, p.hidden_dim, 1, p.w_out, p.status, c.side[1]);
+  } else {
+    ew = launch_proj_f32(p.hidden, p.weights_proj, p.T, p.H, p.hidden_dim, P.w_splits, p.Wp, p.status, c.side[1]);
+    if (ew == cudaSuccess) {
+      const long long n = static_cast<long long>(p.T) * p.H;
+      const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 1024));
+      ew = launch_pdl(sum_planes_kernel, dim3(blocks), dim3(256), 0, c.side[1], static_cast<const float*>(p.Wp),
+                      P.w_splits, n, p.w_out);
+    }
+  }
   // join the side streams back into the caller's stream whatever happened above, so no
   // work of this call is left unordered with the caller's later work
   for (int i = 0; i < 2; ++i) {

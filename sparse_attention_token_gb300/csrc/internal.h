@@ -141,8 +141,24 @@ unsigned* device_status_ptr();  // address of the status word on the current dev
 // e4m3 quantisation with its scale); slots >= n_slots set kStatusBadPage.
 cudaError_t launch_cache_append(const void* k_new, int n, int D, const int64_t* slots, void* cache, bool fp8,
                                 float* scale_cache, long long n_slots, unsigned* status, cudaStream_t st);
-// Indexer front-end (frontend.cu): projections (cuBLAS bf16 GEMMs, fp32 results) and the
-// q / k row kernels (RoPE, layer norm, Hadamard, quantisation, cache write).
+// Front-end projections on the tensor cores (proj_gemm.cu).
+int proj_splits(int M, int N, int K);  // K splits of an fp32 projection of these shapes
+bool proj_q_fused_supported(int H, int rope_dim);
+cudaError_t launch_proj_f32(const void* A, const void* B, int M, int N, int K, int splits, float* C,
+                            unsigned* status, cudaStream_t st);
+cudaError_t launch_proj_q(const void* A, const void* B, int M, int H, int K, const float* cosb, const float* sinb,
+                          int rope_dim, bool interleaved, bool fp8, void* q_out, float* q_scale, unsigned* status,
+                          cudaStream_t st);
+// Workspace of the front-end: fp32 planes of the projections that are not finished in
+// their own epilogue (one plane per K split).
+struct PreparePlan {
+  bool q_fused;
+  int q_splits, k_splits, w_splits;
+  size_t off_q, off_k, off_w, total;
+};
+PreparePlan plan_prepare_launch(int T, int hidden_dim, int q_rank, int H, int D, int rope_dim);
+// Indexer front-end (frontend.cu): the projections and the q / k row kernels (RoPE, layer
+// norm, Hadamard, quantisation, cache write).
 struct PrepareLaunch {
   int T, hidden_dim, q_rank, H, D, rope_dim;
   bool interleaved, fp8;
@@ -154,8 +170,9 @@ struct PrepareLaunch {
   float* scale_cache;
   long long n_slots;
   void* q_out;
-  float *q_scale, *w_out, *Qf, *Kf;
+  float *q_scale, *w_out, *Qf, *Kf, *Wp;
   unsigned* status;
+  PreparePlan plan;
 };
 cudaError_t launch_prepare(const PrepareLaunch& p, cudaStream_t st);
 // Dense scoring and top-k of one sequence (the bodies of dsa_indexer_scores and
