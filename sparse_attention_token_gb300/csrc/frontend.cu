@@ -271,20 +271,18 @@ PreparePlan plan_prepare_launch(int T, int hidden_dim, int q_rank, int H, int D,
   const size_t Tz = static_cast<size_t>(T > 0 ? T : 0);
   p.q_fused = T >= kFusedQMinTokens && proj_q_fused_supported(H, rope_dim);
   p.q_splits = p.q_fused ? 1 : proj_splits(T, H * D, q_rank);
-  p.k_splits = proj_splits(T, D, hidden_dim);
-  p.w_splits = proj_splits(T, H, hidden_dim);
+  p.kw_splits = proj_dual_splits(T, hidden_dim);
   auto up = [](size_t b) { return (b + 255) / 256 * 256; };
   p.off_q = 0;
   p.off_k = p.off_q + (p.q_fused ? 0 : up(static_cast<size_t>(p.q_splits) * Tz * H * D * 4));
-  p.off_w = p.off_k + up(static_cast<size_t>(p.k_splits) * Tz * D * 4);
-  p.total = p.off_w + (p.w_splits > 1 ? up(static_cast<size_t>(p.w_splits) * Tz * H * 4) : 0);
+  p.off_w = p.off_k + up(static_cast<size_t>(p.kw_splits) * Tz * D * 4);
+  p.total = p.off_w + (p.kw_splits > 1 ? up(static_cast<size_t>(p.kw_splits) * Tz * H * 4) : 0);
   return p;
 }
 
-// The three chains are independent until the end: q (projection and its rows) on the
-// caller's stream, k (projection, row kernel, cache write) and w (projection) on two
-// library-owned streams forked from it and joined back, so the small k and w projections
-// overlap the q projection.
+// The two chains are independent until the end: q (projection and its rows) on the
+// caller's stream, k and w (one projection, the k row kernel and cache write, the w
+// planes' sum) on a library-owned stream forked from it and joined back.
 cudaError_t launch_prepare(const PrepareLaunch& p, cudaStream_t st) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -309,23 +307,21 @@ cudaError_t launch_prepare(const PrepareLaunch& p, cudaStream_t st) {
       eq = launch_frontend_q(p.Qf, P.q_splits, static_cast<long long>(p.T) * p.H, p.H, p.cosb, p.sinb, p.rope_dim,
                              p.interleaved, fp8, p.q_out, p.q_scale, st);
   }
-  // k: projection, layer norm, RoPE, (rotation, quantisation), cache write
-  cudaError_t ek = launch_proj_f32(p.hidden, p.wk, p.T, p.D, p.hidden_dim, P.k_splits, p.Kf, p.status, c.side[0]);
+  // k and w: one projection over hidden_states (its columns 0..127 are k, the rest w), then
+  // the k rows (layer norm, RoPE, rotation, quantisation, cache write) and, when split over
+  // K, the sum of w's planes
+  const int S = P.kw_splits;
+  cudaError_t ek = launch_proj_dual(p.hidden, p.wk, p.weights_proj, p.T, p.H, p.hidden_dim, S, p.Kf,
+                                    S == 1 ? p.w_out : p.Wp, p.status, c.side[0]);
   if (ek == cudaSuccess)
-    ek = launch_frontend_k(p.Kf, P.k_splits, p.T, p.cosb, p.sinb, p.rope_dim, p.interleaved, p.ln_w, p.ln_b, p.eps,
-                           fp8, p.slots, p.cache, p.scale_cache, p.n_slots, p.status, c.side[0]);
-  // w: the head-weight projection, straight into the output or as planes then their sum
-  cudaError_t ew;
-  if (P.w_splits == 1) {
-    ew = launch_proj_f32(p.hidden, p.weights_proj, p.T, p.H, p.hidden_dim, 1, p.w_out, p.status, c.side[1]);
-  } else {
-    ew = launch_proj_f32(p.hidden, p.weights_proj, p.T, p.H, p.hidden_dim, P.w_splits, p.Wp, p.status, c.side[1]);
-    if (ew == cudaSuccess) {
-      const long long n = static_cast<long long>(p.T) * p.H;
-      const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 1024));
-      ew = launch_pdl(sum_planes_kernel, dim3(blocks), dim3(256), 0, c.side[1], static_cast<const float*>(p.Wp),
-                      P.w_splits, n, p.w_out);
-    }
+    ek = launch_frontend_k(p.Kf, S, p.T, p.cosb, p.sinb, p.rope_dim, p.interleaved, p.ln_w, p.ln_b, p.eps, fp8,
+                           p.slots, p.cache, p.scale_cache, p.n_slots, p.status, c.side[0]);
+  cudaError_t ew = cudaSuccess;
+  if (ek == cudaSuccess && S > 1) {
+    const long long n = static_cast<long long>(p.T) * p.H;
+    const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 1024));
+    ew = launch_pdl(sum_planes_kernel, dim3(blocks), dim3(256), 0, c.side[0], static_cast<const float*>(p.Wp), S, n,
+                    p.w_out);
   }
   // join the side streams back into the caller's stream whatever happened above, so no
   // work of this call is left unordered with the caller's later work

@@ -146,6 +146,9 @@ int proj_splits(int M, int N, int K);  // K splits of an fp32 projection of thes
 bool proj_q_fused_supported(int H, int rope_dim);
 cudaError_t launch_proj_f32(const void* A, const void* B, int M, int N, int K, int splits, float* C,
                             unsigned* status, cudaStream_t st);
+int proj_dual_splits(int M, int K);
+cudaError_t launch_proj_dual(const void* A, const void* Bk, const void* Bw, int M, int n2, int K, int splits,
+                             float* Kf, float* W, unsigned* status, cudaStream_t st);
 cudaError_t launch_proj_q(const void* A, const void* B, int M, int H, int K, const float* cosb, const float* sinb,
                           int rope_dim, bool interleaved, bool fp8, void* q_out, float* q_scale, unsigned* status,
                           cudaStream_t st);
@@ -153,7 +156,7 @@ cudaError_t launch_proj_q(const void* A, const void* B, int M, int H, int K, con
 // their own epilogue (one plane per K split).
 struct PreparePlan {
   bool q_fused;
-  int q_splits, k_splits, w_splits;
+  int q_splits, kw_splits;  // the k and head-weight projections run as one kernel
   size_t off_q, off_k, off_w, total;
 };
 PreparePlan plan_prepare_launch(int T, int hidden_dim, int q_rank, int H, int D, int rope_dim);

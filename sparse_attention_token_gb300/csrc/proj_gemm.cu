@@ -12,7 +12,8 @@
 //               128-byte swizzle atom of K) into an nS-deep ring;
 //   warp 1      TMEM allocator; lane 0 issues the MMAs (4 per 64-wide K step) into two
 //               BN-column fp32 accumulators, double buffered across tiles;
-//   warps 2..5  epilogue, one token row per thread:
+//   warps 2..9  epilogue, two warpgroups over the same token rows (one row per thread,
+//               TMEM lane quarter = warp % 4), splitting the tile's columns between them:
 //     kOutF32   fp32 rows into C (a K split s writes plane s; the row kernels add the
 //               planes in order), or
 //     kOutQRows the q rows finished in registers: RoPE on the first 2 HALF values of each
@@ -35,10 +36,10 @@ namespace {
 
 constexpr int kPM = 128;          // tokens per tile (TMEM lanes)
 constexpr int kPK = 64;           // K per ring stage: one 128-byte atom of bf16
-constexpr int kPThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kPThreads = 320;    // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue (two warpgroups)
 constexpr int kPSmemBudget = 200 * 1024;
 
-enum { kOutF32 = 0, kOutQRows = 1 };
+enum { kOutF32 = 0, kOutQRows = 1, kOutDual = 2 };
 
 struct ProjArgs {
   int M, N, K;              // C[M, N] = A[M, K] . B[N, K]^T
@@ -48,6 +49,11 @@ struct ProjArgs {
   int b_box;                // weight rows per TMA box: BN, or N when N < BN (rows past N are not stored)
   float* C;                 // kOutF32: plane s at C + s * plane, rows of ldc floats
   long long ldc, plane;
+  // kOutDual: the weight rows are B's first 128 rows then B2's n2 rows; columns 0..127 go
+  // to C as above, columns 128.. to C2 (plane s at C2 + s * plane2, rows of ldc2 floats)
+  int n2;
+  float* C2;
+  long long ldc2, plane2;
   int H, fp8;               // kOutQRows: q_out [M, H, 128] (bf16, or e4m3 with q_scale [M, H])
   const float* cosb;
   const float* sinb;
@@ -146,6 +152,7 @@ __device__ __forceinline__ Tile tile_of(const ProjArgs& a, int tile) {
 template <int BN, int OUT, int HALF, bool INTER>
 __global__ void __launch_bounds__(kPThreads, 1) proj_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                              const __grid_constant__ CUtensorMap tmap_b,
+                                                             const __grid_constant__ CUtensorMap tmap_b2,
                                                              const ProjArgs a) {
   constexpr uint32_t kAStage = kPM * 128, kBStage = BN * 128;
   constexpr uint32_t kCols = 2 * BN;  // two accumulators
@@ -173,7 +180,7 @@ __global__ void __launch_bounds__(kPThreads, 1) proj_kernel(const __grid_constan
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&tfull[s], 1);
-      ptx::mbar_init(&tempty[s], 4);  // one arrival per epilogue warp
+      ptx::mbar_init(&tempty[s], 8);  // one arrival per epilogue warp
     }
     ptx::mbar_init(done, 1);
     *abort = 0;
@@ -186,6 +193,7 @@ __global__ void __launch_bounds__(kPThreads, 1) proj_kernel(const __grid_constan
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmap_a);
     ptx::prefetch_tmap(&tmap_b);
+    if (OUT == kOutDual) ptx::prefetch_tmap(&tmap_b2);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -206,9 +214,11 @@ __global__ void __launch_bounds__(kPThreads, 1) proj_kernel(const __grid_constan
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&full[s], kAStage + static_cast<uint32_t>(a.b_box) * 128u);
+          const uint32_t b_rows = OUT == kOutDual ? 128u + static_cast<uint32_t>(a.n2) : static_cast<uint32_t>(a.b_box);
+          ptx::mbar_arrive_expect_tx(&full[s], kAStage + b_rows * 128u);
           ptx::tma_load_2d(sa + s * kAStage, &tmap_a, &full[s], k * kPK, T.mb * kPM);
           ptx::tma_load_2d(sb + s * kBStage, &tmap_b, &full[s], k * kPK, T.nb * BN);
+          if (OUT == kOutDual) ptx::tma_load_2d(sb + s * kBStage + 128 * 128, &tmap_b2, &full[s], k * kPK, 0);
         }
       }
       // drain: the copies issued into the ring land before the CTA can exit
@@ -255,6 +265,7 @@ __global__ void __launch_bounds__(kPThreads, 1) proj_kernel(const __grid_constan
     __syncwarp();
   } else {
     const int quarter = warp & 3;  // the TMEM lane quarter this warp may read
+    const int grp = (warp - 2) >> 2;  // epilogue warpgroup: 32-column chunks (heads) of its parity
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t nt = 0;
     for (int tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++nt) {
@@ -265,18 +276,22 @@ __global__ void __launch_bounds__(kPThreads, 1) proj_kernel(const __grid_constan
       ptx::tc_fence_after();
       const long long t = static_cast<long long>(T.mb) * kPM + quarter * 32 + lane;
       const uint32_t tcol = tmem_base + lane_addr + acc * BN;
-      if constexpr (OUT == kOutF32) {
-        float* crow = a.C + T.s * a.plane + t * a.ldc + static_cast<long long>(T.nb) * BN;
+      if constexpr (OUT == kOutF32 || OUT == kOutDual) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          const int col0 = T.nb * BN + 32 * c;  // columns past N are not stored
-          if (col0 >= a.N) break;
+        for (int c = grp; c < BN / 32; c += 2) {
+          // columns past N are not stored; kOutDual: columns 128.. belong to C2
+          const bool second = OUT == kOutDual && c >= 4;
+          const int ncols = OUT == kOutDual ? (second ? a.n2 : 128) : a.N;
+          const int col0 = OUT == kOutDual ? 32 * (second ? c - 4 : c) : T.nb * BN + 32 * c;
+          if (col0 >= ncols) break;
+          float* crow = second ? a.C2 + T.s * a.plane2 + t * a.ldc2 + col0
+                               : a.C + T.s * a.plane + t * a.ldc + col0;
           uint32_t r[32];
           ptx::tmem_ld_32x32b_x32(tcol + 32 * c, r);
           ptx::tmem_ld_wait_regs(r);
           if (t < a.M) {
-            if (col0 + 32 <= a.N) {
-              float4* dst = reinterpret_cast<float4*>(crow + 32 * c);
+            if (col0 + 32 <= ncols && ((reinterpret_cast<uintptr_t>(crow) & 15u) == 0)) {
+              float4* dst = reinterpret_cast<float4*>(crow);
 #pragma unroll
               for (int i = 0; i < 8; ++i)
                 dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
@@ -284,13 +299,13 @@ __global__ void __launch_bounds__(kPThreads, 1) proj_kernel(const __grid_constan
             } else {
 #pragma unroll
               for (int i = 0; i < 32; ++i)
-                if (col0 + i < a.N) crow[32 * c + i] = __uint_as_float(r[i]);
+                if (col0 + i < ncols) crow[i] = __uint_as_float(r[i]);
             }
           }
         }
       } else {
 #pragma unroll 1
-        for (int hh = 0; hh < BN / 128; ++hh) {
+        for (int hh = grp; hh < BN / 128; hh += 2) {
           float v[128];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -345,10 +360,13 @@ int sm_count() {
 }
 
 template <int BN, int OUT, int HALF, bool INTER>
-cudaError_t launch_proj_t(const void* A, const void* B, ProjArgs a, cudaStream_t st) {
-  CUtensorMap ta, tb;
-  a.b_box = a.N < BN ? a.N : BN;
-  if (!proj_map(&ta, A, a.M, a.K, kPM) || !proj_map(&tb, B, a.N, a.K, a.b_box)) return cudaErrorInvalidValue;
+cudaError_t launch_proj_t(const void* A, const void* B, ProjArgs a, cudaStream_t st, const void* B2 = nullptr) {
+  CUtensorMap ta, tb, tb2;
+  a.b_box = OUT == kOutDual ? 128 : (a.N < BN ? a.N : BN);
+  if (!proj_map(&ta, A, a.M, a.K, kPM) || !proj_map(&tb, B, OUT == kOutDual ? 128 : a.N, a.K, a.b_box))
+    return cudaErrorInvalidValue;
+  if (OUT == kOutDual ? !proj_map(&tb2, B2, a.n2, a.K, a.n2) : false) return cudaErrorInvalidValue;
+  if (OUT != kOutDual) tb2 = tb;
   const size_t stage = static_cast<size_t>(kPM) * 128 + static_cast<size_t>(BN) * 128;
   a.stages = static_cast<int>((kPSmemBudget - 256) / stage);
   if (a.stages > 8) a.stages = 8;
@@ -357,7 +375,7 @@ cudaError_t launch_proj_t(const void* A, const void* B, ProjArgs a, cudaStream_t
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = std::min(a.n_tiles, sm_count());
-  e = launch_pdl(kern, dim3(grid), dim3(kPThreads), smem, st, ta, tb, a);
+  e = launch_pdl(kern, dim3(grid), dim3(kPThreads), smem, st, ta, tb, tb2, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -410,6 +428,32 @@ cudaError_t launch_proj_f32(const void* A, const void* B, int M, int N, int K, i
   if (BN == 256) return launch_proj_t<256, kOutF32, 0, false>(A, B, a, st);
   if (BN == 128) return launch_proj_t<128, kOutF32, 0, false>(A, B, a, st);
   return launch_proj_t<64, kOutF32, 0, false>(A, B, a, st);
+}
+
+// The k and head-weight projections share their token operand: one pass over it.
+// Kf planes [splits][M, 128] = A . Bk[128, K]^T, and W [M, n2] = A . Bw[n2, K]^T (planes
+// [splits][M, n2] when split, else straight into W); n2 <= 128.
+int proj_dual_splits(int M, int K) { return proj_splits(M, 256, K); }
+
+cudaError_t launch_proj_dual(const void* A, const void* Bk, const void* Bw, int M, int n2, int K, int splits,
+                             float* Kf, float* W, unsigned* status, cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  if (K % 8 || K <= 0 || n2 < 1 || n2 > 128 || (n2 % 4)) return cudaErrorInvalidValue;
+  ProjArgs a{};
+  a.M = M;
+  a.N = 128 + n2;
+  a.K = K;
+  a.C = Kf;
+  a.ldc = 128;
+  a.plane = static_cast<long long>(M) * 128;
+  a.n2 = n2;
+  a.C2 = W;
+  a.ldc2 = n2;
+  a.plane2 = static_cast<long long>(M) * n2;
+  a.status = status;
+  fill_tiles(a, 256, splits);
+  if (a.splits != splits) return cudaErrorInvalidValue;
+  return launch_proj_t<256, kOutDual, 0, false>(A, Bk, a, st, Bw);
 }
 
 // Whether the fused q projection covers this RoPE configuration.
