@@ -340,6 +340,44 @@ dsa_status dsa_indexer_merge_candidates(const float* cand_scores, const int32_t*
                                         dsa_stream_t stream);
 
 /*
+ * Sparse MLA over the indexer's top-k (GLM5 TensorCast adaptation design: the fused
+ * indexer hands topk_indices / topk_limit to the multi-head latent attention backend,
+ * whose attention length is capped by the top-k width -- "Sparse MLA 配置兼容", the
+ * performance model's sparse prefill / decode length).  Absorbed multi-head latent
+ * attention on the selected keys only: for query row t of sequence b and head h, over the
+ * logical key positions s = topk[t, j] >= 0 (s < seq_lens[b]; others are skipped),
+ *     logit = scale * (q_nope[t, h] . c_kv[s] + q_rope[t, h] . k_rope[s])
+ *     out[t, h, :] = sum_s softmax_s(logit) * c_kv[s]            (fp32, latent space)
+ * with c_kv[s] = cache_c[block_tables[b, s / page_size], s % page_size] and k_rope[s] the
+ * same row of cache_r.  An empty selection gives zeros.  The value up-projection and the
+ * output projection are the caller's.
+ *   q_nope [total_q, H, kv_rank] bf16, q_rope [total_q, H, rope_dim] bf16
+ *   cache_c [num_pages, page_size, kv_rank] bf16, cache_r [num_pages, page_size, rope_dim] bf16
+ *   topk [total_q, topk_width] int32 (any order, -1 padding); out [total_q, H, kv_rank] fp32
+ * kv_rank = 512 and rope_dim = 64; H = 16, 32 or a multiple of 64; scale > 0.  workspace:
+ * dsa_sparse_mla_workspace_size bytes (the key splits' partial outputs), 16-byte aligned.
+ * A selected position whose page is outside the cache is skipped and reported through
+ * dsa_check_device_status.  Probabilities enter the P.V product rounded to bf16.
+ */
+typedef struct {
+  int B, total_q, H, kv_rank, rope_dim, page_size, num_pages, max_pages_per_seq, topk_width;
+  float scale;
+  const void* q_nope;
+  const void* q_rope;
+  const void* cache_c;
+  const void* cache_r;
+  const int32_t* block_tables;
+  const int32_t* cu_q_lens;
+  const int32_t* seq_lens;
+  const int32_t* topk;
+  float* out;
+  void* workspace;
+  size_t workspace_bytes;
+} dsa_sparse_mla_args;
+dsa_status dsa_sparse_mla_workspace_size(const dsa_sparse_mla_args* args, size_t* bytes);
+dsa_status dsa_sparse_mla(const dsa_sparse_mla_args* args, dsa_stream_t stream);
+
+/*
  * dsa_indexer_static -- dsa_indexer for callers that cannot allocate device memory.
  * The pages have no counterpart of this entry point; it exists for library users.
  *

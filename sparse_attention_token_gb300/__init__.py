@@ -63,6 +63,16 @@ class dsa_indexer_args(ctypes.Structure):
     ]
 
 
+class dsa_sparse_mla_args(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("total_q", ctypes.c_int), ("H", ctypes.c_int), ("kv_rank", ctypes.c_int),
+                ("rope_dim", ctypes.c_int), ("page_size", ctypes.c_int), ("num_pages", ctypes.c_int),
+                ("max_pages_per_seq", ctypes.c_int), ("topk_width", ctypes.c_int), ("scale", ctypes.c_float),
+                ("q_nope", ctypes.c_void_p), ("q_rope", ctypes.c_void_p), ("cache_c", ctypes.c_void_p),
+                ("cache_r", ctypes.c_void_p), ("block_tables", ctypes.c_void_p), ("cu_q_lens", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("topk", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
 class dsa_indexer_prepare_args(ctypes.Structure):
     _fields_ = [
         ("T", ctypes.c_int), ("hidden_dim", ctypes.c_int), ("q_rank", ctypes.c_int), ("H", ctypes.c_int),
@@ -124,6 +134,10 @@ def lib():
         L.dsa_indexer_shard_candidates.argtypes = [P, I, P, P, I, P, P, I, I, I, I, I, I, I, P, P, P, S, P]
         L.dsa_indexer_merge_candidates.restype = I
         L.dsa_indexer_merge_candidates.argtypes = [P, P, I, I, I, I, I, I, P, P]
+        L.dsa_sparse_mla_workspace_size.restype = I
+        L.dsa_sparse_mla_workspace_size.argtypes = [ctypes.POINTER(dsa_sparse_mla_args), ctypes.POINTER(S)]
+        L.dsa_sparse_mla.restype = I
+        L.dsa_sparse_mla.argtypes = [ctypes.POINTER(dsa_sparse_mla_args), P]
         L.dsa_test_arm_score_timeout.restype = I
         L.dsa_test_arm_score_timeout.argtypes = [ctypes.c_ulonglong]
         _LIB = L
@@ -581,6 +595,51 @@ def dsa_indexer_key_sharded(q: torch.Tensor, k_shard: torch.Tensor, w: torch.Ten
     all_idx, all_sc = gather_shard_candidates(ci, cs, group)
     return dsa_indexer_merge_candidates(all_sc, all_idx, topk_limit=topk_limit, k_out=k_out, order=order,
                                         stream=stream)
+
+
+# ---- sparse MLA over the top-k (the attention that consumes topk_indices) -----------------
+
+def make_sparse_mla_args(q_nope, q_rope, cache_c, cache_r, block_tables, cu_q_lens, seq_lens, topk, *,
+                         scale: float, out=None, workspace=None):
+    """dsa_sparse_mla_args for these tensors (every shape checked); returns (args, kept tensors)."""
+    total_q, H, R = q_nope.shape
+    rd = q_rope.shape[2]
+    num_pages, page_size = cache_c.shape[0], cache_c.shape[1]
+    B = seq_lens.shape[0]
+    k = topk.shape[1]
+    _expect([(q_rope, "q_rope", (total_q, H, rd)), (cache_c, "cache_c", (num_pages, page_size, R)),
+             (cache_r, "cache_r", (num_pages, page_size, rd)), (cu_q_lens, "cu_q_lens", (B + 1,)),
+             (block_tables, "block_tables", (B, None)), (topk, "topk", (total_q, k))])
+    if out is None:
+        out = torch.empty((total_q, H, R), dtype=torch.float32, device=q_nope.device)
+    _expect([(out, "out", (total_q, H, R))])
+    a = dsa_sparse_mla_args()
+    a.B, a.total_q, a.H, a.kv_rank, a.rope_dim = B, total_q, H, R, rd
+    a.page_size, a.num_pages, a.max_pages_per_seq, a.topk_width = page_size, num_pages, block_tables.shape[1], k
+    a.scale = float(scale)
+    a.q_nope, a.q_rope = _dev(q_nope, "q_nope", torch.bfloat16), _dev(q_rope, "q_rope", torch.bfloat16)
+    a.cache_c, a.cache_r = _dev(cache_c, "cache_c", torch.bfloat16), _dev(cache_r, "cache_r", torch.bfloat16)
+    a.block_tables = _dev(block_tables, "block_tables", torch.int32)
+    a.cu_q_lens = _dev(cu_q_lens, "cu_q_lens", torch.int32)
+    a.seq_lens = _dev(seq_lens, "seq_lens", torch.int32)
+    a.topk = _dev(topk, "topk", torch.int32)
+    a.out = _dev(out, "out", torch.float32)
+    if workspace is None:
+        n = ctypes.c_size_t(0)
+        _check(lib().dsa_sparse_mla_workspace_size(ctypes.byref(a), ctypes.byref(n)), "dsa_sparse_mla_workspace_size")
+        workspace = torch.empty(max(n.value, 16), dtype=torch.uint8, device=q_nope.device)
+    a.workspace = _dev(workspace, "workspace")
+    a.workspace_bytes = workspace.numel() * workspace.element_size()
+    return a, (q_nope, q_rope, cache_c, cache_r, block_tables, cu_q_lens, seq_lens, topk, out, workspace)
+
+
+def dsa_sparse_mla(q_nope, q_rope, cache_c, cache_r, block_tables, cu_q_lens, seq_lens, topk, *, scale: float,
+                   out=None, workspace=None, stream=None) -> torch.Tensor:
+    """Latent attention output [total_q, H, kv_rank] fp32 of each query over its selected keys."""
+    a, keep = make_sparse_mla_args(q_nope, q_rope, cache_c, cache_r, block_tables, cu_q_lens, seq_lens, topk,
+                                   scale=scale, out=out, workspace=workspace)
+    _check(lib().dsa_sparse_mla(ctypes.byref(a), _stream_ptr(stream)), "dsa_sparse_mla")
+    return keep[8]
 
 
 def dsa_test_arm_score_timeout(limit_ns: int) -> None:
