@@ -569,6 +569,53 @@ def _key_sharded_prefill(dev, stream, peaks, iters=10):
     return out
 
 
+def _sparse_mla_decode(dev, stream, peaks, iters=10):
+    """Sparse MLA after the indexer: decode B=64, one query per sequence, contexts U[4096, 65536],
+    64 heads, 2048 selected keys per query, bf16 latent cache (kv_rank 512, rope 64, page 64)."""
+    import ctypes
+    import sparse_attention_token_gb300 as dsa
+    import workloads
+    hbm = float(peaks["hbm_gbs"])
+    g = torch.Generator(device=dev)
+    g.manual_seed(13)
+    B, Hh, K, page, R, rd = 64, 64, 2048, 64, 512, 64
+    lens = workloads.decode_lens(B, 4096, 65536, 0)
+    pages = [(L + page - 1) // page for L in lens]
+    num_pages = sum(pages) + 1
+    perm = torch.randperm(num_pages, generator=g, device=dev).to(torch.int32)
+    bt = torch.full((B, max(pages)), -1, dtype=torch.int32, device=dev)
+    cur = 0
+    for b, npg in enumerate(pages):
+        bt[b, :npg] = perm[cur:cur + npg]
+        cur += npg
+    cache_c = torch.randn((num_pages, page, R), generator=g, device=dev).to(torch.bfloat16)
+    cache_r = torch.randn((num_pages, page, rd), generator=g, device=dev).to(torch.bfloat16)
+    q_nope = torch.randn((B, Hh, R), generator=g, device=dev).to(torch.bfloat16)
+    q_rope = torch.randn((B, Hh, rd), generator=g, device=dev).to(torch.bfloat16)
+    # each query's selection: 2048 distinct positions of its context, in random order
+    topk = torch.stack([torch.randperm(L, generator=g, device=dev)[:K] for L in lens]).to(torch.int32)
+    cu = torch.arange(0, B + 1, dtype=torch.int32, device=dev)
+    seq = torch.tensor(lens, dtype=torch.int32, device=dev)
+    a, keep = dsa.make_sparse_mla_args(q_nope, q_rope, cache_c, cache_r, bt, cu, seq, topk,
+                                       scale=1.0 / (R + rd) ** 0.5)
+    L = dsa.lib()
+    rc = L.dsa_sparse_mla(ctypes.byref(a), stream.cuda_stream)
+    if rc != 0:
+        raise RuntimeError(f"dsa_sparse_mla: {dsa.dsa_status_string(rc)}")
+    ms = _time_events(lambda: L.dsa_sparse_mla(ctypes.byref(a), stream.cuda_stream), iters, stream)
+    # algorithmic bytes: the selected latent rows, q, the selection and the fp32 output
+    nbytes = B * K * (R + rd) * 2 + B * Hh * (R + rd) * 2 + B * K * 4 + B * Hh * R * 4
+    flops = 2.0 * B * Hh * K * (R + rd + R)
+    out = {"workload": "sparse MLA decode B=64, one query per sequence, contexts U[4096, 65536], 64 heads, "
+                       "2048 selected keys per query, bf16 latent cache (kv_rank 512, rope 64, page 64)",
+           "ms_per_step": ms, "queries_per_s": B / (ms / 1e3), "algorithmic_bytes": nbytes,
+           "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm,
+           "tflops": flops / (ms / 1e3) / 1e12}
+    del a, keep, cache_c, cache_r, q_nope, q_rope, topk
+    torch.cuda.empty_cache()
+    return out
+
+
 OTHER_WORKLOADS = {
     "frontend_fp8": _frontend_fp8,
     "cache_append_fp8": _cache_append_fp8,
@@ -576,6 +623,7 @@ OTHER_WORKLOADS = {
     "decode_b64_fp8_cache": _decode_b64_fp8_cache,
     "indexshare_stack": _indexshare_stack,
     "key_sharded_prefill": _key_sharded_prefill,
+    "sparse_mla_decode": _sparse_mla_decode,
 }
 
 
