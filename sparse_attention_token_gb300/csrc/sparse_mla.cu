@@ -23,11 +23,11 @@
 //                                                            A; P K-major B, K = 64 keys)
 //               with S double buffered and O^T (4 x heads columns) resident in TMEM;
 //   warps 0..3  softmax and rescale: the threads of the head lanes take their head's 64
-//               logits, keep the running maximum and sum (base-2 exponentials of the
-//               scaled logits), write p as bf16 into P; every epilogue thread then scales
-//               its O^T lanes by the heads' correction factors before the next P . V
-//               accumulates, and at the end writes the unnormalised O, the maximum and
-//               the sum of its split.
+//               logits, keep a reference maximum and the sum (base-2 exponentials of the
+//               scaled logits), write p as bf16 into P; when a head's reference moves,
+//               every epilogue thread scales its O^T lanes by the heads' correction
+//               factors before the next P . V accumulates; at the end they write the
+//               unnormalised O, the reference maximum and the sum of the split.
 // A second kernel combines the splits: out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j.
 // Every wait is bounded; on a timeout every role stops, copies and MMAs in flight are
 // drained (bounded) and TMEM is freed.
@@ -153,11 +153,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
       const uint32_t id1 = ptx::idesc_f32acc(128, kBlockKeys, true);   // S: 128 q rows x 64 keys
       const uint32_t id2 = ptx::idesc_f32acc_bf16_amn(128, hg);        // O^T: 128 latent x heads
       bool ok = nblk == 0 || ptx::mbar_wait(&bars->qfull, 0, abort, a.status, kStatusTimeout);
-      auto gemm1 = [&](int blk) -> bool {
+      auto gemm1 = [&](int blk) {
         const int tb = blk & 1;
-        if (!ptx::mbar_wait(&bars->tfull[tb], (blk >> 1) & 1, abort, a.status, kStatusTimeout) ||
-            !ptx::mbar_wait(&bars->sempty[tb], ((blk >> 1) & 1) ^ 1, abort, a.status, kStatusTimeout))
-          return false;
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + tb * kSCols;
         for (int at = 0; at < kAtoms; ++at) {
@@ -168,12 +165,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
             ptx::mma_bf16(d, ad + 2 * s, bd + 2 * s, id1, (at > 0 || s > 0) ? 1u : 0u);
         }
         ptx::mma_commit(&bars->sfull[tb]);
-        return true;
       };
-      if (ok && nblk > 0) ok = gemm1(0);
-      for (int blk = 0; ok && blk < nblk; ++blk) {
-        if (blk + 1 < nblk && !gemm1(blk + 1)) break;
-        if (!ptx::mbar_wait(&bars->pfull, blk & 1, abort, a.status, kStatusTimeout)) break;
+      auto gemm2 = [&](int blk) {
         ptx::tc_fence_after();
         const int tb = blk & 1;
         const uint32_t tile = sbase + kOffTile + tb * kTileBytes;
@@ -188,6 +181,33 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
         }
         ptx::mma_commit(&bars->tempty[tb]);
         ptx::mma_commit(&bars->ofree);
+      };
+      // Issue whichever product has its inputs first: the next block's S (its key tile
+      // gathered and its S buffer released) or this block's P . V (its P written), so
+      // neither waits behind the other's inputs.  Bounded like every other wait.
+      int n1 = 0, n2 = 0;
+      uint64_t t0 = ptx::globaltimer();
+      for (uint32_t spin = 0; ok && n2 < nblk; ++spin) {
+        bool progress = false;
+        if (n1 < nblk && n1 <= n2 + 1 && ptx::mbar_try_wait(&bars->tfull[n1 & 1], (n1 >> 1) & 1) &&
+            ptx::mbar_try_wait(&bars->sempty[n1 & 1], ((n1 >> 1) & 1) ^ 1)) {
+          gemm1(n1++);
+          progress = true;
+        }
+        if (n2 < n1 && ptx::mbar_try_wait(&bars->pfull, n2 & 1)) {
+          gemm2(n2++);
+          progress = true;
+        }
+        if (progress) {
+          t0 = ptx::globaltimer();
+        } else if ((spin & 15u) == 15u) {
+          if (*abort) break;
+          if (ptx::globaltimer() - t0 > 2000000000ull) {
+            *abort = 1;
+            atomicOr(a.status, kStatusTimeout);
+            break;
+          }
+        }
       }
       ptx::mma_commit(&bars->done);
       ptx::mbar_wait_drain(&bars->done, 0, a.status, kStatusTimeout, 200000000ull);
@@ -292,8 +312,14 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
             x[i] = v ? x[i] : -INFINITY;
             mb = fmaxf(mb, x[i]);
           }
-          const float mn = fmaxf(m, mb);
-          cr = mn == -INFINITY ? 1.f : exp2f(m - mn);  // the first finite maximum: m = -inf gives 0
+          // The reference maximum moves only when the block's maximum exceeds it by more
+          // than 8 (a factor 256 in probability): p stays below 256 and the output, which
+          // divides by the sum taken against the same reference, is unchanged, while most
+          // blocks need no rescaling of the accumulated output.
+          float mn = m;
+          if (m == -INFINITY) mn = mb;  // nothing accumulated yet (O is still zero)
+          else if (mb > m + 8.f) mn = mb;
+          cr = (m == -INFINITY || mn == m) ? 1.f : exp2f(m - mn);
           float ls = 0.f;
           uint32_t pk[32];
 #pragma unroll
@@ -325,8 +351,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
         ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->ofree, (blk - 1) & 1, abort, a.status,
                                                     kStatusTimeout)) != 0;
       }
-      ptx::named_bar_sync(2, 128);  // P and the correction factors are written
-      if (blk > 0 && ok && !*abort) {
+      // P and the correction factors are written; does any head need its output rescaled?
+      uint32_t any;
+      asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.f32 q, %1, 0f3F800000;\n\t"
+                   "bar.red.or.pred p, 2, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                   : "=r"(any) : "f"(head_lane && h < hg ? cr : 1.f) : "memory");
+      if (any && blk > 0 && ok && !*abort) {
         // O^T *= corr per head column, for this thread's latent lane in each chunk
         ptx::tc_fence_after();
         for (int c = 0; c < 4; ++c) {
@@ -343,7 +373,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
         ptx::tmem_st_wait();
       }
       ptx::tc_fence_before();
-      ptx::named_bar_sync(2, 128);  // corr is read by everyone before the next block rewrites it
+      if (any) ptx::named_bar_sync(2, 128);  // corr is read by everyone before the next block rewrites it
       if (lane == 0) ptx::mbar_arrive(&bars->pfull);
     }
     // the split's unnormalised output, maximum and sum
