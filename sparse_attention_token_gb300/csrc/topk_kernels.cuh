@@ -862,9 +862,9 @@ __device__ __forceinline__ void red_add_cluster(uint32_t addr, uint32_t v) {
 // keys fill a few hundred of the 4096 bins), between two cluster barriers.  Every CTA
 // zeroes its own m.merged before the call, after its last read of the previous merge.
 template <int CL>
-__device__ void cluster_merge_hist(const TopkSmem& m, uint32_t rank) {
+__device__ void cluster_merge_hist(const TopkSmem& m, uint32_t rank, int bmin = 0) {
   cluster_barrier();  // every local histogram complete, every merged histogram zeroed
-  for (int b = threadIdx.x; b < kBins; b += kThreads) {
+  for (int b = threadIdx.x + bmin; b < kBins; b += kThreads) {
     const uint32_t c = m.hist[hslot(b)];
     if (c != 0) {
 #pragma unroll
@@ -872,6 +872,160 @@ __device__ void cluster_merge_hist(const TopkSmem& m, uint32_t rank) {
     }
   }
   cluster_barrier();  // every contribution has landed
+}
+
+__device__ __forceinline__ uint32_t atom_add_cluster(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void red_min_cluster(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.min.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_max_cluster(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// The score-order fast path of linear_bucket_topk spread over a cluster: the row's extreme
+// keys are exchanged between the CL CTAs, each CTA counts its part into linear buckets, the
+// merged histogram (the same in every CTA) gives the threshold bucket and every bucket's
+// start, the candidates go straight from registers to CTA 0's buffer at their bucket's
+// slots (the bucket cursors live in CTA 0), and CTA 0 ranks them inside their buckets.
+// Returns false in every CTA, having written no output, when the row's scores are all
+// equal, a bucket at or above the threshold holds more than kBucketLimit keys, or the
+// candidates overflow CTA 0's buffer; the caller then takes the general path.
+template <int NB, int CL>
+__device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, long long n, int keep, int32_t* out,
+                                    int cand_cap, const TopkSmem& m, uint32_t* red, uint32_t* info, uint32_t* cmm,
+                                    uint32_t rank) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (cand_cap < kBins) return false;  // the bucket cursors need kBins words of m.ci (same in every CTA)
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  rs.visit([&](const uint32_t (&u)[4], long long, int c) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < c) { kmin = min(kmin, u[e]); kmax = max(kmax, u[e]); }
+  });
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) { red[warp] = kmin; red[kWarps + warp] = kmax; }
+  if (tid == 0) { cmm[0] = 0xFFFFFFFFu; cmm[1] = 0u; cmm[2] = 0xFFFFFFFFu; }
+  for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = m.merged[i] = 0;
+  __syncthreads();
+  cluster_barrier();  // every CTA's exchange slots are initialised
+  if (tid == 0) {
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) { kmin = min(kmin, red[w]); kmax = max(kmax, red[kWarps + w]); }
+#pragma unroll
+    for (int j = 0; j < CL; ++j) {
+      red_min_cluster(mapa(&cmm[0], static_cast<uint32_t>(j)), kmin);
+      red_max_cluster(mapa(&cmm[1], static_cast<uint32_t>(j)), kmax);
+    }
+  }
+  cluster_barrier();  // every CTA holds the row's extremes
+  const float lo = key_value(cmm[0]), hi = key_value(cmm[1]);
+  const float width = __fsub_rn(hi, lo);
+  const float scale = __fdiv_rn(static_cast<float>(kBins), width);
+  if (!(width > 0.f) || !(scale > 0.f) || isinf(width) || isinf(scale)) return false;  // the same in every CTA
+  rs.visit([&](const uint32_t (&u)[4], long long, int c) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < c) atomicAdd(&m.hist[hslot(lin_bucket(u[e], lo, scale))], 1u);
+  });
+  __syncthreads();
+  // Only the buckets at and above the lowest of the CTAs' own thresholds for keep / CL keys
+  // are merged: every CTA holds at least that many keys there, so the row's threshold
+  // bucket is among them (a CTA with fewer keys takes bucket 0, and everything is merged).
+  if (tid == 0) info[0] = 0u;
+  __syncthreads();
+  find_bucket(m.hist, kBins, static_cast<uint32_t>((keep + CL - 1) / CL), red, info);
+  if (tid == 0) {
+#pragma unroll
+    for (int j = 0; j < CL; ++j) red_min_cluster(mapa(&cmm[2], static_cast<uint32_t>(j)), info[0]);
+  }
+  cluster_barrier();  // every CTA holds the lowest local threshold
+  const int bmin = static_cast<int>(cmm[2]);
+  cluster_merge_hist<CL>(m, rank, bmin);
+  // descending exclusive scan of the merged histogram, identical in every CTA (exact at
+  // and above bmin, which the threshold bucket is)
+  const uint32_t want = static_cast<uint32_t>(keep);
+  const int b_hi = kBins - 16 * tid;
+  uint32_t sum = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) sum += m.merged[hslot(static_cast<uint32_t>(b_hi - 1 - j))];
+  uint32_t tot;
+  uint32_t r = block_excl_scan(sum, red, &tot);
+  uint32_t mx = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t b = static_cast<uint32_t>(b_hi - 1 - j);
+    const uint32_t cj = m.merged[hslot(b)];
+    if (r < want) {
+      mx = max(mx, cj);
+      if (r + cj >= want) {
+        info[0] = b;
+        info[1] = r + cj;
+      }
+    }
+    m.merged[hslot(b)] = r;  // start of bucket b
+    r += cj;
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  const uint32_t d1 = info[0], n_cand = info[1];
+  mx = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) mx = max(mx, red[w]);
+  if (mx > static_cast<uint32_t>(kBucketLimit) || n_cand > static_cast<uint32_t>(cand_cap)) return false;
+  // this CTA's slots in bucket b start after the lower-ranked CTAs' keys of that bucket:
+  // cursor[b] = start[b] + sum of their local counts (read from their shared memory)
+  uint32_t* cursor = m.ci;  // kBins words, plain bucket index
+  for (int b = tid + static_cast<int>(d1); b < kBins; b += kThreads) {
+    uint32_t pre = 0;
+#pragma unroll
+    for (int j = 0; j < CL; ++j)
+      if (j < static_cast<int>(rank)) pre += dsmem_ld(mapa(&m.hist[hslot(b)], static_cast<uint32_t>(j)));
+    cursor[b] = m.merged[hslot(b)] + pre;
+  }
+  __syncthreads();
+  const uint32_t bw0 = mapa(m.tk, 0);
+  // One integer compare rejects most keys: every key of a bucket >= d1 is at least the key
+  // of lo + (d1 - 1) / scale - (|lo| + |hi|) 2^-20 -- a whole bucket below the boundary, less
+  // a margin far above the roundings of lin_bucket and of this bound (each at most 2^-24 of
+  // |lo| + |hi|).  The exact bucket is taken only for the keys that pass.
+  const float tpre = lo + static_cast<float>(d1 > 0 ? d1 - 1 : 0) / scale - (fabsf(lo) + fabsf(hi)) * 0x1p-20f;
+  const uint32_t kpre = tpre > lo ? order_key(tpre) : 0u;
+  rs.visit([&](const uint32_t (&u)[4], long long i, int c4) {
+    const uint32_t i0 = static_cast<uint32_t>(part_lo + i);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (e < c4 && u[e] >= kpre) {
+        const uint32_t b = lin_bucket(u[e], lo, scale);
+        if (b >= d1) {
+          const uint32_t pos = atomicAdd(&cursor[b], 1u);
+          dsmem_st(bw0 + 8u * pos, ~(i0 + e));
+          dsmem_st(bw0 + 8u * pos + 4u, u[e]);
+        }
+      }
+    }
+  });
+  cluster_barrier();  // every candidate has landed in CTA 0; nobody touches its memory after this
+  if (rank != 0) return true;
+  // CTA 0: bucket b spans [start[b], start[b - 1]) (the buckets below follow it); the last
+  // candidate bucket d1 ends at n_cand
+  const uint64_t* bw = reinterpret_cast<const uint64_t*>(m.tk);
+  for (uint32_t p = tid; p < n_cand; p += kThreads) {
+    const uint64_t x = bw[p];
+    const uint32_t b = lin_bucket(static_cast<uint32_t>(x >> 32), lo, scale);
+    const uint32_t q0 = m.merged[hslot(b)], q1 = b > d1 ? m.merged[hslot(b - 1)] : n_cand;
+    uint32_t rk = q0;
+    for (uint32_t q = q0; q < q1; ++q) rk += bw[q] > x ? 1u : 0u;
+    if (rk < want) m.ck[rk] = ~static_cast<uint32_t>(x);
+  }
+  __syncthreads();
+  for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(m.ck[i]);
+  return true;
 }
 
 template <int NB, int CL>  // CL CTAs per row, each holding up to kWarps * NB * 128 keys in registers
@@ -882,6 +1036,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkArg
   __shared__ uint32_t red[2 * kWarps];
   __shared__ uint32_t info[4];
   __shared__ uint32_t counts[CL];
+  __shared__ uint32_t cmm[3];
   const TopkSmem m = topk_smem(smem, cand_cap);
   const uint32_t rank = cluster_rank();
   const RowInfo R = row_info(a, blockIdx.x / CL);
@@ -894,8 +1049,22 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkArg
   const long long part = ((R.n + CL - 1) / CL + 1023) & ~1023LL;
   const long long lo = min(R.n, static_cast<long long>(rank) * part);
   const long long len = min(R.n - lo, part);
+  const int row_id = static_cast<int>(blockIdx.x / CL);
+  if (a.prefetch_ahead > 0 && tid == 32 && row_id + a.prefetch_ahead < a.n_rows) {
+    // this CTA's part of the row a cluster one resident wave later reads: into L2 now
+    const RowInfo P = row_info(a, row_id + a.prefetch_ahead);
+    const long long ppart = ((P.n + CL - 1) / CL + 1023) & ~1023LL;
+    const long long plo = min(P.n, static_cast<long long>(rank) * ppart);
+    const long long plen = min(P.n - plo, ppart);
+    const long long bytes = ((plen + 3) & ~3LL) * 4;
+    if (plen > 0 && (reinterpret_cast<uintptr_t>(P.src + plo) & 15u) == 0)
+      ptx::bulk_prefetch_l2(P.src + plo, static_cast<uint32_t>(bytes));
+  }
   RegSeg<NB> rs;
   rs.init(R.src + lo, len);
+  if (by_score && cluster_linear_topk<NB, CL>(rs, lo, R.n, R.keep, R.out, cand_cap, m, red, info, cmm, rank))
+    return;
+  cluster_barrier();  // the general path below starts from clean buffers in every CTA
 
   const bool take_all = R.n <= R.keep;
   uint32_t T = 0;         // candidates: keys > T (every key when take_all)
@@ -1069,7 +1238,16 @@ cudaError_t launch_cluster_rows(const TopkArgs& a, int ccap, size_t csmem, cudaS
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_off() ? 1 : 2;
-  e = cudaLaunchKernelEx(&cfg, kern, a, ccap);
+  // rows one resident wave of clusters ahead are prefetched into L2 (clusters per SM pair
+  // from the occupancy of one CTA; cluster placement only lowers the real count)
+  TopkArgs b = a;
+  b.prefetch_ahead = 0;
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ==
+                                                cudaSuccess &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, csmem) == cudaSuccess)
+    b.prefetch_ahead = sms * per_sm / CL;
+  e = cudaLaunchKernelEx(&cfg, kern, b, ccap);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
