@@ -25,8 +25,9 @@
 //               coalesced fp32 stores.  Prefill tiles (N = 256) are split by columns
 //               between two warpgroups; decode tiles (N = max(64, H)) alternate
 //               between the warpgroups tile by tile.
-//   warps 10-13 only for bf16 queries against e4m3 keys (decode): widen each staged
-//               e4m3 key tile to bf16 into TMEM, the MMA's A operand there.
+//   bf16 queries against e4m3 keys (decode): the queries come as exact e4m3 hi / lo row
+//               pairs (qsplit.cuh), so the MMAs are FP8 and the epilogue adds the pair
+//               before the ReLU.
 // Every wait is bounded; on a timeout the kernel records kStatusTimeout, all roles
 // leave their loops, in-flight copies and MMAs are drained (bounded) and TMEM freed.
 #include "internal.h"
