@@ -578,7 +578,8 @@ def _sparse_mla_decode(dev, stream, peaks, iters=10):
     hbm = float(peaks["hbm_gbs"])
     g = torch.Generator(device=dev)
     g.manual_seed(13)
-    B, Hh, K, page, R, rd = 64, 64, 2048, 64, 512, 64
+    B = _env_int("DSA_BENCH_MLA_BATCH", 64)  # a smaller batch only for profiler captures
+    Hh, K, page, R, rd = 64, 2048, 64, 512, 64
     lens = workloads.decode_lens(B, 4096, 65536, 0)
     pages = [(L + page - 1) // page for L in lens]
     num_pages = sum(pages) + 1
@@ -606,7 +607,7 @@ def _sparse_mla_decode(dev, stream, peaks, iters=10):
     # algorithmic bytes: the selected latent rows, q, the selection and the fp32 output
     nbytes = B * K * (R + rd) * 2 + B * Hh * (R + rd) * 2 + B * K * 4 + B * Hh * R * 4
     flops = 2.0 * B * Hh * K * (R + rd + R)
-    out = {"workload": "sparse MLA decode B=64, one query per sequence, contexts U[4096, 65536], 64 heads, "
+    out = {"workload": f"sparse MLA decode B={B}, one query per sequence, contexts U[4096, 65536], 64 heads, "
                        "2048 selected keys per query, bf16 latent cache (kv_rank 512, rope 64, page 64)",
            "ms_per_step": ms, "queries_per_s": B / (ms / 1e3), "algorithmic_bytes": nbytes,
            "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm,
