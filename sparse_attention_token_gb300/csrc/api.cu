@@ -300,7 +300,8 @@ bool make_map_paged(CUtensorMap* m, const void* base, bool fp8, int D, int page_
 // Deepest key-tile ring that fits in shared memory (>= 2), or 0.  Decode tiles (N < 256
 // or split queries) have two key producers that own alternate stages: an even ring.
 int pick_stages(const ScoreArgs& a) {
-  const int step = (a.split || a.N != 256) ? 2 : 1;
+  // an even ring depth lets two producer warps alternate tiles (decode tiles, e4m3 tiles)
+  const int step = (a.split || a.N != 256 || a.k_fp8) ? 2 : 1;
   for (int s = kMaxKStages - kMaxKStages % step; s >= 2; s -= step)
     if (score_smem_bytes(a, s) <= kMaxSmem) return s;
   return 0;

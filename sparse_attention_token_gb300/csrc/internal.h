@@ -64,6 +64,9 @@ struct ScoreArgs {
   float* scores;
   long long ld;
   unsigned* status;   // device status word
+  // two key producers (warps 0 and 10 take alternate tiles, the ring depth even); else
+  // warp 0 alone (set by launch_score)
+  int two_producers;
   // failure-path test hook (0 = off): the MMA issuer first waits this many ns on a
   // barrier nothing arrives at, so the kernel takes its timeout-and-drain path
   unsigned long long probe_wait_ns;

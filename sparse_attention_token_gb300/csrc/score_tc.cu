@@ -11,14 +11,15 @@
 // (each query's H heads are H consecutive TMEM columns), K = D.  A TMEM lane then
 // holds every head of one (key, query) pair, so the head reduction is in-thread.
 //
-// Warp roles (one CTA per SM, persistent over work items; 320 threads, 352 for decode):
+// Warp roles (one CTA per SM, persistent over work items; 352 threads):
 //   warp 0      TMA producer: q tile (N x D) per item into a 2-deep ring, key tiles
 //               (128 x D, dense or gathered page by page through block_tables) into
 //               an nK-deep ring, per-item w / q_scale by cp.async, per-tile k_scale by
 //               cp.async (dense keys) or a bulk copy per page (paged keys).
-//   warp 10     decode only: a second key producer.  Warp 0 takes the even key tiles,
-//               warp 10 the odd ones (each owns alternate stages of an even ring), so
-//               the address work and TMA issue of one overlap the other's.
+//   warp 10     a second key producer when the key ring depth is even (decode tiles;
+//               e4m3 prefill tiles): warp 0 takes the even key tiles, warp 10 the odd
+//               ones (each owns alternate stages of the ring), so the address work and
+//               TMA issue of one overlap the other's.
 //   warp 1      TMEM allocator; lane 0 issues tcgen05.mma into two 256-column fp32
 //               accumulators (double buffered) and commits to mbarriers.
 //   warps 2..9  epilogue: tcgen05.ld, ReLU, head-weighted sum, k scale, causal mask,
@@ -118,8 +119,12 @@ struct Cfg {
   static constexpr int QROWS = SPLIT ? 2 * H : H;
   // decode tiles are short (16 or 32 KB) and HBM-bound: a second producer warp (warp 10)
   // takes every other key tile, which needs an even ring
-  static constexpr int NPROD = DECODE ? 2 : 1;
-  static constexpr int THREADS = kScoreThreads + 32 * (NPROD - 1);    // q rows per query
+  // a second key producer (warp 10) takes every other key tile when the ring depth is even:
+  // decode tiles are short and HBM-bound, and paged e4m3 prefill tiles cost the copy
+  // engine two instructions (page boxes, scale rows) per 16 KB, more than one warp's TMA
+  // issue keeps up with at the e4m3 MMA rate
+  static constexpr int NPROD = 2;
+  static constexpr int THREADS = kScoreThreads + 32 * (NPROD - 1);
 };
 
 // ------------------------------------------------------------------ producer (warp 0)
@@ -127,6 +132,7 @@ template <int H, bool DECODE, bool SPLIT>
 __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensorMap* tmap_q,
                                               const CUtensorMap* tmap_k, uint8_t* smem, const SmemPlan& P,
                                               uint64_t* bars, volatile int* abort, int n_items, int pw) {
+  if (pw == 1 && !a.two_producers) return;  // one producer: warp 0 takes every tile
   using C = Cfg<H, DECODE, SPLIT>;
   constexpr int N = C::N;
   const int lane = threadIdx.x & 31;
@@ -182,7 +188,7 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
     int pg_win = -1;
     const int pos_last = I.pos0 + I.nrows - 1;
     for (int kt = I.kt0; kt < I.kt1; ++kt) {
-      if (C::NPROD == 2 && (nk & 1u) != static_cast<uint32_t>(pw)) {
+      if (a.two_producers && (nk & 1u) != static_cast<uint32_t>(pw)) {
         ++nk;  // the other producer's tile (and stage)
         continue;
       }
@@ -258,7 +264,7 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
     const int kk = nk < static_cast<uint32_t>(nK) ? static_cast<int>(nk) : nK;
     for (int i = 1; i <= kk; ++i) {
       const uint32_t u = nk - i;
-      if (C::NPROD == 2 && (u & 1u) != static_cast<uint32_t>(pw)) continue;  // the other producer's copy
+      if (a.two_producers && (u & 1u) != static_cast<uint32_t>(pw)) continue;  // the other producer's copy
       ptx::mbar_wait_drain(&bars[kBarKFull + (u % nK)], (u / nK) & 1, a.status, kStatusTimeout, 200000000ull);
     }
   }
@@ -585,7 +591,7 @@ cudaError_t launch_t(const ScoreArgs& a, const CUtensorMap* tq, const CUtensorMa
   auto kern = score_kernel<H, DECODE, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  if (Cfg<H, DECODE, SPLIT>::NPROD == 2 && (a.num_k_stages & 1)) return cudaErrorInvalidValue;
+  if (a.two_producers && (a.num_k_stages & 1)) return cudaErrorInvalidValue;
   e = launch_pdl(kern, dim3(grid), dim3(Cfg<H, DECODE, SPLIT>::THREADS), smem, st, *tq, *tk, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -602,6 +608,9 @@ cudaError_t launch_score(const ScoreArgs& args, const CUtensorMap* tmap_q, const
   ScoreArgs a = args;
   a.probe_wait_ns = armed_probe_wait_ns();
   armed_probe_wait_ns() = 0;
+  // decode tiles always use both producers (their ring depth is even); prefill tiles when
+  // the ring depth is even (e4m3 tiles: ~10 stages; bf16 tiles fit 3 and keep one)
+  a.two_producers = (a.num_k_stages % 2 == 0) ? 1 : 0;
   const bool dec = a.split || a.N != 256;
 #define DSA_CASE(HH)                                                                        \
   case HH:                                                                                  \
