@@ -162,25 +162,38 @@ struct GlobalSeg {
   }
 };
 
-// Segment held in registers, loaded once with every load in flight (rows up to
-// kWarps * NB * 128 keys).
+// Segment held in registers as raw fp32 bits (rows up to kWarps * NB * 128 keys).  Every
+// load is issued before any loaded value is used, so a row costs one memory latency, not
+// one per block.  visit() hands out order-preserving keys (the general path); visit_f()
+// hands out the raw bits, and calls f with a constant count of 4 on the blocks that are
+// full for every lane of the warp.
 template <int NB>
 struct RegSeg {
   uint32_t v[NB][4];
   long long s0;
-  int len;  // keys of this warp's segment
-  int nb;
+  int len;    // keys of this warp's segment
+  int nb;     // blocks holding at least one key
+  int nfull;  // blocks full for every lane
   __device__ void init(const float* row, long long n) {
     const long long seg = seg_len(n);
     s0 = (threadIdx.x >> 5) * seg;
     const long long s1 = min(n, s0 + seg);
     len = s1 > s0 ? static_cast<int>(s1 - s0) : 0;
     nb = (len + 127) / 128;
+    nfull = len / 128;
+    const int l4 = 4 * static_cast<int>(threadIdx.x & 31);
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
-      const long long i = s0 + 128LL * j + 4 * (threadIdx.x & 31);
-      const int c = (j < nb && i < s1) ? load4(row, s1, i, v[j]) : 0;
-      if (c == 0) v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0u;
+      const int r = len - 128 * j - l4;  // keys of block j left from this lane's first one
+      const float* p = row + s0 + 128 * j + l4;
+      if (r >= 4) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(p));
+        v[j][0] = __float_as_uint(f.x); v[j][1] = __float_as_uint(f.y);
+        v[j][2] = __float_as_uint(f.z); v[j][3] = __float_as_uint(f.w);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[j][e] = e < r ? __float_as_uint(__ldg(p + e)) : 0u;
+      }
     }
   }
   // valid keys of block j for this lane (recomputed instead of held in registers)
@@ -194,9 +207,20 @@ struct RegSeg {
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
       if (j < nb) {
-        uint32_t u[4] = {v[j][0], v[j][1], v[j][2], v[j][3]};
+        uint32_t u[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) u[e] = order_key(__uint_as_float(v[j][e]));
         f(u, s0 + 128LL * j + 4 * lane, count(j));
       }
+    }
+  }
+  template <class F>
+  __device__ __forceinline__ void visit_f(F f) const {
+    const uint32_t i0 = static_cast<uint32_t>(s0) + 4u * (threadIdx.x & 31);
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      if (j < nfull) f(v[j], i0 + 128u * j, 4);
+      else if (j < nb) f(v[j], i0 + 128u * j, count(j));
     }
   }
 };
@@ -550,14 +574,64 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Bucket of a score on a linear grid of kBins equal-width buckets between the row's
+// Bucket of score x on a linear grid of kBins equal-width buckets between the row's
 // smallest score lo and its largest: floor((x - lo) * scale), at most kBins - 1.  Every
 // step is a correctly rounded IEEE operation (no contraction), so the bucket is a
-// non-decreasing function of x and the same key always lands in the same bucket.
-__device__ __forceinline__ uint32_t lin_bucket(uint32_t k, float lo, float scale) {
-  const float f = __fmul_rn(__fsub_rn(key_value(k), lo), scale);
-  const int b = __float2int_rz(f);
+// non-decreasing function of x and the same score always lands in the same bucket.
+__device__ __forceinline__ uint32_t lin_bucket(float x, float lo, float scale) {
+  const int b = __float2int_rz(__fmul_rn(__fsub_rn(x, lo), scale));
   return static_cast<uint32_t>(b < kBins - 1 ? b : kBins - 1);
+}
+
+// A candidate of the linear-bucket paths as one 8-byte word: the order-preserving key in
+// the high half; the bucket (12 bits) and the complemented key index (20 bits) in the low
+// half.  Words of one bucket compare like (key, then lower index first), so ranking a
+// candidate among its bucket-mates is one compare per mate, and the word itself says
+// which bucket to look in.
+constexpr int kIndexBits = 20;
+__device__ __forceinline__ uint2 cand_word(float x, uint32_t b, uint32_t idx) {
+  return make_uint2((b << kIndexBits) | (~idx & ((1u << kIndexBits) - 1u)), order_key(x));
+}
+__device__ __forceinline__ uint32_t cand_bucket(uint64_t w) { return static_cast<uint32_t>(w) >> kIndexBits; }
+__device__ __forceinline__ uint32_t cand_index(uint64_t w) {
+  return ~static_cast<uint32_t>(w) & ((1u << kIndexBits) - 1u);
+}
+
+// Descending exclusive scan of a kBins histogram in place: h[b] becomes the number of keys
+// in the buckets above b, the start of bucket b in descending order.  Thread t owns bins
+// 4095 - 16t .. 4080 - 16t.  The bucket where the running count from the top reaches want
+// goes to info[0] and the keys of the buckets at and above it to info[1]; info[2] is set
+// when one of those buckets holds more than kBucketLimit keys.  info[2] must be zero and
+// red free at entry; ends with a barrier.
+__device__ __forceinline__ void scan_desc_starts(uint32_t* h, uint32_t want, uint32_t* red, uint32_t* info) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b_hi = kBins - 16 * tid;
+  uint32_t c[16], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    c[j] = h[hslot(static_cast<uint32_t>(b_hi - 1 - j))];
+    sum += c[j];
+  }
+  const uint32_t incl = warp_incl_scan(sum);
+  if (lane == 31) red[warp] = incl;
+  __syncthreads();
+  uint32_t r = incl - sum;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) r += w < warp ? red[w] : 0u;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t b = static_cast<uint32_t>(b_hi - 1 - j);
+    if (r < want) {
+      if (c[j] > static_cast<uint32_t>(kBucketLimit)) info[2] = 1u;
+      if (r + c[j] >= want) {
+        info[0] = b;
+        info[1] = r + c[j];
+      }
+    }
+    h[hslot(b)] = r;
+    r += c[j];
+  }
+  __syncthreads();
 }
 
 // Score-order top-k of a row held in registers, in one histogram: the keys are counted
@@ -570,20 +644,23 @@ __device__ __forceinline__ uint32_t lin_bucket(uint32_t k, float lo, float scale
 // more than kBucketLimit keys, the candidates overflow the buffers, or the row's scores
 // are all equal; the caller then takes the general path.
 template <int NB>
-__device__ bool linear_bucket_topk(const RegSeg<NB>& rs, long long n, int keep, int32_t* out, int cand_cap,
-                                   const TopkSmem& m, uint32_t* red, uint32_t* info) {
+__device__ bool linear_bucket_topk(const RegSeg<NB>& rs, int keep, int32_t* out, int cand_cap, const TopkSmem& m,
+                                   uint32_t* red, uint32_t* info) {
+  static_assert(kWarps * NB * 128 <= (1 << kIndexBits), "key indices must fit the candidate word");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // the row's extreme keys
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  rs.visit([&](const uint32_t (&u)[4], long long, int c) {
+  // the histogram is cleared while the row's loads are still in flight
+  for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = 0;
+  if (tid == 0) info[2] = 0u;
+  // the row's extremes
+  float fmin = __int_as_float(0x7f800000), fmax = -fmin;
+  rs.visit_f([&](const uint32_t (&x)[4], uint32_t, int c) {
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      if (e < c) { kmin = min(kmin, u[e]); kmax = max(kmax, u[e]); }
+      if (e < c) { fmin = fminf(fmin, __uint_as_float(x[e])); fmax = fmaxf(fmax, __uint_as_float(x[e])); }
   });
-  kmin = __reduce_min_sync(0xffffffffu, kmin);
-  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  uint32_t kmin = __reduce_min_sync(0xffffffffu, order_key(fmin));
+  uint32_t kmax = __reduce_max_sync(0xffffffffu, order_key(fmax));
   if (lane == 0) { red[warp] = kmin; red[kWarps + warp] = kmax; }
-  for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = 0;
   __syncthreads();
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) { kmin = min(kmin, red[w]); kmax = max(kmax, red[kWarps + w]); }
@@ -592,71 +669,39 @@ __device__ bool linear_bucket_topk(const RegSeg<NB>& rs, long long n, int keep, 
   const float scale = __fdiv_rn(static_cast<float>(kBins), width);
   // all-equal rows, and ranges whose width or scale is not a positive finite number
   if (!(width > 0.f) || !(scale > 0.f) || isinf(width) || isinf(scale)) return false;  // uniform: same inputs
-  rs.visit([&](const uint32_t (&u)[4], long long, int c) {
+  rs.visit_f([&](const uint32_t (&x)[4], uint32_t, int c) {
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      if (e < c) atomicAdd(&m.hist[hslot(lin_bucket(u[e], lo, scale))], 1u);
+      if (e < c) atomicAdd(&m.hist[hslot(lin_bucket(__uint_as_float(x[e]), lo, scale))], 1u);
   });
   __syncthreads();
-  // descending exclusive scan: thread t owns bins 4095 - 16t .. 4080 - 16t, highest first.
-  // The threshold bucket d1 is where the running count from the top reaches keep; the
-  // buckets at and above it are exactly those that start below keep.
+  // red is free: its last readers passed the barrier above
   const uint32_t want = static_cast<uint32_t>(keep);
-  const int b_hi = kBins - 16 * tid;
-  uint32_t sum = 0;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) sum += m.hist[hslot(static_cast<uint32_t>(b_hi - 1 - j))];
-  uint32_t tot;
-  uint32_t r = block_excl_scan(sum, red, &tot);
-  uint32_t mx = 0;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const uint32_t b = static_cast<uint32_t>(b_hi - 1 - j);
-    const uint32_t cj = m.hist[hslot(b)];
-    if (r < want) {
-      mx = max(mx, cj);
-      if (r + cj >= want) {
-        info[0] = b;       // d1
-        info[1] = r + cj;  // candidates: every key of the buckets >= d1
-      }
-    }
-    m.hist[hslot(b)] = r;  // start of bucket b (each thread rewrites only its own bins)
-    r += cj;
-  }
-  mx = __reduce_max_sync(0xffffffffu, mx);
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
+  scan_desc_starts(m.hist, want, red, info);
   const uint32_t d1 = info[0], n_cand = info[1];
-  mx = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) mx = max(mx, red[w]);
-  // bw (n_cand 8-byte words) lives in tk and ti, 2 * cand_cap adjacent words
-  if (mx > static_cast<uint32_t>(kBucketLimit) || n_cand > static_cast<uint32_t>(cand_cap)) return false;
-  // scatter the candidates: key and complemented index in one word, so a larger word is a
-  // better key or the same key at a lower index
-  uint64_t* bw = reinterpret_cast<uint64_t*>(m.tk);
-  rs.visit([&](const uint32_t (&u)[4], long long i, int c4) {
-    const uint32_t i0 = static_cast<uint32_t>(i);
+  // candidate words (n_cand of 8 bytes) live in tk and ti, 2 * cand_cap adjacent words
+  if (info[2] != 0u || n_cand > static_cast<uint32_t>(cand_cap)) return false;
+  uint2* bw2 = reinterpret_cast<uint2*>(m.tk);
+  rs.visit_f([&](const uint32_t (&x)[4], uint32_t i, int c) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      if (e < c4) {
-        const uint32_t b = lin_bucket(u[e], lo, scale);
-        if (b >= d1) {
-          const uint32_t pos = atomicAdd(&m.hist[hslot(b)], 1u);
-          reinterpret_cast<uint2*>(bw)[pos] = make_uint2(~(i0 + e), u[e]);
-        }
+      if (e < c) {
+        const float f = __uint_as_float(x[e]);
+        const uint32_t b = lin_bucket(f, lo, scale);
+        if (b >= d1) bw2[atomicAdd(&m.hist[hslot(b)], 1u)] = cand_word(f, b, i + e);
       }
     }
   });
   __syncthreads();
   // hist[b] is now the end of bucket b; bucket b starts where bucket b + 1 ends
+  const uint64_t* bw = reinterpret_cast<const uint64_t*>(m.tk);
   for (uint32_t p = tid; p < n_cand; p += kThreads) {
     const uint64_t x = bw[p];
-    const uint32_t b = lin_bucket(static_cast<uint32_t>(x >> 32), lo, scale);
+    const uint32_t b = cand_bucket(x);
     const uint32_t q0 = b + 1 < static_cast<uint32_t>(kBins) ? m.hist[hslot(b + 1)] : 0u, q1 = m.hist[hslot(b)];
     uint32_t rank = q0;
     for (uint32_t q = q0; q < q1; ++q) rank += bw[q] > x ? 1u : 0u;
-    if (rank < want) m.ck[rank] = ~static_cast<uint32_t>(x);
+    if (rank < want) m.ck[rank] = cand_index(x);
   }
   __syncthreads();
   for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(m.ck[i]);
@@ -821,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, NB == 8 ? 3 : 2) topk_kernel(const T
   RS rs;
   rs.init(R.src, R.n);
   if constexpr (NB > 0) {
-    if (a.order == 0 && linear_bucket_topk(rs, R.n, R.keep, R.out, cand_cap, m, red, info)) return;
+    if (a.order == 0 && linear_bucket_topk(rs, R.keep, R.out, cand_cap, m, red, info)) return;
     __syncthreads();  // the general path reuses the shared buffers
   }
   row_topk(rs, R.n, R.keep, a.order == 0, R.out, cand_cap, m, red, info);
@@ -899,18 +944,20 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
                                     int cand_cap, const TopkSmem& m, uint32_t* red, uint32_t* info, uint32_t* cmm,
                                     uint32_t rank) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  static_assert(CL * kWarps * NB * 128 <= (1 << kIndexBits), "key indices must fit the candidate word");
   if (cand_cap < kBins) return false;  // the bucket cursors need kBins words of m.ci (same in every CTA)
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  rs.visit([&](const uint32_t (&u)[4], long long, int c) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (e < c) { kmin = min(kmin, u[e]); kmax = max(kmax, u[e]); }
-  });
-  kmin = __reduce_min_sync(0xffffffffu, kmin);
-  kmax = __reduce_max_sync(0xffffffffu, kmax);
-  if (lane == 0) { red[warp] = kmin; red[kWarps + warp] = kmax; }
+  // the histograms are cleared while the row's loads are still in flight
   if (tid == 0) { cmm[0] = 0xFFFFFFFFu; cmm[1] = 0u; cmm[2] = 0xFFFFFFFFu; }
   for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = m.merged[i] = 0;
+  float fmin = __int_as_float(0x7f800000), fmax = -fmin;
+  rs.visit_f([&](const uint32_t (&x)[4], uint32_t, int c) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < c) { fmin = fminf(fmin, __uint_as_float(x[e])); fmax = fmaxf(fmax, __uint_as_float(x[e])); }
+  });
+  uint32_t kmin = __reduce_min_sync(0xffffffffu, order_key(fmin));
+  uint32_t kmax = __reduce_max_sync(0xffffffffu, order_key(fmax));
+  if (lane == 0) { red[warp] = kmin; red[kWarps + warp] = kmax; }
   __syncthreads();
   cluster_barrier();  // every CTA's exchange slots are initialised
   if (tid == 0) {
@@ -927,10 +974,10 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
   const float width = __fsub_rn(hi, lo);
   const float scale = __fdiv_rn(static_cast<float>(kBins), width);
   if (!(width > 0.f) || !(scale > 0.f) || isinf(width) || isinf(scale)) return false;  // the same in every CTA
-  rs.visit([&](const uint32_t (&u)[4], long long, int c) {
+  rs.visit_f([&](const uint32_t (&x)[4], uint32_t, int c) {
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      if (e < c) atomicAdd(&m.hist[hslot(lin_bucket(u[e], lo, scale))], 1u);
+      if (e < c) atomicAdd(&m.hist[hslot(lin_bucket(__uint_as_float(x[e]), lo, scale))], 1u);
   });
   __syncthreads();
   // Only the buckets at and above the lowest of the CTAs' own thresholds for keep / CL keys
@@ -942,6 +989,7 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
   if (tid == 0) {
 #pragma unroll
     for (int j = 0; j < CL; ++j) red_min_cluster(mapa(&cmm[2], static_cast<uint32_t>(j)), info[0]);
+    info[2] = 0u;  // the overflow flag of the scan below
   }
   cluster_barrier();  // every CTA holds the lowest local threshold
   const int bmin = static_cast<int>(cmm[2]);
@@ -949,35 +997,9 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
   // descending exclusive scan of the merged histogram, identical in every CTA (exact at
   // and above bmin, which the threshold bucket is)
   const uint32_t want = static_cast<uint32_t>(keep);
-  const int b_hi = kBins - 16 * tid;
-  uint32_t sum = 0;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) sum += m.merged[hslot(static_cast<uint32_t>(b_hi - 1 - j))];
-  uint32_t tot;
-  uint32_t r = block_excl_scan(sum, red, &tot);
-  uint32_t mx = 0;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const uint32_t b = static_cast<uint32_t>(b_hi - 1 - j);
-    const uint32_t cj = m.merged[hslot(b)];
-    if (r < want) {
-      mx = max(mx, cj);
-      if (r + cj >= want) {
-        info[0] = b;
-        info[1] = r + cj;
-      }
-    }
-    m.merged[hslot(b)] = r;  // start of bucket b
-    r += cj;
-  }
-  mx = __reduce_max_sync(0xffffffffu, mx);
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
+  scan_desc_starts(m.merged, want, red, info);
   const uint32_t d1 = info[0], n_cand = info[1];
-  mx = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) mx = max(mx, red[w]);
-  if (mx > static_cast<uint32_t>(kBucketLimit) || n_cand > static_cast<uint32_t>(cand_cap)) return false;
+  if (info[2] != 0u || n_cand > static_cast<uint32_t>(cand_cap)) return false;
   // this CTA's slots in bucket b start after the lower-ranked CTAs' keys of that bucket:
   // cursor[b] = start[b] + sum of their local counts (read from their shared memory)
   uint32_t* cursor = m.ci;  // kBins words, plain bucket index
@@ -990,22 +1012,24 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
   }
   __syncthreads();
   const uint32_t bw0 = mapa(m.tk, 0);
-  // One integer compare rejects most keys: every key of a bucket >= d1 is at least the key
-  // of lo + (d1 - 1) / scale - (|lo| + |hi|) 2^-20 -- a whole bucket below the boundary, less
-  // a margin far above the roundings of lin_bucket and of this bound (each at most 2^-24 of
-  // |lo| + |hi|).  The exact bucket is taken only for the keys that pass.
+  // One compare rejects most keys: every score of a bucket >= d1 is at least
+  // lo + (d1 - 1) / scale - (|lo| + |hi|) 2^-20 -- a whole bucket below the boundary, less a
+  // margin far above the roundings of lin_bucket and of this bound (each at most 2^-24 of
+  // |lo| + |hi|).  The exact bucket is taken only for the scores that pass.
   const float tpre = lo + static_cast<float>(d1 > 0 ? d1 - 1 : 0) / scale - (fabsf(lo) + fabsf(hi)) * 0x1p-20f;
-  const uint32_t kpre = tpre > lo ? order_key(tpre) : 0u;
-  rs.visit([&](const uint32_t (&u)[4], long long i, int c4) {
-    const uint32_t i0 = static_cast<uint32_t>(part_lo + i);
+  const float fpre = tpre > lo ? tpre : lo;
+  rs.visit_f([&](const uint32_t (&x)[4], uint32_t i, int c4) {
+    const uint32_t i0 = static_cast<uint32_t>(part_lo) + i;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      if (e < c4 && u[e] >= kpre) {
-        const uint32_t b = lin_bucket(u[e], lo, scale);
+      const float f = __uint_as_float(x[e]);
+      if (e < c4 && f >= fpre) {
+        const uint32_t b = lin_bucket(f, lo, scale);
         if (b >= d1) {
           const uint32_t pos = atomicAdd(&cursor[b], 1u);
-          dsmem_st(bw0 + 8u * pos, ~(i0 + e));
-          dsmem_st(bw0 + 8u * pos + 4u, u[e]);
+          const uint2 w = cand_word(f, b, i0 + e);
+          dsmem_st(bw0 + 8u * pos, w.x);
+          dsmem_st(bw0 + 8u * pos + 4u, w.y);
         }
       }
     }
@@ -1017,11 +1041,11 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
   const uint64_t* bw = reinterpret_cast<const uint64_t*>(m.tk);
   for (uint32_t p = tid; p < n_cand; p += kThreads) {
     const uint64_t x = bw[p];
-    const uint32_t b = lin_bucket(static_cast<uint32_t>(x >> 32), lo, scale);
+    const uint32_t b = cand_bucket(x);
     const uint32_t q0 = m.merged[hslot(b)], q1 = b > d1 ? m.merged[hslot(b - 1)] : n_cand;
     uint32_t rk = q0;
     for (uint32_t q = q0; q < q1; ++q) rk += bw[q] > x ? 1u : 0u;
-    if (rk < want) m.ck[rk] = ~static_cast<uint32_t>(x);
+    if (rk < want) m.ck[rk] = cand_index(x);
   }
   __syncthreads();
   for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(m.ck[i]);
