@@ -597,6 +597,20 @@ __device__ __forceinline__ uint32_t cand_index(uint64_t w) {
   return ~static_cast<uint32_t>(w) & ((1u << kIndexBits) - 1u);
 }
 
+// Words in bw[q0, q1) greater than x (x's bucket-mates that beat it), four loads at a time
+// so that a bucket of a few keys costs one shared-memory latency.
+__device__ __forceinline__ uint32_t mates_above(const uint64_t* bw, uint32_t q0, uint32_t q1, uint64_t x) {
+  uint32_t n = 0;
+  for (uint32_t q = q0; q < q1; q += 4) {
+    const uint64_t y0 = bw[q];
+    const uint64_t y1 = q + 1 < q1 ? bw[q + 1] : 0ull;
+    const uint64_t y2 = q + 2 < q1 ? bw[q + 2] : 0ull;
+    const uint64_t y3 = q + 3 < q1 ? bw[q + 3] : 0ull;
+    n += (y0 > x ? 1u : 0u) + (y1 > x ? 1u : 0u) + (y2 > x ? 1u : 0u) + (y3 > x ? 1u : 0u);
+  }
+  return n;
+}
+
 // Descending exclusive scan of a kBins histogram in place: h[b] becomes the number of keys
 // in the buckets above b, the start of bucket b in descending order.  Thread t owns bins
 // 4095 - 16t .. 4080 - 16t.  The bucket where the running count from the top reaches want
@@ -604,12 +618,15 @@ __device__ __forceinline__ uint32_t cand_index(uint64_t w) {
 // when one of those buckets holds more than kBucketLimit keys.  info[2] must be zero and
 // red free at entry; ends with a barrier.
 __device__ __forceinline__ void scan_desc_starts(uint32_t* h, uint32_t want, uint32_t* red, uint32_t* info) {
+  static_assert(kBins == 16 * kThreads, "one group of 16 bins per thread");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b_hi = kBins - 16 * tid;
+  // bins b_hi - 1 - j of this thread's group g = 255 - tid sit at slots 17 g + 15 - j
+  uint32_t* hg = h + hslot(static_cast<uint32_t>(b_hi - 1));
   uint32_t c[16], sum = 0;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    c[j] = h[hslot(static_cast<uint32_t>(b_hi - 1 - j))];
+    c[j] = hg[-j];
     sum += c[j];
   }
   const uint32_t incl = warp_incl_scan(sum);
@@ -628,7 +645,7 @@ __device__ __forceinline__ void scan_desc_starts(uint32_t* h, uint32_t want, uin
         info[1] = r + c[j];
       }
     }
-    h[hslot(b)] = r;
+    hg[-j] = r;
     r += c[j];
   }
   __syncthreads();
@@ -699,8 +716,7 @@ __device__ bool linear_bucket_topk(const RegSeg<NB>& rs, int keep, int32_t* out,
     const uint64_t x = bw[p];
     const uint32_t b = cand_bucket(x);
     const uint32_t q0 = b + 1 < static_cast<uint32_t>(kBins) ? m.hist[hslot(b + 1)] : 0u, q1 = m.hist[hslot(b)];
-    uint32_t rank = q0;
-    for (uint32_t q = q0; q < q1; ++q) rank += bw[q] > x ? 1u : 0u;
+    const uint32_t rank = q0 + mates_above(bw, q0, q1, x);
     if (rank < want) m.ck[rank] = cand_index(x);
   }
   __syncthreads();
@@ -1043,8 +1059,7 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
     const uint64_t x = bw[p];
     const uint32_t b = cand_bucket(x);
     const uint32_t q0 = m.merged[hslot(b)], q1 = b > d1 ? m.merged[hslot(b - 1)] : n_cand;
-    uint32_t rk = q0;
-    for (uint32_t q = q0; q < q1; ++q) rk += bw[q] > x ? 1u : 0u;
+    const uint32_t rk = q0 + mates_above(bw, q0, q1, x);
     if (rk < want) m.ck[rk] = cand_index(x);
   }
   __syncthreads();
