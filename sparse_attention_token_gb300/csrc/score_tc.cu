@@ -68,6 +68,25 @@ enum {
 };
 static_assert(kBarEnd <= 64, "barrier region");
 
+// Advance a ring position (slot, phase parity) by one: no division on the per-tile path.
+__device__ __forceinline__ void ring_next(uint32_t& slot, uint32_t& phase, int n) {
+  if (++slot == static_cast<uint32_t>(n)) {
+    slot = 0;
+    phase ^= 1u;
+  }
+}
+
+// A wait of a role that has slack.  e4m3 prefill tiles are bound by the epilogue: the
+// producers (free ring slots) and the MMA issuer (free accumulators) wait most of the
+// time, and spinning there takes issue slots from the epilogue warps sharing their
+// schedulers, so those waits suspend in hardware until the phase completes.  Elsewhere
+// these roles are on the critical path and poll.
+__device__ __forceinline__ bool slack_wait(uint64_t* bar, uint32_t parity, bool suspend, volatile int* abort,
+                                           unsigned* status) {
+  return suspend ? ptx::mbar_wait_hint(bar, parity, abort, status, kStatusTimeout)
+                 : ptx::mbar_wait(bar, parity, abort, status, kStatusTimeout);
+}
+
 struct ItemInfo {
   int row0, pos0, kt0, kt1, b, nrows;
 };
@@ -149,6 +168,7 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
   const uint32_t page_bytes = static_cast<uint32_t>(PS) * a.D * k_esz;
 
   uint32_t nq = 0, nk = 0;
+  uint32_t ks_slot = 0, ks_phase = 0;  // key ring slot of tile nk and its phase parity
   bool ok = true;
   for (int it = 0; ok; ++it) {
     ItemInfo I;
@@ -190,12 +210,13 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
     for (int kt = I.kt0; kt < I.kt1; ++kt) {
       if (a.two_producers && (nk & 1u) != static_cast<uint32_t>(pw)) {
         ++nk;  // the other producer's tile (and stage)
+        ring_next(ks_slot, ks_phase, nK);
         continue;
       }
-      const int s = nk % nK;
+      const int s = static_cast<int>(ks_slot);
       int good = 1;
       if (lane == 0) {
-        good = ptx::mbar_wait(&bars[kBarKEmpty + s], ((nk / nK) & 1) ^ 1, abort, a.status, kStatusTimeout);
+        good = slack_wait(&bars[kBarKEmpty + s], ks_phase ^ 1u, a.q_fp8 && !DECODE, abort, a.status);
       }
       good = __shfl_sync(0xffffffffu, good, 0);
       if (!good) { ok = false; break; }
@@ -251,6 +272,7 @@ __device__ __forceinline__ void producer_role(const ScoreArgs& a, const CUtensor
         }
       }
       ++nk;
+      ring_next(ks_slot, ks_phase, nK);
     }
   }
   // Drain: wait (bounded) until the copies this warp issued into the rings have
@@ -300,7 +322,7 @@ __device__ __forceinline__ void mma_loop(const ScoreArgs& a, uint8_t* smem, cons
     for (int kt = I.kt0; kt < I.kt1; ++kt) {
       const int acc = nt & 1;
       if (!ptx::mbar_wait(&bars[kBarKFull + sk], kphase, abort, a.status, kStatusTimeout) ||
-          !ptx::mbar_wait(&bars[kBarTEmpty + acc], ((nt >> 1) & 1) ^ 1, abort, a.status, kStatusTimeout)) {
+          !slack_wait(&bars[kBarTEmpty + acc], ((nt >> 1) & 1) ^ 1, F8 && !DECODE, abort, a.status)) {
         ok = false;
         break;
       }
@@ -369,6 +391,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
   const int fold_t = DECODE ? static_cast<int>(threadIdx.x) - 64 : static_cast<int>(threadIdx.x) - 64 - half * 128;
 
   uint32_t nq = 0, nk = 0, nt = 0;
+  uint32_t ks_slot = 0, ks_phase = 0;  // key ring slot of tile nk and its phase parity
   bool ok = true;
   for (int it = 0; ok; ++it) {
     ItemInfo I;
@@ -385,7 +408,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
       if (!warp_wait(fb, (nq >> 1) & 1, abort, a.status)) break;
     }
     for (int kt = I.kt0; kt < I.kt1; ++kt) {
-      const int sk = nk % nK;
+      const int sk = static_cast<int>(ks_slot);
       const int acc = nt & 1;
       const bool mine = DECODE ? (acc == half) : true;
       if (mine) {
@@ -393,7 +416,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
         // accumulator wait, so the ring turns over as soon as the MMA is done with it
         float ks = 1.f;
         if (a.k_fp8) {
-          if (!warp_wait(&bars[kBarKFull + sk], (nk / nK) & 1, abort, a.status)) {
+          if (!warp_wait(&bars[kBarKFull + sk], ks_phase, abort, a.status)) {
             ok = false;
             break;
           }
@@ -500,6 +523,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
         }
       }
       ++nk;
+      ring_next(ks_slot, ks_phase, nK);
       ++nt;
     }
     if (!ok) break;

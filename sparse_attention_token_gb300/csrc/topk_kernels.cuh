@@ -578,9 +578,14 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // smallest score lo and its largest: floor((x - lo) * scale), at most kBins - 1.  Every
 // step is a correctly rounded IEEE operation (no contraction), so the bucket is a
 // non-decreasing function of x and the same score always lands in the same bucket.
+// The floor is taken without a conversion instruction (those issue at a quarter of the
+// FP32 rate): for 0 <= y < 2^23, y + 2^23 rounded toward zero is 2^23 + floor(y), whose
+// low 23 bits are floor(y).  y = (x - lo) * scale is never negative (x >= lo) and at most
+// about kBins.
 __device__ __forceinline__ uint32_t lin_bucket(float x, float lo, float scale) {
-  const int b = __float2int_rz(__fmul_rn(__fsub_rn(x, lo), scale));
-  return static_cast<uint32_t>(b < kBins - 1 ? b : kBins - 1);
+  const float y = __fmul_rn(__fsub_rn(x, lo), scale);
+  const uint32_t b = __float_as_uint(__fadd_rz(y, 0x1p23f)) & 0x7FFFFFu;
+  return b < static_cast<uint32_t>(kBins - 1) ? b : static_cast<uint32_t>(kBins - 1);
 }
 
 // A candidate of the linear-bucket paths as one 8-byte word: the order-preserving key in
@@ -898,6 +903,9 @@ __device__ __forceinline__ uint32_t dsmem_ld(uint32_t addr) {
 __device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ void dsmem_st2(uint32_t addr, uint2 v) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -1043,9 +1051,7 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
         const uint32_t b = lin_bucket(f, lo, scale);
         if (b >= d1) {
           const uint32_t pos = atomicAdd(&cursor[b], 1u);
-          const uint2 w = cand_word(f, b, i0 + e);
-          dsmem_st(bw0 + 8u * pos, w.x);
-          dsmem_st(bw0 + 8u * pos + 4u, w.y);
+          dsmem_st2(bw0 + 8u * pos, cand_word(f, b, i0 + e));
         }
       }
     }
