@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdsa_indexer.so")
-SOURCES = ["api.cu", "score_tc.cu", "score_tc2.cu", "topk.cu", "topk_cluster_8x4.cu", "topk_cluster_16x4.cu", "topk_cluster_16x8.cu", "static_ws.cu", "host_pipe.cu", "cache_append.cu", "qsplit.cu", "frontend.cu", "proj_gemm.cu", "shard.cu", "sparse_mla.cu"]
+SOURCES = ["api.cu", "score_tc.cu", "topk.cu", "topk_cluster_8x4.cu", "topk_cluster_16x4.cu", "topk_cluster_16x8.cu", "static_ws.cu", "host_pipe.cu", "cache_append.cu", "qsplit.cu", "frontend.cu", "proj_gemm.cu", "shard.cu", "sparse_mla.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 

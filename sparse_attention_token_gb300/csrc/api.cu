@@ -307,35 +307,14 @@ int pick_stages(const ScoreArgs& a) {
   return 0;
 }
 
-int pick_stages_pair(const ScoreArgs& a) {
-  for (int s = kMaxKStages; s >= 2; --s)
-    if (score_pair_smem_bytes(a, s) <= kMaxSmem) return s;
-  return 0;
-}
-
-// Prefill tiles (N = 256) run on the single-SM kernel; DSA_PAIR_MMA=1 selects the
-// CTA-pair (2-SM MMA) kernel instead, which is correct but measured slower on GB300.
-bool use_pair_mma() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = std::getenv("DSA_PAIR_MMA");
-    v = (e && e[0] == '1') ? 1 : 0;
-  }
-  return v == 1;
-}
-
 size_t score_launch_smem(const ScoreArgs& a) {
   return std::max<size_t>(score_smem_bytes(a, a.num_k_stages), 120 * 1024);
-}
-
-size_t score_pair_launch_smem(const ScoreArgs& a) {
-  return std::max<size_t>(score_pair_smem_bytes(a, a.num_k_stages), 120 * 1024);
 }
 
 dsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
 struct PagedPlan {
-  bool decode, pair, split;
+  bool decode, split;
   bool balanced;  // one chunk of split key ranges: per-CTA balanced lists (prep_balanced_kernel)
   int NQ, N, KC, R, n_chunks, cap, tile_keys;
   int G, per_cta, q_max;
@@ -371,8 +350,7 @@ dsa_status plan_paged(const dsa_indexer_args* a, PagedPlan* p) {
   const int ns = std::max(num_sms(), 1);
   p->N = p->split ? std::max(64, 2 * a->H) : (p->decode ? std::max(64, a->H) : 256);
   p->NQ = p->split ? 1 : p->N / a->H;
-  p->pair = !p->decode && use_pair_mma();
-  p->tile_keys = p->pair ? 2 * kBlockM : kBlockM;
+  p->tile_keys = kBlockM;
   p->ld = (std::max(a->max_seq_len, 1) + 3) & ~3LL;
   long long R = static_cast<long long>(kScoreChunkBudget / (static_cast<size_t>(p->ld) * 4));
   R = std::max<long long>(R - R % p->NQ, p->NQ);
@@ -380,11 +358,11 @@ dsa_status plan_paged(const dsa_indexer_args* a, PagedPlan* p) {
   p->R = static_cast<int>(R);
   p->n_chunks = std::max(1, (a->total_q + p->R - 1) / p->R);
   const long long qb_per_chunk = (p->R + p->NQ - 1) / p->NQ + std::min<long long>(a->B, p->R) + 1;
-  p->KC = qb_per_chunk < 2LL * ns ? (p->pair ? 8 : 16) : 0;
+  p->KC = qb_per_chunk < 2LL * ns ? 16 : 0;
   const long long kt_max = (a->max_seq_len + p->tile_keys - 1) / p->tile_keys;
   const long long per_qb = p->KC > 0 ? (kt_max + p->KC - 1) / p->KC : 1;
   long long cap = qb_per_chunk * std::max<long long>(per_qb, 1);
-  p->balanced = p->KC > 0 && !p->pair && p->n_chunks == 1;
+  p->balanced = p->KC > 0 && p->n_chunks == 1;
   p->G = ns;
   p->q_max = static_cast<int>(qb_per_chunk);
   p->per_cta = p->q_max + 1;  // a CTA's share meets at most every query block
@@ -444,7 +422,7 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
   s.scores = scores;
   s.ld = p.ld;
   s.status = status;
-  s.num_k_stages = p.pair ? pick_stages_pair(s) : pick_stages(s);
+  s.num_k_stages = pick_stages(s);
   if (s.num_k_stages < 2) return DSA_ERR_UNSUPPORTED;
 
   CUtensorMap tq, tk;
@@ -461,8 +439,7 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
     s.num_k_stages = pick_stages(s);
     if (s.num_k_stages < 2) return DSA_ERR_UNSUPPORTED;
     if (!make_map_2d(&tq, q8, true, a->D, static_cast<long long>(a->total_q) * 2 * a->H, p.N)) return DSA_ERR_CUDA;
-  } else if (!make_map_2d(&tq, a->q, fp8, a->D, static_cast<long long>(a->total_q) * a->H,
-                          p.pair ? p.N / 2 : p.N)) {
+  } else if (!make_map_2d(&tq, a->q, fp8, a->D, static_cast<long long>(a->total_q) * a->H, p.N)) {
     return DSA_ERR_CUDA;
   }
   if (!make_map_paged(&tk, a->k_cache, s.k_fp8 != 0, a->D, a->page_size, std::max(a->num_pages, 1)))
@@ -493,14 +470,13 @@ dsa_status run_paged(const dsa_indexer_args* a, const PagedPlan& p, cudaStream_t
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return DSA_ERR_CUDA;
   const int ns = std::max(num_sms(), 1);
-  const size_t smem = p.pair ? score_pair_launch_smem(s) : score_launch_smem(s);
+  const size_t smem = score_launch_smem(s);
   for (int c = 0; c < p.n_chunks; ++c) {
     s.items = items + static_cast<long long>(c) * p.cap;
     s.n_items = counts + c;
     s.items_cap = p.cap;
     s.row_base = c * p.R;
-    e = p.pair ? launch_score_pair(s, &tq, &tk, std::max(2, ns & ~1), smem, st)
-               : launch_score(s, &tq, &tk, p.balanced ? p.G : ns, smem, st);
+    e = launch_score(s, &tq, &tk, p.balanced ? p.G : ns, smem, st);
     if (e != cudaSuccess) return DSA_ERR_CUDA;
     TopkArgs t{};
     t.scores = scores;
@@ -609,18 +585,13 @@ dsa_status dense_scores(const void* q, int q_dtype, const float* q_scale, const 
   a.scores = scores;
   a.ld = ld_scores;
   a.status = status;
-  const bool pair = use_pair_mma();
-  a.num_k_stages = pair ? pick_stages_pair(a) : pick_stages(a);
+  a.num_k_stages = pick_stages(a);
   if (a.num_k_stages < 2) return DSA_ERR_UNSUPPORTED;
 
   CUtensorMap tq, tk;
-  if (!make_map_2d(&tq, q, fp8, D, static_cast<long long>(T) * H, pair ? a.N / 2 : a.N)) return DSA_ERR_CUDA;
+  if (!make_map_2d(&tq, q, fp8, D, static_cast<long long>(T) * H, a.N)) return DSA_ERR_CUDA;
   if (!make_map_2d(&tk, k, fp8, D, S, kBlockM)) return DSA_ERR_CUDA;
   const int ns = std::max(num_sms(), 1);
-  if (pair) {
-    const int pairs = std::max(1, std::min(ns / 2, a.n_dense_items));
-    return from_cuda(launch_score_pair(a, &tq, &tk, 2 * pairs, score_pair_launch_smem(a), stream));
-  }
   const int grid = std::min(ns, a.n_dense_items);
   return from_cuda(launch_score(a, &tq, &tk, grid, score_launch_smem(a), stream));
 }

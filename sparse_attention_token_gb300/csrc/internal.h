@@ -134,10 +134,6 @@ inline unsigned long long& armed_probe_wait_ns() {
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
                          int grid, size_t smem_bytes, cudaStream_t st);
 size_t score_smem_bytes(const ScoreArgs& a, int num_k_stages);
-// Prefill (N = 256) on CTA pairs: grid = 2 x pairs, work items in 256-key tiles.
-cudaError_t launch_score_pair(const ScoreArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k, int grid,
-                              size_t smem_bytes, cudaStream_t st);
-size_t score_pair_smem_bytes(const ScoreArgs& a, int num_k_stages);
 cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st);
 unsigned* device_status_ptr();  // address of the status word on the current device
 // New indexer keys through slot_mapping into the paged cache (bf16 copy or per-token

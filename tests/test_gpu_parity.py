@@ -361,34 +361,6 @@ def test_indexshare_rejects_before_launch():
         dsa.dsa_indexer_stack(["full", "full"], [a, None])      # a full layer without its cache
 
 
-# ----------------------------------------------------------------------------- CTA-pair kernel
-
-def test_pair_kernel_matches_oracle_in_subprocess():
-    """The 2-SM (CTA pair) prefill kernel, selected by DSA_PAIR_MMA=1, on dense and paged
-    integer inputs: run in a fresh process so the selection takes effect."""
-    import os, subprocess, sys
-    code = r"""
-import numpy as np, torch, oracle, workloads, sparse_attention_token_gb300 as dsa
-c = workloads.dense_case(300, 700, 64, 128, 96, q_pos0=400, integer=True, int_range=(-2, 2), seed=51)
-sc = dsa.dsa_indexer_scores(c.q.cuda(), c.k.cuda(), c.w.cuda(), q_pos0=c.q_pos0)
-tk = dsa.dsa_indexer_topk(sc, T=c.T, S=c.S, q_pos0=c.q_pos0, topk_limit=96)
-rt, rs, _ = oracle.dense(c.q, c.k, c.w, T=c.T, S=c.S, H=64, D=128, q_pos0=c.q_pos0, topk_limit=96, k_out=96, want_scores=True)
-g = sc.cpu().numpy()[:, :c.S]; vis = np.isfinite(rs)
-assert np.array_equal(g[vis], rs[vis]) and np.array_equal(tk.cpu().numpy(), rt)
-pc = workloads.paged_case([900, 300], [260, 40], 64, 128, 128, page_size=64, q_dtype="fp8_e4m3", k_dtype="fp8_e4m3", integer=True, seed=52)
-to = lambda t: None if t is None else t.cuda()
-got = dsa.dsa_indexer(to(pc.q), to(pc.w), to(pc.k_cache), to(pc.cu_q_lens), to(pc.seq_lens), to(pc.block_tables), max_seq_len=pc.max_seq_len, topk_limit=128, q_scale=to(pc.q_scale), k_scale_cache=to(pc.k_scale_cache))
-ref, _, _ = oracle.paged(pc)
-assert np.array_equal(got.cpu().numpy(), ref)
-assert dsa.dsa_check_device_status() == 0
-print("pair ok")
-"""
-    env = dict(os.environ, DSA_PAIR_MMA="1")
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0 and "pair ok" in r.stdout, r.stdout + r.stderr
-
-
 # --------------------------------------------------- host-memory entry point (pipelined)
 
 @pytest.mark.parametrize("chunk_rows,order", [(0, 0), (700, 1), (3000, 0), (97, 0)])
