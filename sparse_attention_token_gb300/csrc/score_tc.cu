@@ -422,7 +422,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
           }
           ks = ksbuf[sk * kBlockM + m];
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&bars[kBarKEmpty + sk]);
+          ptx::mbar_arrive_elect(&bars[kBarKEmpty + sk]);
         }
         if (!warp_wait(&bars[kBarTFull + acc], (nt >> 1) & 1, abort, a.status)) {
           ok = false;
@@ -510,16 +510,14 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bars[kBarTEmpty + acc]);
+        ptx::mbar_arrive_elect(&bars[kBarTEmpty + acc]);
         const int s = kt * kBlockM + m;
         const bool key_ok = a.paged || s < a.S;
 #pragma unroll
         for (int j = 0; j < QH; ++j) {
           const int qi = q0 + j;
-          if (qi < I.nrows && key_ok && s <= I.pos0 + qi) {
-            float* dst = a.scores + static_cast<long long>(I.row0 + qi - a.row_base) * a.ld + s;
-            *dst = accq[j] * ks;
-          }
+          float* dst = a.scores + static_cast<long long>(I.row0 + qi - a.row_base) * a.ld + s;
+          ptx::st_global_if(dst, accq[j] * ks, qi < I.nrows && key_ok && s <= I.pos0 + qi);
         }
       }
       ++nk;
@@ -528,7 +526,7 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
     }
     if (!ok) break;
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&bars[kBarQEmpty + sq]);
+    ptx::mbar_arrive_elect(&bars[kBarQEmpty + sq]);
     ++nq;
   }
 }
