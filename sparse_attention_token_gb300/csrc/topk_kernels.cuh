@@ -431,6 +431,7 @@ __device__ __forceinline__ uint32_t bucket_key(uint32_t u, uint32_t floor_mag) {
 }
 
 constexpr int kBucketLimit = 64;
+constexpr int kScatterQueue = 160;  // a warp's queue: 31 left over + 4 x 32 from one block
 constexpr int kSortBuckets = 4096;
 
 __device__ bool bucket_rank_out(uint32_t* ck, const uint32_t* ci, int n, int keep, uint32_t* bk,
@@ -1042,20 +1043,37 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
   // |lo| + |hi|).  The exact bucket is taken only for the scores that pass.
   const float tpre = lo + static_cast<float>(d1 > 0 ? d1 - 1 : 0) / scale - (fabsf(lo) + fabsf(hi)) * 0x1p-20f;
   const float fpre = tpre > lo ? tpre : lo;
+  // The keys that pass go through a per-warp queue in shared memory (ballots give their
+  // slots), and the queue is placed 32 entries at a time with every lane busy: a few
+  // percent of a long row's keys pass, so placing them where they lie would run the
+  // placement code for most of the warp's key slots with one or two lanes active.
+  // m.ck is free until CTA 0 ranks (after the cluster barrier below).
+  static_assert(kWarps * kScatterQueue * 2 <= kBins, "scatter queues fit m.ck");
+  uint2* q = reinterpret_cast<uint2*>(m.ck) + warp * kScatterQueue;
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t qn = 0;  // entries in this warp's queue (the same in every lane)
+  auto place = [&](uint2 w) {
+    const float f = __uint_as_float(w.x);
+    const uint32_t b = lin_bucket(f, lo, scale);
+    if (b >= d1) dsmem_st2(bw0 + 8u * atomicAdd(&cursor[b], 1u), cand_word(f, b, w.y));
+  };
   rs.visit_f([&](const uint32_t (&x)[4], uint32_t i, int c4) {
     const uint32_t i0 = static_cast<uint32_t>(part_lo) + i;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float f = __uint_as_float(x[e]);
-      if (e < c4 && f >= fpre) {
-        const uint32_t b = lin_bucket(f, lo, scale);
-        if (b >= d1) {
-          const uint32_t pos = atomicAdd(&cursor[b], 1u);
-          dsmem_st2(bw0 + 8u * pos, cand_word(f, b, i0 + e));
-        }
-      }
+      const bool pass = e < c4 && __uint_as_float(x[e]) >= fpre;
+      const uint32_t bal = __ballot_sync(0xffffffffu, pass);
+      if (pass) q[qn + __popc(bal & lt)] = make_uint2(x[e], i0 + e);
+      qn += __popc(bal);
+    }
+    __syncwarp();
+    while (qn >= 32) {
+      qn -= 32;
+      place(q[qn + lane]);
+      __syncwarp();  // the slots just read are refilled by the next block
     }
   });
+  if (lane < qn) place(q[lane]);
   cluster_barrier();  // every candidate has landed in CTA 0; nobody touches its memory after this
   if (rank != 0) return true;
   // CTA 0: bucket b spans [start[b], start[b - 1]) (the buckets below follow it); the last
