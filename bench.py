@@ -196,6 +196,28 @@ def make_inputs(seed: int = 0):
     return workloads.prefill_8k(seed=seed)
 
 
+def sm_clock_in_band(a, b):
+    """Average SM clock of every SM over the timed region: (cycle counter after - before) /
+    (global ns timer after - before) per SM, from two samples on the launch stream that
+    bracket the region (one-thread blocks, a few per SM)."""
+    first, last = {}, {}
+    for row in a.tolist():
+        sm, c, t = row
+        if sm not in first or t < first[sm][1]:
+            first[sm] = (c, t)
+    for row in b.tolist():
+        sm, c, t = row
+        if sm not in last or t > last[sm][1]:
+            last[sm] = (c, t)
+    mhz = sorted(1e3 * (last[s][0] - first[s][0]) / (last[s][1] - first[s][1])
+                 for s in first if s in last and last[s][1] > first[s][1])
+    if not mhz:
+        return None
+    return {"sm_mhz_mean": sum(mhz) / len(mhz), "sm_mhz_min": mhz[0], "sm_mhz_max": mhz[-1], "sms": len(mhz),
+            "how": "cycle counter and global ns timer read on every SM just before and just after the timed "
+                   "region (dsa_clock_sample on the launch stream)"}
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     import sparse_attention_token_gb300 as dsa
     torch.cuda.set_device(local_rank)
@@ -227,8 +249,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
+    n_probe = 4 * torch.cuda.get_device_properties(dev).multi_processor_count
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
+    clk0 = dsa.dsa_clock_sample(n_probe, stream)  # just outside the timed region, same stream
     start.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
@@ -237,6 +261,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         dsa.dsa_indexer_topk(scores, T=T, S=S, q_pos0=0, topk_limit=TOPK, topk=topk, stream=stream)
         ev[i][2].record(stream)
     end.record(stream)
+    clk1 = dsa.dsa_clock_sample(n_probe, stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     if world > 1:
@@ -275,6 +300,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     t_wall2 = time.time()
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
+    clocks["in_band"] = sm_clock_in_band(clk0.cpu(), clk1.cpu())
     # the timed region is short next to the sampling period: also report the samples
     # over the timed region and the end-to-end loop that follows it
     clocks_e2e = sampler.summary(t_wall0, t_wall2)

@@ -435,6 +435,17 @@ dsa_status dsa_indexer_stack(int L, const int32_t* types, const dsa_indexer_args
 dsa_status dsa_check_device_status(dsa_stream_t stream);
 
 /*
+ * Clock sample (diagnostic, not part of the method): n_ctas one-thread blocks each write
+ * {SM id, that SM's cycle counter (clock64), the global nanosecond timer} as three
+ * uint64 to out[3 * i .. 3 * i + 2].  Two samples on a stream bracket an interval; per SM,
+ * (cycles after - cycles before) / (ns after - ns before) is its average clock over it.
+ *   out     device [3 * n_ctas] uint64, caller-owned
+ *   n_ctas  >= 1 (a few per SM reach every SM)
+ * Asynchronous on `stream`; DSA_ERR_INVALID_ARGUMENT for a null out or n_ctas < 1.
+ */
+dsa_status dsa_clock_sample(uint64_t* out, int n_ctas, dsa_stream_t stream);
+
+/*
  * dsa_test_arm_score_timeout -- failure-path test hook; the pages have no counterpart.
  * Every wait inside the library's kernels is bounded: a wait that runs out records
  * DSA_ERR_TIMEOUT in the device status word and makes the kernel stop, wait (bounded)

@@ -9,7 +9,8 @@ Function names mirror the C ABI:
   dsa_indexer_scores, dsa_indexer_topk, dsa_indexer, dsa_indexer_workspace_size,
   dsa_indexer_dense_host, dsa_indexer_dense_host_workspace_size, dsa_indexer_cache_append,
   dsa_resolve_indexer_sources, dsa_indexer_stack, dsa_check_device_status,
-  dsa_topk_width, dsa_status_string, dsa_version.
+  dsa_topk_width, dsa_status_string, dsa_version (and the others the header declares;
+  dsa_clock_sample is a diagnostic for measuring the SM clock over an interval).
 Host helpers from the GLM5 TensorCast adaptation design ("Sparse MLA 配置兼容",
 "GLM-5.2 IndexShare"): resolve_topk_limit, extend_indexer_types_for_mtp,
 indexer_types_to_codes.
@@ -118,6 +119,8 @@ def lib():
         L.dsa_indexer_stack.argtypes = [I, P, P, P, P, P]
         L.dsa_check_device_status.restype = I
         L.dsa_check_device_status.argtypes = [P]
+        L.dsa_clock_sample.restype = I
+        L.dsa_clock_sample.argtypes = [P, I, P]
         L.dsa_indexer_prepare_workspace_size.restype = I
         L.dsa_indexer_prepare_workspace_size.argtypes = [ctypes.POINTER(dsa_indexer_prepare_args), ctypes.POINTER(S)]
         L.dsa_indexer_prepare.restype = I
@@ -652,6 +655,14 @@ def dsa_test_arm_score_timeout(limit_ns: int) -> None:
 def dsa_check_device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status (DSA_OK, ...)."""
     return int(lib().dsa_check_device_status(_stream_ptr(stream)))
+
+
+def dsa_clock_sample(n_ctas: int, stream=None):
+    """Device tensor [n_ctas, 3] int64 of (SM id, SM cycle counter, global ns timer), one
+    row per one-thread block; two samples bracket an interval (diagnostic)."""
+    out = torch.empty((n_ctas, 3), dtype=torch.int64, device="cuda")
+    _check(lib().dsa_clock_sample(out.data_ptr(), int(n_ctas), _stream_ptr(stream)), "dsa_clock_sample")
+    return out
 
 
 # ---- host helpers (GLM5 TensorCast adaptation design) -----------------------------

@@ -313,6 +313,18 @@ size_t score_launch_smem(const ScoreArgs& a) {
 
 dsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
+// One thread per block: {SM id, SM cycle counter, global ns timer} of the block's SM.
+__global__ void clock_sample_kernel(uint64_t* out) {
+  uint32_t smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  const uint64_t c = clock64();
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  out[3 * blockIdx.x + 0] = smid;
+  out[3 * blockIdx.x + 1] = c;
+  out[3 * blockIdx.x + 2] = t;
+}
+
 struct PagedPlan {
   bool decode, split;
   bool balanced;  // one chunk of split key ranges: per-CTA balanced lists (prep_balanced_kernel)
@@ -810,6 +822,12 @@ dsa_status dsa_indexer_stack(int L, const int32_t* types, const dsa_indexer_args
 dsa_status dsa_test_arm_score_timeout(unsigned long long limit_ns) {
   armed_probe_wait_ns() = limit_ns;
   return DSA_OK;
+}
+
+dsa_status dsa_clock_sample(uint64_t* out, int n_ctas, dsa_stream_t stream) {
+  if (!out || n_ctas < 1) return DSA_ERR_INVALID_ARGUMENT;
+  clock_sample_kernel<<<n_ctas, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(out);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 dsa_status dsa_check_device_status(dsa_stream_t stream) {

@@ -391,3 +391,22 @@ def test_sharded_validation(dsa):
     assert merge(n=3, kc=8192) == dsa.DSA_ERR_UNSUPPORTED              # more than 16384 per row
     assert merge(out=None) == dsa.DSA_ERR_INVALID_ARGUMENT
     assert merge(T=0) == dsa.DSA_OK
+
+
+def test_clock_sample_validation(dsa):
+    L = dsa.lib()
+    assert L.dsa_clock_sample(None, 4, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert L.dsa_clock_sample(1 << 20, 0, None) == dsa.DSA_ERR_INVALID_ARGUMENT   # never dereferenced
+
+
+def test_bench_in_band_clock_from_two_samples():
+    import torch
+    import bench
+    # SM 0: 2.07e6 cycles over 1e6 ns (2070 MHz); SM 1: 1.0e6 cycles over 1e6 ns, sampled twice
+    a = torch.tensor([[0, 100, 5_000], [1, 50, 5_000], [1, 60, 5_100]], dtype=torch.int64)
+    b = torch.tensor([[0, 2_070_100, 1_005_000], [1, 1_000_050, 1_005_000], [1, 999_990, 1_004_900]],
+                     dtype=torch.int64)
+    r = bench.sm_clock_in_band(a, b)
+    assert r["sms"] == 2
+    assert abs(r["sm_mhz_max"] - 2070.0) < 1e-9 and abs(r["sm_mhz_min"] - 1000.0) < 1e-9
+    assert bench.sm_clock_in_band(a, torch.tensor([[7, 1, 1]], dtype=torch.int64)) is None  # no SM in both

@@ -472,3 +472,19 @@ def test_indexer_appends_new_keys_before_scoring(q_dtype, k_dtype, decode):
     pc.k_cache, pc.k_scale_cache = ref_c, ref_s
     ref, _, _ = oracle.paged(pc)
     assert np.array_equal(got.cpu().numpy(), ref)
+
+
+# ----------------------------------------------------------------------------- clock sample
+
+def test_clock_sample_reads_every_sm():
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    a = dsa.dsa_clock_sample(4 * n_sm)
+    torch.cuda._sleep(2_000_000)
+    b = dsa.dsa_clock_sample(4 * n_sm)
+    torch.cuda.synchronize()
+    a, b = a.cpu(), b.cpu()
+    assert int(a[:, 0].max()) < n_sm and int(a[:, 0].min()) >= 0
+    assert len(set(a[:, 0].tolist())) >= n_sm // 2      # blocks spread over the SMs
+    import bench
+    r = bench.sm_clock_in_band(a, b)
+    assert r["sms"] >= n_sm // 2 and 100.0 < r["sm_mhz_min"] <= r["sm_mhz_max"] < 5000.0
