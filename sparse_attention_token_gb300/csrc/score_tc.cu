@@ -23,9 +23,9 @@
 //   warp 1      TMEM allocator; lane 0 issues tcgen05.mma into two 256-column fp32
 //               accumulators (double buffered) and commits to mbarriers.
 //   warps 2..9  epilogue: tcgen05.ld, ReLU, head-weighted sum, k scale, causal mask,
-//               coalesced fp32 stores.  Prefill tiles (N = 256) are split by columns
-//               between two warpgroups; decode tiles (N = max(64, H)) alternate
-//               between the warpgroups tile by tile.
+//               coalesced fp32 stores.  bf16 prefill tiles (N = 256) are split by
+//               columns between two warpgroups; decode tiles (N = max(64, H)) and e4m3
+//               prefill tiles alternate between the warpgroups tile by tile.
 //   bf16 queries against e4m3 keys (decode): the queries come as exact e4m3 hi / lo row
 //               pairs (qsplit.cuh), so the MMAs are FP8 and the epilogue adds the pair
 //               before the ReLU.
@@ -132,9 +132,6 @@ template <int H, bool DECODE, bool SPLIT = false>
 struct Cfg {
   static constexpr int N = SPLIT ? (2 * H >= 64 ? 2 * H : 64) : (DECODE ? (H >= 64 ? H : 64) : 256);
   static constexpr int NQ = SPLIT ? 1 : N / H;
-  static constexpr int NCOLS = DECODE ? N : N / 2;  // columns one epilogue thread reduces
-  static constexpr int QH = SPLIT ? 1 : NCOLS / H;   // queries in those columns
-  static constexpr int EPI_T_ARRIVALS = DECODE ? 4 : 8;
   static constexpr int QROWS = SPLIT ? 2 * H : H;
   // decode tiles are short (16 or 32 KB) and HBM-bound: a second producer warp (warp 10)
   // takes every other key tile, which needs an even ring
@@ -368,27 +365,31 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // ------------------------------------------------------------------ epilogue (warps 2..9)
-template <int H, bool DECODE, bool SPLIT>
+// ALT: whole tiles alternate between the two epilogue warpgroups (each thread reduces all
+// N columns of its key); otherwise both warpgroups take every tile, split by columns.
+// Decode tiles and e4m3 prefill tiles alternate: a tile's fixed per-warp work (waits,
+// arrives, stores) is then spread over twice the columns.
+template <int H, bool DECODE, bool SPLIT, bool ALT>
 __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem, const SmemPlan& P,
                                               uint64_t* bars, volatile int* abort, int n_items,
                                               uint32_t tmem_base) {
   using C = Cfg<H, DECODE, SPLIT>;
   constexpr int N = C::N;
-  constexpr int NCOLS = C::NCOLS;
-  constexpr int QH = C::QH;
+  constexpr int NCOLS = ALT ? N : N / 2;     // columns one epilogue thread reduces
+  constexpr int QH = SPLIT ? 1 : NCOLS / H;  // queries in those columns
   constexpr int NCH = NCOLS / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = (warp - 2) >> 2;
   const int quarter = warp & 3;            // TMEM lane quarter this warp may access
   const int m = quarter * 32 + lane;       // key row of the tile
   const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-  const int col0 = DECODE ? 0 : half * NCOLS;
+  const int col0 = ALT ? 0 : half * NCOLS;
   const int q0 = col0 / H;
   const int nK = a.num_k_stages;
   float* wbuf = reinterpret_cast<float*>(smem + P.wbuf);
   const float* qsbuf = reinterpret_cast<const float*>(smem + P.qsbuf);
   const float* ksbuf = reinterpret_cast<const float*>(smem + P.ksbuf);
-  const int fold_t = DECODE ? static_cast<int>(threadIdx.x) - 64 : static_cast<int>(threadIdx.x) - 64 - half * 128;
+  const int fold_t = ALT ? static_cast<int>(threadIdx.x) - 64 : static_cast<int>(threadIdx.x) - 64 - half * 128;
 
   uint32_t nq = 0, nk = 0, nt = 0;
   uint32_t ks_slot = 0, ks_phase = 0;  // key ring slot of tile nk and its phase parity
@@ -401,16 +402,16 @@ __device__ __forceinline__ void epilogue_role(const ScoreArgs& a, uint8_t* smem,
     float* wq = wbuf + sq * N;
     if (a.q_fp8 && !SPLIT) {
       // fold the q scale into w once per item (in place, each thread one column)
-      const int c = DECODE ? fold_t : col0 + fold_t;
-      if (!DECODE || fold_t < N) wq[c] *= qsbuf[sq * N + c];
-      uint64_t* fb = &bars[kBarFold + sq * 2 + (DECODE ? 0 : half)];
+      const int c = ALT ? fold_t : col0 + fold_t;
+      if (!ALT || fold_t < N) wq[c] *= qsbuf[sq * N + c];
+      uint64_t* fb = &bars[kBarFold + sq * 2 + (ALT ? 0 : half)];
       ptx::mbar_arrive(fb);
       if (!warp_wait(fb, (nq >> 1) & 1, abort, a.status)) break;
     }
     for (int kt = I.kt0; kt < I.kt1; ++kt) {
       const int sk = static_cast<int>(ks_slot);
       const int acc = nt & 1;
-      const bool mine = DECODE ? (acc == half) : true;
+      const bool mine = ALT ? (acc == half) : true;
       if (mine) {
         // e4m3 keys: take this key's scale and release the stage's scale slot before the
         // accumulator wait, so the ring turns over as soon as the MMA is done with it
@@ -546,14 +547,15 @@ __global__ void __launch_bounds__(Cfg<H, DECODE, SPLIT>::THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + P.misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + P.misc + 4);
+  const bool alt = DECODE || a.q_fp8;  // whole tiles alternate between the epilogue warpgroups
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&bars[kBarQFull + s], 1 + 32);
       ptx::mbar_init(&bars[kBarQEmpty + s], 1 + 8);
       ptx::mbar_init(&bars[kBarTFull + s], 1);
-      ptx::mbar_init(&bars[kBarTEmpty + s], C::EPI_T_ARRIVALS);
-      ptx::mbar_init(&bars[kBarFold + 2 * s + 0], DECODE ? 256 : 128);
+      ptx::mbar_init(&bars[kBarTEmpty + s], alt ? 4 : 8);  // the warps that read the accumulator
+      ptx::mbar_init(&bars[kBarFold + 2 * s + 0], alt ? 256 : 128);
       ptx::mbar_init(&bars[kBarFold + 2 * s + 1], 128);
     }
     ptx::mbar_init(&bars[kBarDone], 1);
@@ -563,7 +565,7 @@ __global__ void __launch_bounds__(Cfg<H, DECODE, SPLIT>::THREADS, 1)
       // paged tiles by one bulk copy per page
       ptx::mbar_init(&bars[kBarKFull + s], 1 + ((a.k_fp8 && !a.paged) ? 32 : 0));
       // the epilogue also releases a stage when it reads that stage's key scales from ksbuf
-      ptx::mbar_init(&bars[kBarKEmpty + s], 1 + (a.k_fp8 ? C::EPI_T_ARRIVALS : 0));
+      ptx::mbar_init(&bars[kBarKEmpty + s], 1 + (a.k_fp8 ? (alt ? 4 : 8) : 0));
     }
     *abort = 0;
     ptx::fence_mbar_init();
@@ -597,7 +599,9 @@ __global__ void __launch_bounds__(Cfg<H, DECODE, SPLIT>::THREADS, 1)
     if (lane == 0) mma_role<H, DECODE, SPLIT>(a, smem, P, bars, abort, n_items, tmem_base);
     __syncwarp();
   } else {
-    epilogue_role<H, DECODE, SPLIT>(a, smem, P, bars, abort, n_items, tmem_base);
+    if constexpr (DECODE) epilogue_role<H, DECODE, SPLIT, true>(a, smem, P, bars, abort, n_items, tmem_base);
+    else if (alt) epilogue_role<H, DECODE, SPLIT, true>(a, smem, P, bars, abort, n_items, tmem_base);
+    else epilogue_role<H, DECODE, SPLIT, false>(a, smem, P, bars, abort, n_items, tmem_base);
   }
   ptx::tc_fence_before();
   __syncthreads();
