@@ -1016,25 +1016,32 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
     for (int j = 0; j < CL; ++j) red_min_cluster(mapa(&cmm[2], static_cast<uint32_t>(j)), info[0]);
     info[2] = 0u;  // the overflow flag of the scan below
   }
-  cluster_barrier();  // every CTA holds the lowest local threshold
+  cluster_barrier();  // every CTA holds the lowest local threshold; every local histogram is complete
   const int bmin = static_cast<int>(cmm[2]);
-  cluster_merge_hist<CL>(m, rank, bmin);
+  // Each CTA sums the CTAs' local histograms at and above bmin itself, reading them in place
+  // (they stay unchanged until the barrier after the placement), and keeps the lower-ranked
+  // CTAs' share of every bucket: its own slots in bucket b start after their keys.
+  uint32_t* cursor = m.ci;  // kBins words, plain bucket index
+  for (int b = tid + bmin; b < kBins; b += kThreads) {
+    uint32_t tot = m.hist[hslot(b)], pre = 0;
+#pragma unroll
+    for (int j = 0; j < CL; ++j) {
+      if (j == static_cast<int>(rank)) continue;
+      const uint32_t v = dsmem_ld(mapa(&m.hist[hslot(b)], static_cast<uint32_t>(j)));
+      tot += v;
+      pre += j < static_cast<int>(rank) ? v : 0u;
+    }
+    m.merged[hslot(b)] = tot;
+    cursor[b] = pre;
+  }
+  __syncthreads();
   // descending exclusive scan of the merged histogram, identical in every CTA (exact at
-  // and above bmin, which the threshold bucket is)
+  // and above bmin, which the threshold bucket is; zero below)
   const uint32_t want = static_cast<uint32_t>(keep);
   scan_desc_starts(m.merged, want, red, info);
   const uint32_t d1 = info[0], n_cand = info[1];
   if (info[2] != 0u || n_cand > static_cast<uint32_t>(cand_cap)) return false;
-  // this CTA's slots in bucket b start after the lower-ranked CTAs' keys of that bucket:
-  // cursor[b] = start[b] + sum of their local counts (read from their shared memory)
-  uint32_t* cursor = m.ci;  // kBins words, plain bucket index
-  for (int b = tid + static_cast<int>(d1); b < kBins; b += kThreads) {
-    uint32_t pre = 0;
-#pragma unroll
-    for (int j = 0; j < CL; ++j)
-      if (j < static_cast<int>(rank)) pre += dsmem_ld(mapa(&m.hist[hslot(b)], static_cast<uint32_t>(j)));
-    cursor[b] = m.merged[hslot(b)] + pre;
-  }
+  for (int b = tid + static_cast<int>(d1); b < kBins; b += kThreads) cursor[b] += m.merged[hslot(b)];
   __syncthreads();
   const uint32_t bw0 = mapa(m.tk, 0);
   // One compare rejects most keys: every score of a bucket >= d1 is at least
