@@ -604,16 +604,16 @@ __device__ __forceinline__ uint32_t cand_index(uint64_t w) {
 }
 
 // Words in bw[q0, q1) greater than x (x's bucket-mates that beat it), four loads at a time
-// so that a bucket of a few keys costs one shared-memory latency.
+// so that a bucket of a few keys costs one shared-memory latency.  The loads run up to three
+// words past q1 without a bound check: those hold lower buckets' candidates, whose scores
+// are below every score of x's bucket (the bucket is a non-decreasing function of the
+// score), or the kMatePad zero words the caller keeps after the last candidate -- either
+// way smaller than x, so they never count.
+constexpr uint32_t kMatePad = 4;
 __device__ __forceinline__ uint32_t mates_above(const uint64_t* bw, uint32_t q0, uint32_t q1, uint64_t x) {
   uint32_t n = 0;
-  for (uint32_t q = q0; q < q1; q += 4) {
-    const uint64_t y0 = bw[q];
-    const uint64_t y1 = q + 1 < q1 ? bw[q + 1] : 0ull;
-    const uint64_t y2 = q + 2 < q1 ? bw[q + 2] : 0ull;
-    const uint64_t y3 = q + 3 < q1 ? bw[q + 3] : 0ull;
-    n += (y0 > x ? 1u : 0u) + (y1 > x ? 1u : 0u) + (y2 > x ? 1u : 0u) + (y3 > x ? 1u : 0u);
-  }
+  for (uint32_t q = q0; q < q1; q += 4)
+    n += (bw[q] > x ? 1u : 0u) + (bw[q + 1] > x ? 1u : 0u) + (bw[q + 2] > x ? 1u : 0u) + (bw[q + 3] > x ? 1u : 0u);
   return n;
 }
 
@@ -702,9 +702,11 @@ __device__ bool linear_bucket_topk(const RegSeg<NB>& rs, int keep, int32_t* out,
   const uint32_t want = static_cast<uint32_t>(keep);
   scan_desc_starts(m.hist, want, red, info);
   const uint32_t d1 = info[0], n_cand = info[1];
-  // candidate words (n_cand of 8 bytes) live in tk and ti, 2 * cand_cap adjacent words
-  if (info[2] != 0u || n_cand > static_cast<uint32_t>(cand_cap)) return false;
+  // candidate words (n_cand of 8 bytes, then kMatePad zero words) live in tk and ti,
+  // 2 * cand_cap adjacent words
+  if (info[2] != 0u || n_cand + kMatePad > static_cast<uint32_t>(cand_cap)) return false;
   uint2* bw2 = reinterpret_cast<uint2*>(m.tk);
+  if (tid < static_cast<int>(kMatePad)) bw2[n_cand + tid] = make_uint2(0u, 0u);
   rs.visit_f([&](const uint32_t (&x)[4], uint32_t i, int c) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -1040,8 +1042,11 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
   const uint32_t want = static_cast<uint32_t>(keep);
   scan_desc_starts(m.merged, want, red, info);
   const uint32_t d1 = info[0], n_cand = info[1];
-  if (info[2] != 0u || n_cand > static_cast<uint32_t>(cand_cap)) return false;
+  if (info[2] != 0u || n_cand + kMatePad > static_cast<uint32_t>(cand_cap)) return false;
   for (int b = tid + static_cast<int>(d1); b < kBins; b += kThreads) cursor[b] += m.merged[hslot(b)];
+  // CTA 0 keeps kMatePad zero words after the last candidate slot (see mates_above)
+  if (rank == 0 && tid < static_cast<int>(kMatePad))
+    reinterpret_cast<uint2*>(m.tk)[n_cand + tid] = make_uint2(0u, 0u);
   __syncthreads();
   const uint32_t bw0 = mapa(m.tk, 0);
   // One compare rejects most keys: every score of a bucket >= d1 is at least
