@@ -416,7 +416,8 @@ def _decode_b64_fp8_cache(dev, stream, peaks, iters=10):
     import workloads
     hbm = float(peaks["hbm_gbs"])
     lens = workloads.decode_lens(64, 4096, 65536, 0)
-    c = _paged_on_device(64, lens, 1, 64, 128, 64, False, True, 5, dev)
+    page = _env_int("DSA_BENCH_DECODE_PAGE", 64)  # another page size only for the page-size study
+    c = _paged_on_device(64, lens, 1, 64, 128, page, False, True, 5, dev)
     args, keep = dsa.make_indexer_args(c["q"], c["w"], c["k_cache"], c["cu_q_lens"], c["seq_lens"],
                                        c["block_tables"], max_seq_len=c["max_seq_len"], topk_limit=2048,
                                        k_scale_cache=c["k_scale_cache"])
@@ -427,11 +428,11 @@ def _decode_b64_fp8_cache(dev, stream, peaks, iters=10):
     ms = _time_events(lambda: L.dsa_indexer(ctypes.byref(args), stream.cuda_stream), iters, stream)
     keys = sum(lens)
     # algorithmic bytes: e4m3 keys + fp32 key scales + page ids + q + w + int32 top-k out
-    dec_bytes = keys * (128 + 4) + sum((x + 63) // 64 for x in lens) * 4 + 64 * 64 * 128 * 2 + 64 * 64 * 4 \
+    dec_bytes = keys * (128 + 4) + sum((x + page - 1) // page for x in lens) * 4 + 64 * 64 * 128 * 2 + 64 * 64 * 4 \
         + 64 * 2048 * 4
     out = {
         "workload": "decode B=64, one query per sequence, contexts U[4096, 65536] (seeded), bf16 q, "
-                    "paged e4m3 cache (page 64) with fp32 per-token scales, H=64, D=128, index_topk=2048",
+                    f"paged e4m3 cache (page {page}) with fp32 per-token scales, H=64, D=128, index_topk=2048",
         "ms_per_step": ms, "keys_per_s": keys / (ms / 1e3), "keys": keys,
         "algorithmic_bytes": dec_bytes, "hbm_gbs": dec_bytes / (ms / 1e3) / 1e9,
         "hbm_frac": dec_bytes / (ms / 1e3) / 1e9 / hbm,
