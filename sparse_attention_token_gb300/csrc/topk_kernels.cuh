@@ -2,18 +2,30 @@
 // topk_kernels.cuh -- per-row top-k of indexer scores (GLM5 TensorCast adaptation design,
 // "性能模型设计" bucket 8, top-k selection; output width min(topk_limit, n_visible)).
 //
-// One CTA of 256 threads per row.  Scores become order-preserving unsigned keys
-// (larger score -> larger key; -0.0 folded onto +0.0).  The best `keep` keys under
-// (score desc, index asc) are found as follows.
+// One CTA of 256 threads per row (rows up to 8192 keys, held in registers), or a cluster
+// of CTAs per row (longer rows), or one CTA streaming the row from memory (any length).
+// The best `keep` keys under (score desc, index asc) are found as follows.
+//   Score order, rows in registers -- the linear-bucket path (linear_bucket_topk,
+//      cluster_linear_topk): one histogram of 4096 equal-width buckets between the row's
+//      extremes, a descending scan for the threshold bucket and every bucket's start, the
+//      keys of the buckets at and above it placed straight at their bucket's slots as
+//      (key, bucket, index) words, and each word ranked among its bucket-mates.  It
+//      declines rows whose scores are all equal, whose candidate buckets hold more than
+//      kBucketLimit keys, or whose candidates overflow the buffers, and the general path
+//      takes them.
+//   General path (index order, declined rows, streamed rows): scores become
+//      order-preserving unsigned keys (larger score -> larger key; -0.0 folded onto
+//      +0.0).
 //   1. One pass over the row builds a histogram of the top 12 key bits; a suffix
 //      scan finds the bucket b where the running count reaches `keep`.
 //   2. Fast path (the keys in buckets >= b fit the candidate buffer): an
 //      order-preserving compaction (each warp owns a contiguous segment of the row;
 //      ballots and warp prefix sums, no block-wide scans) copies every key of
 //      bucket >= b with its index, in index order.
-//        score order: a stable LSD radix sort (8-bit digits, descending, digits that
-//        never change skipped) of the candidates; the first `keep` are the answer
-//        (ties keep ascending index because the input was in index order);
+//        score order: the candidates are counted into buckets of a compressed key
+//        and ranked within them (bucket_rank_out), or, when a bucket is too full, sorted
+//        by a stable LSD radix sort over the differing 9-bit digits; the first `keep`
+//        are the answer (ties keep ascending index: the input was in index order);
 //        index order: the exact threshold inside bucket b is refined on the
 //        candidates alone, then one ordered pass writes the selected indices.
 //   3. Slow path (a huge threshold bucket, e.g. many equal scores): the exact
