@@ -466,12 +466,26 @@ struct MlaPlan {
 MlaPlan plan_mla(const dsa_sparse_mla_args* a, int sms) {
   MlaPlan p{};
   p.groups = (a->H + kHeadsPerCta - 1) / kHeadsPerCta;
-  // about two CTAs' worth of items per SM, whole 64-key blocks per split
-  const long long base = static_cast<long long>(a->total_q) * p.groups;
-  int splits = static_cast<int>(std::max<long long>(1, (2LL * sms + base - 1) / std::max<long long>(base, 1)));
+  // Whole 64-key blocks per split.  One CTA fills an SM (shared memory), so the launch runs
+  // in waves of `sms` CTAs, and a wave lasts as long as its CTAs' blocks plus about one
+  // block's worth of fixed work (its q load, its partial output of 64 heads x 512 fp32,
+  // which the combine reads back).  Take the blocks-per-split that minimises
+  // waves x (blocks + 1); on a tie the larger one (fewer splits: the loop runs downwards).
+  const long long base = std::max<long long>(1, static_cast<long long>(a->total_q) * p.groups);
   const int blocks = std::max(1, (a->topk_width + kBlockKeys - 1) / kBlockKeys);
-  splits = std::min(splits, blocks);
-  const int bps = (blocks + splits - 1) / splits;
+  const long long n_sm = std::max(sms, 1);
+  int best_bps = blocks;
+  long long best_cost = -1;
+  for (int bps = blocks; bps >= 1; --bps) {
+    const long long splits = (blocks + bps - 1) / bps;
+    const long long waves = (base * splits + n_sm - 1) / n_sm;
+    const long long cost = waves * (bps + 1);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_bps = bps;
+    }
+  }
+  const int bps = best_bps;
   p.keys_per_split = bps * kBlockKeys;
   p.splits = (blocks + bps - 1) / bps;
   const size_t rows = static_cast<size_t>(a->total_q) * p.splits * a->H;
