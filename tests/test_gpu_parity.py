@@ -175,6 +175,30 @@ def test_topk_quantised_scores_exact(S, step, order):
     assert np.array_equal(got, ref)
 
 
+# the linear-bucket paths' limits: few huge outliers (nearly every key in the lowest
+# bucket), an infinite score (no finite width), one distinct value among equal ones, a
+# heavy tail, and widths of keep from 1 to near the candidate buffer of the cluster form
+@pytest.mark.parametrize("kind", ["outliers", "inf", "one_distinct", "heavy_tail"])
+@pytest.mark.parametrize("S,limit", [(5000, 1), (5000, 2048), (30000, 64), (30000, 3900), (100000, 2048)])
+def test_topk_linear_bucket_edges_exact(kind, S, limit):
+    g = torch.Generator().manual_seed(S * 7 + limit)
+    T = 3
+    sc = torch.randn((T, S), generator=g).numpy().astype(np.float32)
+    if kind == "outliers":
+        sc[:, ::997] = 1e30
+    elif kind == "inf":
+        sc[0, S // 2] = np.inf
+        sc[1, 3] = -np.inf
+        sc[2, -1] = np.inf
+    elif kind == "one_distinct":
+        sc[:] = 1.5
+        sc[:, S // 3] = 2.0
+    else:
+        sc = np.exp(4.0 * sc).astype(np.float32)
+    got, ref = _topk_on(sc, S - T, S, limit, min(limit + 3, 4096), 0)
+    assert np.array_equal(got, ref)
+
+
 def test_topk_causal_rows_prefill_shape():
     g = torch.Generator().manual_seed(1)
     T = S = 3000
