@@ -11,7 +11,8 @@
 //
 // The merge ranks every candidate directly: its position in its own (sorted) list plus,
 // for every other list, the number of that list's entries that beat it (a binary search
-// over the list held in shared memory).  Candidates compare as one 64-bit word
+// over the list held in shared memory); two lists are merged along a merge path instead
+// (one binary search per thread, then a sequential merge of its share of the output).  Candidates compare as one 64-bit word
 // (order-preserving score key, complemented index): a larger word is a higher score, or
 // the same score at a lower index.  Indices are distinct across shards (disjoint key
 // ranges), so ranks are distinct.
@@ -82,12 +83,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* cand_
     const int j = e / k_cand, p = e - j * k_cand;
     const long long g = (static_cast<long long>(j) * T + r) * k_cand + p;
     const int32_t id = cand_idx[g];
-    uint64_t w = 0;  // padding: below every candidate
-    if (id >= 0) {
+    uint64_t w = 0;  // padding: below every candidate (a candidate's word is never 0)
+    if (id >= 0)
       w = (static_cast<uint64_t>(score_key(cand_scores[g])) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(id));
-      atomicAdd(&valid[j], 1u);
-    }
     W[e] = w;
+  }
+  __syncthreads();
+  // a list's valid entries come first: its count is one past its last candidate
+  for (int e = tid; e < n; e += kMergeThreads) {
+    const int j = e / k_cand, p = e - j * k_cand;
+    if (W[e] != 0 && (p + 1 == k_cand || W[e + 1] == 0)) valid[j] = static_cast<uint32_t>(p + 1);
   }
   __syncthreads();
   uint32_t total = 0;
@@ -97,7 +102,32 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* cand_
   if (keep > k_out) keep = k_out;
   int32_t* out = topk + static_cast<long long>(r) * k_out;
   for (int i = keep + tid; i < k_out; i += kMergeThreads) out[i] = -1;
-  for (int e = tid; e < n; e += kMergeThreads) {
+  if (n_shards == 2) {
+    // two lists: a merge path.  Thread t writes outputs [o0, o1): one binary search finds
+    // how many of the first o0 merged entries come from the first list, then it merges.
+    const uint64_t* A = W;
+    const uint64_t* Bl = W + k_cand;
+    const int nA = static_cast<int>(valid[0]), nB = static_cast<int>(valid[1]);
+    const int per = (keep + kMergeThreads - 1) / kMergeThreads;
+    const int o0 = tid * per, o1 = min(keep, o0 + per);
+    if (o0 < o1) {
+      int lo = max(0, o0 - nB), hi = min(o0, nA);
+      while (lo < hi) {  // the first i with A[i] not among the first o0
+        const int mid = (lo + hi) >> 1;
+        if (A[mid] > Bl[o0 - mid - 1]) lo = mid + 1;
+        else hi = mid;
+      }
+      int i = lo, jb = o0 - lo;
+      for (int o = o0; o < o1; ++o) {
+        const bool take_a = jb >= nB || (i < nA && A[i] > Bl[jb]);
+        const uint64_t x = take_a ? A[i++] : Bl[jb++];
+        const int32_t id = static_cast<int32_t>(~static_cast<uint32_t>(x));
+        if (order == DSA_ORDER_SCORE) out[o] = id;
+        else sel[o] = id;
+      }
+    }
+  }
+  for (int e = tid; n_shards != 2 && e < n; e += kMergeThreads) {
     const int j = e / k_cand, p = e - j * k_cand;
     if (p >= keep || static_cast<uint32_t>(p) >= valid[j]) continue;  // ranked at least p
     const uint64_t x = W[e];

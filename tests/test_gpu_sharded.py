@@ -48,7 +48,7 @@ def _run_shards(c, bounds, k_cand, order=0, topk_limit=None):
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
 @pytest.mark.parametrize("bounds", [[0, 1000], [0, 250, 251, 640, 1000], [0, 128, 256, 384, 1000],
-                                    [0, 999, 1000]])
+                                    [0, 999, 1000], [0, 500, 1000], [0, 3, 1000]])
 def test_sharded_integer_exact(dtype, bounds):
     T, S, K, q_pos0 = 300, 1000, 128, 700
     c = workloads.dense_case(T, S, 64, 128, K, q_pos0=q_pos0, dtype=dtype, integer=True, int_range=(-2, 2),
@@ -80,10 +80,11 @@ def test_sharded_rows_that_see_no_shard_keys_and_short_rows():
     assert np.array_equal(got, rt)
 
 
-def test_sharded_gaussian_valid_topk():
+@pytest.mark.parametrize("bounds", [[0, 700, 1500, 2300, 3000], [0, 1400, 3000]])
+def test_sharded_gaussian_valid_topk(bounds):
     T, S, K, q_pos0 = 256, 3000, 512, 2744
     c = workloads.dense_case(T, S, 64, 128, K, q_pos0=q_pos0, seed=92)
-    _, _, got = _run_shards(c, [0, 700, 1500, 2300, 3000], K)
+    _, _, got = _run_shards(c, bounds, K)
     rt, rs, rb = oracle.dense(c.q, c.k, c.w, T=T, S=S, H=64, D=128, q_pos0=q_pos0, topk_limit=K, k_out=K + 5,
                               want_scores=True, want_bound=True)
     for t in range(T):
