@@ -68,7 +68,7 @@ __device__ __forceinline__ uint32_t count_greater(const uint64_t* w, uint32_t le
 // One CTA per query row: rank the n_shards * k_cand candidates, keep the best `keep`.
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* cand_scores, const int32_t* cand_idx,
                                                               int n_shards, int T, int k_cand, int topk_limit,
-                                                              int k_out, int order, int32_t* topk) {
+                                                              int k_out, int order, int32_t* topk, int vec4) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint64_t* W = reinterpret_cast<uint64_t*>(smem);                       // [n_shards][k_cand]
   int32_t* sel = reinterpret_cast<int32_t*>(W + n_shards * k_cand);      // index order staging
@@ -79,14 +79,29 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* cand_
   const int n = n_shards * k_cand;
   if (tid < n_shards) valid[tid] = 0;
   __syncthreads();
-  for (int e = tid; e < n; e += kMergeThreads) {
-    const int j = e / k_cand, p = e - j * k_cand;
-    const long long g = (static_cast<long long>(j) * T + r) * k_cand + p;
-    const int32_t id = cand_idx[g];
-    uint64_t w = 0;  // padding: below every candidate (a candidate's word is never 0)
-    if (id >= 0)
-      w = (static_cast<uint64_t>(score_key(cand_scores[g])) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(id));
-    W[e] = w;
+  // padding: 0, below every candidate (a candidate's word is never 0)
+  auto word = [](int32_t id, float sc) -> uint64_t {
+    return id < 0 ? 0ull
+                  : (static_cast<uint64_t>(score_key(sc)) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(id));
+  };
+  if (vec4) {
+    // four entries per 16-byte load (k_cand a multiple of 4, 16-byte aligned lists)
+    for (int e = 4 * tid; e < n; e += 4 * kMergeThreads) {
+      const int j = e / k_cand, p = e - j * k_cand;
+      const long long g = (static_cast<long long>(j) * T + r) * k_cand + p;
+      const int4 id = *reinterpret_cast<const int4*>(cand_idx + g);
+      const float4 sc = *reinterpret_cast<const float4*>(cand_scores + g);
+      W[e] = word(id.x, sc.x);
+      W[e + 1] = word(id.y, sc.y);
+      W[e + 2] = word(id.z, sc.z);
+      W[e + 3] = word(id.w, sc.w);
+    }
+  } else {
+    for (int e = tid; e < n; e += kMergeThreads) {
+      const int j = e / k_cand, p = e - j * k_cand;
+      const long long g = (static_cast<long long>(j) * T + r) * k_cand + p;
+      W[e] = word(cand_idx[g], cand_scores[g]);
+    }
   }
   __syncthreads();
   // a list's valid entries come first: its count is one past its last candidate
@@ -234,8 +249,12 @@ dsa_status dsa_indexer_merge_candidates(const float* cand_scores, const int32_t*
   auto kern = merge_kernel;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return DSA_ERR_CUDA;
+  const int vec4 = (k_cand % 4 == 0 && (reinterpret_cast<uintptr_t>(cand_scores) & 15u) == 0 &&
+                    (reinterpret_cast<uintptr_t>(cand_idx) & 15u) == 0)
+                       ? 1
+                       : 0;
   const cudaError_t e = launch_pdl(kern, dim3(T), dim3(kMergeThreads), smem, reinterpret_cast<cudaStream_t>(stream),
-                                   cand_scores, cand_idx, n_shards, T, k_cand, topk_limit, k_out, order, topk);
+                                   cand_scores, cand_idx, n_shards, T, k_cand, topk_limit, k_out, order, topk, vec4);
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
