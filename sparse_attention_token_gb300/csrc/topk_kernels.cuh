@@ -958,17 +958,6 @@ __device__ void cluster_merge_hist(const TopkSmem& m, uint32_t rank, int bmin = 
   cluster_barrier();  // every contribution has landed
 }
 
-__device__ __forceinline__ uint32_t atom_add_cluster(uint32_t addr, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
-  return old;
-}
-__device__ __forceinline__ void red_min_cluster(uint32_t addr, uint32_t v) {
-  asm volatile("red.shared::cluster.min.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ void red_max_cluster(uint32_t addr, uint32_t v) {
-  asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
 
 // The score-order fast path of linear_bucket_topk spread over a cluster: the row's extreme
 // keys are exchanged between the CL CTAs, each CTA counts its part into linear buckets, the
@@ -986,7 +975,6 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
   static_assert(CL * kWarps * NB * 128 <= (1 << kIndexBits), "key indices must fit the candidate word");
   if (cand_cap < kBins) return false;  // the bucket cursors need kBins words of m.ci (same in every CTA)
   // the histograms are cleared while the row's loads are still in flight
-  if (tid == 0) { cmm[0] = 0xFFFFFFFFu; cmm[1] = 0u; cmm[2] = 0xFFFFFFFFu; }
   for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = m.merged[i] = 0;
   float fmin = __int_as_float(0x7f800000), fmax = -fmin;
   rs.visit_f([&](const uint32_t (&x)[4], uint32_t, int c) {
@@ -998,18 +986,27 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
   uint32_t kmax = __reduce_max_sync(0xffffffffu, order_key(fmax));
   if (lane == 0) { red[warp] = kmin; red[kWarps + warp] = kmax; }
   __syncthreads();
-  cluster_barrier();  // every CTA's exchange slots are initialised
+  // Exchange through each CTA's own slots: write this CTA's extremes, one cluster barrier,
+  // then warp 0 reads every CTA's slots and reduces them.
   if (tid == 0) {
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) { kmin = min(kmin, red[w]); kmax = max(kmax, red[kWarps + w]); }
-#pragma unroll
-    for (int j = 0; j < CL; ++j) {
-      red_min_cluster(mapa(&cmm[0], static_cast<uint32_t>(j)), kmin);
-      red_max_cluster(mapa(&cmm[1], static_cast<uint32_t>(j)), kmax);
-    }
+    cmm[0] = kmin;
+    cmm[1] = kmax;
   }
-  cluster_barrier();  // every CTA holds the row's extremes
-  const float lo = key_value(cmm[0]), hi = key_value(cmm[1]);
+  cluster_barrier();  // every CTA's extremes are in its slots
+  if (warp == 0) {
+    uint32_t gmin = 0xFFFFFFFFu, gmax = 0u;
+    if (lane < CL) {
+      gmin = dsmem_ld(mapa(&cmm[0], static_cast<uint32_t>(lane)));
+      gmax = dsmem_ld(mapa(&cmm[1], static_cast<uint32_t>(lane)));
+    }
+    gmin = __reduce_min_sync(0xffffffffu, gmin);
+    gmax = __reduce_max_sync(0xffffffffu, gmax);
+    if (lane == 0) { red[0] = gmin; red[1] = gmax; }
+  }
+  __syncthreads();
+  const float lo = key_value(red[0]), hi = key_value(red[1]);
   const float width = __fsub_rn(hi, lo);
   const float scale = __fdiv_rn(static_cast<float>(kBins), width);
   if (!(width > 0.f) || !(scale > 0.f) || isinf(width) || isinf(scale)) return false;  // the same in every CTA
@@ -1023,15 +1020,21 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
   // are merged: every CTA holds at least that many keys there, so the row's threshold
   // bucket is among them (a CTA with fewer keys takes bucket 0, and everything is merged).
   if (tid == 0) info[0] = 0u;
-  __syncthreads();
+  __syncthreads();  // also: every thread has read lo and hi from red
   find_bucket(m.hist, kBins, static_cast<uint32_t>((keep + CL - 1) / CL), red, info);
   if (tid == 0) {
-#pragma unroll
-    for (int j = 0; j < CL; ++j) red_min_cluster(mapa(&cmm[2], static_cast<uint32_t>(j)), info[0]);
+    cmm[2] = info[0];
     info[2] = 0u;  // the overflow flag of the scan below
   }
-  cluster_barrier();  // every CTA holds the lowest local threshold; every local histogram is complete
-  const int bmin = static_cast<int>(cmm[2]);
+  cluster_barrier();  // every CTA's own threshold is in its slot; every local histogram is complete
+  if (warp == 0) {
+    uint32_t b = 0xFFFFFFFFu;
+    if (lane < CL) b = dsmem_ld(mapa(&cmm[2], static_cast<uint32_t>(lane)));
+    b = __reduce_min_sync(0xffffffffu, b);
+    if (lane == 0) red[0] = b;
+  }
+  __syncthreads();
+  const int bmin = static_cast<int>(red[0]);
   // Each CTA sums the CTAs' local histograms at and above bmin itself, reading them in place
   // (they stay unchanged until the barrier after the placement), and keeps the lower-ranked
   // CTAs' share of every bucket: its own slots in bucket b start after their keys.
