@@ -582,6 +582,23 @@ __device__ __forceinline__ TopkSmem topk_smem(uint8_t* smem, int cand_cap) {
   return m;
 }
 
+// Zero the n words at p (16-byte aligned, n a multiple of 4) with 16-byte stores.
+__device__ __forceinline__ void zero_words(uint32_t* p, int n) {
+  uint4* q = reinterpret_cast<uint4*>(p);
+  for (int i = threadIdx.x; i < n / 4; i += kThreads) q[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+// out[0..keep) = src[0..keep) (src 16-byte aligned), 16 bytes per store when out allows.
+__device__ __forceinline__ void copy_out(int32_t* out, const uint32_t* src, int keep) {
+  int i0 = 0;
+  if ((reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+    const int n4 = keep / 4;
+    for (int i = threadIdx.x; i < n4; i += kThreads)
+      reinterpret_cast<int4*>(out)[i] = reinterpret_cast<const int4*>(src)[i];
+    i0 = 4 * n4;
+  }
+  for (int i = i0 + threadIdx.x; i < keep; i += kThreads) out[i] = static_cast<int32_t>(src[i]);
+}
+
 // Score of an order-preserving key (inverse of order_key; -0.0 comes back as +0.0).
 __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
@@ -684,7 +701,8 @@ __device__ bool linear_bucket_topk(const RegSeg<NB>& rs, int keep, int32_t* out,
   static_assert(kWarps * NB * 128 <= (1 << kIndexBits), "key indices must fit the candidate word");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // the histogram is cleared while the row's loads are still in flight
-  for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = 0;
+  static_assert(kHistWords % 4 == 0, "16-byte clears");
+  zero_words(m.hist, kHistWords);
   if (tid == 0) info[2] = 0u;
   // the row's extremes
   float fmin = __int_as_float(0x7f800000), fmax = -fmin;
@@ -740,7 +758,7 @@ __device__ bool linear_bucket_topk(const RegSeg<NB>& rs, int keep, int32_t* out,
     if (rank < want) m.ck[rank] = cand_index(x);
   }
   __syncthreads();
-  for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(m.ck[i]);
+  copy_out(out, m.ck, keep);
   return true;
 }
 
@@ -975,7 +993,8 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
   static_assert(CL * kWarps * NB * 128 <= (1 << kIndexBits), "key indices must fit the candidate word");
   if (cand_cap < kBins) return false;  // the bucket cursors need kBins words of m.ci (same in every CTA)
   // the histograms are cleared while the row's loads are still in flight
-  for (int i = tid; i < kHistWords; i += kThreads) m.hist[i] = m.merged[i] = 0;
+  zero_words(m.hist, kHistWords);
+  zero_words(m.merged, kHistWords);
   float fmin = __int_as_float(0x7f800000), fmax = -fmin;
   rs.visit_f([&](const uint32_t (&x)[4], uint32_t, int c) {
 #pragma unroll
@@ -1114,7 +1133,7 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
     if (rk < want) m.ck[rk] = cand_index(x);
   }
   __syncthreads();
-  for (int i = tid; i < keep; i += kThreads) out[i] = static_cast<int32_t>(m.ck[i]);
+  copy_out(out, m.ck, keep);
   return true;
 }
 
