@@ -647,11 +647,12 @@ __device__ __forceinline__ uint32_t mates_above(const uint64_t* bw, uint32_t q0,
 }
 
 // Descending exclusive scan of a kBins histogram in place: h[b] becomes the number of keys
-// in the buckets above b, the start of bucket b in descending order.  Thread t owns bins
-// 4095 - 16t .. 4080 - 16t.  The bucket where the running count from the top reaches want
-// goes to info[0] and the keys of the buckets at and above it to info[1]; info[2] is set
-// when one of those buckets holds more than kBucketLimit keys.  info[2] must be zero and
-// red free at entry; ends with a barrier.
+// in the buckets above b, the start of bucket b in descending order, for the buckets at
+// and above the threshold (a group of 16 wholly below it keeps its counts: nothing reads
+// starts there).  Thread t owns bins 4095 - 16t .. 4080 - 16t.  The bucket where the
+// running count from the top reaches want goes to info[0] and the keys of the buckets at
+// and above it to info[1]; info[2] is set when one of those buckets holds more than
+// kBucketLimit keys.  info[2] must be zero and red free at entry; ends with a barrier.
 __device__ __forceinline__ void scan_desc_starts(uint32_t* h, uint32_t want, uint32_t* red, uint32_t* info) {
   static_assert(kBins == 16 * kThreads, "one group of 16 bins per thread");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -670,18 +671,20 @@ __device__ __forceinline__ void scan_desc_starts(uint32_t* h, uint32_t want, uin
   uint32_t r = incl - sum;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) r += w < warp ? red[w] : 0u;
+  if (r < want) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const uint32_t b = static_cast<uint32_t>(b_hi - 1 - j);
-    if (r < want) {
-      if (c[j] > static_cast<uint32_t>(kBucketLimit)) info[2] = 1u;
-      if (r + c[j] >= want) {
-        info[0] = b;
-        info[1] = r + c[j];
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t b = static_cast<uint32_t>(b_hi - 1 - j);
+      if (r < want) {
+        if (c[j] > static_cast<uint32_t>(kBucketLimit)) info[2] = 1u;
+        if (r + c[j] >= want) {
+          info[0] = b;
+          info[1] = r + c[j];
+        }
       }
+      hg[-j] = r;
+      r += c[j];
     }
-    hg[-j] = r;
-    r += c[j];
   }
   __syncthreads();
 }
