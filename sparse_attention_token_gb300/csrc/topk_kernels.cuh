@@ -605,17 +605,20 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 }
 
 // Bucket of score x on a linear grid of kBins equal-width buckets between the row's
-// smallest score lo and its largest: floor((x - lo) * scale), at most kBins - 1.  Every
-// step is a correctly rounded IEEE operation (no contraction), so the bucket is a
-// non-decreasing function of x and the same score always lands in the same bucket.
-// The floor is taken without a conversion instruction (those issue at a quarter of the
-// FP32 rate): for 0 <= y < 2^23, y + 2^23 rounded toward zero is 2^23 + floor(y), whose
-// low 23 bits are floor(y).  y = (x - lo) * scale is never negative (x >= lo) and at most
-// about kBins.
+// smallest score lo and its largest hi: floor((x - lo) * scale) with
+// scale = bucket_scale(hi - lo).  Every step is a correctly rounded IEEE operation (no
+// contraction), so the bucket is a non-decreasing function of x and the same score always
+// lands in the same bucket.  The floor is taken without a conversion instruction (those
+// issue at a quarter of the FP32 rate): for 0 <= y < 2^23, y + 2^23 rounded toward zero is
+// 2^23 + floor(y), whose low 23 bits are floor(y).  y = (x - lo) * scale is never negative
+// (x >= lo) and below kBins, so no clamp: x - lo <= hi - lo = width (the same rounded
+// subtraction at its largest), and scale rounds (kBins - 2^-10) / width, so
+// y <= (kBins - 2^-10)(1 + 2^-24)^2 < kBins - 2^-11.
+constexpr float kBucketSpan = static_cast<float>(kBins) - 0x1p-10f;
+__device__ __forceinline__ float bucket_scale(float width) { return __fdiv_rn(kBucketSpan, width); }
 __device__ __forceinline__ uint32_t lin_bucket(float x, float lo, float scale) {
   const float y = __fmul_rn(__fsub_rn(x, lo), scale);
-  const uint32_t b = __float_as_uint(__fadd_rz(y, 0x1p23f)) & 0x7FFFFFu;
-  return b < static_cast<uint32_t>(kBins - 1) ? b : static_cast<uint32_t>(kBins - 1);
+  return __float_as_uint(__fadd_rz(y, 0x1p23f)) & 0x7FFFFFu;
 }
 
 // A candidate of the linear-bucket paths as one 8-byte word: the order-preserving key in
@@ -722,7 +725,7 @@ __device__ bool linear_bucket_topk(const RegSeg<NB>& rs, int keep, int32_t* out,
   for (int w = 0; w < kWarps; ++w) { kmin = min(kmin, red[w]); kmax = max(kmax, red[kWarps + w]); }
   const float lo = key_value(kmin), hi = key_value(kmax);
   const float width = __fsub_rn(hi, lo);
-  const float scale = __fdiv_rn(static_cast<float>(kBins), width);
+  const float scale = bucket_scale(width);
   // all-equal rows, and ranges whose width or scale is not a positive finite number
   if (!(width > 0.f) || !(scale > 0.f) || isinf(width) || isinf(scale)) return false;  // uniform: same inputs
   rs.visit_f([&](const uint32_t (&x)[4], uint32_t, int c) {
@@ -1030,7 +1033,7 @@ __device__ bool cluster_linear_topk(const RegSeg<NB>& rs, long long part_lo, lon
   __syncthreads();
   const float lo = key_value(red[0]), hi = key_value(red[1]);
   const float width = __fsub_rn(hi, lo);
-  const float scale = __fdiv_rn(static_cast<float>(kBins), width);
+  const float scale = bucket_scale(width);
   if (!(width > 0.f) || !(scale > 0.f) || isinf(width) || isinf(scale)) return false;  // the same in every CTA
   rs.visit_f([&](const uint32_t (&x)[4], uint32_t, int c) {
 #pragma unroll

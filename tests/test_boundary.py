@@ -410,3 +410,22 @@ def test_bench_in_band_clock_from_two_samples():
     assert r["sms"] == 2
     assert abs(r["sm_mhz_max"] - 2070.0) < 1e-9 and abs(r["sm_mhz_min"] - 1000.0) < 1e-9
     assert bench.sm_clock_in_band(a, torch.tensor([[7, 1, 1]], dtype=torch.int64)) is None  # no SM in both
+
+
+def test_linear_bucket_scale_keeps_the_floor_below_the_bin_count():
+    # the top-k kernels' linear buckets: y = RN(RN(x - lo) * RN((4096 - 2^-10) / width)) must
+    # stay below 4096 for every x <= hi (the kernels take floor(y) with no clamp); the
+    # largest y comes with x = hi, where x - lo is exactly the rounded width
+    import numpy as np
+    span = np.float32(4096) - np.float32(2.0 ** -10)
+    assert float(span) == 4096 - 2.0 ** -10
+    rng = np.random.default_rng(0)
+    lo = (rng.standard_normal(400_000) * 10.0 ** rng.integers(-20, 20, 400_000)).astype(np.float32)
+    hi = (lo + np.abs(rng.standard_normal(400_000)) * 10.0 ** rng.integers(-20, 20, 400_000)).astype(np.float32)
+    width = (hi - lo).astype(np.float32)
+    ok = (width > 0) & np.isfinite(width)
+    lo, hi, width = lo[ok], hi[ok], width[ok]
+    scale = (span / width).astype(np.float32)
+    ok = np.isfinite(scale) & (scale > 0)
+    y = ((hi[ok] - lo[ok]).astype(np.float32) * scale[ok]).astype(np.float32)
+    assert (y < 4096).all() and y.max() > 4095
