@@ -34,8 +34,9 @@ constexpr size_t kMaxSmem = 232448;          // opt-in dynamic shared memory per
 // Target bytes of fp32 scores per chunk of query rows (the workspace holds one chunk).
 // Large chunks amortise the launch tails of the score and top-k kernels more than they
 // lose by the scores leaving L2: chunked prefill of 8192 rows against 65536 keys took
-// 9.67 ms with 64 MiB chunks, 9.18 ms with 256 MiB and 8.59 ms with 1 GiB.
-constexpr size_t kScoreChunkBudget = 1ull << 30;
+// 9.67 ms with 64 MiB chunks, 9.18 ms with 256 MiB and 8.59 ms with 1 GiB; on later
+// kernels 5.70 ms with 1 GiB (two chunks) and 5.65 ms with 2 GiB (one).
+constexpr size_t kScoreChunkBudget = 2ull << 30;
 
 // ---------------------------------------------------------------- work list (paged path)
 __global__ void prep_items_kernel(const int32_t* cu_q_lens, const int32_t* seq_lens, int NQ, int KC, int R, int cap,
