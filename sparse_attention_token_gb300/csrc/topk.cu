@@ -15,15 +15,20 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
   if (cap < keep_cap) return cudaErrorInvalidValue;
   cap = (cap + 31) & ~31;
   const size_t smem = (static_cast<size_t>(kHistWords) + 4 * static_cast<size_t>(cap)) * 4;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 0;
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     TopkArgs b = a;
     b.prefetch_ahead = 0;
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) == cudaSuccess)
+    int per_sm = 0;
+    // the rows one wave ahead go to L2 only while they and the wave being read take a
+    // small part of it (a streamed row is read three times from L2)
+    if (sms > 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) == cudaSuccess &&
+        static_cast<long long>(sms) * per_sm * max_row_len * 4 <= (32LL << 20))
       b.prefetch_ahead = sms * per_sm;
     e = launch_pdl(kern, dim3(static_cast<unsigned>(a.n_rows)), dim3(kThreads), smem, st, b, cap);
     if (e != cudaSuccess) return e;
@@ -36,8 +41,12 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
   const size_t csmem = (static_cast<size_t>(kHistWords) + 4 * static_cast<size_t>(ccap)) * 4 +
                        static_cast<size_t>(kHistWords) * 4;  // + merged histogram
   if (max_row_len <= kWarps * 8 * 128) return go(topk_kernel<8>);
-  // a cluster per row: 4 CTAs of 8192 or 16384 keys up to 65536 keys (few CTAs, few merge
-  // partners), then 8 of 16384
+  // many long rows: one CTA per row reading its row from memory (once from DRAM, twice
+  // more from L2) keeps every SM busy with several rows; a cluster's rows wait on
+  // exchanges between its CTAs, with two CTAs resident per SM
+  if (sms > 0 && a.n_rows > sms / 2) return go(topk_kernel<0>);
+  // few long rows: a cluster per row, 4 CTAs of 8192 or 16384 keys up to 65536 keys (few
+  // CTAs, few merge partners), then 8 of 16384
   if (max_row_len <= 4 * kWarps * 8 * 128) return launch_topk_cluster_8_4(a, ccap, csmem, st);
   if (max_row_len <= 4 * kWarps * 16 * 128) return launch_topk_cluster_16_4(a, ccap, csmem, st);
   if (max_row_len <= 8 * kWarps * 16 * 128) return launch_topk_cluster_16_8(a, ccap, csmem, st);

@@ -3,17 +3,18 @@
 // "性能模型设计" bucket 8, top-k selection; output width min(topk_limit, n_visible)).
 //
 // One CTA of 256 threads per row (rows up to 8192 keys, held in registers), or a cluster
-// of CTAs per row (longer rows), or one CTA streaming the row from memory (any length).
+// of CTAs per row (longer rows, few of them), or one CTA streaming the row from memory
+// (longer rows when there are enough of them to fill the GPU, and rows of any length).
 // The best `keep` keys under (score desc, index asc) are found as follows.
-//   Score order, rows in registers -- the linear-bucket path (linear_bucket_topk,
-//      cluster_linear_topk): one histogram of 4096 equal-width buckets between the row's
+//   Score order -- the linear-bucket path (linear_bucket_topk on a row in registers or
+//      streamed from memory, cluster_linear_topk): one histogram of 4096 equal-width buckets between the row's
 //      extremes, a descending scan for the threshold bucket and every bucket's start, the
 //      keys of the buckets at and above it placed straight at their bucket's slots as
 //      (key, bucket, index) words, and each word ranked among its bucket-mates.  It
 //      declines rows whose scores are all equal, whose candidate buckets hold more than
 //      kBucketLimit keys, or whose candidates overflow the buffers, and the general path
 //      takes them.
-//   General path (index order, declined rows, streamed rows): scores become
+//   General path (index order, declined rows): scores become
 //      order-preserving unsigned keys (larger score -> larger key; -0.0 folded onto
 //      +0.0).
 //   1. One pass over the row builds a histogram of the top 12 key bits; a suffix
@@ -134,6 +135,20 @@ __device__ __forceinline__ int load4(const float* p, long long n, long long i, u
   return c;
 }
 
+// Four consecutive scores of the row starting at i as raw fp32 bits (cnt of them valid, the
+// rest 0).
+__device__ __forceinline__ int load4_raw(const float* p, long long n, long long i, uint32_t (&x)[4]) {
+  const long long rem = n - i;
+  if (rem >= 4) {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(p + i));
+    x[0] = __float_as_uint(f.x); x[1] = __float_as_uint(f.y); x[2] = __float_as_uint(f.z); x[3] = __float_as_uint(f.w);
+    return 4;
+  }
+  const int c = rem > 0 ? static_cast<int>(rem) : 0;
+  for (int j = 0; j < 4; ++j) x[j] = j < c ? __float_as_uint(__ldg(p + i + j)) : 0u;
+  return c;
+}
+
 // A row is split into kWarps contiguous segments, one per warp; a segment is read
 // in blocks of 128 keys (lane l holds keys 4l..4l+3 of the block), so the order
 // (segment, block, lane, element) is the key-index order.
@@ -147,12 +162,44 @@ struct GlobalSeg {
   const float* p;
   long long s0, s1;
   int nb;
+  int nfull;  // blocks full for every lane
   __device__ void init(const float* row, long long n) {
     const long long seg = seg_len(n);
     p = row;
     s0 = (threadIdx.x >> 5) * seg;
     s1 = min(n, s0 + seg);
     nb = s1 > s0 ? static_cast<int>((s1 - s0 + 127) / 128) : 0;
+    nfull = s1 > s0 ? static_cast<int>((s1 - s0) / 128) : 0;
+  }
+  // f(x[4] raw fp32 bits, first index, valid count) for every block of this lane, in index
+  // order; batches whose blocks are all full for every lane pass a constant count of 4.
+  template <class F>
+  __device__ __forceinline__ void visit_f(F f) const {
+    const uint32_t i0 = static_cast<uint32_t>(s0) + 4u * (threadIdx.x & 31);
+    int j0 = 0;
+    for (; j0 + kBatch <= nfull; j0 += kBatch) {
+      uint32_t x[kBatch][4];
+#pragma unroll
+      for (int jj = 0; jj < kBatch; ++jj) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(p + i0 + 128u * (j0 + jj)));
+        x[jj][0] = __float_as_uint(v.x); x[jj][1] = __float_as_uint(v.y);
+        x[jj][2] = __float_as_uint(v.z); x[jj][3] = __float_as_uint(v.w);
+      }
+#pragma unroll
+      for (int jj = 0; jj < kBatch; ++jj) f(x[jj], i0 + 128u * (j0 + jj), 4);
+    }
+    for (; j0 < nb; j0 += kBatch) {
+      uint32_t x[kBatch][4];
+      int c[kBatch];
+#pragma unroll
+      for (int jj = 0; jj < kBatch; ++jj) {
+        const long long i = static_cast<long long>(i0) + 128LL * (j0 + jj);
+        c[jj] = (j0 + jj < nb && i < s1) ? load4_raw(p, s1, i, x[jj]) : 0;
+      }
+#pragma unroll
+      for (int jj = 0; jj < kBatch; ++jj)
+        if (c[jj] > 0) f(x[jj], i0 + 128u * (j0 + jj), c[jj]);
+    }
   }
   // f(u[4], first index, valid count) for every block of this lane, in index order.
   template <class F>
@@ -700,11 +747,12 @@ __device__ __forceinline__ void scan_desc_starts(uint32_t* h, uint32_t want, uin
 // plus the bucket-mates that beat it (higher key, or the same key at a lower index).
 // Returns false, having written nothing, when a bucket at or above the threshold holds
 // more than kBucketLimit keys, the candidates overflow the buffers, or the row's scores
-// are all equal; the caller then takes the general path.
-template <int NB>
-__device__ bool linear_bucket_topk(const RegSeg<NB>& rs, int keep, int32_t* out, int cand_cap, const TopkSmem& m,
+// are all equal; the caller then takes the general path.  RS is a row held in registers
+// (RegSeg) or read from memory on each of the three passes (GlobalSeg, rows of at most
+// 2^kIndexBits keys: the caller checks).
+template <class RS>
+__device__ bool linear_bucket_topk(const RS& rs, int keep, int32_t* out, int cand_cap, const TopkSmem& m,
                                    uint32_t* red, uint32_t* info) {
-  static_assert(kWarps * NB * 128 <= (1 << kIndexBits), "key indices must fit the candidate word");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // the histogram is cleared while the row's loads are still in flight
   static_assert(kHistWords % 4 == 0, "16-byte clears");
@@ -923,10 +971,11 @@ __global__ void __launch_bounds__(kThreads, NB == 8 ? 3 : 2) topk_kernel(const T
   for (int i = R.keep + threadIdx.x; i < a.k_out; i += kThreads) R.out[i] = -1;
   if (R.keep == 0) return;
   using RS = typename std::conditional<NB == 0, GlobalSeg, RegSeg<(NB > 0 ? NB : 1)>>::type;
+  static_assert(NB == 0 || kWarps * NB * 128 <= (1 << kIndexBits), "key indices must fit the candidate word");
   RS rs;
   rs.init(R.src, R.n);
-  if constexpr (NB > 0) {
-    if (a.order == 0 && linear_bucket_topk(rs, R.keep, R.out, cand_cap, m, red, info)) return;
+  if (a.order == 0 && (NB > 0 || R.n <= (1LL << kIndexBits))) {
+    if (linear_bucket_topk(rs, R.keep, R.out, cand_cap, m, red, info)) return;
     __syncthreads();  // the general path reuses the shared buffers
   }
   row_topk(rs, R.n, R.keep, a.order == 0, R.out, cand_cap, m, red, info);

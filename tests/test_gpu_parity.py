@@ -199,6 +199,36 @@ def test_topk_linear_bucket_edges_exact(kind, S, limit):
     assert np.array_equal(got, ref)
 
 
+# many rows longer than one CTA's registers hold (more rows than half the SMs): one CTA
+# streams each row from memory, linear buckets in score order with the general path for the
+# rows they decline, and the general path in index order
+@pytest.mark.parametrize("order", [0, 1])
+@pytest.mark.parametrize("kind,S,limit", [("gaussian", 20000, 2048), ("gaussian", 70000, 2048),
+                                          ("gaussian", 9000, 1), ("heavy_tail", 30000, 3900),
+                                          ("outliers", 20000, 2048), ("one_distinct", 12000, 2048),
+                                          ("quantised", 20000, 2048), ("ties", 20000, 64)])
+def test_topk_many_long_rows_exact(kind, S, limit, order):
+    g = torch.Generator().manual_seed(S * 13 + limit + len(kind))
+    T = 120
+    sc = torch.randn((T, S), generator=g).numpy().astype(np.float32)
+    if kind == "heavy_tail":
+        sc = np.exp(4.0 * sc).astype(np.float32)
+    elif kind == "outliers":
+        sc[:, ::997] = 1e30
+        sc[7, 11] = np.inf
+    elif kind == "one_distinct":
+        sc[:] = -0.75
+        sc[:, S // 5] = 0.5
+    elif kind == "quantised":
+        sc = (np.round(sc / 0.01) * 0.01).astype(np.float32)
+    elif kind == "ties":
+        sc = np.round(sc).astype(np.float32)
+        sc[3] = 0.0
+        sc[4, ::2] = -0.0
+    got, ref = _topk_on(sc, S - T, S, limit, min(limit + 3, 4096), order)
+    assert np.array_equal(got, ref)
+
+
 def test_topk_causal_rows_prefill_shape():
     g = torch.Generator().manual_seed(1)
     T = S = 3000
