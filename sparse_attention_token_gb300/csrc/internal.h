@@ -89,6 +89,9 @@ struct TopkArgs {
   // single-CTA rows: CTA i prefetches into L2 the row of CTA i + prefetch_ahead (about one
   // wave of resident CTAs later); 0 = no prefetch
   int prefetch_ahead;
+  // rows streamed from memory in score order: room (keys) for the one-pass selection's
+  // kept keys, in shared memory after the candidate arrays; 0 = three passes over the row
+  int spec_cap;
 };
 
 // Programmatic dependent launch may be switched off for the calling host thread: the

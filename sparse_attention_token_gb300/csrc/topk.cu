@@ -19,18 +19,20 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 0;
-  auto go = [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  auto go = [&](auto kern, int spec_cap) -> cudaError_t {
+    const size_t ksmem = smem + static_cast<size_t>(spec_cap) * 8;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ksmem));
     if (e != cudaSuccess) return e;
     TopkArgs b = a;
     b.prefetch_ahead = 0;
+    b.spec_cap = spec_cap;
     int per_sm = 0;
     // the rows one wave ahead go to L2 only while they and the wave being read take a
-    // small part of it (a streamed row is read three times from L2)
-    if (sms > 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) == cudaSuccess &&
+    // small part of it (a streamed row may be read three times from L2)
+    if (sms > 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, ksmem) == cudaSuccess &&
         static_cast<long long>(sms) * per_sm * max_row_len * 4 <= (32LL << 20))
       b.prefetch_ahead = sms * per_sm;
-    e = launch_pdl(kern, dim3(static_cast<unsigned>(a.n_rows)), dim3(kThreads), smem, st, b, cap);
+    e = launch_pdl(kern, dim3(static_cast<unsigned>(a.n_rows)), dim3(kThreads), ksmem, st, b, cap);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   };
@@ -40,17 +42,28 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
   const int ccap = max_cap;
   const size_t csmem = (static_cast<size_t>(kHistWords) + 4 * static_cast<size_t>(ccap)) * 4 +
                        static_cast<size_t>(kHistWords) * 4;  // + merged histogram
-  if (max_row_len <= kWarps * 8 * 128) return go(topk_kernel<8>);
-  // many long rows: one CTA per row reading its row from memory (once from DRAM, twice
-  // more from L2) keeps every SM busy with several rows; a cluster's rows wait on
-  // exchanges between its CTAs, with two CTAs resident per SM
-  if (sms > 0 && a.n_rows > sms / 2) return go(topk_kernel<0>);
+  // streamed rows in score order: room for about three times the kept keys (at least 4096)
+  // for the one-pass selection, within 200 KB of shared memory per CTA
+  int spec_cap = 0;
+  if (a.order == 0) {
+    long long sc = 3LL * keep_cap;
+    if (sc < 4096) sc = 4096;
+    const long long room = ((200LL << 10) - static_cast<long long>(smem)) / 8;
+    if (sc > room) sc = room;
+    sc &= ~31LL;
+    if (sc >= 2LL * keep_cap) spec_cap = static_cast<int>(sc);
+  }
+  if (max_row_len <= kWarps * 8 * 128) return go(topk_kernel<8>, 0);
+  // many long rows: one CTA per row reading its row from memory (in score order once, the
+  // selection running on the keys above a threshold taken from a sample) keeps every SM
+  // busy with several rows; a cluster's rows wait on exchanges between its CTAs
+  if (sms > 0 && a.n_rows > sms / 2) return go(topk_kernel<0>, spec_cap);
   // few long rows: a cluster per row, 4 CTAs of 8192 or 16384 keys up to 65536 keys (few
   // CTAs, few merge partners), then 8 of 16384
   if (max_row_len <= 4 * kWarps * 8 * 128) return launch_topk_cluster_8_4(a, ccap, csmem, st);
   if (max_row_len <= 4 * kWarps * 16 * 128) return launch_topk_cluster_16_4(a, ccap, csmem, st);
   if (max_row_len <= 8 * kWarps * 16 * 128) return launch_topk_cluster_16_8(a, ccap, csmem, st);
-  return go(topk_kernel<0>);
+  return go(topk_kernel<0>, spec_cap);
 }
 
 }  // namespace dsa

@@ -173,6 +173,7 @@ struct GlobalSeg {
   }
   // f(x[4] raw fp32 bits, first index, valid count) for every block of this lane, in index
   // order; batches whose blocks are all full for every lane pass a constant count of 4.
+  // Every lane of the warp calls f for the same blocks (f may use warp collectives).
   template <class F>
   __device__ __forceinline__ void visit_f(F f) const {
     const uint32_t i0 = static_cast<uint32_t>(s0) + 4u * (threadIdx.x & 31);
@@ -194,11 +195,12 @@ struct GlobalSeg {
 #pragma unroll
       for (int jj = 0; jj < kBatch; ++jj) {
         const long long i = static_cast<long long>(i0) + 128LL * (j0 + jj);
+        x[jj][0] = x[jj][1] = x[jj][2] = x[jj][3] = 0u;
         c[jj] = (j0 + jj < nb && i < s1) ? load4_raw(p, s1, i, x[jj]) : 0;
       }
 #pragma unroll
       for (int jj = 0; jj < kBatch; ++jj)
-        if (c[jj] > 0) f(x[jj], i0 + 128u * (j0 + jj), c[jj]);
+        if (j0 + jj < nb) f(x[jj], i0 + 128u * (j0 + jj), c[jj]);
     }
   }
   // f(u[4], first index, valid count) for every block of this lane, in index order.
@@ -816,6 +818,169 @@ __device__ bool linear_bucket_topk(const RS& rs, int keep, int32_t* out, int can
   return true;
 }
 
+// Score-order top-k of a long row read from memory, in one pass over the row.  A sample of
+// the row (32 runs of 128 keys spread over it) gives a value t above which about
+// (keep + spec_cap) / 2 of the row's keys should lie; one pass keeps every key >= t, with
+// its index, in shared memory (spec, room for spec_cap); when at least `keep` keys were
+// kept and they fit, the answer lies among them (the keep-th best key is >= t), and the
+// linear-bucket selection runs on them: extremes, one histogram of 4096 buckets, the
+// descending scan, placement at each bucket's slots, the rank among bucket-mates.  Rows of
+// at most spec_cap keys are kept whole.  Returns 1 when the output is written; 0 when the
+// sample misjudged t (too few kept keys, or too many for spec) -- the caller then reads the
+// row in three passes; -1 when the kept keys defeat the buckets (all equal, a bucket of
+// more than kBucketLimit keys at or above the threshold) -- the caller takes the general
+// path.  Rows of at most 2^kIndexBits keys (the caller checks).
+constexpr int kSampleRuns = 32;  // 4 per warp, 128 keys each: 16 keys per thread
+__device__ int stream_topk(const GlobalSeg& rs, const float* row, long long n, int keep, int32_t* out, int cand_cap,
+                           uint2* spec, int spec_cap, const TopkSmem& m, uint32_t* red, uint32_t* info) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t want = static_cast<uint32_t>(keep);
+  // -- the threshold t from a sample (every key of a row that spec holds whole)
+  float t = -__int_as_float(0x7f800000);
+  zero_words(m.hist, kHistWords);
+  if (tid == 0) { info[2] = 0u; info[3] = 0u; }
+  if (n > spec_cap) {
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int run = 4 * warp + r;
+      const long long o = ((n - 128) * run / (kSampleRuns - 1)) & ~3LL;  // o + 128 <= n, 16-byte aligned
+      const float4 v = __ldg(reinterpret_cast<const float4*>(row + o + 4 * lane));
+      x[4 * r] = v.x; x[4 * r + 1] = v.y; x[4 * r + 2] = v.z; x[4 * r + 3] = v.w;
+    }
+    float fmin = x[0], fmax = x[0];
+#pragma unroll
+    for (int j = 1; j < 16; ++j) { fmin = fminf(fmin, x[j]); fmax = fmaxf(fmax, x[j]); }
+    uint32_t kmin = __reduce_min_sync(0xffffffffu, order_key(fmin));
+    uint32_t kmax = __reduce_max_sync(0xffffffffu, order_key(fmax));
+    if (lane == 0) { red[warp] = kmin; red[kWarps + warp] = kmax; }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) { kmin = min(kmin, red[w]); kmax = max(kmax, red[kWarps + w]); }
+    const float lo = key_value(kmin), hi = key_value(kmax);
+    const float width = __fsub_rn(hi, lo);
+    const float scale = bucket_scale(width);
+    __syncthreads();  // red is reused below
+    if (!(width > 0.f) || !(scale > 0.f) || isinf(width) || isinf(scale)) {
+      t = hi;  // a flat or unbounded sample: keep the keys at its top
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) atomicAdd(&m.hist[hslot(lin_bucket(x[j], lo, scale))], 1u);
+      __syncthreads();
+      // sample keys at and above the bucket that should hold the target count
+      const long long target = (static_cast<long long>(keep) + spec_cap) / 2;
+      long long r_s = (target * (kSampleRuns * 128) + n - 1) / n;
+      if (r_s < 1) r_s = 1;
+      find_bucket(m.hist, kBins, static_cast<uint32_t>(r_s), red, info);  // r_s <= the 4096 sample keys
+      t = __fadd_rn(lo, __fdiv_rn(static_cast<float>(info[0]), scale));
+      zero_words(m.hist, kHistWords);
+      if (tid == 0) info[2] = 0u;
+    }
+  }
+  __syncthreads();
+  // -- one pass: keep every key >= t with its index.  Each warp takes its segment in
+  // batches of 8 blocks (all loads issued first); a lane counts its kept keys in the batch,
+  // one warp scan and one shared atomic give every lane its first slot, and the lane
+  // writes its keys there in index order (predicated stores, no per-key vote).
+  uint32_t* kept = &info[3];
+  {
+    constexpr int kB = 8;  // blocks per batch: 32 keys per lane in registers
+    const uint32_t i0 = static_cast<uint32_t>(rs.s0) + 4u * static_cast<uint32_t>(lane);
+    const uint32_t s1 = static_cast<uint32_t>(rs.s1);
+    for (int j0 = 0; j0 < rs.nb; j0 += kB) {
+      uint32_t x[kB][4];
+      const bool full = j0 + kB <= rs.nfull;  // uniform in the warp
+      if (full) {
+#pragma unroll
+        for (int jj = 0; jj < kB; ++jj) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(rs.p + i0 + 128u * (j0 + jj)));
+          x[jj][0] = __float_as_uint(v.x); x[jj][1] = __float_as_uint(v.y);
+          x[jj][2] = __float_as_uint(v.z); x[jj][3] = __float_as_uint(v.w);
+        }
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < kB; ++jj) {
+          const uint32_t i = i0 + 128u * (j0 + jj);
+          x[jj][0] = x[jj][1] = x[jj][2] = x[jj][3] = 0u;
+          if (j0 + jj < rs.nb && i < s1) load4_raw(rs.p, rs.s1, i, x[jj]);
+        }
+      }
+      auto keeps = [&](int jj, int e) {
+        return (full || i0 + 128u * (j0 + jj) + e < s1) && __uint_as_float(x[jj][e]) >= t;
+      };
+      uint32_t cnt = 0;
+#pragma unroll
+      for (int jj = 0; jj < kB; ++jj)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cnt += keeps(jj, e) ? 1u : 0u;
+      const uint32_t incl = warp_incl_scan(cnt);
+      const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+      if (tot == 0) continue;  // uniform in the warp
+      uint32_t base = 0;
+      if (lane == 31) base = atomicAdd(kept, tot);
+      uint32_t pos = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+      if (cnt == 0) continue;
+#pragma unroll
+      for (int jj = 0; jj < kB; ++jj)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (keeps(jj, e)) {
+            if (pos < static_cast<uint32_t>(spec_cap)) spec[pos] = make_uint2(x[jj][e], i0 + 128u * (j0 + jj) + e);
+            ++pos;
+          }
+        }
+    }
+  }
+  __syncthreads();
+  const uint32_t n_spec = *kept;
+  if (n_spec < want || n_spec > static_cast<uint32_t>(spec_cap)) return 0;  // uniform: shared value
+  // -- the linear-bucket selection on the kept keys
+  float fmin = __int_as_float(0x7f800000), fmax = -fmin;
+  for (uint32_t p = tid; p < n_spec; p += kThreads) {
+    const float f = __uint_as_float(spec[p].x);
+    fmin = fminf(fmin, f);
+    fmax = fmaxf(fmax, f);
+  }
+  uint32_t kmin = __reduce_min_sync(0xffffffffu, order_key(fmin));
+  uint32_t kmax = __reduce_max_sync(0xffffffffu, order_key(fmax));
+  if (lane == 0) { red[warp] = kmin; red[kWarps + warp] = kmax; }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) { kmin = min(kmin, red[w]); kmax = max(kmax, red[kWarps + w]); }
+  const float lo = key_value(kmin), hi = key_value(kmax);
+  const float width = __fsub_rn(hi, lo);
+  const float scale = bucket_scale(width);
+  if (!(width > 0.f) || !(scale > 0.f) || isinf(width) || isinf(scale)) return -1;  // uniform: same inputs
+  for (uint32_t p = tid; p < n_spec; p += kThreads)
+    atomicAdd(&m.hist[hslot(lin_bucket(__uint_as_float(spec[p].x), lo, scale))], 1u);
+  __syncthreads();
+  // red is free: its last readers passed the barrier above
+  scan_desc_starts(m.hist, want, red, info);
+  const uint32_t d1 = info[0], n_cand = info[1];
+  if (info[2] != 0u || n_cand + kMatePad > static_cast<uint32_t>(cand_cap)) return -1;
+  uint2* bw2 = reinterpret_cast<uint2*>(m.tk);
+  if (tid < static_cast<int>(kMatePad)) bw2[n_cand + tid] = make_uint2(0u, 0u);
+  for (uint32_t p = tid; p < n_spec; p += kThreads) {
+    const uint2 v = spec[p];
+    const float f = __uint_as_float(v.x);
+    const uint32_t b = lin_bucket(f, lo, scale);
+    if (b >= d1) bw2[atomicAdd(&m.hist[hslot(b)], 1u)] = cand_word(f, b, v.y);
+  }
+  __syncthreads();
+  // hist[b] is now the end of bucket b; bucket b starts where bucket b + 1 ends
+  const uint64_t* bw = reinterpret_cast<const uint64_t*>(m.tk);
+  for (uint32_t p = tid; p < n_cand; p += kThreads) {
+    const uint64_t x = bw[p];
+    const uint32_t b = cand_bucket(x);
+    const uint32_t q0 = b + 1 < static_cast<uint32_t>(kBins) ? m.hist[hslot(b + 1)] : 0u, q1 = m.hist[hslot(b)];
+    const uint32_t rank = q0 + mates_above(bw, q0, q1, x);
+    if (rank < want) m.ck[rank] = cand_index(x);
+  }
+  __syncthreads();
+  copy_out(out, m.ck, keep);
+  return 1;
+}
+
 struct RowInfo {
   long long n;
   const float* src;
@@ -968,6 +1133,13 @@ __global__ void __launch_bounds__(kThreads, NB == 8 ? 3 : 2) topk_kernel(const T
     if (bytes > 0 && (reinterpret_cast<uintptr_t>(P.src) & 15u) == 0)
       ptx::bulk_prefetch_l2(P.src, static_cast<uint32_t>(bytes));
   }
+  if (NB == 0 && a.spec_cap > 0 && threadIdx.x == 32 && R.n > a.spec_cap && (reinterpret_cast<uintptr_t>(R.src) & 15u) == 0) {
+    // a long row read once: all of it into L2 now, in 64 KB pieces, while the sample that
+    // sets the threshold is taken (the pass then reads from L2)
+    const long long bytes = ((R.n + 3) & ~3LL) * 4;  // whole 16-byte units inside the row's ld
+    for (long long o = 0; o < bytes; o += 65536)
+      ptx::bulk_prefetch_l2(reinterpret_cast<const char*>(R.src) + o, static_cast<uint32_t>(min(65536LL, bytes - o)));
+  }
   for (int i = R.keep + threadIdx.x; i < a.k_out; i += kThreads) R.out[i] = -1;
   if (R.keep == 0) return;
   using RS = typename std::conditional<NB == 0, GlobalSeg, RegSeg<(NB > 0 ? NB : 1)>>::type;
@@ -975,8 +1147,19 @@ __global__ void __launch_bounds__(kThreads, NB == 8 ? 3 : 2) topk_kernel(const T
   RS rs;
   rs.init(R.src, R.n);
   if (a.order == 0 && (NB > 0 || R.n <= (1LL << kIndexBits))) {
-    if (linear_bucket_topk(rs, R.keep, R.out, cand_cap, m, red, info)) return;
-    __syncthreads();  // the general path reuses the shared buffers
+    int got = 0;
+    if constexpr (NB == 0) {
+      if (a.spec_cap > 0) {
+        uint2* spec = reinterpret_cast<uint2*>(m.ti + cand_cap);  // after the four candidate arrays
+        got = stream_topk(rs, R.src, R.n, R.keep, R.out, cand_cap, spec, a.spec_cap, m, red, info);
+        if (got > 0) return;
+        __syncthreads();  // the next path reuses the shared buffers
+      }
+    }
+    if (got == 0) {
+      if (linear_bucket_topk(rs, R.keep, R.out, cand_cap, m, red, info)) return;
+      __syncthreads();  // the general path reuses the shared buffers
+    }
   }
   row_topk(rs, R.n, R.keep, a.order == 0, R.out, cand_cap, m, red, info);
 }

@@ -206,7 +206,8 @@ def test_topk_linear_bucket_edges_exact(kind, S, limit):
 @pytest.mark.parametrize("kind,S,limit", [("gaussian", 20000, 2048), ("gaussian", 70000, 2048),
                                           ("gaussian", 9000, 1), ("heavy_tail", 30000, 3900),
                                           ("outliers", 20000, 2048), ("one_distinct", 12000, 2048),
-                                          ("quantised", 20000, 2048), ("ties", 20000, 64)])
+                                          ("quantised", 20000, 2048), ("ties", 20000, 64),
+                                          ("sampled_runs_high", 20000, 2048)])
 def test_topk_many_long_rows_exact(kind, S, limit, order):
     g = torch.Generator().manual_seed(S * 13 + limit + len(kind))
     T = 120
@@ -225,6 +226,15 @@ def test_topk_many_long_rows_exact(kind, S, limit, order):
         sc = np.round(sc).astype(np.float32)
         sc[3] = 0.0
         sc[4, ::2] = -0.0
+    elif kind == "sampled_runs_high":
+        # the 32 runs of 128 keys that the one-pass selection samples sit far above the
+        # rest of the row, so the threshold it takes from them keeps too few keys and the
+        # row is read again in three passes
+        for t in range(T):
+            n = S - T + t + 1
+            for r in range(32):
+                o = ((n - 128) * r // 31) & ~3
+                sc[t, o:o + 128] += 10.0
     got, ref = _topk_on(sc, S - T, S, limit, min(limit + 3, 4096), order)
     assert np.array_equal(got, ref)
 
