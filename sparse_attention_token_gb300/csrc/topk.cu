@@ -42,11 +42,12 @@ cudaError_t launch_topk(const TopkArgs& a, int max_row_len, cudaStream_t st) {
   const int ccap = max_cap;
   const size_t csmem = (static_cast<size_t>(kHistWords) + 4 * static_cast<size_t>(ccap)) * 4 +
                        static_cast<size_t>(kHistWords) * 4;  // + merged histogram
-  // streamed rows in score order: room for about three times the kept keys (at least 4096)
-  // for the one-pass selection, within 200 KB of shared memory per CTA
+  // streamed rows in score order: room for 2.25 times the kept keys (at least 4096) for the
+  // one-pass selection (the sample aims halfway between keep and that), within 200 KB of
+  // shared memory per CTA
   int spec_cap = 0;
   if (a.order == 0) {
-    long long sc = 3LL * keep_cap;
+    long long sc = 9LL * keep_cap / 4;
     if (sc < 4096) sc = 4096;
     const long long room = ((200LL << 10) - static_cast<long long>(smem)) / 8;
     if (sc > room) sc = room;

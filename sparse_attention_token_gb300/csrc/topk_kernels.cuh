@@ -883,30 +883,29 @@ __device__ int stream_topk(const GlobalSeg& rs, const float* row, long long n, i
   // one warp scan and one shared atomic give every lane its first slot, and the lane
   // writes its keys there in index order (predicated stores, no per-key vote).
   uint32_t* kept = &info[3];
+  float fmin = __int_as_float(0x7f800000), fmax = -fmin;  // the kept keys' extremes
   {
     constexpr int kB = 8;  // blocks per batch: 32 keys per lane in registers
     const uint32_t i0 = static_cast<uint32_t>(rs.s0) + 4u * static_cast<uint32_t>(lane);
     const uint32_t s1 = static_cast<uint32_t>(rs.s1);
-    for (int j0 = 0; j0 < rs.nb; j0 += kB) {
+    // FULL: the batch's blocks are full for every lane (no bound checks)
+    auto batch = [&](auto full_tag, int j0) {
+      constexpr bool FULL = decltype(full_tag)::value;
       uint32_t x[kB][4];
-      const bool full = j0 + kB <= rs.nfull;  // uniform in the warp
-      if (full) {
 #pragma unroll
-        for (int jj = 0; jj < kB; ++jj) {
-          const float4 v = __ldg(reinterpret_cast<const float4*>(rs.p + i0 + 128u * (j0 + jj)));
+      for (int jj = 0; jj < kB; ++jj) {
+        const uint32_t i = i0 + 128u * (j0 + jj);
+        if constexpr (FULL) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(rs.p + i));
           x[jj][0] = __float_as_uint(v.x); x[jj][1] = __float_as_uint(v.y);
           x[jj][2] = __float_as_uint(v.z); x[jj][3] = __float_as_uint(v.w);
-        }
-      } else {
-#pragma unroll
-        for (int jj = 0; jj < kB; ++jj) {
-          const uint32_t i = i0 + 128u * (j0 + jj);
+        } else {
           x[jj][0] = x[jj][1] = x[jj][2] = x[jj][3] = 0u;
           if (j0 + jj < rs.nb && i < s1) load4_raw(rs.p, rs.s1, i, x[jj]);
         }
       }
       auto keeps = [&](int jj, int e) {
-        return (full || i0 + 128u * (j0 + jj) + e < s1) && __uint_as_float(x[jj][e]) >= t;
+        return (FULL || i0 + 128u * (j0 + jj) + e < s1) && __uint_as_float(x[jj][e]) >= t;
       };
       uint32_t cnt = 0;
 #pragma unroll
@@ -915,36 +914,35 @@ __device__ int stream_topk(const GlobalSeg& rs, const float* row, long long n, i
         for (int e = 0; e < 4; ++e) cnt += keeps(jj, e) ? 1u : 0u;
       const uint32_t incl = warp_incl_scan(cnt);
       const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
-      if (tot == 0) continue;  // uniform in the warp
+      if (tot == 0) return;  // uniform in the warp
       uint32_t base = 0;
       if (lane == 31) base = atomicAdd(kept, tot);
       uint32_t pos = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
-      if (cnt == 0) continue;
+      if (cnt == 0) return;
 #pragma unroll
       for (int jj = 0; jj < kB; ++jj)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           if (keeps(jj, e)) {
+            const float f = __uint_as_float(x[jj][e]);
+            fmin = fminf(fmin, f);
+            fmax = fmaxf(fmax, f);
             if (pos < static_cast<uint32_t>(spec_cap)) spec[pos] = make_uint2(x[jj][e], i0 + 128u * (j0 + jj) + e);
             ++pos;
           }
         }
-    }
-  }
-  __syncthreads();
-  const uint32_t n_spec = *kept;
-  if (n_spec < want || n_spec > static_cast<uint32_t>(spec_cap)) return 0;  // uniform: shared value
-  // -- the linear-bucket selection on the kept keys
-  float fmin = __int_as_float(0x7f800000), fmax = -fmin;
-  for (uint32_t p = tid; p < n_spec; p += kThreads) {
-    const float f = __uint_as_float(spec[p].x);
-    fmin = fminf(fmin, f);
-    fmax = fmaxf(fmax, f);
+    };
+    int j0 = 0;
+    for (; j0 + kB <= rs.nfull; j0 += kB) batch(std::true_type{}, j0);
+    for (; j0 < rs.nb; j0 += kB) batch(std::false_type{}, j0);
   }
   uint32_t kmin = __reduce_min_sync(0xffffffffu, order_key(fmin));
   uint32_t kmax = __reduce_max_sync(0xffffffffu, order_key(fmax));
-  if (lane == 0) { red[warp] = kmin; red[kWarps + warp] = kmax; }
+  if (lane == 0) { red[warp] = kmin; red[kWarps + warp] = kmax; }  // red is free since the sample
   __syncthreads();
+  const uint32_t n_spec = *kept;
+  if (n_spec < want || n_spec > static_cast<uint32_t>(spec_cap)) return 0;  // uniform: shared value
+  // -- the linear-bucket selection on the kept keys (their extremes came with the pass)
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) { kmin = min(kmin, red[w]); kmax = max(kmax, red[kWarps + w]); }
   const float lo = key_value(kmin), hi = key_value(kmax);
