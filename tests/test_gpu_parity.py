@@ -304,6 +304,20 @@ def test_paged_decode_balanced_many_short():
     assert np.array_equal(got, ref)
 
 
+def test_paged_decode_many_mixed_lengths_streamed_exact():
+    # 100 decode rows from 1 to 30000 keys in one launch: more rows than half the SMs and
+    # rows beyond 8192 keys, so every row streams through one CTA -- rows shorter than
+    # keep, rows kept whole by the one-pass selection, and sampled rows side by side
+    lens = [(i * 7919) % 30000 + 1 for i in range(88)] + [1, 2, 2047, 2048, 2049, 4608, 4609, 6144,
+                                                          8192, 8193, 12000, 30000]
+    pc = workloads.paged_case(lens, [1] * len(lens), 16, 128, 2048, page_size=64, k_out=2051,
+                              integer=True, seed=78)
+    for order in (0, 1):
+        got = run_paged(pc, order=order)
+        ref, _, _ = oracle.paged(pc, order=order)
+        assert np.array_equal(got, ref)
+
+
 def test_paged_varlen_prefill_integer_exact():
     lens, qlens = [900, 40, 1500, 300], [300, 40, 17, 1]
     pc = workloads.paged_case(lens, qlens, 64, 128, 128, page_size=64, integer=True, seed=11)
