@@ -823,8 +823,9 @@ __device__ bool linear_bucket_topk(const RS& rs, int keep, int32_t* out, int can
 // (keep + spec_cap) / 2 of the row's keys should lie; one pass keeps every key >= t, with
 // its index, in shared memory (spec, room for spec_cap); when at least `keep` keys were
 // kept and they fit, the answer lies among them (the keep-th best key is >= t), and the
-// linear-bucket selection runs on them: extremes, one histogram of 4096 buckets, the
-// descending scan, placement at each bucket's slots, the rank among bucket-mates.  Rows of
+// linear-bucket selection runs on them: their extremes (taken in the pass), one histogram
+// of 4096 buckets, the descending scan, placement at each bucket's slots, the rank among
+// bucket-mates.  Rows of
 // at most spec_cap keys are kept whole.  Returns 1 when the output is written; 0 when the
 // sample misjudged t (too few kept keys, or too many for spec) -- the caller then reads the
 // row in three passes; -1 when the kept keys defeat the buckets (all equal, a bucket of
