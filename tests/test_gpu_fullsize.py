@@ -67,6 +67,38 @@ def test_prefill_8k_full_size_sampled_rows():
         check_topk_row(tk[t], rt[i], rs[i, :n], RTOL["bf16"] * rb[i, :n], n, min(K, n), True)
 
 
+def test_key_sharded_prefill_8k_full_size_sampled_rows():
+    # the benchmark's key-sharded configuration: the 8K prefill's keys in two shards
+    # (0..4095, 4096..8191), each shard's (score, global index) candidates, then the merge
+    c = workloads.prefill_8k()
+    T, S, K = c.T, c.S, c.topk_limit
+    q, k, w = c.q.cuda(), c.k.cuda(), c.w.cuda()
+    bounds = (0, 4096, 8192)
+    cands = [dsa.dsa_indexer_shard_candidates(q, k[b0:b1].contiguous(), w, q_pos0=0, key_offset=b0, k_cand=K)
+             for b0, b1 in zip(bounds[:-1], bounds[1:])]
+    ci = torch.stack([x[0] for x in cands])
+    cs = torch.stack([x[1] for x in cands])
+    topk = dsa.dsa_indexer_merge_candidates(cs, ci, topk_limit=K)
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_status() == dsa.DSA_OK
+    tk = topk.cpu().numpy()
+    # properties on every row: width, padding, visibility, uniqueness
+    n_vis = np.arange(1, T + 1)
+    keep = np.minimum(n_vis, K)
+    for t in range(T):
+        sel = tk[t, :keep[t]]
+        assert np.all(tk[t, keep[t]:] == -1), t
+        assert sel.min() >= 0 and sel.max() < n_vis[t], t
+        assert len(np.unique(sel)) == keep[t], t
+    # oracle on sampled rows
+    rows = sample_rows(T, K, seed=2)
+    rt, rs, rb = oracle.dense(c.q, c.k, c.w, T=T, S=S, H=c.H, D=c.D, q_pos0=0, topk_limit=K, k_out=K,
+                              rows=rows, want_scores=True, want_bound=True)
+    for i, t in enumerate(rows):
+        n = t + 1
+        check_topk_row(tk[t], rt[i], rs[i, :n], RTOL["bf16"] * rb[i, :n], n, min(K, n), True)
+
+
 def test_chunked_prefill_fp8_full_size_sampled_rows():
     pc = workloads.chunked_prefill_fp8()
     to = lambda t: None if t is None else t.cuda()
